@@ -1,0 +1,158 @@
+"""fp64 CPU oracle for paged grouped-query attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, the smoke check and the benchmark's CPU-baseline / reference
+legs may import this package.  The product library never calls it, and it shares
+no code with the CUDA path: the arithmetic lives in ``oracle.c`` (plain C,
+double precision, the textbook definition written out loop by loop).
+
+Functions take CPU tensors (torch or numpy) holding the same bf16 bit patterns the
+GPU sees and return float64 results.
+
+Parity status: every function here is pinned by the CPU tests in
+``tests/test_oracle_pins.py`` (closed forms, a library routine on tiny cases,
+invariants and a high-precision brute force).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (-O2, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def load_library(path: str):
+    """Load an oracle shared object (the default one, or a test-built variant)."""
+    lib = ctypes.CDLL(path)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    ci = ctypes.c_int
+    lib.oracle_kv_append.argtypes = [u16p, u16p, u16p, u16p, i32p, ci, ci, i32p, i32p, ci,
+                                     ci, ci, ci]
+    lib.oracle_kv_append.restype = ci
+    lib.oracle_attention_rows.argtypes = [f64p, f64p, i32p, i32p, ci, u16p, u16p, u16p,
+                                          i32p, ci, ci, i32p, i32p, ci, ci, ci, ci, ci,
+                                          ctypes.c_double, ci]
+    lib.oracle_attention_rows.restype = ci
+    lib.oracle_paged_attention.argtypes = [f64p, f64p, u16p, u16p, u16p, i32p, ci, ci, i32p,
+                                           i32p, ci, ci, ci, ci, ci, ctypes.c_double, ci]
+    lib.oracle_paged_attention.restype = ci
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = ci
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = load_library(build())
+    return _lib
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 tensor (torch) or uint16 array -> contiguous uint16 numpy array of its bits."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint16
+        return np.ascontiguousarray(x)
+    import torch
+
+    assert x.dtype == torch.bfloat16 and x.device.type == "cpu"
+    return np.ascontiguousarray(x.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _i32(x) -> np.ndarray:
+    if not isinstance(x, np.ndarray):
+        x = x.cpu().numpy()
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _p(a, ct):
+    return a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def max_threads() -> int:
+    return _load().oracle_max_threads()
+
+
+def kv_append(k_pool, v_pool, k_new, v_new, block_table, cu_q_lens, seq_lens, *,
+              block_size: int = 256, lib=None):
+    """Return (k_pool', v_pool') as uint16 arrays: the pools after appending the new rows.
+
+    k_pool/v_pool: [num_blocks, block_size, Hkv, D]; k_new/v_new: [total_tokens, Hkv, D].
+    """
+    kp = _bits(k_pool).copy()
+    vp = _bits(v_pool).copy()
+    kn, vn = _bits(k_new), _bits(v_new)
+    bt, cu, sl = _i32(block_table), _i32(cu_q_lens), _i32(seq_lens)
+    num_blocks, bs, hkv, d = kp.shape
+    assert bs == block_size
+    lib = lib or _load()
+    rc = lib.oracle_kv_append(_p(kp, ctypes.c_uint16), _p(vp, ctypes.c_uint16),
+                              _p(kn, ctypes.c_uint16), _p(vn, ctypes.c_uint16),
+                              _p(bt, ctypes.c_int32), bt.shape[1], num_blocks,
+                              _p(cu, ctypes.c_int32), _p(sl, ctypes.c_int32), len(sl),
+                              hkv, d, bs)
+    if rc:
+        raise ValueError(f"oracle_kv_append rejected its input (code {rc})")
+    return kp, vp
+
+
+def attention(q, k_pool, v_pool, block_table, cu_q_lens, seq_lens, *, scale: float,
+              rows=None, num_threads: int = 0, lib=None):
+    """Paged causal GQA attention in fp64.
+
+    q: [total_tokens, Hq, D] bf16; pools: [num_blocks, block_size, Hkv, D] bf16.
+    rows: None for every (token, head), else a pair of int sequences (tokens, heads).
+    Returns (out, lse) float64: out [T, Hq, D] and lse [T, Hq] for rows=None,
+    else out [n, D] and lse [n].
+    """
+    qb, kb, vb = _bits(q), _bits(k_pool), _bits(v_pool)
+    bt, cu, sl = _i32(block_table), _i32(cu_q_lens), _i32(seq_lens)
+    t, hq, d = qb.shape
+    num_blocks, bs, hkv, d2 = kb.shape
+    assert d == d2 and vb.shape == kb.shape
+    if bt.ndim == 1:
+        bt = bt.reshape(len(sl), -1)
+    lib = lib or _load()
+    if rows is None:
+        out = np.zeros((t, hq, d), np.float64)
+        lse = np.zeros((t, hq), np.float64)
+        rc = lib.oracle_paged_attention(_p(out, ctypes.c_double), _p(lse, ctypes.c_double),
+                                        _p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16),
+                                        _p(vb, ctypes.c_uint16), _p(bt, ctypes.c_int32),
+                                        bt.shape[1], num_blocks, _p(cu, ctypes.c_int32),
+                                        _p(sl, ctypes.c_int32), len(sl), hq, hkv, d, bs,
+                                        float(scale), int(num_threads))
+    else:
+        toks = _i32(np.asarray(rows[0]))
+        hds = _i32(np.asarray(rows[1]))
+        n = len(toks)
+        out = np.zeros((n, d), np.float64)
+        lse = np.zeros((n,), np.float64)
+        rc = lib.oracle_attention_rows(_p(out, ctypes.c_double), _p(lse, ctypes.c_double),
+                                       _p(toks, ctypes.c_int32), _p(hds, ctypes.c_int32), n,
+                                       _p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16),
+                                       _p(vb, ctypes.c_uint16), _p(bt, ctypes.c_int32),
+                                       bt.shape[1], num_blocks, _p(cu, ctypes.c_int32),
+                                       _p(sl, ctypes.c_int32), len(sl), hq, hkv, d, bs,
+                                       float(scale), int(num_threads))
+    if rc:
+        raise ValueError(f"oracle attention rejected its input (code {rc})")
+    return out, lse
