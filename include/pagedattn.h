@@ -1,0 +1,179 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn.so: grouped-query attention over a paged
+ * KV cache on one GB300 (sm_103a).
+ *
+ * Sources (page titles; sections cited as [P1 §x.y] etc.):
+ *   [P1] "扔掉 vLLM！从零构建 Qwen3-8B 推理引擎，C++/CUDA 实现性能追平 98%"
+ *   [P2] "从零手搓AI推理引擎：避开调包陷阱的工程实践指南"
+ *   [P3] "从零搭建AI工程能力：手写KV Cache与动态批处理实战"
+ *
+ * The three compute calls are the per-layer attention work behind the engine's
+ * Prefill / DecodeStep requests [P1 §4.1.2]:
+ *   kv_append           writes the new tokens' K/V into their cache blocks
+ *                       [P1 §4.3.1 KVBlockManager::append]
+ *   paged_attn_decode   one query token per sequence over its whole cached context,
+ *                       the four query heads of a KV group sharing each KV read
+ *                       [P1 §4.4.2 gqa_decode_attn]
+ *   paged_attn_prefill  causal attention of a chunk of new tokens over the earlier
+ *                       context plus itself [P1 §4.4.1 flash_attn_prefill; P3 §3.3
+ *                       chunked prefill]
+ * All three compute softmax(Q K^T * scale) V [P2 §2.2] with the causal rule "a
+ * position sees itself and earlier positions" [P2 §2.2]; the caller appends before
+ * attending, so a context length always counts the new tokens [P3 §4.2].
+ *
+ * Shapes.  Only {num_q_heads 32, num_kv_heads 8, head_dim 128, block_size 256} is
+ * built; anything else returns PA_ERR_UNSUPPORTED.  Query head h reads KV head
+ * h / 4 [P1 §4.4.2].  Token j of a sequence lives in slot j % 256 of physical block
+ * block_table[s][j / 256] [P1 §4.3.1].
+ *
+ * Layouts (row-major, contiguous, device memory, 16-byte aligned):
+ *   q, out        bf16 [tokens][32][128]
+ *   k_new, v_new  bf16 [tokens][8][128]
+ *   k_pool,v_pool bf16 [num_blocks][256][8][128]
+ *   lse           fp32 [tokens][32], natural-log log-sum-exp of the scaled scores
+ *   block_table   int32 [num_seqs][max_blocks_per_seq]
+ *   seq_lens      int32 [num_seqs]     context length including the new tokens
+ *   cu_q_lens     int32 [num_seqs + 1] offsets of each sequence's new tokens
+ *
+ * Ownership.  Every pointer is caller-owned device memory; the library allocates
+ * nothing and keeps no per-call state outside the caller's workspace.
+ *
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ * are asynchronous and stream-ordered; PA_OK means "validated and launched".
+ *
+ * Errors.  Scalar arguments and pointers are checked on the host (PA_ERR_INVALID_ARG,
+ * PA_ERR_UNSUPPORTED) before anything is launched.  Device arrays the host does not
+ * read (block_table, seq_lens, cu_q_lens) are checked by the kernels: a block id
+ * outside [0, num_blocks), a length outside its bound or an inconsistent cu_q_lens
+ * makes the affected work skip its memory accesses and records PA_ERR_DEVICE in the
+ * workspace error word; a bounded device wait that expires records PA_ERR_TIMEOUT.
+ * Kernels never trap.  pa_check_error() reports and clears the word.
+ *
+ * Workspace.  Caller-allocated device memory of pa_workspace_bytes() bytes, zeroed
+ * once by pa_workspace_init() (or cudaMemset to 0) before its first use.  It holds
+ * the error word, split-K partial results and self-resetting counters.  One
+ * workspace must not be used by two calls that may run at the same time.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* bad scalar argument, null or misaligned pointer */
+    PA_ERR_UNSUPPORTED = 2, /* shape other than 32/8/128/256 */
+    PA_ERR_CUDA = 3,        /* a CUDA runtime call failed */
+    PA_ERR_DEVICE = 4,      /* a device-side check of block_table/seq_lens/cu_q_lens failed */
+    PA_ERR_TIMEOUT = 5,     /* a bounded device wait expired */
+    PA_ERR_WORKSPACE = 6    /* workspace smaller than pa_workspace_bytes() requires */
+} pa_status;
+
+typedef struct {
+    int32_t num_q_heads;  /* 32 */
+    int32_t num_kv_heads; /* 8 */
+    int32_t head_dim;     /* 128 */
+    int32_t block_size;   /* 256 */
+} pa_shape;
+
+/* Human-readable name of a status code (static string). */
+const char *pa_status_string(pa_status status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t pa_version(void);
+
+/*
+ * Workspace bytes enough for any of the three calls with up to max_batch sequences
+ * and block tables max_blocks_per_seq wide.  Returns 0 for an unsupported shape or
+ * non-positive sizes.
+ */
+size_t pa_workspace_bytes(pa_shape shape, int32_t max_batch, int32_t max_blocks_per_seq);
+
+/* Zero a workspace on `stream` (asynchronous). */
+pa_status pa_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronise `stream`, read the workspace error word, clear it and return its
+ * status: PA_OK, PA_ERR_DEVICE or PA_ERR_TIMEOUT (PA_ERR_TIMEOUT wins when both
+ * were recorded).  If detail is non-NULL it receives the raw word
+ * (bit 0 device check, bit 1 timeout, bits 8.. the kind of device check).
+ */
+pa_status pa_check_error(void *workspace, void *stream, uint32_t *detail);
+
+/*
+ * kv_append: K/V of the new tokens into their cache slots [P1 §4.3.1].
+ * For sequence s with q_len = cu_q_lens[s+1] - cu_q_lens[s], new token i (row
+ * cu_q_lens[s] + i of k_new/v_new) goes to absolute position
+ * p = seq_lens[s] - q_len + i, i.e. slot p % 256 of block block_table[s][p / 256].
+ * Bit-exact copy; no other pool byte is written.  The blocks written must belong
+ * to one sequence only, and no two new tokens may map to the same slot.
+ *   total_tokens = cu_q_lens[num_seqs]; q_len 0 is allowed (nothing to write).
+ */
+pa_status kv_append(pa_shape shape, void *k_pool, void *v_pool,
+                    const void *k_new, const void *v_new,
+                    const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
+                    const int32_t *cu_q_lens, const int32_t *seq_lens, int32_t num_seqs,
+                    int32_t total_tokens, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/*
+ * paged_attn_decode: one query token per sequence [P1 §4.4.2].
+ * out[b][h] = sum_{j < seq_lens[b]} softmax_j(scale * q[b][h] . K_b[j][h/4]) V_b[j][h/4]
+ * where K_b[j] is slot j % 256 of block block_table[b][j / 256].  seq_lens[b] >= 1
+ * counts the current token (appended before the call).  lse may be NULL.
+ * The context is split over CTAs (split-K over KV blocks) and the partial results
+ * are merged by log-sum-exp; the split depends only on batch, max_blocks_per_seq
+ * and the device's SM count, never on the physical block ids.
+ */
+pa_status paged_attn_decode(pa_shape shape, void *out, float *lse, const void *q,
+                            const void *k_pool, const void *v_pool,
+                            const int32_t *block_table, int32_t max_blocks_per_seq,
+                            int32_t num_blocks, const int32_t *seq_lens, int32_t batch,
+                            float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * As paged_attn_decode, with the split length fixed by the caller: split_tokens is
+ * the number of context tokens one CTA handles (a positive multiple of 64), or 0
+ * for the library's own choice.  Exposed for tuning and for split-invariance tests.
+ */
+pa_status paged_attn_decode_split(pa_shape shape, void *out, float *lse, const void *q,
+                                  const void *k_pool, const void *v_pool,
+                                  const int32_t *block_table, int32_t max_blocks_per_seq,
+                                  int32_t num_blocks, const int32_t *seq_lens, int32_t batch,
+                                  float scale, int32_t split_tokens, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/*
+ * paged_attn_prefill: causal attention of each sequence's new tokens
+ * [P1 §4.4.1; P3 §3.3].  New token i of sequence s sits at absolute position
+ * p = seq_lens[s] - q_len + i and attends to context positions 0..p (its own key
+ * included).  A sequence with q_len 0 is skipped.  max_q_len must bound every
+ * q_len (checked on the device).  lse may be NULL.
+ */
+pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *q,
+                             const void *k_pool, const void *v_pool,
+                             const int32_t *block_table, int32_t max_blocks_per_seq,
+                             int32_t num_blocks, const int32_t *cu_q_lens,
+                             const int32_t *seq_lens, int32_t num_seqs, int32_t total_tokens,
+                             int32_t max_q_len, float scale, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one CTA that waits on a
+ * barrier nothing will ever complete, with a limit of timeout_us microseconds.
+ * The kernel gives up, records PA_ERR_TIMEOUT in the workspace and exits; the GPU
+ * context stays usable.  Used by the tests of the failure path.
+ */
+pa_status pa_selftest_wait_timeout(void *workspace, size_t workspace_bytes, uint32_t timeout_us,
+                                   void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,307 @@
+// api.cu -- the extern "C" entry points declared in include/pagedattn.h: argument
+// validation, tensor-map encoding, the decode split choice and kernel launches.
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/pagedattn.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+using namespace pa;
+
+constexpr int32_t kVersion = 1 * 10000 + 0 * 100 + 0;
+
+bool shape_ok(const pa_shape &s) {
+    return s.num_q_heads == kHq && s.num_kv_heads == kHkv && s.head_dim == kD && s.block_size == kBlock;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// ------------------------------------------------------------------ driver entry point
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// Pool [num_blocks][256][8][128] bf16 seen as a 4-D tensor (dim, head, slot, block),
+// box {64 dims, 1 head, rows slots, 1 block}, 128-byte swizzle.
+bool encode_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int rows) {
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kHkv, (cuuint64_t)kBlock, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)kRowBytes, (cuuint64_t)kTokenBytes,
+                                   (cuuint64_t)kTokenBytes * kBlock};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q [tokens][32][128] bf16 as a 3-D tensor (dim, head, token), box {64, 4, 32}.
+bool encode_q_map(CUtensorMap *map, const void *q, int tokens) {
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kHq, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)kRowBytes * kHq};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kGroup, (cuuint32_t)kPrefillQPositions};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ device facts
+std::atomic<int> g_sms[64];
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) {
+        int v = g_sms[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) g_sms[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+// ------------------------------------------------------------------ decode split
+// Context tokens per CTA.  Enough CTAs to keep every SM streaming (about 16 per SM
+// over the widest table), capped; a multiple of the 64-token tile.  Depends only on
+// batch, table width and SM count.
+int auto_split_tokens(int batch, int max_blocks_per_seq, int num_sms) {
+    const long long max_tokens = (long long)max_blocks_per_seq * kBlock;
+    const long long pairs = (long long)batch * kHkv;
+    long long target = (long long)num_sms * 16;
+    if (target > kDecodeCtaCap) target = kDecodeCtaCap;
+    long long nsplit = (target + pairs - 1) / pairs;
+    if (nsplit < 1) nsplit = 1;
+    long long split = (max_tokens + nsplit - 1) / nsplit;
+    split = (split + kDecodeTileTokens - 1) / kDecodeTileTokens * kDecodeTileTokens;
+    return (int)split;
+}
+
+size_t partial_entries_bound(int max_batch, int max_blocks_per_seq) {
+    // auto split: pairs * ceil(target / pairs) <= target + pairs; never more than one
+    // entry per 64-token tile of the widest context either.
+    const long long pairs = (long long)max_batch * kHkv;
+    const long long by_target = kDecodeCtaCap + pairs;
+    const long long by_tiles = pairs * (((long long)max_blocks_per_seq * kBlock + kDecodeTileTokens - 1) /
+                                        kDecodeTileTokens);
+    return (size_t)(by_target < by_tiles ? by_target : by_tiles);
+}
+
+size_t workspace_bytes_for(size_t entries) {
+    return kPartialOffset + entries * (kPartialOBytes + kPartialMLBytes);
+}
+
+pa_status decode_impl(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
+                      const void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
+                      int32_t num_blocks, const int32_t *seq_lens, int32_t batch, float scale,
+                      int32_t split_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
+    if (batch < 0 || batch > kMaxBatch || max_blocks_per_seq < 1 || num_blocks < 1 || !std::isfinite(scale) ||
+        split_tokens < 0 || split_tokens % kDecodeTileTokens != 0)
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kPartialOffset || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
+    if (batch == 0) return PA_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_table || !seq_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned4(block_table) ||
+        !aligned4(seq_lens) || (lse && !aligned4(lse)))
+        return PA_ERR_INVALID_ARG;
+    if ((long long)max_blocks_per_seq * kBlock > (1ll << 30)) return PA_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms <= 0) return PA_ERR_CUDA;
+    if (!get_encoder()) return PA_ERR_CUDA;
+    const int split = split_tokens ? split_tokens : auto_split_tokens(batch, max_blocks_per_seq, sms);
+    const long long max_tokens = (long long)max_blocks_per_seq * kBlock;
+    const long long nsplit = (max_tokens + split - 1) / split;
+    if (nsplit > 65535) return PA_ERR_INVALID_ARG;
+    const size_t entries = (size_t)batch * kHkv * (size_t)nsplit;
+    if (workspace_bytes_for(entries) > workspace_bytes) return PA_ERR_WORKSPACE;
+
+    CUtensorMap k_map, v_map;
+    if (!encode_pool_map(&k_map, k_pool, num_blocks, kDecodeTileTokens) ||
+        !encode_pool_map(&v_map, v_pool, num_blocks, kDecodeTileTokens))
+        return PA_ERR_INVALID_ARG;
+
+    char *ws = static_cast<char *>(workspace);
+    DecodeArgs a;
+    a.out = out;
+    a.lse = lse;
+    a.q = q;
+    a.block_table = block_table;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.split_tokens = split;
+    a.nsplit = (int)nsplit;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.counters = reinterpret_cast<int32_t *>(ws + kCounterOffset);
+    a.part_o = reinterpret_cast<float *>(ws + kPartialOffset);
+    a.part_ml = reinterpret_cast<float *>(ws + kPartialOffset + entries * kPartialOBytes);
+    a.err = reinterpret_cast<uint32_t *>(ws);
+    return launch_decode(a, k_map, v_map, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                                 : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(pa_status status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_DEVICE: return "PA_ERR_DEVICE";
+        case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    }
+    return "PA_ERR_UNKNOWN";
+}
+
+int32_t pa_version(void) { return kVersion; }
+
+size_t pa_workspace_bytes(pa_shape shape, int32_t max_batch, int32_t max_blocks_per_seq) {
+    if (!shape_ok(shape) || max_batch < 1 || max_batch > kMaxBatch || max_blocks_per_seq < 1) return 0;
+    return workspace_bytes_for(partial_entries_bound(max_batch, max_blocks_per_seq));
+}
+
+pa_status pa_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+    if (!workspace || workspace_bytes < kPartialOffset) return PA_ERR_INVALID_ARG;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+pa_status pa_check_error(void *workspace, void *stream, uint32_t *detail) {
+    if (!workspace) return PA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(workspace, 0, sizeof word, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (detail) *detail = word;
+    if (word & kErrTimeout) return PA_ERR_TIMEOUT;
+    if (word & kErrDevice) return PA_ERR_DEVICE;
+    return PA_OK;
+}
+
+pa_status kv_append(pa_shape shape, void *k_pool, void *v_pool, const void *k_new, const void *v_new,
+                    const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
+                    const int32_t *cu_q_lens, const int32_t *seq_lens, int32_t num_seqs, int32_t total_tokens,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+    if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+        (num_seqs == 0 && total_tokens != 0))
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kHeaderBytes || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
+    if (total_tokens == 0) return PA_OK;
+    if (!k_pool || !v_pool || !k_new || !v_new || !block_table || !cu_q_lens || !seq_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new) ||
+        !aligned4(block_table) || !aligned4(cu_q_lens) || !aligned4(seq_lens))
+        return PA_ERR_INVALID_ARG;
+    AppendArgs a;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.block_table = block_table;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.cu_q_lens = cu_q_lens;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.total_tokens = total_tokens;
+    a.err = static_cast<uint32_t *>(workspace);
+    return launch_kv_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status paged_attn_decode(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
+                            const void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
+                            int32_t num_blocks, const int32_t *seq_lens, int32_t batch, float scale,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+    return decode_impl(shape, out, lse, q, k_pool, v_pool, block_table, max_blocks_per_seq, num_blocks, seq_lens,
+                       batch, scale, 0, workspace, workspace_bytes, stream);
+}
+
+pa_status paged_attn_decode_split(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
+                                  const void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
+                                  int32_t num_blocks, const int32_t *seq_lens, int32_t batch, float scale,
+                                  int32_t split_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+    return decode_impl(shape, out, lse, q, k_pool, v_pool, block_table, max_blocks_per_seq, num_blocks, seq_lens,
+                       batch, scale, split_tokens, workspace, workspace_bytes, stream);
+}
+
+pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
+                             const void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
+                             int32_t num_blocks, const int32_t *cu_q_lens, const int32_t *seq_lens, int32_t num_seqs,
+                             int32_t total_tokens, int32_t max_q_len, float scale, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || max_q_len < 0 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+        !std::isfinite(scale) || (num_seqs == 0 && total_tokens != 0) || max_q_len > total_tokens ||
+        (total_tokens > 0 && max_q_len == 0))
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kHeaderBytes || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
+    if (total_tokens == 0) return PA_OK;
+    if ((long long)num_seqs * kHkv * ((max_q_len + kPrefillQPositions - 1) / kPrefillQPositions) > (1ll << 30) ||
+        (long long)max_blocks_per_seq * kBlock > (1ll << 30))
+        return PA_ERR_INVALID_ARG;
+    if (!out || !q || !k_pool || !v_pool || !block_table || !cu_q_lens || !seq_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned4(block_table) ||
+        !aligned4(cu_q_lens) || !aligned4(seq_lens) || (lse && !aligned4(lse)))
+        return PA_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms <= 0) return PA_ERR_CUDA;
+    if (!get_encoder()) return PA_ERR_CUDA;
+    CUtensorMap q_map, k_map, v_map;
+    if (!encode_q_map(&q_map, q, total_tokens) || !encode_pool_map(&k_map, k_pool, num_blocks, kPrefillKvTile) ||
+        !encode_pool_map(&v_map, v_pool, num_blocks, kPrefillKvTile))
+        return PA_ERR_INVALID_ARG;
+    PrefillArgs a;
+    a.out = out;
+    a.lse = lse;
+    a.block_table = block_table;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.cu_q_lens = cu_q_lens;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.total_tokens = total_tokens;
+    a.max_q_len = max_q_len;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.err = static_cast<uint32_t *>(workspace);
+    return launch_prefill(a, q_map, k_map, v_map, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+pa_status pa_selftest_wait_timeout(void *workspace, size_t workspace_bytes, uint32_t timeout_us, void *stream) {
+    if (!workspace || workspace_bytes < kHeaderBytes || timeout_us == 0 || timeout_us > 10000000u)
+        return PA_ERR_INVALID_ARG;
+    return launch_wait_selftest(static_cast<uint32_t *>(workspace), (uint64_t)timeout_us * 1000ull,
+                                static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,360 @@
+// decode.cu -- batched single-token GQA attention over the paged KV cache.
+//
+// Page "扔掉 vLLM！从零构建 Qwen3-8B 推理引擎，C++/CUDA 实现性能追平 98%":
+//   §4.4.2 gqa_decode_attn  the query heads of one group share one KV read
+//                           (head_idx = g * heads_per_group + h);
+//   §4.3.1                  KV in 256-token blocks reached through a block table.
+// Page "从零手搓AI推理引擎：避开调包陷阱的工程实践指南" §2.2: softmax(QK^T/sqrt(d))V with
+// the maximum subtracted first.
+//
+// Decode reads every context byte once and does ~4 flops per byte, so it is bound by
+// HBM bandwidth.  Design:
+//   * grid (sequence x KV head, split): one CTA streams a contiguous range of the
+//     context (split-K over KV blocks) for ONE KV head and serves all 4 query heads of
+//     that group, so each K/V byte is read once;
+//   * a producer warp issues TMA tile loads (64 tokens x 128 dims of one KV head,
+//     128-byte swizzle) straight from the paged pool: the block-table walk is the TMA
+//     coordinate; a 3-stage mbarrier ring keeps ~64 KiB per CTA in flight;
+//   * 4 consumer warps each take 16 tokens of a tile: S^T = K Q^T and O^T += V^T P^T
+//     on mma.sync (bf16 in, fp32 accumulate) -- the tensor cores here only save
+//     issue slots, the bound is HBM -- with an online softmax in fp32 (exp2 with
+//     scale*log2(e) folded in) and warp-shuffle row reductions;
+//   * the warps' partial states merge in shared memory; with several splits each CTA
+//     writes (O, m, l) to the workspace and the last CTA of the (sequence, KV head)
+//     merges them by log-sum-exp and writes bf16 output (+ optional lse).
+// Tokens past the context end inside the last tile are masked in the scores and
+// their V rows are zeroed in registers, so uninitialised (even NaN) slots never
+// reach the result.
+#include "common.cuh"
+#include "launch.h"
+
+namespace pa {
+namespace {
+
+constexpr int kTile = kDecodeTileTokens;      // 64 tokens per stage
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = kTile / 16;    // 4
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kHalfBytes = kTile * 128;       // 64 tokens x 64 dims x 2 B
+constexpr int kStageBytes = 4 * kHalfBytes;   // K lo/hi + V lo/hi = 32 KiB
+constexpr float kLn2 = 0.693147180559945309f;
+
+struct DecodeSmem {
+    uint8_t tiles[kStages][4][kHalfBytes];    // [stage][K lo, K hi, V lo, V hi]
+    float o[kConsumerWarps][kGroup][kD];
+    float m[kConsumerWarps][kGroup];
+    float l[kConsumerWarps][kGroup];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    int last_cta;
+};
+
+constexpr size_t kSmemBytes = sizeof(DecodeSmem) + 1024;  // + alignment slack
+
+__device__ __forceinline__ void store_out4(__nv_bfloat16 *dst, const float (&v)[4], float inv) {
+    uint2 w;
+    w.x = pack_bf16x2(v[0] * inv, v[1] * inv);
+    w.y = pack_bf16x2(v[2] * inv, v[3] * inv);
+    *reinterpret_cast<uint2 *>(dst) = w;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+              const DecodeArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    DecodeSmem &sm = *reinterpret_cast<DecodeSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int pair = blockIdx.x;          // sequence * 8 + kv head
+    const int b = pair / kHkv;
+    const int g = pair % kHkv;
+    const int split = blockIdx.y;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const int seq_len = __ldg(a.seq_lens + b);
+    if (seq_len < 1 || seq_len > a.max_blocks_per_seq * kBlock) {
+        if (split == 0 && g == 0 && threadIdx.x == 0) record_error(a.err, kErrDevice | kErrBadSeqLen);
+        return;  // every CTA of this sequence takes the same exit: counters untouched
+    }
+    const int t_begin = split * a.split_tokens;
+    if (t_begin >= seq_len) return;       // this split lies past the context
+    const int t_end = min(t_begin + a.split_tokens, seq_len);
+    const int nsplit_b = (seq_len + a.split_tokens - 1) / a.split_tokens;
+    const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
+    const int32_t *bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
+
+    // Block ids of this split must address the pool; a bad one poisons the result.
+    bool bad = false;
+    for (int j = t_begin / kBlock + threadIdx.x; j <= (t_end - 1) / kBlock; j += kThreads) {
+        const int blk = __ldg(bt + j);
+        bad |= (blk < 0 || blk >= a.num_blocks);
+    }
+    bad = __syncthreads_or(bad);
+    if (bad && threadIdx.x == 0) record_error(a.err, kErrDevice | kErrBadBlock);
+
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.empty[s]), kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && !bad) {
+            tma_prefetch_map(&k_map);
+            tma_prefetch_map(&v_map);
+            int issued = 0;
+            for (int i = 0; i < n_tiles; ++i) {
+                const int st = i % kStages;
+                if (i >= kStages && !mbar_wait(smem_u32(&sm.empty[st]), ((i / kStages) - 1) & 1)) {
+                    record_error(a.err, kErrTimeout);
+                    break;
+                }
+                const int tok = t_begin + i * kTile;
+                const int blk = __ldg(bt + tok / kBlock);
+                const int off = tok % kBlock;
+                const uint32_t bar = smem_u32(&sm.full[st]);
+                mbar_arrive_expect_tx(bar, kStageBytes);
+                tma_load_4d(smem_u32(sm.tiles[st][0]), &k_map, bar, 0, g, off, blk);
+                tma_load_4d(smem_u32(sm.tiles[st][1]), &k_map, bar, 64, g, off, blk);
+                tma_load_4d(smem_u32(sm.tiles[st][2]), &v_map, bar, 0, g, off, blk);
+                tma_load_4d(smem_u32(sm.tiles[st][3]), &v_map, bar, 64, g, off, blk);
+                issued = i + 1;
+            }
+            // No copy may still be landing in shared memory when the CTA exits.
+            for (int i = max(0, issued - kStages); i < issued; ++i)
+                mbar_wait(smem_u32(&sm.full[i % kStages]), (i / kStages) & 1);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int w = warp;
+    const int gq = lane >> 2;   // fragment row group
+    const int tq = lane & 3;    // fragment column pair
+    const int mi = lane >> 3;   // ldmatrix: which 8x8 matrix this lane addresses
+    const int ri = lane & 7;    // ldmatrix: row within it
+
+    // Q^T as the B operand of S^T = K Q^T: [k = 16 dims] x [n = 8 heads], heads 4..7 zero.
+    uint32_t qb[8][2];
+    {
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+            static_cast<const __nv_bfloat16 *>(a.q) + ((size_t)b * kHq + g * kGroup + (gq & 3)) * kD);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            qb[kk][0] = gq < kGroup ? __ldg(qrow + kk * 8 + tq) : 0u;
+            qb[kk][1] = gq < kGroup ? __ldg(qrow + kk * 8 + 4 + tq) : 0u;
+        }
+    }
+
+    float m0 = -INFINITY, m1 = -INFINITY;   // running max (log2 units) of heads 2tq, 2tq+1
+    float l0 = 0.f, l1 = 0.f;               // this thread's share of the running sums
+    float acc[8][4];                        // O^T tiles: 16 dims x 8 heads each
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+
+    const int row_qk = w * 16 + ri + ((mi & 1) << 3);   // token row for the K fragment
+    const int row_pv = w * 16 + ri + ((mi >> 1) << 3);  // token row for the V^T fragment
+
+    for (int i = 0; i < (bad ? 0 : n_tiles); ++i) {
+        const int st = i % kStages;
+        if (!mbar_wait(smem_u32(&sm.full[st]), (i / kStages) & 1)) {
+            if (lane == 0) record_error(a.err, kErrTimeout);
+            break;
+        }
+        const int my_valid = min(max(t_end - (t_begin + i * kTile) - w * 16, 0), 16);
+        if (my_valid > 0) {
+            const uint32_t k_lo = smem_u32(sm.tiles[st][0]);
+            const uint32_t k_hi = smem_u32(sm.tiles[st][1]);
+            const uint32_t v_lo = smem_u32(sm.tiles[st][2]);
+            const uint32_t v_hi = smem_u32(sm.tiles[st][3]);
+
+            // S^T[16 tokens x 8 heads] = K[16 x 128] . Q^T[128 x 8]
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t af[4];
+                const uint32_t base = kk < 4 ? k_lo : k_hi;
+                ldsm_x4(af, base + sw128(row_qk, ((kk & 3) << 1) + (mi >> 1)));
+                mma_16816(s, af, qb[kk][0], qb[kk][1]);
+            }
+            // s[0]: (token gq, head 2tq)   s[1]: (token gq, head 2tq+1)
+            // s[2]: (token gq+8, head 2tq) s[3]: (token gq+8, head 2tq+1)
+            float x0, x1, x2, x3;
+            if (tq < 2) {
+                const bool v_lo_ok = gq < my_valid;
+                const bool v_hi_ok = gq + 8 < my_valid;
+                x0 = v_lo_ok ? s[0] * a.scale_log2 : -INFINITY;
+                x1 = v_lo_ok ? s[1] * a.scale_log2 : -INFINITY;
+                x2 = v_hi_ok ? s[2] * a.scale_log2 : -INFINITY;
+                x3 = v_hi_ok ? s[3] * a.scale_log2 : -INFINITY;
+            } else {  // padding heads 4..7: finite dummies, results discarded
+                x0 = x1 = x2 = x3 = 0.f;
+            }
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float alpha0 = fast_exp2(m0 - mn0), alpha1 = fast_exp2(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            const float p0 = fast_exp2(x0 - m0), p1 = fast_exp2(x1 - m1);
+            const float p2 = fast_exp2(x2 - m0), p3 = fast_exp2(x3 - m1);
+            // P enters the PV product as bf16; the sums use those same rounded weights.
+            const uint32_t pp_lo = pack_bf16x2(p0, p1);   // token gq:   heads 2tq, 2tq+1
+            const uint32_t pp_hi = pack_bf16x2(p2, p3);   // token gq+8: heads 2tq, 2tq+1
+            l0 = l0 * alpha0 + bf16_lo(pp_lo) + bf16_lo(pp_hi);
+            l1 = l1 * alpha1 + bf16_hi(pp_lo) + bf16_hi(pp_hi);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                acc[mt][0] *= alpha0;
+                acc[mt][1] *= alpha1;
+                acc[mt][2] *= alpha0;
+                acc[mt][3] *= alpha1;
+            }
+            // P^T as the B operand of O^T += V^T P^T: transpose the 8x8 bf16 blocks.
+            const uint32_t pb0 = movmatrix_trans(pp_lo);
+            const uint32_t pb1 = movmatrix_trans(pp_hi);
+            // V rows past the context end are zeroed in the fragment (0 * NaN = NaN).
+            const uint32_t keep_lo = (2 * tq < my_valid ? 0x0000ffffu : 0u) |
+                                     (2 * tq + 1 < my_valid ? 0xffff0000u : 0u);
+            const uint32_t keep_hi = (2 * tq + 8 < my_valid ? 0x0000ffffu : 0u) |
+                                     (2 * tq + 9 < my_valid ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                uint32_t af[4];
+                const uint32_t base = mt < 4 ? v_lo : v_hi;
+                ldsm_x4_trans(af, base + sw128(row_pv, ((mt & 3) << 1) + (mi & 1)));
+                af[0] &= keep_lo;
+                af[1] &= keep_lo;
+                af[2] &= keep_hi;
+                af[3] &= keep_hi;
+                mma_16816(acc[mt], af, pb0, pb1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
+    }
+
+    // ------------------------------------------------------------ merge the 4 warps
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    if (tq < 2) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int d = mt * 16 + gq;
+            sm.o[w][2 * tq][d] = acc[mt][0];
+            sm.o[w][2 * tq + 1][d] = acc[mt][1];
+            sm.o[w][2 * tq][d + 8] = acc[mt][2];
+            sm.o[w][2 * tq + 1][d + 8] = acc[mt][3];
+        }
+        if (gq == 0) {
+            sm.m[w][2 * tq] = m0;
+            sm.m[w][2 * tq + 1] = m1;
+            sm.l[w][2 * tq] = l0;
+            sm.l[w][2 * tq + 1] = l1;
+        }
+    }
+    named_barrier(1, kConsumerWarps * 32);
+
+    const int c = threadIdx.x;          // 0..127
+    const int h = c >> 5;               // query head within the group
+    const int d0 = (c & 31) * 4;        // 4 dims per thread
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, sm.m[ww][h]);
+    float L = 0.f, o4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ww = 0; ww < kConsumerWarps; ++ww) {
+        const float e = fast_exp2(sm.m[ww][h] - M);
+        L += sm.l[ww][h] * e;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o4[k] += sm.o[ww][h][d0 + k] * e;
+    }
+    if (bad) {
+        M = L = __int_as_float(0x7fc00000);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o4[k] = __int_as_float(0x7fc00000);
+    }
+    const int qh = g * kGroup + h;      // query head
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + ((size_t)b * kHq + qh) * kD + d0;
+
+    if (nsplit_b == 1) {
+        store_out4(out, o4, 1.f / L);
+        if (a.lse && (c & 31) == 0) a.lse[(size_t)b * kHq + qh] = (M + __log2f(L)) * kLn2;
+        return;
+    }
+
+    // ------------------------------------------------------------ split-K partials
+    const size_t entry = (size_t)pair * a.nsplit + split;
+    *reinterpret_cast<float4 *>(a.part_o + (entry * kGroup + h) * kD + d0) =
+        make_float4(o4[0], o4[1], o4[2], o4[3]);
+    if ((c & 31) == 0) {
+        a.part_ml[(entry * kGroup + h) * 2 + 0] = M;
+        a.part_ml[(entry * kGroup + h) * 2 + 1] = L;
+    }
+    __threadfence();
+    named_barrier(1, kConsumerWarps * 32);
+    if (c == 0) {
+        const int prev = atomicAdd(a.counters + pair, 1);
+        sm.last_cta = (prev == nsplit_b - 1);
+    }
+    named_barrier(1, kConsumerWarps * 32);
+    if (!sm.last_cta) return;
+
+    // The last CTA of this (sequence, KV head) merges every split by log-sum-exp.
+    __threadfence();
+    if (c == 0) a.counters[pair] = 0;   // ready for the next call
+    const size_t e0 = (size_t)pair * a.nsplit;
+    float GM = -INFINITY;
+    for (int k = 0; k < nsplit_b; ++k) GM = fmaxf(GM, __ldcg(a.part_ml + ((e0 + k) * kGroup + h) * 2));
+    float GL = 0.f, go[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < nsplit_b; ++k) {
+        const float mk = __ldcg(a.part_ml + ((e0 + k) * kGroup + h) * 2);
+        const float lk = __ldcg(a.part_ml + ((e0 + k) * kGroup + h) * 2 + 1);
+        const float e = fast_exp2(mk - GM);
+        const float4 ok = __ldcg(reinterpret_cast<const float4 *>(a.part_o + ((e0 + k) * kGroup + h) * kD + d0));
+        GL += lk * e;
+        go[0] += ok.x * e;
+        go[1] += ok.y * e;
+        go[2] += ok.z * e;
+        go[3] += ok.w * e;
+    }
+    store_out4(out, go, 1.f / GL);
+    if (a.lse && (c & 31) == 0) a.lse[(size_t)b * kHq + qh] = (GM + __log2f(GL)) * kLn2;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
+                          int num_sms, cudaStream_t stream) {
+    (void)num_sms;
+    if (a.batch == 0) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool configured[64] = {};
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    dim3 grid(a.batch * kHkv, a.nsplit);
+    decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(k_map, v_map, a);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

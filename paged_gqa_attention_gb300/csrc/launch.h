@@ -1,0 +1,77 @@
+// launch.h -- internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+struct AppendArgs {
+    void *k_pool;
+    void *v_pool;
+    const void *k_new;
+    const void *v_new;
+    const int32_t *block_table;
+    int32_t max_blocks_per_seq;
+    int32_t num_blocks;
+    const int32_t *cu_q_lens;
+    const int32_t *seq_lens;
+    int32_t num_seqs;
+    int32_t total_tokens;
+    uint32_t *err;
+};
+
+struct DecodeArgs {
+    void *out;
+    float *lse;
+    const void *q;
+    const int32_t *block_table;
+    int32_t max_blocks_per_seq;
+    int32_t num_blocks;
+    const int32_t *seq_lens;
+    int32_t batch;
+    int32_t split_tokens;  // context tokens per CTA (multiple of 64)
+    int32_t nsplit;        // splits per (sequence, KV head) at the maximum context
+    float scale_log2;      // softmax scale * log2(e)
+    int32_t *counters;     // [batch * 8], zero on entry, zero again on exit
+    float *part_o;         // [batch * 8 * nsplit][4][128]
+    float *part_ml;        // [batch * 8 * nsplit][4][2]
+    uint32_t *err;
+};
+
+struct PrefillArgs {
+    void *out;
+    float *lse;
+    const int32_t *block_table;
+    int32_t max_blocks_per_seq;
+    int32_t num_blocks;
+    const int32_t *cu_q_lens;
+    const int32_t *seq_lens;
+    int32_t num_seqs;
+    int32_t total_tokens;
+    int32_t max_q_len;
+    float scale_log2;
+    uint32_t *err;
+};
+
+cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
+
+// k_map / v_map: 4-D tensor maps over the pools (see api.cu for the boxes).
+cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
+                          const CUtensorMap &v_map, int num_sms, cudaStream_t stream);
+
+// q_map: 3-D map over q; k_map / v_map: 4-D maps over the pools.
+cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
+                           const CUtensorMap &k_map, const CUtensorMap &v_map, int num_sms,
+                           cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(uint32_t *err, uint64_t limit_ns, cudaStream_t stream);
+
+// Tile sizes the tensor maps must be encoded with.
+constexpr int kDecodeTileTokens = 64;    // decode: rows per TMA box
+constexpr int kPrefillKvTile = 128;      // prefill: K/V rows per TMA box
+constexpr int kPrefillQPositions = 32;   // prefill: query positions per tile (x4 heads)
+
+}  // namespace pa

@@ -1,0 +1,238 @@
+"""Thin ctypes binding over libpagedattn.so (the C ABI in include/pagedattn.h).
+
+Argument marshalling only: dtype/shape/device checks, raw pointers and the current
+CUDA stream go to the library, which does every step of the computation in its own
+sm_103a kernels.  PyTorch supplies device memory and streams.  There is no fallback:
+if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedattn.so")
+
+NUM_Q_HEADS, NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE = 32, 8, 128, 256
+DEFAULT_SCALE = 1.0 / math.sqrt(HEAD_DIM)
+
+STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
+          4: "PA_ERR_DEVICE", 5: "PA_ERR_TIMEOUT", 6: "PA_ERR_WORKSPACE"}
+
+
+class PagedAttnError(RuntimeError):
+    """A library call returned a status other than PA_OK."""
+
+    def __init__(self, fn: str, status: int, detail: int | None = None):
+        self.status = status
+        self.detail = detail
+        msg = f"{fn}: {STATUS.get(status, status)}"
+        if detail is not None:
+            msg += f" (error word 0x{detail:x})"
+        super().__init__(msg)
+
+
+class pa_shape(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32)]
+
+
+SHAPE = pa_shape(NUM_Q_HEADS, NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE)
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libpagedattn.so (built by paged_gqa_attention_gb300.build); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                           "`python -m paged_gqa_attention_gb300.build` (no fallback exists)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, sz, i32, f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_float
+    u32p = ctypes.POINTER(ctypes.c_uint32)
+    lib.pa_status_string.argtypes = [ctypes.c_int]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_version.argtypes = []
+    lib.pa_version.restype = i32
+    lib.pa_workspace_bytes.argtypes = [pa_shape, i32, i32]
+    lib.pa_workspace_bytes.restype = sz
+    lib.pa_workspace_init.argtypes = [vp, sz, vp]
+    lib.pa_workspace_init.restype = ctypes.c_int
+    lib.pa_check_error.argtypes = [vp, vp, u32p]
+    lib.pa_check_error.restype = ctypes.c_int
+    lib.kv_append.argtypes = [pa_shape, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32, vp, sz, vp]
+    lib.kv_append.restype = ctypes.c_int
+    lib.paged_attn_decode.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, f32, vp,
+                                      sz, vp]
+    lib.paged_attn_decode.restype = ctypes.c_int
+    lib.paged_attn_decode_split.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32,
+                                            f32, i32, vp, sz, vp]
+    lib.paged_attn_decode_split.restype = ctypes.c_int
+    lib.paged_attn_prefill.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32,
+                                       i32, f32, vp, sz, vp]
+    lib.paged_attn_prefill.restype = ctypes.c_int
+    lib.pa_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint32, vp]
+    lib.pa_selftest_wait_timeout.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise PagedAttnError(fn, status)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None:
+        for i, (a, b) in enumerate(zip(t.shape, shape)):
+            if b is not None and a != b:
+                raise ValueError(f"{name} has shape {tuple(t.shape)}, dim {i} must be {b}")
+        if len(t.shape) != len(shape):
+            raise ValueError(f"{name} must have {len(shape)} dims, got {tuple(t.shape)}")
+
+
+# ------------------------------------------------------------------ workspace
+
+def workspace_bytes(max_batch: int, max_blocks_per_seq: int) -> int:
+    n = load().pa_workspace_bytes(SHAPE, int(max_batch), int(max_blocks_per_seq))
+    if n == 0:
+        raise ValueError("unsupported workspace request")
+    return int(n)
+
+
+def make_workspace(max_batch: int, max_blocks_per_seq: int, device=None, stream=None) -> torch.Tensor:
+    """Allocate (with PyTorch) and zero (with pa_workspace_init) a workspace."""
+    n = workspace_bytes(max_batch, max_blocks_per_seq)
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    _check("pa_workspace_init", load().pa_workspace_init(ws.data_ptr(), n, _stream(stream)))
+    return ws
+
+
+def check_error(workspace: torch.Tensor, stream=None) -> None:
+    """Synchronise, read and clear the device error word; raise PagedAttnError if set."""
+    word = ctypes.c_uint32(0)
+    st = load().pa_check_error(workspace.data_ptr(), _stream(stream), ctypes.byref(word))
+    if st != 0:
+        raise PagedAttnError("pa_check_error", st, word.value)
+
+
+# ------------------------------------------------------------------ the three calls
+
+def kv_append(k_pool, v_pool, k_new, v_new, block_table, cu_q_lens, seq_lens, workspace,
+              stream=None) -> None:
+    """Write k_new/v_new [T, 8, 128] into the pools at each sequence's tail positions."""
+    dev = k_pool.device
+    _need(k_pool, "k_pool", torch.bfloat16, (None, BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_pool, "v_pool", torch.bfloat16, tuple(k_pool.shape), dev)
+    _need(k_new, "k_new", torch.bfloat16, (None, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_new, "v_new", torch.bfloat16, tuple(k_new.shape), dev)
+    _need(block_table, "block_table", torch.int32, (None, None), dev)
+    num_seqs = block_table.shape[0]
+    _need(cu_q_lens, "cu_q_lens", torch.int32, (num_seqs + 1,), dev)
+    _need(seq_lens, "seq_lens", torch.int32, (num_seqs,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    st = load().kv_append(SHAPE, k_pool.data_ptr(), v_pool.data_ptr(), k_new.data_ptr(),
+                          v_new.data_ptr(), block_table.data_ptr(), block_table.shape[1],
+                          k_pool.shape[0], cu_q_lens.data_ptr(), seq_lens.data_ptr(), num_seqs,
+                          k_new.shape[0], workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check("kv_append", st)
+
+
+def paged_attn_decode(q, k_pool, v_pool, block_table, seq_lens, workspace, *,
+                      scale: float = DEFAULT_SCALE, out=None, lse=None, split_tokens: int = 0,
+                      stream=None) -> torch.Tensor:
+    """One query token per sequence: q [B, 32, 128] -> out [B, 32, 128] (bf16).
+
+    lse: optional fp32 [B, 32] tensor that receives the log-sum-exp of each row.
+    split_tokens: context tokens per CTA (multiple of 64), 0 = the library's choice.
+    """
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (None, NUM_Q_HEADS, HEAD_DIM), dev)
+    batch = q.shape[0]
+    _need(k_pool, "k_pool", torch.bfloat16, (None, BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_pool, "v_pool", torch.bfloat16, tuple(k_pool.shape), dev)
+    _need(block_table, "block_table", torch.int32, (batch, None), dev)
+    _need(seq_lens, "seq_lens", torch.int32, (batch,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, tuple(q.shape), dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (batch, NUM_Q_HEADS), dev)
+    lib = load()
+    if split_tokens:
+        st = lib.paged_attn_decode_split(SHAPE, out.data_ptr(), _ptr(lse), q.data_ptr(),
+                                         k_pool.data_ptr(), v_pool.data_ptr(), block_table.data_ptr(),
+                                         block_table.shape[1], k_pool.shape[0], seq_lens.data_ptr(),
+                                         batch, float(scale), int(split_tokens), workspace.data_ptr(),
+                                         workspace.numel(), _stream(stream))
+    else:
+        st = lib.paged_attn_decode(SHAPE, out.data_ptr(), _ptr(lse), q.data_ptr(), k_pool.data_ptr(),
+                                   v_pool.data_ptr(), block_table.data_ptr(), block_table.shape[1],
+                                   k_pool.shape[0], seq_lens.data_ptr(), batch, float(scale),
+                                   workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check("paged_attn_decode", st)
+    return out
+
+
+def paged_attn_prefill(q, k_pool, v_pool, block_table, cu_q_lens, seq_lens, max_q_len: int,
+                       workspace, *, scale: float = DEFAULT_SCALE, out=None, lse=None,
+                       stream=None) -> torch.Tensor:
+    """Causal attention of each sequence's new tokens: q [T, 32, 128] -> out [T, 32, 128]."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (None, NUM_Q_HEADS, HEAD_DIM), dev)
+    _need(k_pool, "k_pool", torch.bfloat16, (None, BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_pool, "v_pool", torch.bfloat16, tuple(k_pool.shape), dev)
+    _need(block_table, "block_table", torch.int32, (None, None), dev)
+    num_seqs = block_table.shape[0]
+    _need(cu_q_lens, "cu_q_lens", torch.int32, (num_seqs + 1,), dev)
+    _need(seq_lens, "seq_lens", torch.int32, (num_seqs,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, tuple(q.shape), dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (q.shape[0], NUM_Q_HEADS), dev)
+    st = load().paged_attn_prefill(SHAPE, out.data_ptr(), _ptr(lse), q.data_ptr(), k_pool.data_ptr(),
+                                   v_pool.data_ptr(), block_table.data_ptr(), block_table.shape[1],
+                                   k_pool.shape[0], cu_q_lens.data_ptr(), seq_lens.data_ptr(),
+                                   num_seqs, q.shape[0], int(max_q_len), float(scale),
+                                   workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check("paged_attn_prefill", st)
+    return out
+
+
+def selftest_wait_timeout(workspace: torch.Tensor, timeout_us: int = 20000, stream=None) -> None:
+    """Launch the bounded-wait self-test kernel (it always times out by design)."""
+    _check("pa_selftest_wait_timeout",
+           load().pa_selftest_wait_timeout(workspace.data_ptr(), workspace.numel(),
+                                           int(timeout_us), _stream(stream)))

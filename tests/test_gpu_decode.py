@@ -1,0 +1,169 @@
+"""Decode parity: paged_attn_decode (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import (assert_close, assert_lse_close, gpu, lib_ready, oracle_appended_pools,
+                         oracle_attention, workspace_for)
+from paged_gqa_attention_gb300 import ops
+from paged_gqa_attention_gb300 import workloads as wl
+
+pytestmark = gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lib_ready()
+
+
+def run_decode(batch, ws=None, split_tokens=0, with_lse=True):
+    ws = workspace_for(batch) if ws is None else ws
+    lse = torch.empty(batch.num_seqs, 32, dtype=torch.float32, device="cuda") if with_lse else None
+    out = ops.paged_attn_decode(batch.q, batch.k_pool, batch.v_pool, batch.block_table,
+                                batch.seq_lens, ws, lse=lse, split_tokens=split_tokens)
+    ops.check_error(ws)
+    return out, lse
+
+
+def decode_batch(lens, seed=0, num_blocks=None, maxb=None):
+    """Pre-filled context (every position present) and one query per sequence."""
+    need = sum((l + 255) // 256 for l in lens)
+    b = wl.build_batch("decode_case", seed, lens, [0] * len(lens), num_blocks=num_blocks or need + 3,
+                       device="cuda", max_blocks_per_seq=maxb)
+    return _with_queries(b, seed)
+
+
+def _with_queries(b, seed):
+    """Give a q_len-0 batch one query per sequence (its context already holds every key)."""
+    g = torch.Generator(device="cuda").manual_seed(seed + 77)
+    n = b.num_seqs
+    b.q = torch.randn(n, 32, 128, generator=g, device="cuda").to(torch.bfloat16)
+    b.cu_q_lens = torch.arange(n + 1, dtype=torch.int32, device="cuda")
+    b.q_lens_host = [1] * n
+    b.max_q_len = 1
+    return b
+
+
+def test_single_sequence_512():
+    b = wl.single_decode(device="cuda")
+    kp, vp = oracle_appended_pools(b)
+    ws = workspace_for(b)
+    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    out, lse = run_decode(b, ws)
+    ref, ref_lse = oracle_attention(b, kp, vp)
+    assert_close(out, ref, "single_decode")
+    assert_lse_close(lse, ref_lse, "single_decode")
+
+
+def test_batched_decode_full_size():
+    b = wl.batched_decode(device="cuda")
+    kp, vp = oracle_appended_pools(b)
+    ws = workspace_for(b)
+    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    out, lse = run_decode(b, ws)
+    ref, ref_lse = oracle_attention(b, kp, vp)
+    assert_close(out, ref, "batched_decode")
+    assert_lse_close(lse, ref_lse, "batched_decode")
+
+
+@pytest.mark.parametrize("seed", [0, 2])
+def test_batched_decode_other_seeds(seed):
+    b = wl.batched_decode(device="cuda", seed=seed)
+    kp, vp = oracle_appended_pools(b)
+    ws = workspace_for(b)
+    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    out, _ = run_decode(b, ws)
+    ref, _ = oracle_attention(b, kp, vp)
+    assert_close(out, ref, f"batched_decode seed {seed}")
+
+
+BOUNDARY_LENS = [1, 2, 63, 64, 65, 127, 128, 255, 256, 257, 511, 512, 513, 1000, 4096]
+
+
+def test_ragged_boundary_lengths():
+    b = decode_batch(BOUNDARY_LENS, seed=5)
+    out, lse = run_decode(b)
+    ref, ref_lse = oracle_attention(b)
+    assert_close(out, ref, "boundary lengths")
+    assert_lse_close(lse, ref_lse, "boundary lengths")
+
+
+@pytest.mark.parametrize("split", [64, 128, 256, 448, 1024, 4096])
+def test_split_length_does_not_change_the_result(split):
+    b = decode_batch([3000, 1, 700, 4096, 129], seed=6, maxb=16)
+    ref, ref_lse = oracle_attention(b)
+    out, lse = run_decode(b, split_tokens=split)
+    assert_close(out, ref, f"split {split}")
+    assert_lse_close(lse, ref_lse, f"split {split}")
+
+
+def test_block_placement_is_bit_exact():
+    b = decode_batch([900, 33, 2048], seed=7, num_blocks=40)
+    out1, lse1 = run_decode(b)
+    # move every block to another physical slot and rewrite the tables accordingly
+    perm = torch.randperm(b.num_blocks, generator=torch.Generator().manual_seed(1)).to("cuda")
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(b.num_blocks, device="cuda")
+    k2 = torch.empty_like(b.k_pool)
+    v2 = torch.empty_like(b.v_pool)
+    k2[perm] = b.k_pool
+    v2[perm] = b.v_pool
+    bt = b.block_table.clone()
+    valid = bt >= 0
+    bt[valid] = perm[bt[valid].long()].to(torch.int32)
+    b.k_pool, b.v_pool, b.block_table = k2, v2, bt
+    out2, lse2 = run_decode(b)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+
+
+def test_single_key_returns_v_bit_exactly():
+    b = decode_batch([1, 1, 1], seed=8)
+    out, _ = run_decode(b)
+    bt = b.block_table.cpu()
+    for s in range(3):
+        v = b.v_pool[int(bt[s, 0]), 0]                      # [8, 128]
+        expect = v.repeat_interleave(4, dim=0)              # q-head h reads kv-head h // 4
+        assert torch.equal(out[s].view(torch.int16), expect.view(torch.int16))
+
+
+def test_identical_keys_give_mean_of_v():
+    b = decode_batch([777], seed=9)
+    bt = b.block_table.cpu()
+    k0 = b.k_pool[int(bt[0, 0]), 0].clone()
+    for j in range(4):
+        blk = int(bt[0, j])
+        n = min(256, 777 - 256 * j)
+        b.k_pool[blk, :n] = k0
+    out, _ = run_decode(b)
+    vs = torch.cat([b.v_pool[int(bt[0, j]), :min(256, 777 - 256 * j)] for j in range(4)])
+    mean = vs.double().mean(0).repeat_interleave(4, dim=0).cpu().numpy()
+    assert_close(out[0], mean, "identical keys")
+
+
+def test_append_then_decode_step_matches_oracle():
+    b = wl.batched_decode(device="cuda", seed=11, batch=8, hi=1500, num_blocks=64)
+    kp, vp = oracle_appended_pools(b)
+    ws = workspace_for(b)
+    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    out, _ = run_decode(b, ws)
+    ref, _ = oracle_attention(b, kp, vp)
+    assert_close(out, ref, "append + decode")
+
+
+def test_repeated_calls_reuse_the_workspace():
+    """The merge counters reset themselves: ten calls on one workspace agree bit for bit."""
+    b = decode_batch([3000, 2500, 100], seed=12, maxb=16)
+    ws = workspace_for(b)
+    first, _ = run_decode(b, ws)
+    for _ in range(9):
+        again, _ = run_decode(b, ws)
+        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+
+
+def test_empty_batch_is_a_no_op():
+    b = decode_batch([10], seed=13)
+    ws = workspace_for(b)
+    out = ops.paged_attn_decode(b.q[:0], b.k_pool, b.v_pool, b.block_table[:0], b.seq_lens[:0], ws)
+    ops.check_error(ws)
+    assert out.shape[0] == 0

@@ -1,0 +1,145 @@
+"""Prefill parity: paged_attn_prefill (tcgen05 kernel, through the C ABI) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import (assert_close, assert_lse_close, gpu, lib_ready, oracle_appended_pools,
+                         oracle_attention, workspace_for)
+from paged_gqa_attention_gb300 import ops
+from paged_gqa_attention_gb300 import workloads as wl
+
+pytestmark = gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lib_ready()
+
+
+def append_and_prefill(b, ws=None, with_lse=True):
+    ws = workspace_for(b) if ws is None else ws
+    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    lse = torch.empty(b.total_tokens, 32, dtype=torch.float32, device="cuda") if with_lse else None
+    out = ops.paged_attn_prefill(b.q, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens,
+                                 b.max_q_len, ws, lse=lse)
+    ops.check_error(ws)
+    return out, lse
+
+
+def small_batch(ctx_and_q, seed, extra_blocks=3):
+    seq_lens = [c + q for c, q in ctx_and_q]
+    q_lens = [q for _, q in ctx_and_q]
+    need = sum((s + 255) // 256 for s in seq_lens)
+    return wl.build_batch("prefill_case", seed, seq_lens, q_lens, num_blocks=need + extra_blocks,
+                          device="cuda")
+
+
+@pytest.mark.parametrize("ctx_and_q", [
+    [(0, 1)],
+    [(0, 32)],
+    [(0, 128)],
+    [(0, 300)],                       # several query tiles, ragged tail
+    [(0, 777)],                       # crosses block edges, ragged key tile
+    [(200, 100)],                     # chunk after a context ending mid-block
+    [(511, 1), (1, 1), (0, 1)],       # decode-like rows through the prefill path
+    [(0, 64), (37, 1), (255, 130), (1000, 77), (128, 128)],   # mixed batch
+])
+def test_prefill_matches_oracle(ctx_and_q):
+    b = small_batch(ctx_and_q, seed=len(ctx_and_q) * 100 + ctx_and_q[0][1])
+    kp, vp = oracle_appended_pools(b)
+    out, lse = append_and_prefill(b)
+    ref, ref_lse = oracle_attention(b, kp, vp)
+    assert_close(out, ref, f"prefill {ctx_and_q}")
+    assert_lse_close(lse, ref_lse, f"prefill {ctx_and_q}")
+
+
+def test_causal_prefill_4096_sampled():
+    """The 4096-token causal prefill at full size, checked on sampled rows."""
+    b = wl.causal_prefill(device="cuda")
+    kp, vp = oracle_appended_pools(b)
+    out, lse = append_and_prefill(b)
+    g = np.random.default_rng(0)
+    toks = np.concatenate([np.arange(0, 40), np.arange(4056, 4096), g.integers(0, 4096, 176)])
+    heads = g.integers(0, 32, len(toks))
+    ref, ref_lse = oracle_attention(b, kp, vp, rows=(toks, heads))
+    sel = out[torch.as_tensor(toks, device="cuda"), torch.as_tensor(heads, device="cuda")]
+    assert_close(sel, ref, "causal_prefill sampled rows")
+    sel_lse = lse[torch.as_tensor(toks, device="cuda"), torch.as_tensor(heads, device="cuda")]
+    assert_lse_close(sel_lse, ref_lse, "causal_prefill sampled lse")
+    assert torch.isfinite(out.float()).all()
+
+
+def test_mixed_batch_full_size():
+    """One append for 120 decode tokens + 8 chunks of 512, then decode and prefill."""
+    b = wl.mixed_batch(device="cuda")
+    kp, vp = oracle_appended_pools(b)
+    ws = workspace_for(b)
+    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    dec = b.select(slice(0, 120))
+    pre = b.select(slice(120, 128))
+    out_d = ops.paged_attn_decode(dec.q, dec.k_pool, dec.v_pool, dec.block_table, dec.seq_lens, ws)
+    out_p = ops.paged_attn_prefill(pre.q, pre.k_pool, pre.v_pool, pre.block_table, pre.cu_q_lens,
+                                   pre.seq_lens, pre.max_q_len, ws)
+    ops.check_error(ws)
+    ref_d, _ = oracle_attention(dec, kp, vp)
+    assert_close(out_d, ref_d, "mixed: decode part")
+    g = np.random.default_rng(1)
+    toks = g.integers(0, pre.total_tokens, 256)
+    heads = g.integers(0, 32, 256)
+    ref_p, _ = oracle_attention(pre, kp, vp, rows=(toks, heads))
+    sel = out_p[torch.as_tensor(toks, device="cuda"), torch.as_tensor(heads, device="cuda")]
+    assert_close(sel, ref_p, "mixed: prefill part (sampled)")
+
+
+def test_decode_equals_last_prefill_row():
+    b = small_batch([(0, 700)], seed=21)
+    out, _ = append_and_prefill(b)
+    ws = workspace_for(b)
+    for p in (0, 255, 256, 699):
+        q = b.q[p:p + 1].contiguous()
+        sl = torch.tensor([p + 1], dtype=torch.int32, device="cuda")
+        d = ops.paged_attn_decode(q, b.k_pool, b.v_pool, b.block_table, sl, ws)
+        ops.check_error(ws)
+        diff = (d[0].float() - out[p].float()).abs().max().item()
+        assert diff <= 1e-2, f"position {p}: decode vs prefill row differ by {diff}"
+
+
+def test_chunked_equals_unchunked():
+    b = small_batch([(0, 600)], seed=22)
+    whole, _ = append_and_prefill(b)
+    ws = workspace_for(b)
+    parts = []
+    for lo, hi in ((0, 129), (129, 300), (300, 600)):
+        cu = torch.tensor([0, hi - lo], dtype=torch.int32, device="cuda")
+        sl = torch.tensor([hi], dtype=torch.int32, device="cuda")
+        parts.append(ops.paged_attn_prefill(b.q[lo:hi].contiguous(), b.k_pool, b.v_pool,
+                                            b.block_table, cu, sl, hi - lo, ws))
+    ops.check_error(ws)
+    chunked = torch.cat(parts)
+    diff = (chunked.float() - whole.float()).abs().max().item()
+    assert diff <= 1e-2
+
+
+def test_prefill_block_placement_is_bit_exact():
+    b = small_batch([(100, 400), (0, 50)], seed=23, extra_blocks=10)
+    out1, _ = append_and_prefill(b)
+    perm = torch.randperm(b.num_blocks, generator=torch.Generator().manual_seed(3)).to("cuda")
+    k2 = torch.empty_like(b.k_pool)
+    v2 = torch.empty_like(b.v_pool)
+    k2[perm] = b.k_pool
+    v2[perm] = b.v_pool
+    bt = b.block_table.clone()
+    valid = bt >= 0
+    bt[valid] = perm[bt[valid].long()].to(torch.int32)
+    ws = workspace_for(b)
+    out2 = ops.paged_attn_prefill(b.q, k2, v2, bt, b.cu_q_lens, b.seq_lens, b.max_q_len, ws)
+    ops.check_error(ws)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_empty_sequences_are_skipped():
+    b = small_batch([(10, 0), (0, 40), (300, 0)], seed=24)
+    kp, vp = oracle_appended_pools(b)
+    out, _ = append_and_prefill(b)
+    ref, _ = oracle_attention(b, kp, vp)
+    assert_close(out, ref, "empty sequences")
