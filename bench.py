@@ -1,0 +1,608 @@
+#!/usr/bin/env python
+"""Benchmark of the paged GQA attention hot path on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the hot path over one batch: kv_append of the batch's new
+tokens, then the attention call(s).  Default workload: batched decode (batch 32,
+context ~U{128..4096}, 32 q / 8 KV heads x 128, 256-token blocks in a 1024-block
+pool); the line also carries the causal-prefill half of the metric (4096-token
+prompt appended into 16 blocks, then causal attention) measured in the same run.
+
+Timing: W untimed warm-up steps, then K timed steps.  Before every timed step the
+L2 is flushed (a 512 MiB device write, outside the timed region) and the GPU is
+given a short head start so that every launch of the step is queued before it
+begins; each step is bracketed by CUDA events on the launching stream.  Inputs are
+resident in HBM for `value`; `e2e` repeats the step through the public API with
+host (pinned) inputs copied in and the output copied back inside the timed region.
+
+--impl reference times the fp64 CPU oracle on this host's cores on the same
+workload (rank 0 only).  With N > 1 ranks (torchrun) every rank runs its own
+replica of the workload (weak scaling, no collective on the data path); timing is
+the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode KV-read GB/s (% of HBM peak); causal prefill attn TFLOP/s (% BF16 peak)"
+FLUSH_BYTES = 512 << 20
+HEAD_START_CYCLES = 200_000      # ~0.1 ms spin so a step's launches are all queued
+
+# Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu
+# capture, keyed by kernel, with the hash of the sources it was taken on.  A kernel
+# whose sources changed since reports traffic null.
+TRAFFIC = {}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default="batched_decode",
+                   choices=["single_decode", "batched_decode", "causal_prefill", "mixed_batch",
+                            "prefix_shared_decode"])
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target duration of the CPU oracle sample")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_setup():
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def dist_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi in the background; clocks and throttle reasons of one GPU."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+        self.windows = []
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def mark(self, t0: float, t1: float):
+        self.windows.append((t0, t1))
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10], parts[5]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if any(a - 0.15 <= r[0] <= b + 0.15 for a, b in self.windows)]
+        used = inside if len(inside) >= 3 else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median([r[1] for r in used]) if used else None,
+                "sm_max_mhz": max(r[2] for r in used) if used else None,
+                "reasons": reasons, "samples": len(used),
+                "window": "timed region" if used is inside else "whole run (timed region too short)"}
+
+
+# ------------------------------------------------------------------ helpers
+
+def source_hash(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_gqa_attention_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class Timer:
+    """Per-step CUDA events on one stream: marks[i] recorded between the step's calls."""
+
+    def __init__(self, n_marks: int, stream):
+        import torch
+
+        self.stream = stream
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_marks)]
+
+    def record(self, i):
+        self.ev[i].record(self.stream)
+
+    def spans_ms(self):
+        return [self.ev[i].elapsed_time(self.ev[i + 1]) for i in range(len(self.ev) - 1)]
+
+
+def run_timed(step, n_marks, steps, warmup, flush_buf, stream, clocks=None):
+    """W warm-up steps, then `steps` timed steps; returns per-step lists of span times (ms)."""
+    import torch
+
+    for _ in range(warmup):
+        flush_buf.zero_()
+        step(None)
+    torch.cuda.synchronize()
+    spans = []
+    t0 = time.time()
+    for _ in range(steps):
+        flush_buf.zero_()
+        torch.cuda._sleep(HEAD_START_CYCLES)
+        tm = Timer(n_marks, stream)
+        step(tm)
+        spans.append(tm)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if clocks is not None:
+        clocks.mark(t0, t1)
+    return [tm.spans_ms() for tm in spans], t1 - t0
+
+
+def mean(xs):
+    return sum(xs) / len(xs) if xs else float("nan")
+
+
+# ------------------------------------------------------------------ the two measured paths
+
+def decode_measure(batch, steps, warmup, flush_buf, stream, clocks):
+    """kv_append (one new token per sequence) + decode; returns numbers in ms / bytes."""
+    import torch
+
+    from paged_gqa_attention_gb300 import ops
+
+    ws = ops.make_workspace(batch.num_seqs, batch.max_blocks_per_seq)
+    out = torch.empty_like(batch.q)
+
+    def step(tm):
+        if tm: tm.record(0)
+        ops.kv_append(batch.k_pool, batch.v_pool, batch.k_new, batch.v_new, batch.block_table,
+                      batch.cu_q_lens, batch.seq_lens, ws)
+        if tm: tm.record(1)
+        ops.paged_attn_decode(batch.q, batch.k_pool, batch.v_pool, batch.block_table,
+                              batch.seq_lens, ws, out=out)
+        if tm: tm.record(2)
+
+    spans, wall = run_timed(step, 3, steps, warmup, flush_buf, stream, clocks)
+    ops.check_error(ws)
+    return {"append_ms": mean([s[0] for s in spans]), "attn_ms": mean([s[1] for s in spans]),
+            "step_ms": mean([s[0] + s[1] for s in spans]), "wall_s": wall, "launches": 2 * steps}
+
+
+def prefill_measure(batch, steps, warmup, flush_buf, stream, clocks):
+    import torch
+
+    from paged_gqa_attention_gb300 import ops
+
+    ws = ops.make_workspace(batch.num_seqs, batch.max_blocks_per_seq)
+    out = torch.empty_like(batch.q)
+
+    def step(tm):
+        if tm: tm.record(0)
+        ops.kv_append(batch.k_pool, batch.v_pool, batch.k_new, batch.v_new, batch.block_table,
+                      batch.cu_q_lens, batch.seq_lens, ws)
+        if tm: tm.record(1)
+        ops.paged_attn_prefill(batch.q, batch.k_pool, batch.v_pool, batch.block_table,
+                               batch.cu_q_lens, batch.seq_lens, batch.max_q_len, ws, out=out)
+        if tm: tm.record(2)
+
+    spans, wall = run_timed(step, 3, steps, warmup, flush_buf, stream, clocks)
+    ops.check_error(ws)
+    return {"append_ms": mean([s[0] for s in spans]), "attn_ms": mean([s[1] for s in spans]),
+            "step_ms": mean([s[0] + s[1] for s in spans]), "wall_s": wall, "launches": 2 * steps}
+
+
+def mixed_measure(batch, steps, warmup, flush_buf, stream, clocks):
+    import torch
+
+    from paged_gqa_attention_gb300 import ops
+
+    n_dec = batch.info["n_decode"]
+    dec = batch.select(slice(0, n_dec))
+    pre = batch.select(slice(n_dec, batch.num_seqs))
+    ws = ops.make_workspace(batch.num_seqs, batch.max_blocks_per_seq)
+    out_d = torch.empty_like(dec.q)
+    out_p = torch.empty_like(pre.q)
+
+    def step(tm):
+        if tm: tm.record(0)
+        ops.kv_append(batch.k_pool, batch.v_pool, batch.k_new, batch.v_new, batch.block_table,
+                      batch.cu_q_lens, batch.seq_lens, ws)
+        if tm: tm.record(1)
+        ops.paged_attn_decode(dec.q, dec.k_pool, dec.v_pool, dec.block_table, dec.seq_lens, ws,
+                              out=out_d)
+        if tm: tm.record(2)
+        ops.paged_attn_prefill(pre.q, pre.k_pool, pre.v_pool, pre.block_table, pre.cu_q_lens,
+                               pre.seq_lens, pre.max_q_len, ws, out=out_p)
+        if tm: tm.record(3)
+
+    spans, wall = run_timed(step, 4, steps, warmup, flush_buf, stream, clocks)
+    ops.check_error(ws)
+    return {"append_ms": mean([s[0] for s in spans]), "decode_ms": mean([s[1] for s in spans]),
+            "prefill_ms": mean([s[2] for s in spans]),
+            "step_ms": mean([sum(s) for s in spans]), "wall_s": wall, "launches": 3 * steps,
+            "dec": dec, "pre": pre}
+
+
+def e2e_measure(batch, kind, steps, warmup, stream):
+    """The same step through the public API with pinned host inputs and a host result."""
+    import torch
+
+    from paged_gqa_attention_gb300 import ops
+
+    host = {k: getattr(batch, k).cpu().pin_memory()
+            for k in ("q", "k_new", "v_new", "block_table", "seq_lens", "cu_q_lens")}
+    dev = {k: torch.empty_like(getattr(batch, k)) for k in host}
+    out_host = torch.empty(batch.q.shape, dtype=batch.q.dtype).pin_memory()
+    out_dev = torch.empty_like(batch.q)
+    ws = ops.make_workspace(batch.num_seqs, batch.max_blocks_per_seq)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    n_dec = batch.info.get("n_decode", 0)
+    t_dec = n_dec          # decode tokens come first in a mixed batch (one per sequence)
+
+    def step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        ops.kv_append(batch.k_pool, batch.v_pool, dev["k_new"], dev["v_new"], dev["block_table"],
+                      dev["cu_q_lens"], dev["seq_lens"], ws)
+        if kind == "decode":
+            ops.paged_attn_decode(dev["q"], batch.k_pool, batch.v_pool, dev["block_table"],
+                                  dev["seq_lens"], ws, out=out_dev)
+        elif kind == "prefill":
+            ops.paged_attn_prefill(dev["q"], batch.k_pool, batch.v_pool, dev["block_table"],
+                                   dev["cu_q_lens"], dev["seq_lens"], batch.max_q_len, ws,
+                                   out=out_dev)
+        else:  # mixed: decode sequences, then prefill chunks, from the same device copies
+            ops.paged_attn_decode(dev["q"][:t_dec], batch.k_pool, batch.v_pool,
+                                  dev["block_table"][:n_dec], dev["seq_lens"][:n_dec], ws,
+                                  out=out_dev[:t_dec])
+            cu_p = dev["cu_q_lens"][n_dec:] - t_dec
+            ops.paged_attn_prefill(dev["q"][t_dec:], batch.k_pool, batch.v_pool,
+                                   dev["block_table"][n_dec:], cu_p, dev["seq_lens"][n_dec:],
+                                   batch.max_q_len, ws, out=out_dev[t_dec:])
+        out_host.copy_(out_dev, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()          # the result is on the host when the step ends
+        times.append(e0.elapsed_time(e1))
+    ops.check_error(ws)
+    return {"step_ms": mean(times), "h2d": h2d, "d2h": d2h}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def cpu_baseline(batch, kind, target_s, rows_cap=None):
+    """Time the oracle (as it stands) on a bounded sample of the workload.
+
+    The sample is the first sequences of the batch whose total work fits the time
+    target (at least one sequence); the throughput is scaled to the metric's unit by
+    the sample's own bytes or flops.
+    """
+    import numpy as np
+
+    import oracle
+    from paged_gqa_attention_gb300 import workloads as wl
+
+    kp, vp = oracle.kv_append(batch.k_pool.cpu(), batch.v_pool.cpu(), batch.k_new.cpu(),
+                              batch.v_new.cpu(), batch.block_table.cpu(), batch.cu_q_lens.cpu(),
+                              batch.seq_lens.cpu())
+    q = batch.q.cpu()
+    bt, cu, sl = batch.block_table.cpu(), batch.cu_q_lens.cpu(), batch.seq_lens.cpu()
+    cores = oracle.max_threads()
+    # rows of the sample: all heads of the first n sequences' tokens (capped for prefill)
+    toks_all = []
+    n_seq = 0
+    t_probe = time.time()
+    for s in range(batch.num_seqs):
+        n_seq += 1
+        lo, hi = int(cu[s]), int(cu[s + 1])
+        toks_all.extend(range(lo, hi))
+        if rows_cap and len(toks_all) * 32 >= rows_cap:
+            break
+    toks = np.repeat(np.array(toks_all, dtype=np.int32), 32)
+    heads = np.tile(np.arange(32, dtype=np.int32), len(toks_all))
+    if rows_cap and len(toks) > rows_cap:
+        sel = np.linspace(0, len(toks) - 1, rows_cap).astype(np.int64)
+        toks, heads = toks[sel], heads[sel]
+    reps = 0
+    t0 = time.time()
+    while True:
+        oracle.attention(q, kp, vp, bt, cu, sl, scale=wl.SCALE, rows=(toks, heads))
+        reps += 1
+        if time.time() - t0 >= target_s:
+            break
+    dt = time.time() - t0
+    # work of the sample
+    sl_l = batch.seq_lens_host
+    cu_l = [int(x) for x in cu]
+    ql_l = batch.q_lens_host
+    pairs = 0
+    kv_tokens = 0
+    for t, h in zip(toks.tolist(), heads.tolist()):
+        s = int(np.searchsorted(cu_l, t, side="right") - 1)
+        p = sl_l[s] - ql_l[s] + (t - cu_l[s])
+        pairs += p + 1
+    if kind == "decode":
+        # decode KV bytes: every (sequence, kv-head) context row read once -> per q-head
+        # row the share is (p + 1) tokens x 2 (K, V) x 128 x 2 B / 4 heads
+        value = pairs * (2 * 128 * 2) / 4 * reps / dt / 1e9
+        unit = "GB/s"
+    else:
+        value = pairs * 4 * 128 * reps / dt / 1e12
+        unit = "TFLOP/s"
+    return {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+            "sample": f"{len(toks)} (token, head) rows of the workload, {reps} pass(es), "
+                      f"{dt:.1f} s, fp64 C oracle with OpenMP"}
+
+
+# ------------------------------------------------------------------ main paths
+
+def reference_arm(args, world, rank):
+    """--impl reference: the oracle on the host cores, rank 0 only."""
+    if rank != 0:
+        return
+    import torch
+
+    from paged_gqa_attention_gb300 import workloads as wl
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    batch = wl.WORKLOADS[args.workload](device=dev)
+    kind = "decode" if "decode" in args.workload else "prefill"
+    if args.workload == "mixed_batch":
+        kind = "decode"
+    per_step_s = max(args.cpu_seconds / max(args.steps, 1), 0.05)
+    rows_cap = rows_cap_for(args.workload)
+    for _ in range(min(args.warmup, 1)):
+        cpu_baseline(batch, kind, 0.0, rows_cap)
+    res = [cpu_baseline(batch, kind, per_step_s, rows_cap) for _ in range(args.steps)]
+    value = mean([r["value"] for r in res])
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": res[0]["unit"],
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload},
+            "cpu_baseline": {"value": value, "unit": res[0]["unit"], "cores": res[0]["cores"],
+                             "kind": "oracle", "sample": res[0]["sample"]},
+            "e2e": {"value": value, "unit": res[0]["unit"], "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def rows_cap_for(workload):
+    """Bound on the (token, head) rows of one oracle pass (keeps a pass to seconds)."""
+    return {"single_decode": None, "batched_decode": None, "mixed_batch": 1024,
+            "causal_prefill": 2048, "prefix_shared_decode": 256}[workload]
+
+
+def roofline(achieved, peak, unit, bound, traffic):
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak if peak else None, "traffic": traffic}
+
+
+def traffic_for(kernel):
+    t = TRAFFIC.get(kernel)
+    if not t or source_hash(*t["sources"]) != t["sha"]:
+        return None
+    return t["bytes_per_launch"]
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+        return
+    import torch
+
+    from paged_gqa_attention_gb300 import build as pa_build
+    from paged_gqa_attention_gb300 import ops
+    from paged_gqa_attention_gb300 import workloads as wl
+
+    torch.cuda.set_device(local)
+    pa_build.build()
+    ops.load()
+    peaks = measured_peaks()
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    clocks = ClockSampler(local)
+    clocks.start()
+
+    wname = args.workload
+    batch = wl.WORKLOADS[wname](device="cuda")
+    dist_barrier(world)
+    line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic"}
+    cfg = {"workload": wname, **batch.info, "heads": "32 q / 8 kv x 128", "block_tokens": 256,
+           "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)",
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+    if wname in ("single_decode", "batched_decode", "prefix_shared_decode"):
+        r = decode_measure(batch, args.steps, args.warmup, flush_buf, stream, clocks)
+        kv_bytes = batch.kv_bytes()
+        io_bytes = batch.num_seqs * 32 * 128 * 2 * 2 + batch.num_seqs * (batch.max_blocks_per_seq + 1) * 4
+        step_ms = dist_max(r["step_ms"], world)
+        attn_ms = dist_max(r["attn_ms"], world)
+        line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s",
+                    ms_per_step=step_ms)
+        ach = (kv_bytes + io_bytes) / (attn_ms * 1e-3) / 1e9
+        line["roofline"] = roofline(ach, peaks["hbm_gbs"], "GB/s", "hbm", traffic_for("decode"))
+        line["roofline"]["kernel"] = "decode_kernel"
+        line["roofline"]["algorithmic_bytes_per_launch"] = kv_bytes + io_bytes
+        line["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "decode_us": r["attn_ms"] * 1e3,
+                           "kv_bytes_per_step": kv_bytes,
+                           "unique_kv_bytes": wl.unique_kv_bytes(batch)}
+        if wname == "prefix_shared_decode":
+            uniq = wl.unique_kv_bytes(batch)
+            line["kernels"]["unique_kv_gbs"] = uniq / (attn_ms * 1e-3) / 1e9
+            line["kernels"]["unique_kv_frac"] = line["kernels"]["unique_kv_gbs"] / peaks["hbm_gbs"]
+        line["gpu_launches"] = r["launches"]
+        e = e2e_measure(batch, "decode", max(20, min(args.steps, 200)), 5, stream)
+        e_ms = dist_max(e["step_ms"], world)
+        line["e2e"] = {"value": world * kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                       "ms_per_step": e_ms}
+        kind = "decode"
+    elif wname == "causal_prefill":
+        r = prefill_measure(batch, args.steps, args.warmup, flush_buf, stream, clocks)
+        flops = batch.attention_flops()
+        step_ms = dist_max(r["step_ms"], world)
+        attn_ms = dist_max(r["attn_ms"], world)
+        line.update(value=world * flops / (step_ms * 1e-3) / 1e12, unit="TFLOP/s",
+                    ms_per_step=step_ms)
+        line["roofline"] = roofline(flops / (attn_ms * 1e-3) / 1e12, peaks["bf16_tflops"],
+                                    "TFLOP/s", "tensor", traffic_for("prefill"))
+        line["roofline"]["kernel"] = "prefill_kernel"
+        line["roofline"]["algorithmic_flops_per_launch"] = flops
+        line["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "prefill_us": r["attn_ms"] * 1e3}
+        line["gpu_launches"] = r["launches"]
+        e = e2e_measure(batch, "prefill", max(10, min(args.steps, 50)), 3, stream)
+        e_ms = dist_max(e["step_ms"], world)
+        line["e2e"] = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                       "ms_per_step": e_ms}
+        kind = "prefill"
+    else:  # mixed_batch
+        r = mixed_measure(batch, args.steps, args.warmup, flush_buf, stream, clocks)
+        dec, pre = r["dec"], r["pre"]
+        kv_bytes = dec.kv_bytes()
+        flops = pre.attention_flops()
+        step_ms = dist_max(r["step_ms"], world)
+        t_bw = kv_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+        t_tc = flops / (peaks["bf16_tflops"] * 1e12) * 1e3
+        line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s",
+                    ms_per_step=step_ms)
+        line["roofline"] = roofline(kv_bytes / (r["decode_ms"] * 1e-3) / 1e9, peaks["hbm_gbs"],
+                                    "GB/s", "hbm", traffic_for("decode"))
+        line["roofline"]["kernel"] = "decode_kernel"
+        line["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "decode_us": r["decode_ms"] * 1e3,
+                           "prefill_us": r["prefill_ms"] * 1e3,
+                           "prefill_tflops": flops / (r["prefill_ms"] * 1e-3) / 1e12,
+                           "combined_roofline_frac": (t_bw + t_tc) / step_ms}
+        line["gpu_launches"] = r["launches"]
+        e = e2e_measure(batch, "mixed", max(10, min(args.steps, 100)), 3, stream)
+        e_ms = dist_max(e["step_ms"], world)
+        line["e2e"] = {"value": world * kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                       "ms_per_step": e_ms}
+        kind = "decode"
+
+    line["config"] = cfg
+    # the other half of the metric: causal prefill, in the same run
+    if wname in ("single_decode", "batched_decode", "prefix_shared_decode") and not args.no_prefill:
+        del batch
+        torch.cuda.empty_cache()
+        pb = wl.causal_prefill(device="cuda")
+        psteps = max(10, min(args.steps, 200))
+        pr = prefill_measure(pb, psteps, max(3, min(args.warmup, 10)), flush_buf, stream, clocks)
+        flops = pb.attention_flops()
+        p_step = dist_max(pr["step_ms"], world)
+        p_attn = dist_max(pr["attn_ms"], world)
+        line["prefill"] = {
+            "workload": "causal_prefill", "prompt": 4096, "steps": psteps,
+            "value": world * flops / (p_step * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": p_step,
+            "roofline": dict(roofline(flops / (p_attn * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s",
+                                      "tensor", traffic_for("prefill")),
+                             kernel="prefill_kernel", algorithmic_flops_per_launch=flops),
+            "kv_append_us": pr["append_ms"] * 1e3, "prefill_us": pr["attn_ms"] * 1e3,
+            "gpu_launches": pr["launches"]}
+        batch = pb
+    line["clocks"] = clocks.stop()
+    line["peaks"] = peaks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        src = wl.WORKLOADS[wname](device="cuda") if wname != batch.name else batch
+        line["cpu_baseline"] = cpu_baseline(src, kind, args.cpu_seconds, rows_cap_for(wname))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dist_barrier(world)
+
+
+if __name__ == "__main__":
+    main()

@@ -12,9 +12,12 @@ from paged_gqa_attention_gb300 import workloads as wl
 # max |gpu - ref| <= 1e-2 and ||gpu - ref||_2 / ||ref||_2 <= 5e-3.
 MAX_ABS = 1e-2
 REL_RMS = 5e-3
-# lse is fp32 end to end: scores accumulate 128 bf16 products in fp32 and pass through
-# exp2/log2; 1e-3 absolute leaves two orders of magnitude of margin over that error.
-LSE_ABS = 1e-3
+# lse = m + log(sum_j p~_j), where p~_j = bf16(p_j) are the same rounded weights the PV
+# product uses (so the normalised weights sum to one).  bf16 round-to-nearest changes
+# each weight by a relative |d| <= 2^-9, hence the sum by at most 2^-9 relative and the
+# log by at most log(1 + 2^-9) = 1.95e-3; fp32 accumulation of the 128-term scores adds
+# about 1e-4.  Bar: 2.5e-3 absolute.
+LSE_ABS = 2.5e-3
 
 
 def lib_ready():
