@@ -10,7 +10,9 @@ pool); the line also carries the causal-prefill half of the metric (4096-token
 prompt appended into 16 blocks, then causal attention) measured in the same run.
 
 Timing: W untimed warm-up steps, then K timed steps.  Before every timed step the
-L2 is flushed (a 512 MiB device write, outside the timed region) and the GPU is
+L2 is flushed (a 512 MiB device write, then a read of the same buffer so that the
+flush's dirty lines are written back before the step: the step then starts from
+an L2 holding only clean, unrelated lines; outside the timed region) and the GPU is
 given a short head start so that every launch of the step is queued before it
 begins; each step is bracketed by CUDA events on the launching stream.  Inputs are
 resident in HBM for `value`; `e2e` repeats the step through the public API with
@@ -194,18 +196,24 @@ class Timer:
         return [self.ev[i].elapsed_time(self.ev[i + 1]) for i in range(len(self.ev) - 1)]
 
 
+def flush_l2(buf):
+    """Evict the L2: write a buffer 4x its size, then read it back (leaves clean lines)."""
+    buf.zero_()
+    buf.sum(dtype=__import__("torch").int32)
+
+
 def run_timed(step, n_marks, steps, warmup, flush_buf, stream, clocks=None):
     """W warm-up steps, then `steps` timed steps; returns per-step lists of span times (ms)."""
     import torch
 
     for _ in range(warmup):
-        flush_buf.zero_()
+        flush_l2(flush_buf)
         step(None)
     torch.cuda.synchronize()
     spans = []
     t0 = time.time()
     for _ in range(steps):
-        flush_buf.zero_()
+        flush_l2(flush_buf)
         torch.cuda._sleep(HEAD_START_CYCLES)
         tm = Timer(n_marks, stream)
         step(tm)
@@ -501,7 +509,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic"}
     cfg = {"workload": wname, **batch.info, "heads": "32 q / 8 kv x 128", "block_tokens": 256,
-           "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)",
+           "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write + read)",
            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
     if wname in ("single_decode", "batched_decode", "prefix_shared_decode"):

@@ -6,7 +6,7 @@
 
 #include <cudaTypedefs.h>
 
-#include "../../include/pagedattn.h"
+#include "pagedattn.h"
 #include "common.cuh"
 #include "launch.h"
 

@@ -24,7 +24,10 @@
 //     merges them by log-sum-exp and writes bf16 output (+ optional lse).
 // Tokens past the context end inside the last tile are masked in the scores and
 // their V rows are zeroed in registers, so uninitialised (even NaN) slots never
-// reach the result.
+// reach the result.  A block id outside the pool is replaced by block 0 for the read,
+// recorded in the error word and makes the (sequence, KV head)'s output NaN.
+// The kernel is launched as a programmatic dependent of the previous kernel on the
+// stream, so its launch and prologue overlap e.g. the kv_append that precedes it.
 #include "common.cuh"
 #include "launch.h"
 
@@ -47,6 +50,7 @@ struct DecodeSmem {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     int last_cta;
+    int poison;                                // a block id of this split was out of range
 };
 
 constexpr size_t kSmemBytes = sizeof(DecodeSmem) + 1024;  // + alignment slack
@@ -84,30 +88,25 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
     const int32_t *bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
 
-    // Block ids of this split must address the pool; a bad one poisons the result.
-    bool bad = false;
-    for (int j = t_begin / kBlock + threadIdx.x; j <= (t_end - 1) / kBlock; j += kThreads) {
-        const int blk = __ldg(bt + j);
-        bad |= (blk < 0 || blk >= a.num_blocks);
-    }
-    bad = __syncthreads_or(bad);
-    if (bad && threadIdx.x == 0) record_error(a.err, kErrDevice | kErrBadBlock);
-
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sm.full[s]), 1);
             mbar_init(smem_u32(&sm.empty[s]), kConsumerWarps);
         }
+        sm.poison = 0;
         fence_barrier_init();
     }
     __syncthreads();
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && !bad) {
+        if (lane == 0) {
             tma_prefetch_map(&k_map);
             tma_prefetch_map(&v_map);
+            // The pools may be written by the kernel just before this one on the stream
+            // (kv_append lets us launch early): wait for it before the first pool read.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             int issued = 0;
             for (int i = 0; i < n_tiles; ++i) {
                 const int st = i % kStages;
@@ -116,7 +115,13 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                     break;
                 }
                 const int tok = t_begin + i * kTile;
-                const int blk = __ldg(bt + tok / kBlock);
+                int blk = __ldg(bt + tok / kBlock);
+                if (blk < 0 || blk >= a.num_blocks) {
+                    // a block id outside the pool: read block 0 instead and poison the result
+                    record_error(a.err, kErrDevice | kErrBadBlock);
+                    sm.poison = 1;
+                    blk = 0;
+                }
                 const int off = tok % kBlock;
                 const uint32_t bar = smem_u32(&sm.full[st]);
                 mbar_arrive_expect_tx(bar, kStageBytes);
@@ -163,7 +168,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     const int row_qk = w * 16 + ri + ((mi & 1) << 3);   // token row for the K fragment
     const int row_pv = w * 16 + ri + ((mi >> 1) << 3);  // token row for the V^T fragment
 
-    for (int i = 0; i < (bad ? 0 : n_tiles); ++i) {
+    for (int i = 0; i < n_tiles; ++i) {
         const int st = i % kStages;
         if (!mbar_wait(smem_u32(&sm.full[st]), (i / kStages) & 1)) {
             if (lane == 0) record_error(a.err, kErrTimeout);
@@ -269,6 +274,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         }
     }
     named_barrier(1, kConsumerWarps * 32);
+    const bool bad = *reinterpret_cast<volatile int *>(&sm.poison) != 0;
 
     const int c = threadIdx.x;          // 0..127
     const int h = c >> 5;               // query head within the group
@@ -352,9 +358,19 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const C
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
-    dim3 grid(a.batch * kHkv, a.nsplit);
-    decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(k_map, v_map, a);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the prologue may overlap the previous kernel on the
+    // stream; the producer waits for it (griddepcontrol.wait) before reading the pools.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.batch * kHkv, a.nsplit);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_kernel, k_map, v_map, a);
 }
 
 }  // namespace pa

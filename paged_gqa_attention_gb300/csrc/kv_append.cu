@@ -8,6 +8,13 @@
 // block_table[s][p / 256].  In the pool layout [block][slot][kv_head][dim] one
 // token's K (or V) for all 8 KV heads is 2 KiB contiguous, so each copy is one
 // contiguous 2 KiB move: one warp per (token, K|V), 16-byte vector accesses.
+//
+// The kernel is a chain of dependent loads (which sequence owns the token, its
+// length, its block id, then the data), so its time is latency: the owner is first
+// guessed in proportion (exact for one token per sequence and for one sequence) and
+// only on a miss found by a warp-wide 32-way search.  It lets the next kernel on the
+// stream start its own prologue early (programmatic dependent launch); that kernel
+// waits for this one to finish before it reads the pools.
 #include "common.cuh"
 #include "launch.h"
 
@@ -16,17 +23,26 @@ namespace {
 
 constexpr int kWarps = 8;  // 4 tokens x {K, V} per CTA
 
-// Sequence owning new-token row t (largest s with cu[s] <= t); -1 if none.
-__device__ __forceinline__ int find_sequence(const int32_t *cu, int num_seqs, int t) {
-    int lo = 0, hi = num_seqs - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+// Largest s in [0, n) with cu[s] <= t (cu non-decreasing, cu[0] <= t): each round the
+// 32 lanes probe 32 evenly spaced entries, narrowing the range 32-fold.
+__device__ __forceinline__ int warp_find_sequence(const int32_t *cu, int n, int t, int lane) {
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) / 32;
+        const int idx = lo + lane * step;
+        const bool le = idx < hi && __ldg(cu + idx) <= t;
+        const unsigned m = __ballot_sync(0xffffffffu, le);
+        const int last = m ? 31 - __clz(m) : 0;
+        lo = lo + last * step;
+        hi = min(hi, lo + step);
     }
     return lo;
 }
 
 __global__ void __launch_bounds__(kWarps * 32) kv_append_kernel(AppendArgs a) {
+    // The pools are this kernel's only output: a dependent kernel may launch now and
+    // run its prologue; it waits for our completion before touching the pools.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (kWarps / 2) + (warp >> 1);
@@ -38,10 +54,17 @@ __global__ void __launch_bounds__(kWarps * 32) kv_append_kernel(AppendArgs a) {
         if (__ldg(a.cu_q_lens) != 0 || __ldg(a.cu_q_lens + a.num_seqs) != a.total_tokens)
             record_error(a.err, kErrDevice | kErrBadCuQ);
     }
-    const int s = find_sequence(a.cu_q_lens, a.num_seqs, t);
-    const int q0 = __ldg(a.cu_q_lens + s);
-    const int q_len = __ldg(a.cu_q_lens + s + 1) - q0;
-    const int seq_len = __ldg(a.seq_lens + s);
+    int s = (int)((long long)t * a.num_seqs / a.total_tokens);
+    int q0 = __ldg(a.cu_q_lens + s);
+    int q1 = __ldg(a.cu_q_lens + s + 1);
+    int seq_len = __ldg(a.seq_lens + s);
+    if (!(q0 <= t && t < q1)) {
+        s = warp_find_sequence(a.cu_q_lens, a.num_seqs, t, lane);
+        q0 = __ldg(a.cu_q_lens + s);
+        q1 = __ldg(a.cu_q_lens + s + 1);
+        seq_len = __ldg(a.seq_lens + s);
+    }
+    const int q_len = q1 - q0;
     const int i = t - q0;
     if (i < 0 || i >= q_len) {
         if (lane == 0 && !is_v) record_error(a.err, kErrDevice | kErrBadCuQ);

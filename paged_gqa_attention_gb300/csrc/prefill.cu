@@ -18,17 +18,23 @@
 // Key/value tiles are 128 tokens (half a cache block) fetched by TMA straight from
 // the paged pool: the block table lookup is the TMA coordinate.
 //
-// CTA = 6 warps, persistent (one per SM), tiles dealt in a snake order, latest query
+// CTA = 11 warps, persistent (one per SM), tiles dealt in a snake order, latest query
 // blocks (most keys) first:
-//   warps 0-3  softmax + epilogue; thread r owns MMA row r (= TMEM lane r)
-//   warp 4     TMA producer (Q double-buffered, K and V rings of 2 stages)
-//   warp 5     TMEM allocator and the single-thread tcgen05.mma issuer
+//   warps 0-7  softmax + epilogue in two warpgroups; warp w owns MMA rows (= TMEM
+//              lanes) 32*(w%4) .. +31, columns 64*(w/4) .. +63 of each
+//   warp 8     TMA producer of Q and K (ring of 2 stages)
+//   warp 9     TMEM allocator and the single-thread tcgen05.mma issuer
+//   warp 10    TMA producer of V (ring of 3 stages)
 // Tensor memory (512 columns): S0, S1 (fp32 scores, 128 cols each), O (fp32, 128),
-// P0, P1 (bf16 probabilities packed in pairs, 64 cols each).
+// L (fp32 row sums, 16).  P (bf16, packed in pairs) is written over the first 64
+// columns of the S buffer it came from.
 // Per key tile:  S = Q K^T (SS-MMA)  ->  softmax reads S, writes P (bf16) into TMEM
-// and, when its running max rose by more than 2^8, rescales O  ->  O += P V (TS-MMA,
-// P from TMEM, V from shared memory, MN-major).  The MMA warp issues S for tile j+1
-// before O += P V for tile j, so the tensor core works while the softmax runs.
+// and, when its running max rose by more than 2^8, rescales O and L  ->  O += P V
+// (TS-MMA, P from TMEM, V from shared memory, MN-major) and L += P 1 (TS-MMA against a
+// ones tile: the row sums of exactly the bf16 weights that multiply V).  The MMA warp
+// issues S for tile j+1 before O += P V for tile j, so the tensor core works while the
+// softmax runs; tcgen05.mma ops of one thread execute in issue order, so S for tile
+// j+2 cannot overwrite P of tile j before O += P V of tile j has read it.
 // Every wait is bounded; on expiry the CTA records PA_ERR_TIMEOUT, unwinds, waits
 // (bounded) for its own copies and MMAs, frees tensor memory and exits.
 #include "common.cuh"
@@ -40,32 +46,44 @@ namespace {
 constexpr int kRows = 128;                  // MMA M
 constexpr int kKT = kPrefillKvTile;         // keys per tile (MMA N of S, K of PV)
 constexpr int kQPos = kPrefillQPositions;   // query positions per tile
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kSoftmaxWarps = 8;            // two warpgroups, one per half of each row
+constexpr int kProducerWarp = 8;            // Q and K loads
+constexpr int kMmaWarp = 9;
+constexpr int kVProducerWarp = 10;          // V loads
+constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128;   // score buffers
+constexpr uint32_t kColS0 = 0, kColS1 = 128;   // score buffers; P (bf16 pairs) is written
+                                               // over the first 64 columns of its own S
 constexpr uint32_t kColO = 256;                // output accumulator
-constexpr uint32_t kColP0 = 384, kColP1 = 448; // probability buffers
+constexpr uint32_t kColL = 384;                // row sums of P (16 equal columns)
 __device__ __forceinline__ uint32_t col_s(int st) { return st ? kColS1 : kColS0; }
-__device__ __forceinline__ uint32_t col_p(int st) { return st ? kColP1 : kColP0; }
 constexpr int kHalf = kRows * 128;          // 128 rows x 64 dims x 2 B = 16 KiB
+// Shared-memory rings (32 KiB per slot).  The V ring is the deepest: V of key tile j
+// may only be requested once O += P V of tile j-3 has finished with its slot, and an
+// L2-served 32 KiB load takes over a microsecond under this load.
+constexpr int kQBufs = 1;
+constexpr int kKStages = 2;
+constexpr int kVStages = 3;
 constexpr uint32_t kTileBytes = 2 * kHalf;  // a full 128 x 128 bf16 tile
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows > 2^8
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr uint32_t kIdescQK = idesc_bf16(kRows, kKT, false);  // B = K tile, K-major
 constexpr uint32_t kIdescPV = idesc_bf16(kRows, kD, true);    // B = V tile, MN-major
+constexpr uint32_t kIdescL = idesc_bf16(kRows, 16, false);    // B = ones [16 keys x 16]
 
 struct PrefillSmem {
-    uint8_t q[2][2][kHalf];   // [buffer][dims 0-63 | 64-127]
-    uint8_t k[2][2][kHalf];   // [stage][half]
-    uint8_t v[2][2][kHalf];
-    uint64_t q_full[2], q_empty[2];
-    uint64_t k_full[2], k_empty[2];
-    uint64_t v_full[2], v_empty[2];
+    uint8_t q[kQBufs][2][kHalf];    // [buffer][dims 0-63 | 64-127]
+    uint8_t k[kKStages][2][kHalf];  // [stage][half]
+    uint8_t v[kVStages][2][kHalf];
+    uint64_t q_full[kQBufs], q_empty[kQBufs];
+    uint64_t k_full[kKStages], k_empty[kKStages];
+    uint64_t v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2], s_free[2], p_full[2];
     uint64_t o_done;
     uint64_t mma_idle;
+    uint64_t xbar[2];                  // softmax half-row exchange rounds
+    float xchg[2][2][kRows];           // [round parity][half][row]
+    alignas(128) uint16_t ones[512];   // bf16 1.0: B operand of the row-sum MMA
     uint32_t tmem_base;
     int abort;
 };
@@ -148,16 +166,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     const int total = a.num_seqs * kHkv * qblocks;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kQBufs; ++i) {
             mbar_init(smem_u32(&sm.q_full[i]), 1);
             mbar_init(smem_u32(&sm.q_empty[i]), 1);
+        }
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(smem_u32(&sm.k_full[i]), 1);
             mbar_init(smem_u32(&sm.k_empty[i]), 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
             mbar_init(smem_u32(&sm.v_full[i]), 1);
             mbar_init(smem_u32(&sm.v_empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&sm.s_full[i]), 1);
-            mbar_init(smem_u32(&sm.s_free[i]), 4);   // one arrive per softmax warp
-            mbar_init(smem_u32(&sm.p_full[i]), 4);
+            mbar_init(smem_u32(&sm.s_free[i]), kSoftmaxWarps);   // one arrive per softmax warp
+            mbar_init(smem_u32(&sm.p_full[i]), kSoftmaxWarps);
+            mbar_init(smem_u32(&sm.xbar[i]), kSoftmaxWarps);
         }
         mbar_init(smem_u32(&sm.o_done), 1);
         mbar_init(smem_u32(&sm.mma_idle), 1);
@@ -173,89 +198,113 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == kProducerWarp) {
-        // ---------------------------------------------------------------- TMA producer
+    if (warp == kProducerWarp || warp == kVProducerWarp) {
+        // ---------------------------------------------------------------- TMA producers
+        // Two independent producers, so a K tile is requested as soon as its stage is
+        // free, never behind a V tile waiting for its own stage: warp 8 loads Q and K,
+        // warp 10 loads V.
         if (lane == 0) {
-            tma_prefetch_map(&q_map);
-            tma_prefetch_map(&k_map);
-            tma_prefetch_map(&v_map);
+            const bool qk = (warp == kProducerWarp);
+            if (qk) {
+                tma_prefetch_map(&q_map);
+                tma_prefetch_map(&k_map);
+            } else {
+                tma_prefetch_map(&v_map);
+            }
+            // The pools may be written by the kernel just before this one on the stream
+            // (kv_append lets us launch early): wait for it before the first load.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            uint64_t *full = qk ? sm.k_full : sm.v_full;
+            uint64_t *empty = qk ? sm.k_empty : sm.v_empty;
+            const int ns = qk ? kKStages : kVStages;
+            const CUtensorMap *map = qk ? &k_map : &v_map;
             int tcount = 0, it = 0;              // tiles / key tiles started
-            int q_issued = 0, k_issued = 0, v_issued = 0;
+            int q_issued = 0, kv_issued = 0;
             bool ok = true;
             for (int r = 0; ok; ++r) {
                 const int idx = snake(r, total);
                 if (idx < 0) break;
                 const Tile t = tile_at(a, idx, qblocks);
-                if (t.error) record_error(a.err, kErrDevice | kErrQLen);
+                if (qk && t.error) record_error(a.err, kErrDevice | kErrQLen);
                 if (!t.run) continue;
-                const int qbuf = tcount & 1;
-                if (tcount >= 2 &&
-                    !(ok = wait_or_abort(smem_u32(&sm.q_empty[qbuf]), ((tcount >> 1) - 1) & 1, abort_flag, a.err)))
-                    break;
-                const uint32_t qbar = smem_u32(&sm.q_full[qbuf]);
-                mbar_arrive_expect_tx(qbar, kTileBytes);
-                tma_load_3d(smem_u32(sm.q[qbuf][0]), &q_map, qbar, 0, t.g * kGroup, t.tok0);
-                tma_load_3d(smem_u32(sm.q[qbuf][1]), &q_map, qbar, 64, t.g * kGroup, t.tok0);
-                ++q_issued;
+                if (qk) {
+                    const int qbuf = tcount % kQBufs;
+                    if (tcount >= kQBufs &&
+                        !(ok = wait_or_abort(smem_u32(&sm.q_empty[qbuf]), ((tcount / kQBufs) - 1) & 1,
+                                             abort_flag, a.err)))
+                        break;
+                    const uint32_t qbar = smem_u32(&sm.q_full[qbuf]);
+                    mbar_arrive_expect_tx(qbar, kTileBytes);
+                    tma_load_3d(smem_u32(sm.q[qbuf][0]), &q_map, qbar, 0, t.g * kGroup, t.tok0);
+                    tma_load_3d(smem_u32(sm.q[qbuf][1]), &q_map, qbar, 64, t.g * kGroup, t.tok0);
+                    ++q_issued;
+                }
                 const int32_t *bt = a.block_table + (size_t)t.s * a.max_blocks_per_seq;
                 for (int j = 0; j < t.n_kt; ++j, ++it) {
-                    const int st = it & 1;
+                    const int st = it % ns;
                     int blk = __ldg(bt + (j >> 1));
                     if (blk < 0 || blk >= a.num_blocks) {
-                        record_error(a.err, kErrDevice | kErrBadBlock);
+                        if (qk) record_error(a.err, kErrDevice | kErrBadBlock);
                         blk = 0;   // stay inside the pool; the result is flagged as invalid
                     }
                     const int off = (j & 1) * kKT;
-                    if (it >= 2 &&
-                        !(ok = wait_or_abort(smem_u32(&sm.k_empty[st]), ((it >> 1) - 1) & 1, abort_flag, a.err)))
+                    if (it >= ns &&
+                        !(ok = wait_or_abort(smem_u32(&empty[st]), ((it / ns) - 1) & 1, abort_flag, a.err)))
                         break;
-                    const uint32_t kbar = smem_u32(&sm.k_full[st]);
-                    mbar_arrive_expect_tx(kbar, kTileBytes);
-                    tma_load_4d(smem_u32(sm.k[st][0]), &k_map, kbar, 0, t.g, off, blk);
-                    tma_load_4d(smem_u32(sm.k[st][1]), &k_map, kbar, 64, t.g, off, blk);
-                    ++k_issued;
-                    if (it >= 2 &&
-                        !(ok = wait_or_abort(smem_u32(&sm.v_empty[st]), ((it >> 1) - 1) & 1, abort_flag, a.err)))
-                        break;
-                    const uint32_t vbar = smem_u32(&sm.v_full[st]);
-                    mbar_arrive_expect_tx(vbar, kTileBytes);
-                    tma_load_4d(smem_u32(sm.v[st][0]), &v_map, vbar, 0, t.g, off, blk);
-                    tma_load_4d(smem_u32(sm.v[st][1]), &v_map, vbar, 64, t.g, off, blk);
-                    ++v_issued;
+                    const uint32_t bar = smem_u32(&full[st]);
+                    uint8_t (*dst)[kHalf] = qk ? sm.k[st] : sm.v[st];
+                    mbar_arrive_expect_tx(bar, kTileBytes);
+                    tma_load_4d(smem_u32(dst[0]), map, bar, 0, t.g, off, blk);
+                    tma_load_4d(smem_u32(dst[1]), map, bar, 64, t.g, off, blk);
+                    ++kv_issued;
                 }
                 ++tcount;
             }
             // Drain: no TMA copy may still be landing when the CTA exits.  In the normal
             // path every load has been consumed and these waits return at once.
-            for (int i = max(0, q_issued - 2); i < q_issued; ++i)
-                mbar_wait(smem_u32(&sm.q_full[i & 1]), (i >> 1) & 1);
-            for (int i = max(0, k_issued - 2); i < k_issued; ++i)
-                mbar_wait(smem_u32(&sm.k_full[i & 1]), (i >> 1) & 1);
-            for (int i = max(0, v_issued - 2); i < v_issued; ++i)
-                mbar_wait(smem_u32(&sm.v_full[i & 1]), (i >> 1) & 1);
+            for (int i = max(0, q_issued - kQBufs); i < q_issued; ++i)
+                mbar_wait(smem_u32(&sm.q_full[i % kQBufs]), (i / kQBufs) & 1);
+            for (int i = max(0, kv_issued - ns); i < kv_issued; ++i)
+                mbar_wait(smem_u32(&full[i % ns]), (i / ns) & 1);
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
+        // the ones tile of the row-sum MMA (written by the generic proxy, read by the MMA)
+        for (int i = lane; i < 512; i += 32) sm.ones[i] = 0x3F80;   // bf16 1.0
+        fence_proxy_async_smem();
+        __syncwarp();
         if (lane == 0) {
             int tcount = 0, it = 0;
             int pend_it = -1, pend_j = 0;   // O += P V still to issue for key tile pend_it
+            // Matrix descriptors are built once; per MMA only a constant is added to the
+            // start-address field (units of 16 bytes): +2 per 16 dims along a 128-byte row,
+            // +1024 per 64-dim half (16 KiB), +2048 per ring slot (32 KiB), +128 per 16
+            // keys of an MN-major V tile (2 KiB).
+            const uint64_t ones_desc = sdesc_noswizzle(smem_u32(sm.ones), 128, 256);
+            const uint64_t qd0 = sdesc_sw128(smem_u32(sm.q[0][0]), 16, 1024);
+            const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0][0]), 16, 1024);
+            const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0][0]), (uint32_t)kHalf, 1024);
             bool ok = true;
             auto issue_pv = [&](int pit, int pj) -> bool {
-                const int st = pit & 1;
-                if (!wait_or_abort(smem_u32(&sm.v_full[st]), (pit >> 1) & 1, abort_flag, a.err)) return false;
+                const int vs = pit % kVStages;   // V slot
+                const int st = pit & 1;          // S/P buffer
+                if (!wait_or_abort(smem_u32(&sm.v_full[vs]), (pit / kVStages) & 1, abort_flag, a.err)) return false;
                 if (!wait_or_abort(smem_u32(&sm.p_full[st]), (pit >> 1) & 1, abort_flag, a.err)) return false;
                 tc_fence_after();
-                const uint32_t v0 = smem_u32(sm.v[st][0]);
+                // O += P V and L += P 1, 16 keys per step; V is [128 keys][128 dims] with dims
+                // contiguous (MN-major), its two 64-dim halves 16 KiB apart.
+                const uint64_t vb = vd0 + (uint64_t)(vs * 2048);
+                const uint32_t pa = tmem + col_s(st);
+                const uint32_t acc0 = pj > 0 ? 1u : 0u;
+                umma_ts(tmem + kColO, pa, vb, kIdescPV, acc0);
+                umma_ts(tmem + kColL, pa, ones_desc, kIdescL, acc0);
 #pragma unroll
-                for (int kk = 0; kk < kKT / 16; ++kk) {
-                    // V tile [128 keys][128 dims], dims contiguous (MN-major): 16 keys per step
-                    // = two 8-row swizzle atoms (2 KiB); the dim halves are 16 KiB apart.
-                    const uint64_t bdesc = sdesc_sw128(v0 + kk * 2048, (uint32_t)kHalf, 1024);
-                    umma_ts(tmem + kColO, tmem + col_p(st) + kk * 8, bdesc, kIdescPV,
-                            (pj > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 1; kk < kKT / 16; ++kk) {
+                    umma_ts_c<true>(tmem + kColO, pa + kk * 8, vb + (uint64_t)(kk * 128), kIdescPV);
+                    umma_ts_c<true>(tmem + kColL, pa + kk * 8, ones_desc, kIdescL);
                 }
                 umma_commit(smem_u32(&sm.o_done));
-                umma_commit(smem_u32(&sm.v_empty[st]));
+                umma_commit(smem_u32(&sm.v_empty[vs]));
                 return true;
             };
             for (int r = 0; ok; ++r) {
@@ -263,30 +312,30 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                 if (idx < 0) break;
                 const Tile t = tile_at(a, idx, qblocks);
                 if (!t.run) continue;
-                const int qbuf = tcount & 1;
-                if (!(ok = wait_or_abort(smem_u32(&sm.q_full[qbuf]), (tcount >> 1) & 1, abort_flag, a.err)))
+                const int qbuf = tcount % kQBufs;
+                if (!(ok = wait_or_abort(smem_u32(&sm.q_full[qbuf]), (tcount / kQBufs) & 1, abort_flag, a.err)))
                     break;
                 for (int j = 0; j < t.n_kt; ++j, ++it) {
-                    const int st = it & 1;
-                    if (!(ok = wait_or_abort(smem_u32(&sm.k_full[st]), (it >> 1) & 1, abort_flag, a.err))) break;
+                    const int st = it & 1;            // S/P buffer
+                    const int ks = it % kKStages;     // K slot
+                    if (!(ok = wait_or_abort(smem_u32(&sm.k_full[ks]), (it / kKStages) & 1, abort_flag, a.err)))
+                        break;
                     if (it >= 2 &&
                         !(ok = wait_or_abort(smem_u32(&sm.s_free[st]), ((it >> 1) - 1) & 1, abort_flag, a.err)))
                         break;
                     tc_fence_after();
-                    const uint32_t q0 = smem_u32(sm.q[qbuf][0]);
-                    const uint32_t q1 = smem_u32(sm.q[qbuf][1]);
-                    const uint32_t k0 = smem_u32(sm.k[st][0]);
-                    const uint32_t k1 = smem_u32(sm.k[st][1]);
+                    // S = Q K^T over 128 dims in 8 steps of 16 (K-major, 128-byte swizzle)
+                    const uint64_t qa = qd0 + (uint64_t)(qbuf * 2048);
+                    const uint64_t kb = kd0 + (uint64_t)(ks * 2048);
+                    const uint32_t sd = tmem + col_s(st);
+                    umma_ss_c<false>(sd, qa, kb, kIdescQK);
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        // K-major, 128-byte swizzle: 16 dims = 32 bytes along the row
-                        const uint32_t off = (kk & 3) * 32;
-                        const uint64_t adesc = sdesc_sw128((kk < 4 ? q0 : q1) + off, 16, 1024);
-                        const uint64_t bdesc = sdesc_sw128((kk < 4 ? k0 : k1) + off, 16, 1024);
-                        umma_ss(tmem + col_s(st), adesc, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
+                    for (int kk = 1; kk < kD / 16; ++kk) {
+                        const uint64_t off = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);
+                        umma_ss_c<true>(sd, qa + off, kb + off, kIdescQK);
                     }
                     umma_commit(smem_u32(&sm.s_full[st]));
-                    umma_commit(smem_u32(&sm.k_empty[st]));
+                    umma_commit(smem_u32(&sm.k_empty[ks]));
                     if (j == t.n_kt - 1) umma_commit(smem_u32(&sm.q_empty[qbuf]));
                     if (pend_it >= 0 && !(ok = issue_pv(pend_it, pend_j))) break;
                     pend_it = it;
@@ -301,67 +350,87 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         }
     } else {
         // ---------------------------------------------------------------- softmax warps
-        const int row = warp * 32 + lane;          // MMA row == TMEM lane
+        // Two warpgroups share every score row: warpgroup ch (= warp / 4) owns columns
+        // ch*64 .. ch*64+63 of S and O and keys ch*64 .. ch*64+63 of P for the row
+        // (= TMEM lane) row.  The two halves of a row exchange their maxima through
+        // shared memory, synchronised by an mbarrier per exchange round.
+        const int ch = warp >> 2;                  // column half
+        const int row = (warp & 3) * 32 + lane;    // MMA row == TMEM lane
         const int pl = row >> 2;                   // query position within the tile
         const int hl = row & 3;                    // query head within the group
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const float sl2 = a.scale_log2;
         int it = 0;
+        int xc = 0;                                // exchange rounds so far
         bool ok = true;
+        // Publish v for this row, wait for all 8 warps, return the other half's value.
+        auto exchange = [&](float v, bool &good) -> float {
+            const int buf = xc & 1;
+            sm.xchg[buf][ch][row] = v;
+            tc_fence_before();       // this warp's tcgen05.ld of S precede the other half's P stores
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.xbar[buf]));
+            good = wait_or_abort(smem_u32(&sm.xbar[buf]), (xc >> 1) & 1, abort_flag, a.err);
+            good = __all_sync(0xffffffffu, good);
+            tc_fence_after();
+            const float other = sm.xchg[buf][ch ^ 1][row];
+            ++xc;
+            return other;
+        };
         for (int r = 0; ok; ++r) {
             const int idx = snake(r, total);
             if (idx < 0) break;
             const Tile t = tile_at(a, idx, qblocks);
             if (!t.run) continue;
             const int pos = t.pos0 + pl;
-            float m = -INFINITY, l = 0.f;
+            float m = -INFINITY;                   // running max, log2 units (scaled)
             for (int j = 0; j < t.n_kt; ++j, ++it) {
                 const int st = it & 1;
                 ok = wait_or_abort(smem_u32(&sm.s_full[st]), (it >> 1) & 1, abort_flag, a.err);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t x[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + col_s(st) + c * 32, x[c]);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_wait_ld(x[c]);
+                uint32_t x[2][32];
+                tmem_ld32(lane_base + col_s(st) + ch * 64, x[0]);
+                tmem_ld32(lane_base + col_s(st) + ch * 64 + 32, x[1]);
+                tmem_wait_ld(x[0]);
+                tmem_wait_ld(x[1]);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sm.s_free[st]));
 
-                // scaled scores (log2 units), causal mask on the tiles that reach past
-                // this tile's first query position
+                // causal mask (only on tiles reaching past the tile's first query position)
+                // and the row maximum of the raw scores
+                const int key0 = j * kKT + ch * 64;
                 const bool need_mask = (j * kKT + kKT - 1) > t.pos0;
+                if (need_mask) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if ((key0 + c * 32 + e) > pos) x[c][e] = __float_as_uint(-INFINITY);
+                }
                 float rmax = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float v = __uint_as_float(x[c][e]) * a.scale_log2;
-                        if (need_mask && (j * kKT + c * 32 + e) > pos) v = -INFINITY;
-                        x[c][e] = __float_as_uint(v);
-                        rmax = fmaxf(rmax, v);
-                    }
-                }
-                const float m_new = fmaxf(m, rmax);
+                    for (int e = 0; e < 32; e += 2)
+                        rmax = fmax3(rmax, __uint_as_float(x[c][e]), __uint_as_float(x[c][e + 1]));
+                rmax = fmaxf(rmax, exchange(rmax, ok));
+                if (!ok) break;
+                const float m_new = fmaxf(m, rmax * sl2);
                 const bool rescale = m_new > m + kRescaleThreshold;   // also when m == -inf
                 const float m_use = rescale ? m_new : m;
                 const float alpha = rescale ? fast_exp2(m - m_new) : 1.f;
-                float rsum = 0.f;
-                uint32_t pk[2][32];
+                uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float p0 = fast_exp2(__uint_as_float(x[c][e]) - m_use);
-                        const float p1 = fast_exp2(__uint_as_float(x[c][e + 1]) - m_use);
-                        const uint32_t pp = pack_bf16x2(p0, p1);
-                        // the row sum uses the same bf16-rounded weights the PV product uses,
-                        // so the normalised weights sum to one exactly (up to fp32 rounding)
-                        rsum += bf16_lo(pp) + bf16_hi(pp);
-                        pk[c >> 1][(c & 1) * 16 + e / 2] = pp;
+                        const float p0 = fast_exp2(fmaf(__uint_as_float(x[c][e]), sl2, -m_use));
+                        const float p1 = fast_exp2(fmaf(__uint_as_float(x[c][e + 1]), sl2, -m_use));
+                        pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
                     }
                 }
-                l = l * alpha + rsum;
                 m = m_use;
 
                 if (j > 0) {
@@ -372,13 +441,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                     tc_fence_after();
                     if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < 2; ++c) {
                             uint32_t o[32];
-                            tmem_ld32(lane_base + kColO + c * 32, o);
+                            tmem_ld32(lane_base + kColO + ch * 64 + c * 32, o);
                             tmem_wait_ld(o);
 #pragma unroll
                             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tmem_st32(lane_base + kColO + c * 32, o);
+                            tmem_st32(lane_base + kColO + ch * 64 + c * 32, o);
+                        }
+                        if (ch == 0) {   // the row sum (its first column) scales with O
+                            uint32_t lv = tmem_ld1(lane_base + kColL);
+                            tmem_wait_ld1(lv);
+                            tmem_st1(lane_base + kColL, __float_as_uint(__uint_as_float(lv) * alpha));
                         }
                     }
                 }
@@ -386,21 +460,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                 // anything, NaN included; P is 0 there but 0 * NaN is not, so zero them.
                 const int kv_valid = t.seq_len - j * kKT;
                 if (kv_valid < kKT) {
-                    ok = wait_or_abort(smem_u32(&sm.v_full[st]), (it >> 1) & 1, abort_flag, a.err);
+                    const int vs = it % kVStages;
+                    ok = wait_or_abort(smem_u32(&sm.v_full[vs]), (it / kVStages) & 1, abort_flag, a.err);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     if (row >= kv_valid) {
-                        uint4 *r0 = reinterpret_cast<uint4 *>(sm.v[st][0] + row * 128);
-                        uint4 *r1 = reinterpret_cast<uint4 *>(sm.v[st][1] + row * 128);
+                        uint4 *rv = reinterpret_cast<uint4 *>(sm.v[vs][ch] + row * 128);
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            r0[v] = make_uint4(0u, 0u, 0u, 0u);
-                            r1[v] = make_uint4(0u, 0u, 0u, 0u);
-                        }
+                        for (int v = 0; v < 8; ++v) rv[v] = make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();   // generic writes -> visible to the MMA's reads
                 }
-                tmem_st32(lane_base + col_p(st), pk[0]);
-                tmem_st32(lane_base + col_p(st) + 32, pk[1]);
+                tmem_st32(lane_base + col_s(st) + ch * 32, pk);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -412,14 +482,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             ok = wait_or_abort(smem_u32(&sm.o_done), (it - 1) & 1, abort_flag, a.err);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            const float inv_l = 1.f / l;
+            uint32_t lbits = tmem_ld1(lane_base + kColL);
+            tmem_wait_ld1(lbits);
+            const float l_row = __uint_as_float(lbits);
+            const float inv_l = 1.f / l_row;
             const bool row_ok = pl < t.rows;
             __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
-                                 ((size_t)(t.tok0 + pl) * kHq + t.g * kGroup + hl) * kD;
+                                 ((size_t)(t.tok0 + pl) * kHq + t.g * kGroup + hl) * kD + ch * 64;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t o[32];
-                tmem_ld32(lane_base + kColO + c * 32, o);
+                tmem_ld32(lane_base + kColO + ch * 64 + c * 32, o);
                 tmem_wait_ld(o);
                 uint32_t w[16];
 #pragma unroll
@@ -431,8 +504,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                     for (int v = 0; v < 4; ++v) d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
                 }
             }
-            if (row_ok && a.lse)
-                a.lse[(size_t)(t.tok0 + pl) * kHq + t.g * kGroup + hl] = (m + __log2f(l)) * kLn2;
+            if (row_ok && ch == 0 && a.lse)
+                a.lse[(size_t)(t.tok0 + pl) * kHq + t.g * kGroup + hl] = (m + __log2f(l_row)) * kLn2;
             tc_fence_before();
         }
     }
@@ -473,8 +546,18 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map, const
     }
     const long long tiles = (long long)a.num_seqs * kHkv * ((a.max_q_len + kQPos - 1) / kQPos);
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-    prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(q_map, k_map, v_map, a);
-    return cudaGetLastError();
+    // Programmatic dependent launch (see decode): the producer waits before its loads.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_kernel, q_map, k_map, v_map, a);
 }
 
 cudaError_t launch_wait_selftest(uint32_t *err, uint64_t limit_ns, cudaStream_t stream) {
