@@ -13,28 +13,30 @@
 // The pages' FlashAttention-2 loop renormalises nothing between key tiles; here the
 // running max/sum of the online softmax does that (the plain definition is the target).
 //
-// Work tile: 32 query positions x the 4 query heads of one KV head = 128 MMA rows
-// (row r = position (r / 4), head (r % 4)), so every K/V tile fetched serves 4 heads.
-// Key/value tiles are 128 tokens (half a cache block) fetched by TMA straight from
-// the paged pool: the block table lookup is the TMA coordinate.
+// Work unit: 64 query positions x the 4 query heads of one KV head, split into two
+// MMA tiles A and B of 128 rows (row r = position r / 4, head r % 4 within the tile).
+// Key/value tiles are 128 tokens (half a cache block) fetched by TMA straight from the
+// paged pool: the block-table lookup is the TMA coordinate.  Both query tiles consume
+// every K/V tile the unit fetches, so a CTA moves 64 KiB of K/V from L2 per 256 x 128
+// score block; at 128 rows per K/V tile the L2-to-SM delivery (not the tensor core) was
+// the limit.
 //
-// CTA = 11 warps, persistent (one per SM), tiles dealt in a snake order, latest query
+// CTA = 11 warps, persistent (one per SM), units dealt in a snake order, latest query
 // blocks (most keys) first:
-//   warps 0-7  softmax + epilogue in two warpgroups; warp w owns MMA rows (= TMEM
-//              lanes) 32*(w%4) .. +31, columns 64*(w/4) .. +63 of each
-//   warp 8     TMA producer of Q and K (ring of 2 stages)
-//   warp 9     TMEM allocator and the single-thread tcgen05.mma issuer
-//   warp 10    TMA producer of V (ring of 3 stages)
-// Tensor memory (512 columns): S0, S1 (fp32 scores, 128 cols each), O (fp32, 128),
-// L (fp32 row sums, 16).  P (bf16, packed in pairs) is written over the first 64
-// columns of the S buffer it came from.
-// Per key tile:  S = Q K^T (SS-MMA)  ->  softmax reads S, writes P (bf16) into TMEM
-// and, when its running max rose by more than 2^8, rescales O and L  ->  O += P V
-// (TS-MMA, P from TMEM, V from shared memory, MN-major) and L += P 1 (TS-MMA against a
-// ones tile: the row sums of exactly the bf16 weights that multiply V).  The MMA warp
-// issues S for tile j+1 before O += P V for tile j, so the tensor core works while the
-// softmax runs; tcgen05.mma ops of one thread execute in issue order, so S for tile
-// j+2 cannot overwrite P of tile j before O += P V of tile j has read it.
+//   warps 0-3   softmax + epilogue of tile A; thread = one row (= TMEM lane) of A
+//   warps 4-7   softmax + epilogue of tile B
+//   warp 8      TMA producer of Q and K (ring of 2 slots)
+//   warp 9      TMEM allocator and the single-thread tcgen05.mma issuer
+//   warp 10     TMA producer of V (ring of 2 slots)
+// Tensor memory (512 columns): S_A, S_B (fp32 scores), O_A, O_B (fp32 output), 128
+// columns each.  P (bf16, packed in pairs) is written over the first 64 columns of its
+// own S buffer.  Per key tile j the MMA thread issues, in this order,
+//     S_A(j) = Q_A K_j^T,  O_B += P_B(j-1) V_{j-1},  S_B(j) = Q_B K_j^T,  O_A += P_A(j) V_j
+// so the tensor core computes one tile's products while the other tile's softmax runs.
+// tcgen05.mma operations of one thread execute in issue order, hence S_X(j+1) cannot
+// overwrite P_X(j) before O_X += P_X(j) V_j has read it.  The softmax keeps a running
+// max and, only when it grows by more than 2^8, rescales O (lazy rescaling); the row
+// sum accumulates the same bf16-rounded weights the PV product uses.
 // Every wait is bounded; on expiry the CTA records PA_ERR_TIMEOUT, unwinds, waits
 // (bounded) for its own copies and MMAs, frees tensor memory and exits.
 #include "common.cuh"
@@ -43,66 +45,57 @@
 namespace pa {
 namespace {
 
-constexpr int kRows = 128;                  // MMA M
-constexpr int kKT = kPrefillKvTile;         // keys per tile (MMA N of S, K of PV)
-constexpr int kQPos = kPrefillQPositions;   // query positions per tile
-constexpr int kSoftmaxWarps = 8;            // two warpgroups, one per half of each row
-constexpr int kProducerWarp = 8;            // Q and K loads
+constexpr int kRows = 128;                    // MMA M (one query tile)
+constexpr int kKT = kPrefillKvTile;           // keys per K/V tile (MMA N of S, K of PV)
+constexpr int kTilePos = kPrefillQPositions;  // query positions per MMA tile (32)
+constexpr int kUnitPos = 2 * kTilePos;        // query positions per work unit (64)
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarp = 8;              // Q and K loads
 constexpr int kMmaWarp = 9;
-constexpr int kVProducerWarp = 10;          // V loads
+constexpr int kVProducerWarp = 10;            // V loads
 constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128;   // score buffers; P (bf16 pairs) is written
-                                               // over the first 64 columns of its own S
-constexpr uint32_t kColO = 256;                // output accumulator
-constexpr uint32_t kColL = 384;                // row sums of P (16 equal columns)
-__device__ __forceinline__ uint32_t col_s(int st) { return st ? kColS1 : kColS0; }
-constexpr int kHalf = kRows * 128;          // 128 rows x 64 dims x 2 B = 16 KiB
-// Shared-memory rings (32 KiB per slot).  The V ring is the deepest: V of key tile j
-// may only be requested once O += P V of tile j-3 has finished with its slot, and an
-// L2-served 32 KiB load takes over a microsecond under this load.
-constexpr int kQBufs = 1;
+constexpr int kHalf = kRows * 128;            // 128 rows x 64 dims x 2 B = 16 KiB
+constexpr uint32_t kTileBytes = 2 * kHalf;    // a full 128 x 128 bf16 tile
 constexpr int kKStages = 2;
-constexpr int kVStages = 3;
-constexpr uint32_t kTileBytes = 2 * kHalf;  // a full 128 x 128 bf16 tile
-constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows > 2^8
+constexpr int kVStages = 2;
+constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when the max grows > 2^8
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr uint32_t kIdescQK = idesc_bf16(kRows, kKT, false);  // B = K tile, K-major
 constexpr uint32_t kIdescPV = idesc_bf16(kRows, kD, true);    // B = V tile, MN-major
-constexpr uint32_t kIdescL = idesc_bf16(kRows, 16, false);    // B = ones [16 keys x 16]
+
+// TMEM columns of query tile x (0 = A, 1 = B): S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511
+__device__ __forceinline__ uint32_t col_s(int x) { return x ? 128u : 0u; }
+__device__ __forceinline__ uint32_t col_o(int x) { return x ? 384u : 256u; }
 
 struct PrefillSmem {
-    uint8_t q[kQBufs][2][kHalf];    // [buffer][dims 0-63 | 64-127]
-    uint8_t k[kKStages][2][kHalf];  // [stage][half]
+    uint8_t q[2][2][kHalf];          // [tile A|B][dims 0-63 | 64-127]
+    uint8_t k[kKStages][2][kHalf];   // [slot][half]
     uint8_t v[kVStages][2][kHalf];
-    uint64_t q_full[kQBufs], q_empty[kQBufs];
+    uint64_t q_full, q_empty;
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t v_full[kVStages], v_empty[kVStages];
-    uint64_t s_full[2], s_free[2], p_full[2];
-    uint64_t o_done;
+    uint64_t s_full[2], p_full[2], o_done[2];   // per query tile
     uint64_t mma_idle;
-    uint64_t xbar[2];                  // softmax half-row exchange rounds
-    float xchg[2][2][kRows];           // [round parity][half][row]
-    alignas(128) uint16_t ones[512];   // bf16 1.0: B operand of the row-sum MMA
     uint32_t tmem_base;
     int abort;
 };
 
 constexpr size_t kSmemBytes = sizeof(PrefillSmem) + 1024;
 
-struct Tile {
+struct Unit {
     bool run;       // has work
     bool error;     // inconsistent lengths (recorded once, then skipped)
     int s, g;
-    int tok0;       // row of q/out holding the tile's first query position
-    int rows;       // real positions in this tile (1..32)
-    int pos0;       // absolute position of the tile's first query
+    int tok0;       // row of q/out holding the unit's first query position
+    int positions;  // real positions in this unit (1..64)
+    int pos0;       // absolute position of the unit's first query
     int seq_len;    // context length (keys 0 .. seq_len-1 exist)
     int n_kt;       // key tiles to visit: 0 .. (last position) / 128
 };
 
-__device__ __forceinline__ Tile tile_at(const PrefillArgs &a, int idx, int qblocks) {
-    Tile t;
+__device__ __forceinline__ Unit unit_at(const PrefillArgs &a, int idx, int qblocks) {
+    Unit t;
     const int per_qb = a.num_seqs * kHkv;
     const int qb = qblocks - 1 - idx / per_qb;   // latest query block first
     const int rem = idx - (idx / per_qb) * per_qb;
@@ -119,17 +112,17 @@ __device__ __forceinline__ Tile tile_at(const PrefillArgs &a, int idx, int qbloc
         t.error = true;
         return t;
     }
-    if (qb * kQPos >= q_len) return t;
+    if (qb * kUnitPos >= q_len) return t;
     t.run = true;
-    t.tok0 = c0 + qb * kQPos;
-    t.rows = min(kQPos, q_len - qb * kQPos);
-    t.pos0 = seq_len - q_len + qb * kQPos;
+    t.tok0 = c0 + qb * kUnitPos;
+    t.positions = min(kUnitPos, q_len - qb * kUnitPos);
+    t.pos0 = seq_len - q_len + qb * kUnitPos;
     t.seq_len = seq_len;
-    t.n_kt = (t.pos0 + t.rows - 1) / kKT + 1;
+    t.n_kt = (t.pos0 + t.positions - 1) / kKT + 1;
     return t;
 }
 
-// Index of this CTA's r-th tile in the snake order (or -1 past the end).
+// Index of this CTA's r-th unit in the snake order (or -1 past the end).
 __device__ __forceinline__ int snake(int r, int total) {
     const int G = gridDim.x;
     const int idx = r * G + ((r & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
@@ -162,14 +155,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     volatile int *abort_flag = &sm.abort;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int qblocks = (a.max_q_len + kQPos - 1) / kQPos;
+    const int qblocks = (a.max_q_len + kUnitPos - 1) / kUnitPos;
     const int total = a.num_seqs * kHkv * qblocks;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kQBufs; ++i) {
-            mbar_init(smem_u32(&sm.q_full[i]), 1);
-            mbar_init(smem_u32(&sm.q_empty[i]), 1);
-        }
+        mbar_init(smem_u32(&sm.q_full), 1);
+        mbar_init(smem_u32(&sm.q_empty), 1);
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(smem_u32(&sm.k_full[i]), 1);
             mbar_init(smem_u32(&sm.k_empty[i]), 1);
@@ -178,13 +169,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             mbar_init(smem_u32(&sm.v_full[i]), 1);
             mbar_init(smem_u32(&sm.v_empty[i]), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&sm.s_full[i]), 1);
-            mbar_init(smem_u32(&sm.s_free[i]), kSoftmaxWarps);   // one arrive per softmax warp
-            mbar_init(smem_u32(&sm.p_full[i]), kSoftmaxWarps);
-            mbar_init(smem_u32(&sm.xbar[i]), kSoftmaxWarps);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(smem_u32(&sm.s_full[x]), 1);
+            mbar_init(smem_u32(&sm.p_full[x]), 4);   // the 4 warps of the tile's softmax
+            mbar_init(smem_u32(&sm.o_done[x]), 1);
         }
-        mbar_init(smem_u32(&sm.o_done), 1);
         mbar_init(smem_u32(&sm.mma_idle), 1);
         sm.abort = 0;
         fence_barrier_init();
@@ -200,9 +189,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 
     if (warp == kProducerWarp || warp == kVProducerWarp) {
         // ---------------------------------------------------------------- TMA producers
-        // Two independent producers, so a K tile is requested as soon as its stage is
-        // free, never behind a V tile waiting for its own stage: warp 8 loads Q and K,
-        // warp 10 loads V.
+        // Two independent producers, so a K tile is requested as soon as its slot is
+        // free, never behind a V tile waiting for its own slot.
         if (lane == 0) {
             const bool qk = (warp == kProducerWarp);
             if (qk) {
@@ -218,25 +206,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             uint64_t *empty = qk ? sm.k_empty : sm.v_empty;
             const int ns = qk ? kKStages : kVStages;
             const CUtensorMap *map = qk ? &k_map : &v_map;
-            int tcount = 0, it = 0;              // tiles / key tiles started
+            int tcount = 0, it = 0;              // units / key tiles started
             int q_issued = 0, kv_issued = 0;
             bool ok = true;
             for (int r = 0; ok; ++r) {
                 const int idx = snake(r, total);
                 if (idx < 0) break;
-                const Tile t = tile_at(a, idx, qblocks);
+                const Unit t = unit_at(a, idx, qblocks);
                 if (qk && t.error) record_error(a.err, kErrDevice | kErrQLen);
                 if (!t.run) continue;
                 if (qk) {
-                    const int qbuf = tcount % kQBufs;
-                    if (tcount >= kQBufs &&
-                        !(ok = wait_or_abort(smem_u32(&sm.q_empty[qbuf]), ((tcount / kQBufs) - 1) & 1,
-                                             abort_flag, a.err)))
+                    if (tcount >= 1 &&
+                        !(ok = wait_or_abort(smem_u32(&sm.q_empty), (tcount - 1) & 1, abort_flag, a.err)))
                         break;
-                    const uint32_t qbar = smem_u32(&sm.q_full[qbuf]);
-                    mbar_arrive_expect_tx(qbar, kTileBytes);
-                    tma_load_3d(smem_u32(sm.q[qbuf][0]), &q_map, qbar, 0, t.g * kGroup, t.tok0);
-                    tma_load_3d(smem_u32(sm.q[qbuf][1]), &q_map, qbar, 64, t.g * kGroup, t.tok0);
+                    const uint32_t qbar = smem_u32(&sm.q_full);
+                    mbar_arrive_expect_tx(qbar, 2 * kTileBytes);
+                    for (int x = 0; x < 2; ++x) {
+                        tma_load_3d(smem_u32(sm.q[x][0]), &q_map, qbar, 0, t.g * kGroup, t.tok0 + x * kTilePos);
+                        tma_load_3d(smem_u32(sm.q[x][1]), &q_map, qbar, 64, t.g * kGroup, t.tok0 + x * kTilePos);
+                    }
                     ++q_issued;
                 }
                 const int32_t *bt = a.block_table + (size_t)t.s * a.max_blocks_per_seq;
@@ -262,237 +250,205 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             }
             // Drain: no TMA copy may still be landing when the CTA exits.  In the normal
             // path every load has been consumed and these waits return at once.
-            for (int i = max(0, q_issued - kQBufs); i < q_issued; ++i)
-                mbar_wait(smem_u32(&sm.q_full[i % kQBufs]), (i / kQBufs) & 1);
+            if (q_issued > 0) mbar_wait(smem_u32(&sm.q_full), (q_issued - 1) & 1);
             for (int i = max(0, kv_issued - ns); i < kv_issued; ++i)
                 mbar_wait(smem_u32(&full[i % ns]), (i / ns) & 1);
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
-        // the ones tile of the row-sum MMA (written by the generic proxy, read by the MMA)
-        for (int i = lane; i < 512; i += 32) sm.ones[i] = 0x3F80;   // bf16 1.0
-        fence_proxy_async_smem();
-        __syncwarp();
         if (lane == 0) {
-            int tcount = 0, it = 0;
-            int pend_it = -1, pend_j = 0;   // O += P V still to issue for key tile pend_it
             // Matrix descriptors are built once; per MMA only a constant is added to the
             // start-address field (units of 16 bytes): +2 per 16 dims along a 128-byte row,
-            // +1024 per 64-dim half (16 KiB), +2048 per ring slot (32 KiB), +128 per 16
-            // keys of an MN-major V tile (2 KiB).
-            const uint64_t ones_desc = sdesc_noswizzle(smem_u32(sm.ones), 128, 256);
+            // +1024 per 64-dim half (16 KiB), +2048 per tile or ring slot (32 KiB), +128 per
+            // 16 keys of an MN-major V tile (2 KiB).
             const uint64_t qd0 = sdesc_sw128(smem_u32(sm.q[0][0]), 16, 1024);
             const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0][0]), 16, 1024);
             const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0][0]), (uint32_t)kHalf, 1024);
+            int tcount = 0, it = 0;
+            int pend_it = -1, pend_j = 0;   // O_B += P_B V still to issue for key tile pend_it
             bool ok = true;
-            auto issue_pv = [&](int pit, int pj) -> bool {
-                const int vs = pit % kVStages;   // V slot
-                const int st = pit & 1;          // S/P buffer
-                if (!wait_or_abort(smem_u32(&sm.v_full[vs]), (pit / kVStages) & 1, abort_flag, a.err)) return false;
-                if (!wait_or_abort(smem_u32(&sm.p_full[st]), (pit >> 1) & 1, abort_flag, a.err)) return false;
-                tc_fence_after();
-                // O += P V and L += P 1, 16 keys per step; V is [128 keys][128 dims] with dims
-                // contiguous (MN-major), its two 64-dim halves 16 KiB apart.
-                const uint64_t vb = vd0 + (uint64_t)(vs * 2048);
-                const uint32_t pa = tmem + col_s(st);
-                const uint32_t acc0 = pj > 0 ? 1u : 0u;
-                umma_ts(tmem + kColO, pa, vb, kIdescPV, acc0);
-                umma_ts(tmem + kColL, pa, ones_desc, kIdescL, acc0);
+            // S_x = Q_x K^T over 128 dims in 8 steps of 16 (K-major, 128-byte swizzle)
+            auto issue_s = [&](int x, int ks) {
+                const uint64_t qa = qd0 + (uint64_t)(x * 2048);
+                const uint64_t kb = kd0 + (uint64_t)(ks * 2048);
+                const uint32_t sd = tmem + col_s(x);
+                umma_ss_c<false>(sd, qa, kb, kIdescQK);
 #pragma unroll
-                for (int kk = 1; kk < kKT / 16; ++kk) {
-                    umma_ts_c<true>(tmem + kColO, pa + kk * 8, vb + (uint64_t)(kk * 128), kIdescPV);
-                    umma_ts_c<true>(tmem + kColL, pa + kk * 8, ones_desc, kIdescL);
+                for (int kk = 1; kk < kD / 16; ++kk) {
+                    const uint64_t off = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);
+                    umma_ss_c<true>(sd, qa + off, kb + off, kIdescQK);
                 }
-                umma_commit(smem_u32(&sm.o_done));
-                umma_commit(smem_u32(&sm.v_empty[vs]));
+                umma_commit(smem_u32(&sm.s_full[x]));
+            };
+            // O_x += P_x V over 128 keys in 8 steps of 16; V is [128 keys][128 dims] with dims
+            // contiguous (MN-major), its two 64-dim halves 16 KiB apart.
+            auto issue_pv = [&](int x, int pit, int pj) -> bool {
+                const int vs = pit % kVStages;
+                if (!wait_or_abort(smem_u32(&sm.v_full[vs]), (pit / kVStages) & 1, abort_flag, a.err)) return false;
+                if (!wait_or_abort(smem_u32(&sm.p_full[x]), pit & 1, abort_flag, a.err)) return false;
+                tc_fence_after();
+                const uint64_t vb = vd0 + (uint64_t)(vs * 2048);
+                const uint32_t pa = tmem + col_s(x);
+                umma_ts(tmem + col_o(x), pa, vb, kIdescPV, pj > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 1; kk < kKT / 16; ++kk)
+                    umma_ts_c<true>(tmem + col_o(x), pa + kk * 8, vb + (uint64_t)(kk * 128), kIdescPV);
+                umma_commit(smem_u32(&sm.o_done[x]));
+                if (x == 1) umma_commit(smem_u32(&sm.v_empty[vs]));   // B is the V tile's last reader
                 return true;
             };
             for (int r = 0; ok; ++r) {
                 const int idx = snake(r, total);
                 if (idx < 0) break;
-                const Tile t = tile_at(a, idx, qblocks);
+                const Unit t = unit_at(a, idx, qblocks);
                 if (!t.run) continue;
-                const int qbuf = tcount % kQBufs;
-                if (!(ok = wait_or_abort(smem_u32(&sm.q_full[qbuf]), (tcount / kQBufs) & 1, abort_flag, a.err)))
-                    break;
+                if (!(ok = wait_or_abort(smem_u32(&sm.q_full), tcount & 1, abort_flag, a.err))) break;
                 for (int j = 0; j < t.n_kt; ++j, ++it) {
-                    const int st = it & 1;            // S/P buffer
-                    const int ks = it % kKStages;     // K slot
+                    const int ks = it % kKStages;
                     if (!(ok = wait_or_abort(smem_u32(&sm.k_full[ks]), (it / kKStages) & 1, abort_flag, a.err)))
                         break;
-                    if (it >= 2 &&
-                        !(ok = wait_or_abort(smem_u32(&sm.s_free[st]), ((it >> 1) - 1) & 1, abort_flag, a.err)))
-                        break;
                     tc_fence_after();
-                    // S = Q K^T over 128 dims in 8 steps of 16 (K-major, 128-byte swizzle)
-                    const uint64_t qa = qd0 + (uint64_t)(qbuf * 2048);
-                    const uint64_t kb = kd0 + (uint64_t)(ks * 2048);
-                    const uint32_t sd = tmem + col_s(st);
-                    umma_ss_c<false>(sd, qa, kb, kIdescQK);
-#pragma unroll
-                    for (int kk = 1; kk < kD / 16; ++kk) {
-                        const uint64_t off = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);
-                        umma_ss_c<true>(sd, qa + off, kb + off, kIdescQK);
-                    }
-                    umma_commit(smem_u32(&sm.s_full[st]));
+                    issue_s(0, ks);                                        // S_A(j)
+                    if (pend_it >= 0 && !(ok = issue_pv(1, pend_it, pend_j))) break;   // O_B, tile j-1
+                    issue_s(1, ks);                                        // S_B(j)
                     umma_commit(smem_u32(&sm.k_empty[ks]));
-                    if (j == t.n_kt - 1) umma_commit(smem_u32(&sm.q_empty[qbuf]));
-                    if (pend_it >= 0 && !(ok = issue_pv(pend_it, pend_j))) break;
+                    if (j == t.n_kt - 1) umma_commit(smem_u32(&sm.q_empty));
+                    if (!(ok = issue_pv(0, it, j))) break;                 // O_A, tile j
                     pend_it = it;
                     pend_j = j;
                 }
                 ++tcount;
             }
-            if (ok && pend_it >= 0) issue_pv(pend_it, pend_j);
+            if (ok && pend_it >= 0) issue_pv(1, pend_it, pend_j);
             // Every MMA issued must have finished before tensor memory is released.
             umma_commit(smem_u32(&sm.mma_idle));
             mbar_wait(smem_u32(&sm.mma_idle), 0);
         }
     } else {
         // ---------------------------------------------------------------- softmax warps
-        // Two warpgroups share every score row: warpgroup ch (= warp / 4) owns columns
-        // ch*64 .. ch*64+63 of S and O and keys ch*64 .. ch*64+63 of P for the row
-        // (= TMEM lane) row.  The two halves of a row exchange their maxima through
-        // shared memory, synchronised by an mbarrier per exchange round.
-        const int ch = warp >> 2;                  // column half
+        // Warpgroup x (= warp / 4) owns query tile x; thread = one row = one TMEM lane.
+        const int x = warp >> 2;
         const int row = (warp & 3) * 32 + lane;    // MMA row == TMEM lane
         const int pl = row >> 2;                   // query position within the tile
         const int hl = row & 3;                    // query head within the group
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t s_col = col_s(x), o_col = col_o(x);
         const float sl2 = a.scale_log2;
         int it = 0;
-        int xc = 0;                                // exchange rounds so far
         bool ok = true;
-        // Publish v for this row, wait for all 8 warps, return the other half's value.
-        auto exchange = [&](float v, bool &good) -> float {
-            const int buf = xc & 1;
-            sm.xchg[buf][ch][row] = v;
-            tc_fence_before();       // this warp's tcgen05.ld of S precede the other half's P stores
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sm.xbar[buf]));
-            good = wait_or_abort(smem_u32(&sm.xbar[buf]), (xc >> 1) & 1, abort_flag, a.err);
-            good = __all_sync(0xffffffffu, good);
-            tc_fence_after();
-            const float other = sm.xchg[buf][ch ^ 1][row];
-            ++xc;
-            return other;
-        };
         for (int r = 0; ok; ++r) {
             const int idx = snake(r, total);
             if (idx < 0) break;
-            const Tile t = tile_at(a, idx, qblocks);
+            const Unit t = unit_at(a, idx, qblocks);
             if (!t.run) continue;
-            const int pos = t.pos0 + pl;
+            const int pos_first = t.pos0 + x * kTilePos;   // first query position of this tile
+            const int pos = pos_first + pl;
             float m = -INFINITY;                   // running max, log2 units (scaled)
+            float l = 0.f;                         // running sum of the bf16 weights
             for (int j = 0; j < t.n_kt; ++j, ++it) {
-                const int st = it & 1;
-                ok = wait_or_abort(smem_u32(&sm.s_full[st]), (it >> 1) & 1, abort_flag, a.err);
+                ok = wait_or_abort(smem_u32(&sm.s_full[x]), it & 1, abort_flag, a.err);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t x[2][32];
-                tmem_ld32(lane_base + col_s(st) + ch * 64, x[0]);
-                tmem_ld32(lane_base + col_s(st) + ch * 64 + 32, x[1]);
-                tmem_wait_ld(x[0]);
-                tmem_wait_ld(x[1]);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sm.s_free[st]));
+                uint32_t s[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + c * 32, s[c]);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_wait_ld(s[c]);
 
                 // causal mask (only on tiles reaching past the tile's first query position)
                 // and the row maximum of the raw scores
-                const int key0 = j * kKT + ch * 64;
-                const bool need_mask = (j * kKT + kKT - 1) > t.pos0;
-                if (need_mask) {
+                if ((j * kKT + kKT - 1) > pos_first) {
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
+                    for (int c = 0; c < 4; ++c)
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            if ((key0 + c * 32 + e) > pos) x[c][e] = __float_as_uint(-INFINITY);
+                            if ((j * kKT + c * 32 + e) > pos) s[c][e] = __float_as_uint(-INFINITY);
                 }
                 float rmax = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; e += 2)
-                        rmax = fmax3(rmax, __uint_as_float(x[c][e]), __uint_as_float(x[c][e + 1]));
-                rmax = fmaxf(rmax, exchange(rmax, ok));
-                if (!ok) break;
+                        rmax = fmax3(rmax, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
                 const float m_new = fmaxf(m, rmax * sl2);
                 const bool rescale = m_new > m + kRescaleThreshold;   // also when m == -inf
                 const float m_use = rescale ? m_new : m;
                 const float alpha = rescale ? fast_exp2(m - m_new) : 1.f;
-                uint32_t pk[32];
+                // a row with every key so far masked keeps m = -inf; its weights are 0
+                const float m_sub = m_use == -INFINITY ? 0.f : m_use;
+                float rsum = 0.f;
+                uint32_t pk[2][32];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < 4; ++c) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float p0 = fast_exp2(fmaf(__uint_as_float(x[c][e]), sl2, -m_use));
-                        const float p1 = fast_exp2(fmaf(__uint_as_float(x[c][e + 1]), sl2, -m_use));
-                        pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
+                        const float p0 = fast_exp2(fmaf(__uint_as_float(s[c][e]), sl2, -m_sub));
+                        const float p1 = fast_exp2(fmaf(__uint_as_float(s[c][e + 1]), sl2, -m_sub));
+                        const uint32_t pp = pack_bf16x2(p0, p1);
+                        // the row sum uses the same bf16-rounded weights the PV product uses
+                        rsum += bf16_lo(pp) + bf16_hi(pp);
+                        pk[c >> 1][(c & 1) * 16 + e / 2] = pp;
                     }
                 }
+                l = l * alpha + rsum;
                 m = m_use;
 
-                if (j > 0) {
-                    // O must hold the previous tile's P V before it is rescaled, and the
-                    // P buffer being overwritten must have been consumed.
-                    ok = wait_or_abort(smem_u32(&sm.o_done), (it - 1) & 1, abort_flag, a.err);
+                if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                    // O must hold O += P V of the previous tile before it is rescaled (that
+                    // product was issued before this tile's S, so it has completed).
+                    ok = wait_or_abort(smem_u32(&sm.o_done[x]), (it - 1) & 1, abort_flag, a.err);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     tc_fence_after();
-                    if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            uint32_t o[32];
-                            tmem_ld32(lane_base + kColO + ch * 64 + c * 32, o);
-                            tmem_wait_ld(o);
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_base + o_col + c * 32, o);
+                        tmem_wait_ld(o);
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tmem_st32(lane_base + kColO + ch * 64 + c * 32, o);
-                        }
-                        if (ch == 0) {   // the row sum (its first column) scales with O
-                            uint32_t lv = tmem_ld1(lane_base + kColL);
-                            tmem_wait_ld1(lv);
-                            tmem_st1(lane_base + kColL, __float_as_uint(__uint_as_float(lv) * alpha));
-                        }
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(lane_base + o_col + c * 32, o);
                     }
                 }
                 // V rows past the end of the context (the tail of the last block) may hold
-                // anything, NaN included; P is 0 there but 0 * NaN is not, so zero them.
+                // anything, NaN included; P is 0 there but 0 * NaN is not, so tile A (the
+                // V tile's first reader) zeroes them.
                 const int kv_valid = t.seq_len - j * kKT;
-                if (kv_valid < kKT) {
+                if (x == 0 && kv_valid < kKT) {
                     const int vs = it % kVStages;
                     ok = wait_or_abort(smem_u32(&sm.v_full[vs]), (it / kVStages) & 1, abort_flag, a.err);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     if (row >= kv_valid) {
-                        uint4 *rv = reinterpret_cast<uint4 *>(sm.v[vs][ch] + row * 128);
+                        uint4 *r0 = reinterpret_cast<uint4 *>(sm.v[vs][0] + row * 128);
+                        uint4 *r1 = reinterpret_cast<uint4 *>(sm.v[vs][1] + row * 128);
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) rv[v] = make_uint4(0u, 0u, 0u, 0u);
+                        for (int v = 0; v < 8; ++v) {
+                            r0[v] = make_uint4(0u, 0u, 0u, 0u);
+                            r1[v] = make_uint4(0u, 0u, 0u, 0u);
+                        }
                     }
                     fence_proxy_async_smem();   // generic writes -> visible to the MMA's reads
                 }
-                tmem_st32(lane_base + col_s(st) + ch * 32, pk);
+                tmem_st32(lane_base + s_col, pk[0]);
+                tmem_st32(lane_base + s_col + 32, pk[1]);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[st]));
+                if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[x]));
             }
             if (!ok) break;
 
             // ------------------------------------------------------------ epilogue
-            ok = wait_or_abort(smem_u32(&sm.o_done), (it - 1) & 1, abort_flag, a.err);
+            ok = wait_or_abort(smem_u32(&sm.o_done[x]), (it - 1) & 1, abort_flag, a.err);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            uint32_t lbits = tmem_ld1(lane_base + kColL);
-            tmem_wait_ld1(lbits);
-            const float l_row = __uint_as_float(lbits);
-            const float inv_l = 1.f / l_row;
-            const bool row_ok = pl < t.rows;
+            const float inv_l = 1.f / l;
+            const bool row_ok = x * kTilePos + pl < t.positions;
             __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
-                                 ((size_t)(t.tok0 + pl) * kHq + t.g * kGroup + hl) * kD + ch * 64;
+                                 ((size_t)(t.tok0 + x * kTilePos + pl) * kHq + t.g * kGroup + hl) * kD;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
-                tmem_ld32(lane_base + kColO + ch * 64 + c * 32, o);
+                tmem_ld32(lane_base + o_col + c * 32, o);
                 tmem_wait_ld(o);
                 uint32_t w[16];
 #pragma unroll
@@ -504,8 +460,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                     for (int v = 0; v < 4; ++v) d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
                 }
             }
-            if (row_ok && ch == 0 && a.lse)
-                a.lse[(size_t)(t.tok0 + pl) * kHq + t.g * kGroup + hl] = (m + __log2f(l_row)) * kLn2;
+            if (row_ok && a.lse)
+                a.lse[(size_t)(t.tok0 + x * kTilePos + pl) * kHq + t.g * kGroup + hl] = (m + __log2f(l)) * kLn2;
             tc_fence_before();
         }
     }
@@ -544,9 +500,10 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map, const
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
-    const long long tiles = (long long)a.num_seqs * kHkv * ((a.max_q_len + kQPos - 1) / kQPos);
-    const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-    // Programmatic dependent launch (see decode): the producer waits before its loads.
+    const long long units = (long long)a.num_seqs * kHkv * ((a.max_q_len + kUnitPos - 1) / kUnitPos);
+    const int grid = (int)(units < num_sms ? units : num_sms);
+    // Programmatic dependent launch: the producers wait (griddepcontrol.wait) before their
+    // first load, so the launch and prologue may overlap the previous kernel on the stream.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
