@@ -36,7 +36,8 @@
  *   cu_q_lens     int32 [num_seqs + 1] offsets of each sequence's new tokens
  *
  * Ownership.  Every pointer is caller-owned device memory; the library allocates
- * nothing and keeps no per-call state outside the caller's workspace.
+ * nothing and keeps no per-call state outside the caller's workspace (except
+ * paged_attn_decode_static, which uses a fixed array of its own instead).
  *
  * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  * are asynchronous and stream-ordered; PA_OK means "validated and launched".
@@ -147,6 +148,35 @@ pa_status paged_attn_decode_split(pa_shape shape, void *out, float *lse, const v
                                   int32_t num_blocks, const int32_t *seq_lens, int32_t batch,
                                   float scale, int32_t split_tokens, void *workspace,
                                   size_t workspace_bytes, void *stream);
+
+/*
+ * paged_attn_decode_static: paged_attn_decode for callers that cannot allocate device
+ * memory -- code that runs where cudaMalloc is not allowed or not available and that is
+ * handed only its input and output buffers, never a scratch workspace (for example a
+ * plug-in called inside another runtime that owns all device memory).  There is no
+ * counterpart on the source pages; it is a deployment convenience.
+ *
+ * The split-K partial results and merge counters live in a fixed array inside the
+ * library (13 MiB per GPU, reserved on every GPU that loads the library until the
+ * process exits).  The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.  Limits: batch <= 256 sequences; a larger batch returns
+ * PA_ERR_WORKSPACE and launches nothing.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any
+ * stream capture.  Every call shares the one array and first clears, on `stream`, the
+ * parts that must start at zero; calls whose executions may overlap on the GPU (other
+ * streams, other host threads) race on it and must be serialised by the caller.
+ *
+ * error_word: optional caller-owned device word that receives the error bits of
+ * pa_check_error (pass it to pa_check_error as the "workspace"); NULL discards them.
+ * All other arguments, layouts and results are those of paged_attn_decode.
+ */
+pa_status paged_attn_decode_static(pa_shape shape, void *out, float *lse, const void *q,
+                                   const void *k_pool, const void *v_pool,
+                                   const int32_t *block_table, int32_t max_blocks_per_seq,
+                                   int32_t num_blocks, const int32_t *seq_lens, int32_t batch,
+                                   float scale, uint32_t *error_word, void *stream);
 
 /*
  * paged_attn_prefill: causal attention of each sequence's new tokens

@@ -251,6 +251,60 @@ pa_status paged_attn_decode_split(pa_shape shape, void *out, float *lse, const v
                        batch, scale, split_tokens, workspace, workspace_bytes, stream);
 }
 
+pa_status paged_attn_decode_static(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
+                                   const void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
+                                   int32_t num_blocks, const int32_t *seq_lens, int32_t batch, float scale,
+                                   uint32_t *error_word, void *stream) {
+    // Same computation as paged_attn_decode, but the split-K scratch is the library's own
+    // fixed device array, so the caller allocates nothing (see pagedattn.h).
+    if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
+    if (batch < 0 || max_blocks_per_seq < 1 || num_blocks < 1 || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (batch > kStaticMaxBatch) return PA_ERR_WORKSPACE;   // beyond what the fixed scratch holds
+    if (batch == 0) return PA_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_table || !seq_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned4(block_table) ||
+        !aligned4(seq_lens) || (lse && !aligned4(lse)) || (error_word && !aligned4(error_word)))
+        return PA_ERR_INVALID_ARG;
+    if ((long long)max_blocks_per_seq * kBlock > (1ll << 30)) return PA_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms <= 0) return PA_ERR_CUDA;
+    if (!get_encoder()) return PA_ERR_CUDA;
+    const int split = auto_split_tokens(batch, max_blocks_per_seq, sms);
+    const long long nsplit = ((long long)max_blocks_per_seq * kBlock + split - 1) / split;
+    if (nsplit > 65535) return PA_ERR_INVALID_ARG;
+    const size_t entries = (size_t)batch * kHkv * (size_t)nsplit;
+    if (workspace_bytes_for(entries) > kStaticScratchBytes) return PA_ERR_WORKSPACE;
+    cudaError_t e = cudaSuccess;
+    char *ws = static_cast<char *>(static_scratch_address(&e));   // first call per device: symbol lookup
+    if (!ws) return PA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The scratch keeps whatever the previous call left: zero its error word and this
+    // call's merge counters (a call that was cut short may have left them non-zero).
+    if (cudaMemsetAsync(ws, 0, kCounterOffset + sizeof(int32_t) * (size_t)batch * kHkv, st) != cudaSuccess)
+        return PA_ERR_CUDA;
+    CUtensorMap k_map, v_map;
+    if (!encode_pool_map(&k_map, k_pool, num_blocks, kDecodeTileTokens) ||
+        !encode_pool_map(&v_map, v_pool, num_blocks, kDecodeTileTokens))
+        return PA_ERR_INVALID_ARG;
+    DecodeArgs a;
+    a.out = out;
+    a.lse = lse;
+    a.q = q;
+    a.block_table = block_table;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.split_tokens = split;
+    a.nsplit = (int)nsplit;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.counters = reinterpret_cast<int32_t *>(ws + kCounterOffset);
+    a.part_o = reinterpret_cast<float *>(ws + kPartialOffset);
+    a.part_ml = reinterpret_cast<float *>(ws + kPartialOffset + entries * kPartialOBytes);
+    a.err = error_word ? error_word : reinterpret_cast<uint32_t *>(ws);
+    return launch_decode(a, k_map, v_map, sms, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
                              const void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
                              int32_t num_blocks, const int32_t *cu_q_lens, const int32_t *seq_lens, int32_t num_seqs,

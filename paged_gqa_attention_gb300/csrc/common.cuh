@@ -42,6 +42,11 @@ constexpr size_t kPartialOffset = kCounterOffset + sizeof(int32_t) * (size_t)kMa
 constexpr size_t kPartialOBytes = (size_t)kGroup * kD * sizeof(float);   // per entry
 constexpr size_t kPartialMLBytes = (size_t)kGroup * 2 * sizeof(float);   // per entry
 constexpr int kDecodeCtaCap = 4096;  // bound on split CTAs the automatic choice asks for
+// Fixed scratch of paged_attn_decode_static: same layout as a workspace, sized for
+// batches of up to kStaticMaxBatch sequences with the automatic split
+// (256 + 4 * kMaxPairs + (kDecodeCtaCap + 8 * 256) * 2080 bytes fit in 13 MiB).
+constexpr int kStaticMaxBatch = 256;
+constexpr size_t kStaticScratchBytes = 13u << 20;
 
 // Bounded waits: a wait that has not completed after this long gives up.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s

@@ -28,6 +28,8 @@
 // recorded in the error word and makes the (sequence, KV head)'s output NaN.
 // The kernel is launched as a programmatic dependent of the previous kernel on the
 // stream, so its launch and prologue overlap e.g. the kv_append that precedes it.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -371,6 +373,40 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const C
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, decode_kernel, k_map, v_map, a);
+}
+
+// ------------------------------------------------------------------ fixed scratch
+// Scratch for paged_attn_decode_static, for callers that cannot allocate device memory
+// themselves (no cudaMalloc allowed, no workspace handed to them): the split-K partial
+// results, the merge counters and an error word live in this file-scope array instead
+// of a caller workspace.  Every GPU that loads the library keeps these bytes reserved
+// until the process exits, and all calls share them.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+void *static_scratch_address(cudaError_t *status) {
+    // In host code g_static_scratch names a host-side stand-in, not device memory: the
+    // device address comes from cudaGetSymbolAddress, looked up once per device while
+    // that device is current, and cached.
+    static std::mutex mu;
+    static void *cached[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        *status = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) {
+            *status = e;
+            return nullptr;
+        }
+        cached[dev] = p;
+    }
+    *status = cudaSuccess;
+    return cached[dev];
 }
 
 }  // namespace pa

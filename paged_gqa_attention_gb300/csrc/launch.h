@@ -69,6 +69,10 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
 
 cudaError_t launch_wait_selftest(uint32_t *err, uint64_t limit_ns, cudaStream_t stream);
 
+// Device address of the file-scope scratch of paged_attn_decode_static on the current
+// device (looked up on the first call per device); nullptr and *status set on failure.
+void *static_scratch_address(cudaError_t *status);
+
 // Tile sizes the tensor maps must be encoded with.
 constexpr int kDecodeTileTokens = 64;    // decode: rows per TMA box
 constexpr int kPrefillKvTile = 128;      // prefill: K/V rows per TMA box
