@@ -47,7 +47,14 @@ HEAD_START_CYCLES = 200_000      # ~0.1 ms spin so a step's launches are all que
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu
 # capture, keyed by kernel, with the hash of the sources it was taken on.  A kernel
 # whose sources changed since reports traffic null.
-TRAFFIC = {}
+TRAFFIC = {
+    # batched decode (32 sequences, 243.9 MB of K/V): profiles/decode_kernel_batched_decode.md
+    "decode": {"bytes_per_launch": 249581056 + 4862720, "sources": ("decode.cu", "common.cuh"),
+               "sha": "bb1d673b2f9d8bed"},
+    # causal prefill of 4096 tokens: profiles/prefill_kernel_causal_prefill.md
+    "prefill": {"bytes_per_launch": 50701568 + 1832704, "sources": ("prefill.cu", "common.cuh"),
+                "sha": "84c2860de6739000"},
+}
 
 
 def parse_args():
@@ -199,7 +206,7 @@ class Timer:
 def flush_l2(buf):
     """Evict the L2: write a buffer 4x its size, then read it back (leaves clean lines)."""
     buf.zero_()
-    buf.sum(dtype=__import__("torch").int32)
+    buf.view(__import__("torch").int32).max()
 
 
 def run_timed(step, n_marks, steps, warmup, flush_buf, stream, clocks=None):
