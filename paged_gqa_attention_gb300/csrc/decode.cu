@@ -37,7 +37,10 @@ namespace pa {
 namespace {
 
 constexpr int kTile = kDecodeTileTokens;      // 64 tokens per stage
-constexpr int kStages = 3;
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 3
+#endif
+constexpr int kStages = PA_DECODE_STAGES;      // pipeline depth (a compile-time tuning knob)
 constexpr int kConsumerWarps = kTile / 16;    // 4
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kHalfBytes = kTile * 128;       // 64 tokens x 64 dims x 2 B

@@ -167,3 +167,30 @@ def test_empty_batch_is_a_no_op():
     out = ops.paged_attn_decode(b.q[:0], b.k_pool, b.v_pool, b.block_table[:0], b.seq_lens[:0], ws)
     ops.check_error(ws)
     assert out.shape[0] == 0
+
+
+def test_prefix_shared_decode_full_size_sampled():
+    """Batch 128 x 32768 with the first 64 blocks shared by every table: all rows of a few
+    sequences against the oracle.  Only the blocks those sequences use are copied to the
+    host (a compact pool with re-numbered tables), before the GPU append; the oracle
+    applies its own append to that copy."""
+    import oracle
+    b = wl.prefix_shared_decode(device="cuda")
+    seqs = [0, 77, 127]
+    rows = b.block_table[seqs]                              # [3, 128]
+    used = torch.unique(rows[rows >= 0])
+    remap = torch.full((b.num_blocks,), -1, dtype=torch.int64, device="cuda")
+    remap[used] = torch.arange(used.numel(), device="cuda")
+    small_bt = remap[rows.long()].to(torch.int32).cpu()
+    cu = torch.arange(len(seqs) + 1, dtype=torch.int32)
+    kp, vp = oracle.kv_append(b.k_pool.index_select(0, used).cpu(), b.v_pool.index_select(0, used).cpu(),
+                              b.k_new[seqs].cpu(), b.v_new[seqs].cpu(), small_bt, cu,
+                              b.seq_lens[seqs].cpu())
+    ref, ref_lse = oracle.attention(b.q[seqs].cpu(), kp, vp, small_bt, cu, b.seq_lens[seqs].cpu(),
+                                    scale=wl.SCALE)
+    ws = workspace_for(b)
+    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    out, lse = run_decode(b, ws)
+    assert torch.isfinite(out.float()).all()
+    assert_close(out[seqs], ref, "prefix-shared decode (sampled sequences)")
+    assert_lse_close(lse[seqs], ref_lse, "prefix-shared decode (sampled sequences)")

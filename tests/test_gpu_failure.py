@@ -3,7 +3,7 @@ waits report through the workspace error word, and the context stays usable."""
 import pytest
 import torch
 
-from gpu_helpers import assert_close, gpu, lib_ready, oracle_attention, workspace_for
+from gpu_helpers import assert_close, gpu, lib_ready, oracle_appended_pools, oracle_attention, workspace_for
 from paged_gqa_attention_gb300 import ops
 from paged_gqa_attention_gb300 import workloads as wl
 
@@ -23,6 +23,7 @@ def decode_case(lens, seed):
 
 def test_bounded_wait_times_out_and_context_survives():
     b = decode_case([300, 40], seed=41)
+    kp, vp = oracle_appended_pools(b)           # the oracle's own append, on the host
     ws = workspace_for(b)
     ops.selftest_wait_timeout(ws, timeout_us=20000)
     with pytest.raises(ops.PagedAttnError) as e:
@@ -32,16 +33,17 @@ def test_bounded_wait_times_out_and_context_survives():
     ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
     out = ops.paged_attn_decode(b.q, b.k_pool, b.v_pool, b.block_table, b.seq_lens, ws)
     ops.check_error(ws)
-    ref, _ = oracle_attention(b)
+    ref, _ = oracle_attention(b, kp, vp)
     assert_close(out, ref, "after timeout")
 
 
 def test_decode_bad_block_id_is_reported_and_poisons_only_its_sequence():
     b = decode_case([600, 300], seed=42)
+    kp, vp = oracle_appended_pools(b)           # the oracle's own append, on the host
     ws = workspace_for(b)
     ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
     ops.check_error(ws)
-    ref, _ = oracle_attention(b)
+    ref, _ = oracle_attention(b, kp, vp)
     bt = b.block_table.clone()
     bt[0, 1] = b.num_blocks + 5                     # out of range
     out = ops.paged_attn_decode(b.q, b.k_pool, b.v_pool, bt, b.seq_lens, ws)
