@@ -3,8 +3,10 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-A step is one pass of the hot path over one batch: kv_append of the batch's new
-tokens, then the attention call(s).  Default workload: batched decode (batch 32,
+A step is one pass of the hot path over one batch: the append of the batch's new
+tokens, then the attention call(s); for decode the two are one fused call
+(paged_attn_decode_append), and the same step as two calls is timed alongside.
+Default workload: batched decode (batch 32,
 context ~U{128..4096}, 32 q / 8 KV heads x 128, 256-token blocks in a 1024-block
 pool); the line also carries the causal-prefill half of the metric (4096-token
 prompt appended into 16 blocks, then causal attention) measured in the same run.
@@ -239,7 +241,9 @@ def mean(xs):
 # ------------------------------------------------------------------ the two measured paths
 
 def decode_measure(batch, steps, warmup, flush_buf, stream, clocks):
-    """kv_append (one new token per sequence) + decode; returns numbers in ms / bytes."""
+    """One decode step: the append of every sequence's new token fused with the decode
+    (paged_attn_decode_append, one kernel).  The same step as two calls (kv_append, then
+    paged_attn_decode) is timed too, over fewer steps, for comparison."""
     import torch
 
     from paged_gqa_attention_gb300 import ops
@@ -249,6 +253,12 @@ def decode_measure(batch, steps, warmup, flush_buf, stream, clocks):
 
     def step(tm):
         if tm: tm.record(0)
+        ops.paged_attn_decode_append(batch.q, batch.k_new, batch.v_new, batch.k_pool, batch.v_pool,
+                                     batch.block_table, batch.seq_lens, ws, out=out)
+        if tm: tm.record(1)
+
+    def two_calls(tm):
+        if tm: tm.record(0)
         ops.kv_append(batch.k_pool, batch.v_pool, batch.k_new, batch.v_new, batch.block_table,
                       batch.cu_q_lens, batch.seq_lens, ws)
         if tm: tm.record(1)
@@ -256,10 +266,12 @@ def decode_measure(batch, steps, warmup, flush_buf, stream, clocks):
                               batch.seq_lens, ws, out=out)
         if tm: tm.record(2)
 
-    spans, wall = run_timed(step, 3, steps, warmup, flush_buf, stream, clocks)
+    spans, wall = run_timed(step, 2, steps, warmup, flush_buf, stream, clocks)
+    spans2, _ = run_timed(two_calls, 3, max(10, min(steps, 200)), warmup, flush_buf, stream)
     ops.check_error(ws)
-    return {"append_ms": mean([s[0] for s in spans]), "attn_ms": mean([s[1] for s in spans]),
-            "step_ms": mean([s[0] + s[1] for s in spans]), "wall_s": wall, "launches": 2 * steps}
+    return {"attn_ms": mean([s[0] for s in spans]), "step_ms": mean([s[0] for s in spans]),
+            "two_call_append_ms": mean([s[0] for s in spans2]),
+            "two_call_decode_ms": mean([s[1] for s in spans2]), "wall_s": wall, "launches": steps}
 
 
 def prefill_measure(batch, steps, warmup, flush_buf, stream, clocks):
@@ -337,11 +349,13 @@ def e2e_measure(batch, kind, steps, warmup, stream):
     def step():
         for k in host:
             dev[k].copy_(host[k], non_blocking=True)
-        ops.kv_append(batch.k_pool, batch.v_pool, dev["k_new"], dev["v_new"], dev["block_table"],
-                      dev["cu_q_lens"], dev["seq_lens"], ws)
+        if kind != "decode":
+            ops.kv_append(batch.k_pool, batch.v_pool, dev["k_new"], dev["v_new"], dev["block_table"],
+                          dev["cu_q_lens"], dev["seq_lens"], ws)
         if kind == "decode":
-            ops.paged_attn_decode(dev["q"], batch.k_pool, batch.v_pool, dev["block_table"],
-                                  dev["seq_lens"], ws, out=out_dev)
+            ops.paged_attn_decode_append(dev["q"], dev["k_new"], dev["v_new"], batch.k_pool,
+                                         batch.v_pool, dev["block_table"], dev["seq_lens"], ws,
+                                         out=out_dev)
         elif kind == "prefill":
             ops.paged_attn_prefill(dev["q"], batch.k_pool, batch.v_pool, dev["block_table"],
                                    dev["cu_q_lens"], dev["seq_lens"], batch.max_q_len, ws,
@@ -531,7 +545,9 @@ def main():
         line["roofline"] = roofline(ach, peaks["hbm_gbs"], "GB/s", "hbm", traffic_for("decode"))
         line["roofline"]["kernel"] = "decode_kernel"
         line["roofline"]["algorithmic_bytes_per_launch"] = kv_bytes + io_bytes
-        line["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "decode_us": r["attn_ms"] * 1e3,
+        line["kernels"] = {"decode_append_us": r["attn_ms"] * 1e3,
+                           "two_call_step": {"kv_append_us": r["two_call_append_ms"] * 1e3,
+                                             "decode_us": r["two_call_decode_ms"] * 1e3},
                            "kv_bytes_per_step": kv_bytes,
                            "unique_kv_bytes": wl.unique_kv_bytes(batch)}
         if wname == "prefix_shared_decode":

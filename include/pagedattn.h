@@ -150,6 +150,21 @@ pa_status paged_attn_decode_split(pa_shape shape, void *out, float *lse, const v
                                   size_t workspace_bytes, void *stream);
 
 /*
+ * paged_attn_decode_append: kv_append of one new token per sequence followed by
+ * paged_attn_decode, in one kernel [P1 §4.3.1 append, §4.4.2 decode; P3 §4.2 "append,
+ * then attend"].  Row b of k_new / v_new ([batch][8][128] bf16) is written to position
+ * seq_lens[b] - 1 of sequence b (slot (seq_lens[b]-1) % 256 of block
+ * block_table[b][(seq_lens[b]-1) / 256]) and takes part in the attention of the same
+ * call.  Results (pools and outputs) are those of the two separate calls.
+ */
+pa_status paged_attn_decode_append(pa_shape shape, void *out, float *lse, const void *q,
+                                   const void *k_new, const void *v_new, void *k_pool,
+                                   void *v_pool, const int32_t *block_table,
+                                   int32_t max_blocks_per_seq, int32_t num_blocks,
+                                   const int32_t *seq_lens, int32_t batch, float scale,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * paged_attn_decode_static: paged_attn_decode for callers that cannot allocate device
  * memory -- code that runs where cudaMalloc is not allowed or not available and that is
  * handed only its input and output buffers, never a scratch workspace (for example a

@@ -109,10 +109,10 @@ size_t workspace_bytes_for(size_t entries) {
     return kPartialOffset + entries * (kPartialOBytes + kPartialMLBytes);
 }
 
-pa_status decode_impl(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
-                      const void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
-                      int32_t num_blocks, const int32_t *seq_lens, int32_t batch, float scale,
-                      int32_t split_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+pa_status decode_impl(pa_shape shape, void *out, float *lse, const void *q, const void *k_new,
+                      const void *v_new, const void *k_pool, const void *v_pool, const int32_t *block_table,
+                      int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t *seq_lens, int32_t batch,
+                      float scale, int32_t split_tokens, void *workspace, size_t workspace_bytes, void *stream) {
     if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
     if (batch < 0 || batch > kMaxBatch || max_blocks_per_seq < 1 || num_blocks < 1 || !std::isfinite(scale) ||
         split_tokens < 0 || split_tokens % kDecodeTileTokens != 0)
@@ -122,6 +122,8 @@ pa_status decode_impl(pa_shape shape, void *out, float *lse, const void *q, cons
     if (!out || !q || !k_pool || !v_pool || !block_table || !seq_lens) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned4(block_table) ||
         !aligned4(seq_lens) || (lse && !aligned4(lse)))
+        return PA_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
         return PA_ERR_INVALID_ARG;
     if ((long long)max_blocks_per_seq * kBlock > (1ll << 30)) return PA_ERR_INVALID_ARG;
     const int sms = sm_count();
@@ -144,6 +146,10 @@ pa_status decode_impl(pa_shape shape, void *out, float *lse, const void *q, cons
     a.out = out;
     a.lse = lse;
     a.q = q;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_pool_w = const_cast<void *>(k_pool);
+    a.v_pool_w = const_cast<void *>(v_pool);
     a.block_table = block_table;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = num_blocks;
@@ -239,16 +245,26 @@ pa_status paged_attn_decode(pa_shape shape, void *out, float *lse, const void *q
                             const void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
                             int32_t num_blocks, const int32_t *seq_lens, int32_t batch, float scale,
                             void *workspace, size_t workspace_bytes, void *stream) {
-    return decode_impl(shape, out, lse, q, k_pool, v_pool, block_table, max_blocks_per_seq, num_blocks, seq_lens,
-                       batch, scale, 0, workspace, workspace_bytes, stream);
+    return decode_impl(shape, out, lse, q, nullptr, nullptr, k_pool, v_pool, block_table, max_blocks_per_seq,
+                       num_blocks, seq_lens, batch, scale, 0, workspace, workspace_bytes, stream);
 }
 
 pa_status paged_attn_decode_split(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
                                   const void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
                                   int32_t num_blocks, const int32_t *seq_lens, int32_t batch, float scale,
                                   int32_t split_tokens, void *workspace, size_t workspace_bytes, void *stream) {
-    return decode_impl(shape, out, lse, q, k_pool, v_pool, block_table, max_blocks_per_seq, num_blocks, seq_lens,
-                       batch, scale, split_tokens, workspace, workspace_bytes, stream);
+    return decode_impl(shape, out, lse, q, nullptr, nullptr, k_pool, v_pool, block_table, max_blocks_per_seq,
+                       num_blocks, seq_lens, batch, scale, split_tokens, workspace, workspace_bytes, stream);
+}
+
+pa_status paged_attn_decode_append(pa_shape shape, void *out, float *lse, const void *q, const void *k_new,
+                                   const void *v_new, void *k_pool, void *v_pool, const int32_t *block_table,
+                                   int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t *seq_lens,
+                                   int32_t batch, float scale, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
+    if (batch > 0 && (!k_new || !v_new)) return PA_ERR_INVALID_ARG;
+    return decode_impl(shape, out, lse, q, k_new, v_new, k_pool, v_pool, block_table, max_blocks_per_seq,
+                       num_blocks, seq_lens, batch, scale, 0, workspace, workspace_bytes, stream);
 }
 
 pa_status paged_attn_decode_static(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
@@ -290,6 +306,10 @@ pa_status paged_attn_decode_static(pa_shape shape, void *out, float *lse, const 
     a.out = out;
     a.lse = lse;
     a.q = q;
+    a.k_new = nullptr;
+    a.v_new = nullptr;
+    a.k_pool_w = nullptr;
+    a.v_pool_w = nullptr;
     a.block_table = block_table;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = num_blocks;

@@ -173,11 +173,43 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     const int row_qk = w * 16 + ri + ((mi & 1) << 3);   // token row for the K fragment
     const int row_pv = w * 16 + ri + ((mi >> 1) << 3);  // token row for the V^T fragment
 
+    // Fused append (k_new / v_new given): the CTA whose range ends the context owns the new
+    // token at position seq_len-1.  The warp whose 16 rows hold it fetches the token's K and
+    // V row of this KV head now (lanes 0-15: K, 16-31: V, 16 bytes each), stores them into the
+    // pool and patches them over the (stale) row of the landed tile before using it.
+    const int p_new = seq_len - 1;
+    const int i_new = (a.k_new && t_end == seq_len) ? (p_new - t_begin) / kTile : -1;
+    const int r_new = (p_new - t_begin) % kTile;        // row within that tile
+    const bool new_here = i_new >= 0 && (r_new >> 4) == w;
+    uint4 new_chunk = make_uint4(0u, 0u, 0u, 0u);
+    if (new_here) {
+        const int kv = lane >> 4, chunk = lane & 15;
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            static_cast<const char *>(kv ? a.v_new : a.k_new) + ((size_t)b * kHkv + g) * kRowBytes);
+        new_chunk = __ldg(src + chunk);
+        const int blk = __ldg(bt + p_new / kBlock);
+        if (blk >= 0 && blk < a.num_blocks) {
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                static_cast<char *>(kv ? a.v_pool_w : a.k_pool_w) +
+                (((size_t)blk * kBlock + p_new % kBlock) * kHkv + g) * kRowBytes);
+            dst[chunk] = new_chunk;
+        }   // a bad block id is reported by the producer and poisons the result
+    }
+
     for (int i = 0; i < n_tiles; ++i) {
         const int st = i % kStages;
         if (!mbar_wait(smem_u32(&sm.full[st]), (i / kStages) & 1)) {
             if (lane == 0) record_error(a.err, kErrTimeout);
             break;
+        }
+        if (new_here && i == i_new) {
+            // the new token's row: 16-byte chunk c of the K (V) row goes to half c / 8,
+            // swizzled chunk c % 8 of row r_new
+            const int kv = lane >> 4, chunk = lane & 15;
+            uint8_t *tile = sm.tiles[st][kv * 2 + (chunk >> 3)];
+            *reinterpret_cast<uint4 *>(tile + sw128(r_new, chunk & 7)) = new_chunk;
+            fence_proxy_async_smem();   // generic writes before the stage is refilled by TMA
+            __syncwarp();
         }
         const int my_valid = min(max(t_end - (t_begin + i * kTile) - w * 16, 0), 16);
         if (my_valid > 0) {

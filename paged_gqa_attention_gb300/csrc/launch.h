@@ -27,6 +27,12 @@ struct DecodeArgs {
     void *out;
     float *lse;
     const void *q;
+    // fused append (optional): the new token of every sequence, [batch][8][128] bf16, and
+    // the pools it is written into; k_new == nullptr means the pools already hold it
+    const void *k_new;
+    const void *v_new;
+    void *k_pool_w;
+    void *v_pool_w;
     const int32_t *block_table;
     int32_t max_blocks_per_seq;
     int32_t num_blocks;

@@ -194,3 +194,47 @@ def test_prefix_shared_decode_full_size_sampled():
     assert torch.isfinite(out.float()).all()
     assert_close(out[seqs], ref, "prefix-shared decode (sampled sequences)")
     assert_lse_close(lse[seqs], ref_lse, "prefix-shared decode (sampled sequences)")
+
+
+@pytest.mark.parametrize("seed", [1, 3])
+def test_fused_append_decode_equals_the_two_calls(seed):
+    """paged_attn_decode_append == kv_append followed by paged_attn_decode: identical pools
+    (bit for bit) and identical outputs; and both match the oracle."""
+    b = wl.batched_decode(device="cuda", seed=seed)
+    kp, vp = oracle_appended_pools(b)
+    k2, v2 = b.k_pool.clone(), b.v_pool.clone()
+    ws = workspace_for(b)
+    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    lse1 = torch.empty(b.num_seqs, 32, dtype=torch.float32, device="cuda")
+    out1 = ops.paged_attn_decode(b.q, b.k_pool, b.v_pool, b.block_table, b.seq_lens, ws, lse=lse1)
+    ops.check_error(ws)
+    lse2 = torch.empty_like(lse1)
+    out2 = ops.paged_attn_decode_append(b.q, b.k_new, b.v_new, k2, v2, b.block_table, b.seq_lens, ws,
+                                        lse=lse2)
+    ops.check_error(ws)
+    assert torch.equal(k2.view(torch.int16), b.k_pool.view(torch.int16))
+    assert torch.equal(v2.view(torch.int16), b.v_pool.view(torch.int16))
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+    ref, ref_lse = oracle_attention(b, kp, vp)
+    assert_close(out2, ref, "fused append + decode")
+    assert_lse_close(lse2, ref_lse, "fused append + decode")
+
+
+def test_fused_append_decode_boundary_lengths_and_splits():
+    lens = [1, 2, 64, 65, 256, 257, 1000]
+    b = wl.build_batch("fused_edges", 31, lens, [1] * len(lens), num_blocks=16, device="cuda")
+    kp, vp = oracle_appended_pools(b)
+    ws = workspace_for(b)
+    ref, _ = oracle_attention(b, kp, vp)
+    for split in (0, 64, 128):
+        k2, v2 = b.k_pool.clone(), b.v_pool.clone()
+        if split:
+            ops.kv_append(k2, v2, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+            out = ops.paged_attn_decode(b.q, k2, v2, b.block_table, b.seq_lens, ws, split_tokens=split)
+        else:
+            out = ops.paged_attn_decode_append(b.q, b.k_new, b.v_new, k2, v2, b.block_table, b.seq_lens, ws)
+        ops.check_error(ws)
+        assert np.array_equal(k2.view(torch.int16).cpu().numpy().view(np.uint16), kp)
+        assert np.array_equal(v2.view(torch.int16).cpu().numpy().view(np.uint16), vp)
+        assert_close(out, ref, f"fused edges split {split}")
