@@ -81,6 +81,16 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // The first block id of this split does not depend on the context length: the
+    // producer fetches it (and the tensor maps) while everyone fetches seq_len, so the
+    // first tile load is one memory round trip closer to the kernel's start.
+    const int32_t *bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
+    int blk0 = 0;
+    if (warp == kConsumerWarps && lane == 0) {
+        tma_prefetch_map(&k_map);
+        tma_prefetch_map(&v_map);
+        blk0 = __ldg(bt + (split * a.split_tokens) / kBlock);   // < max_blocks_per_seq
+    }
     const int seq_len = __ldg(a.seq_lens + b);
     if (seq_len < 1 || seq_len > a.max_blocks_per_seq * kBlock) {
         if (split == 0 && g == 0 && threadIdx.x == 0) record_error(a.err, kErrDevice | kErrBadSeqLen);
@@ -91,7 +101,6 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     const int t_end = min(t_begin + a.split_tokens, seq_len);
     const int nsplit_b = (seq_len + a.split_tokens - 1) / a.split_tokens;
     const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
-    const int32_t *bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
 
     if (threadIdx.x == 0) {
 #pragma unroll
@@ -107,8 +116,6 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            tma_prefetch_map(&k_map);
-            tma_prefetch_map(&v_map);
             // The pools may be written by the kernel just before this one on the stream
             // (kv_append lets us launch early): wait for it before the first pool read.
             asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -120,7 +127,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                     break;
                 }
                 const int tok = t_begin + i * kTile;
-                int blk = __ldg(bt + tok / kBlock);
+                int blk = i == 0 ? blk0 : __ldg(bt + tok / kBlock);
                 if (blk < 0 || blk >= a.num_blocks) {
                     // a block id outside the pool: read block 0 instead and poison the result
                     record_error(a.err, kErrDevice | kErrBadBlock);
