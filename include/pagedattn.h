@@ -165,6 +165,31 @@ pa_status paged_attn_decode_append(pa_shape shape, void *out, float *lse, const 
                                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * One decode step driven from host memory: runs paged_attn_decode_append (append of each
+ * sequence's new token + decode) on host inputs and leaves the output (and lse, when
+ * lse_host is non-NULL) in host memory -- all enqueued on `stream` without synchronising;
+ * the results are in host memory once the stream has reached that point.  A host buffer
+ * the GPU can address in place (pinned, mapped host memory: on GB300 over NVLink-C2C, as
+ * reported by cudaHostGetDevicePointer) is read or written by the kernel directly; any
+ * other buffer is copied through the caller-provided device staging buffer.  Host layouts are those of the device calls: q [batch][32][128] bf16,
+ * k_new / v_new [batch][8][128] bf16, block_table [batch][max_blocks_per_seq] int32,
+ * seq_lens [batch] int32, out [batch][32][128] bf16, lse [batch][32] fp32.  The pools
+ * stay in device memory.  staging: device memory of pa_decode_step_host_staging_bytes()
+ * bytes (16-byte aligned).  Not on the source pages: the engine's DecodeStep request
+ * [P1 §4.1.2] carries token ids; this is the per-layer data movement around it.
+ */
+size_t pa_decode_step_host_staging_bytes(pa_shape shape, int32_t max_batch,
+                                         int32_t max_blocks_per_seq);
+
+pa_status pa_decode_step_host(pa_shape shape, void *out_host, float *lse_host,
+                              const void *q_host, const void *k_new_host, const void *v_new_host,
+                              const int32_t *block_table_host, const int32_t *seq_lens_host,
+                              int32_t batch, int32_t max_blocks_per_seq, void *k_pool,
+                              void *v_pool, int32_t num_blocks, float scale, void *staging,
+                              size_t staging_bytes, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/*
  * paged_attn_decode_static: paged_attn_decode for callers that cannot allocate device
  * memory -- code that runs where cudaMalloc is not allowed or not available and that is
  * handed only its input and output buffers, never a scratch workspace (for example a

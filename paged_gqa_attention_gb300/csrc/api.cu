@@ -109,6 +109,29 @@ size_t workspace_bytes_for(size_t entries) {
     return kPartialOffset + entries * (kPartialOBytes + kPartialMLBytes);
 }
 
+// Staging layout of pa_decode_step_host, per batch of B sequences and tables W wide (each
+// part rounded up to 256 bytes): q [B][32][128] bf16 | k_new [B][8][128] | v_new | out
+// [B][32][128] bf16 | lse [B][32] fp32 | block_table [B][W] int32 | seq_lens [B] int32.
+struct HostStepLayout {
+    size_t q, k_new, v_new, out, lse, bt, sl, total;
+};
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+HostStepLayout host_step_layout(int batch, int max_blocks_per_seq) {
+    HostStepLayout L;
+    size_t o = 0;
+    L.q = o;     o += round256((size_t)batch * kHq * kD * 2);
+    L.k_new = o; o += round256((size_t)batch * kHkv * kD * 2);
+    L.v_new = o; o += round256((size_t)batch * kHkv * kD * 2);
+    L.out = o;   o += round256((size_t)batch * kHq * kD * 2);
+    L.lse = o;   o += round256((size_t)batch * kHq * 4);
+    L.bt = o;    o += round256((size_t)batch * max_blocks_per_seq * 4);
+    L.sl = o;    o += round256((size_t)batch * 4);
+    L.total = o;
+    return L;
+}
+
 pa_status decode_impl(pa_shape shape, void *out, float *lse, const void *q, const void *k_new,
                       const void *v_new, const void *k_pool, const void *v_pool, const int32_t *block_table,
                       int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t *seq_lens, int32_t batch,
@@ -265,6 +288,75 @@ pa_status paged_attn_decode_append(pa_shape shape, void *out, float *lse, const 
     if (batch > 0 && (!k_new || !v_new)) return PA_ERR_INVALID_ARG;
     return decode_impl(shape, out, lse, q, k_new, v_new, k_pool, v_pool, block_table, max_blocks_per_seq,
                        num_blocks, seq_lens, batch, scale, 0, workspace, workspace_bytes, stream);
+}
+
+size_t pa_decode_step_host_staging_bytes(pa_shape shape, int32_t max_batch, int32_t max_blocks_per_seq) {
+    if (!shape_ok(shape) || max_batch < 1 || max_batch > kMaxBatch || max_blocks_per_seq < 1) return 0;
+    return host_step_layout(max_batch, max_blocks_per_seq).total;
+}
+
+// Device address under which the GPU reaches host buffer p in place (pinned, mapped host
+// memory: on GB300 over NVLink-C2C), or nullptr when the runtime reports none -- then the
+// buffer is staged with a copy instead.
+const void *mapped(const void *p) {
+    void *d = nullptr;
+    if (cudaHostGetDevicePointer(&d, const_cast<void *>(p), 0) != cudaSuccess) {
+        cudaGetLastError();   // reset the runtime's last-error state after the failed query
+        return nullptr;
+    }
+    return d;
+}
+
+pa_status pa_decode_step_host(pa_shape shape, void *out_host, float *lse_host, const void *q_host,
+                              const void *k_new_host, const void *v_new_host, const int32_t *block_table_host,
+                              const int32_t *seq_lens_host, int32_t batch, int32_t max_blocks_per_seq,
+                              void *k_pool, void *v_pool, int32_t num_blocks, float scale, void *staging,
+                              size_t staging_bytes, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
+    if (batch < 0 || batch > kMaxBatch || max_blocks_per_seq < 1) return PA_ERR_INVALID_ARG;
+    if (batch == 0) return PA_OK;
+    if (!out_host || !q_host || !k_new_host || !v_new_host || !block_table_host || !seq_lens_host || !staging ||
+        !aligned16(staging))
+        return PA_ERR_INVALID_ARG;
+    const HostStepLayout L = host_step_layout(batch, max_blocks_per_seq);
+    if (staging_bytes < L.total) return PA_ERR_WORKSPACE;
+    char *st = static_cast<char *>(staging);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t q_bytes = (size_t)batch * kHq * kD * 2, kv_bytes = (size_t)batch * kHkv * kD * 2;
+    const size_t bt_bytes = (size_t)batch * max_blocks_per_seq * 4, sl_bytes = (size_t)batch * 4;
+    const size_t lse_bytes = (size_t)batch * kHq * 4;
+    // Inputs: read in place when mapped, else copied into the staging buffer.
+    auto input = [&](const void *h, size_t off, size_t bytes, const void **d) -> bool {
+        *d = mapped(h);
+        if (*d && aligned16(*d)) return true;
+        *d = st + off;
+        return cudaMemcpyAsync(st + off, h, bytes, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    };
+    const void *q, *kn, *vn, *bt, *sl;
+    if (!input(q_host, L.q, q_bytes, &q) || !input(k_new_host, L.k_new, kv_bytes, &kn) ||
+        !input(v_new_host, L.v_new, kv_bytes, &vn) || !input(block_table_host, L.bt, bt_bytes, &bt) ||
+        !input(seq_lens_host, L.sl, sl_bytes, &sl))
+        return PA_ERR_CUDA;
+    // Outputs: written in place when mapped, else staged and copied back.
+    void *out = const_cast<void *>(mapped(out_host));
+    const bool out_direct = out && aligned16(out);
+    if (!out_direct) out = st + L.out;
+    float *lse = nullptr;
+    bool lse_direct = false;
+    if (lse_host) {
+        lse = static_cast<float *>(const_cast<void *>(mapped(lse_host)));
+        lse_direct = lse && aligned4(lse);
+        if (!lse_direct) lse = reinterpret_cast<float *>(st + L.lse);
+    }
+    const pa_status r = decode_impl(shape, out, lse, q, kn, vn, k_pool, v_pool, static_cast<const int32_t *>(bt),
+                                    max_blocks_per_seq, num_blocks, static_cast<const int32_t *>(sl), batch, scale,
+                                    0, workspace, workspace_bytes, stream);
+    if (r != PA_OK) return r;
+    if (!out_direct && cudaMemcpyAsync(out_host, out, q_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (lse_host && !lse_direct && cudaMemcpyAsync(lse_host, lse, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return PA_OK;
 }
 
 pa_status paged_attn_decode_static(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,

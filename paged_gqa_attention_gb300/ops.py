@@ -83,6 +83,11 @@ def load() -> ctypes.CDLL:
     lib.paged_attn_prefill.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32,
                                        i32, f32, vp, sz, vp]
     lib.paged_attn_prefill.restype = ctypes.c_int
+    lib.pa_decode_step_host_staging_bytes.argtypes = [pa_shape, i32, i32]
+    lib.pa_decode_step_host_staging_bytes.restype = sz
+    lib.pa_decode_step_host.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, f32,
+                                        vp, sz, vp, sz, vp]
+    lib.pa_decode_step_host.restype = ctypes.c_int
     lib.pa_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint32, vp]
     lib.pa_selftest_wait_timeout.restype = ctypes.c_int
     _lib = lib
@@ -262,6 +267,51 @@ def paged_attn_prefill(q, k_pool, v_pool, block_table, cu_q_lens, seq_lens, max_
                                    workspace.data_ptr(), workspace.numel(), _stream(stream))
     _check("paged_attn_prefill", st)
     return out
+
+
+def decode_step_host_staging(max_batch: int, max_blocks_per_seq: int, device=None) -> torch.Tensor:
+    """Device staging buffer for decode_step_host."""
+    n = load().pa_decode_step_host_staging_bytes(SHAPE, int(max_batch), int(max_blocks_per_seq))
+    if n == 0:
+        raise ValueError("unsupported staging request")
+    return torch.empty(int(n), dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_step_host(out_host, q_host, k_new_host, v_new_host, block_table_host, seq_lens_host,
+                     k_pool, v_pool, staging, workspace, *, scale: float = DEFAULT_SCALE,
+                     lse_host=None, stream=None) -> None:
+    """One decode step from host tensors (pinned for asynchronous copies): copy the inputs
+    in, append each sequence's new token and attend (one kernel), copy out [B, 32, 128]
+    (and lse [B, 32]) back.  Asynchronous on the stream; synchronise before reading out_host."""
+    batch = q_host.shape[0]
+    for t, name in ((out_host, "out"), (q_host, "q"), (k_new_host, "k_new"), (v_new_host, "v_new"),
+                    (block_table_host, "block_table"), (seq_lens_host, "seq_lens")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    if q_host.dtype != torch.bfloat16 or tuple(q_host.shape[1:]) != (NUM_Q_HEADS, HEAD_DIM):
+        raise ValueError("q must be bf16 [B, 32, 128]")
+    for t, name in ((k_new_host, "k_new"), (v_new_host, "v_new")):
+        if t.dtype != torch.bfloat16 or tuple(t.shape) != (batch, NUM_KV_HEADS, HEAD_DIM):
+            raise ValueError(f"{name} must be bf16 [B, 8, 128]")
+    if out_host.dtype != torch.bfloat16 or tuple(out_host.shape) != tuple(q_host.shape):
+        raise ValueError("out must be bf16 like q")
+    if block_table_host.dtype != torch.int32 or block_table_host.shape[0] != batch:
+        raise ValueError("block_table must be int32 [B, W]")
+    if seq_lens_host.dtype != torch.int32 or tuple(seq_lens_host.shape) != (batch,):
+        raise ValueError("seq_lens must be int32 [B]")
+    if lse_host is not None and (lse_host.is_cuda or lse_host.dtype != torch.float32):
+        raise ValueError("lse must be a host fp32 tensor [B, 32]")
+    _need(k_pool, "k_pool", torch.bfloat16, (None, BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM))
+    _need(v_pool, "v_pool", torch.bfloat16, tuple(k_pool.shape), k_pool.device)
+    _need(staging, "staging", torch.uint8, None, k_pool.device)
+    _need(workspace, "workspace", torch.uint8, None, k_pool.device)
+    st = load().pa_decode_step_host(SHAPE, out_host.data_ptr(), _ptr(lse_host), q_host.data_ptr(),
+                                    k_new_host.data_ptr(), v_new_host.data_ptr(),
+                                    block_table_host.data_ptr(), seq_lens_host.data_ptr(), batch,
+                                    block_table_host.shape[1], k_pool.data_ptr(), v_pool.data_ptr(),
+                                    k_pool.shape[0], float(scale), staging.data_ptr(), staging.numel(),
+                                    workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check("pa_decode_step_host", st)
 
 
 def selftest_wait_timeout(workspace: torch.Tensor, timeout_us: int = 20000, stream=None) -> None:

@@ -238,3 +238,27 @@ def test_fused_append_decode_boundary_lengths_and_splits():
         assert np.array_equal(k2.view(torch.int16).cpu().numpy().view(np.uint16), kp)
         assert np.array_equal(v2.view(torch.int16).cpu().numpy().view(np.uint16), vp)
         assert_close(out, ref, f"fused edges split {split}")
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_decode_step_from_host_buffers(pinned):
+    """pa_decode_step_host: host inputs in, one fused decode step, host output back.  Pinned
+    buffers are read and written in place by the kernel; pageable ones go through the
+    staging copies."""
+    b = wl.batched_decode(device="cuda", seed=5, batch=16, hi=2000, num_blocks=160)
+    kp, vp = oracle_appended_pools(b)
+    ws = workspace_for(b)
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    host = {k: pin(getattr(b, k).cpu()) for k in ("q", "k_new", "v_new", "block_table", "seq_lens")}
+    out_host = pin(torch.empty(b.q.shape, dtype=torch.bfloat16))
+    lse_host = pin(torch.empty(b.num_seqs, 32, dtype=torch.float32))
+    staging = ops.decode_step_host_staging(b.num_seqs, b.max_blocks_per_seq)
+    for _ in range(2):   # the second step re-appends the same token: results must not change
+        ops.decode_step_host(out_host, host["q"], host["k_new"], host["v_new"], host["block_table"],
+                             host["seq_lens"], b.k_pool, b.v_pool, staging, ws, lse_host=lse_host)
+        torch.cuda.synchronize()
+        ops.check_error(ws)
+        ref, ref_lse = oracle_attention(b, kp, vp)
+        assert_close(out_host, ref, "decode step from host buffers")
+        assert_lse_close(lse_host, ref_lse, "decode step from host buffers")
+    assert np.array_equal(b.k_pool.view(torch.int16).cpu().numpy().view(np.uint16), kp)
