@@ -107,6 +107,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     }
 }
 
+// One lane of a converged warp (elect.sync); the caller's warp must be fully active.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}" : "=r"(pred));
+    return pred != 0;
+}
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -182,6 +189,31 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
+}
+
+// Two independent fused multiply-adds in one packed instruction (sm_100 family):
+// (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1), each rounded to nearest like fmaf.
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1,
+                                      float c0, float c1) {
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// c + (the bf16 in the low / high half of v), one mixed-precision add (sm_100 family);
+// identical to c + bf16_lo(v) / c + bf16_hi(v) since bf16 -> f32 is exact.
+__device__ __forceinline__ float add_bf16_lo(uint32_t v, float c) {
+    float d;
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n add.rn.f32.bf16 %0, lo, %2;\n}"
+        : "=f"(d) : "r"(v), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float add_bf16_hi(uint32_t v, float c) {
+    float d;
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n add.rn.f32.bf16 %0, hi, %2;\n}"
+        : "=f"(d) : "r"(v), "f"(c));
+    return d;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -327,6 +359,14 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
 }
 
 // r[0..31] -> 32 consecutive columns of this thread's lane
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        PA_W8(0), PA_W8(8)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "

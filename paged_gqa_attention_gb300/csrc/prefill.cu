@@ -57,7 +57,7 @@ constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kHalf = kRows * 128;            // 128 rows x 64 dims x 2 B = 16 KiB
 constexpr uint32_t kTileBytes = 2 * kHalf;    // a full 128 x 128 bf16 tile
-constexpr int kKStages = 2;
+constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when the max grows > 2^8
 constexpr float kLn2 = 0.693147180559945309f;
@@ -256,22 +256,30 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            // Matrix descriptors are built once; per MMA only a constant is added to the
-            // start-address field (units of 16 bytes): +2 per 16 dims along a 128-byte row,
-            // +1024 per 64-dim half (16 KiB), +2048 per tile or ring slot (32 KiB), +128 per
-            // 16 keys of an MN-major V tile (2 KiB).
-            const uint64_t qd0 = sdesc_sw128(smem_u32(sm.q[0][0]), 16, 1024);
-            const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0][0]), 16, 1024);
-            const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0][0]), (uint32_t)kHalf, 1024);
-            int tcount = 0, it = 0;
-            int pend_it = -1, pend_j = 0;   // O_B += P_B V still to issue for key tile pend_it
-            bool ok = true;
-            // S_x = Q_x K^T over 128 dims in 8 steps of 16 (K-major, 128-byte swizzle)
-            auto issue_s = [&](int x, int ks) {
-                const uint64_t qa = qd0 + (uint64_t)(x * 2048);
-                const uint64_t kb = kd0 + (uint64_t)(ks * 2048);
-                const uint32_t sd = tmem + col_s(x);
+        // The whole warp runs the loop and the waits, so the descriptors and counters are
+        // warp-uniform; one elected lane issues the MMAs and commits.  Confined to a
+        // single-lane branch, the same stream competed for issue slots with the softmax
+        // warps of its sub-partition and fed the tensor core at about half its rate.
+        const bool leader = elect_one();
+        // Matrix descriptors are built once; per MMA only a constant is added to the
+        // start-address field (units of 16 bytes): +2 per 16 dims along a 128-byte row,
+        // +1024 per 64-dim half (16 KiB), +2048 per tile or ring slot (32 KiB), +128 per
+        // 16 keys of an MN-major V tile (2 KiB).
+        const uint64_t qd0 = sdesc_sw128(smem_u32(sm.q[0][0]), 16, 1024);
+        const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0][0]), 16, 1024);
+        const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0][0]), (uint32_t)kHalf, 1024);
+        int tcount = 0, it = 0;
+        int pend_it = -1, pend_j = 0;   // O_B += P_B V still to issue for key tile pend_it
+        bool ok = true;
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, wait_or_abort(smem_u32(bar), parity, abort_flag, a.err));
+        };
+        // S_x = Q_x K^T over 128 dims in 8 steps of 16 (K-major, 128-byte swizzle)
+        auto issue_s = [&](int x, int ks) {
+            const uint64_t qa = qd0 + (uint64_t)(x * 2048);
+            const uint64_t kb = kd0 + (uint64_t)(ks * 2048);
+            const uint32_t sd = tmem + col_s(x);
+            if (leader) {
                 umma_ss_c<false>(sd, qa, kb, kIdescQK);
 #pragma unroll
                 for (int kk = 1; kk < kD / 16; ++kk) {
@@ -279,51 +287,58 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                     umma_ss_c<true>(sd, qa + off, kb + off, kIdescQK);
                 }
                 umma_commit(smem_u32(&sm.s_full[x]));
-            };
-            // O_x += P_x V over 128 keys in 8 steps of 16; V is [128 keys][128 dims] with dims
-            // contiguous (MN-major), its two 64-dim halves 16 KiB apart.
-            auto issue_pv = [&](int x, int pit, int pj) -> bool {
-                const int vs = pit % kVStages;
-                if (!wait_or_abort(smem_u32(&sm.v_full[vs]), (pit / kVStages) & 1, abort_flag, a.err)) return false;
-                if (!wait_or_abort(smem_u32(&sm.p_full[x]), pit & 1, abort_flag, a.err)) return false;
-                tc_fence_after();
-                const uint64_t vb = vd0 + (uint64_t)(vs * 2048);
-                const uint32_t pa = tmem + col_s(x);
+            }
+            __syncwarp();
+        };
+        // O_x += P_x V over 128 keys in 8 steps of 16; V is [128 keys][128 dims] with dims
+        // contiguous (MN-major), its two 64-dim halves 16 KiB apart.
+        auto issue_pv = [&](int x, int pit, int pj) -> bool {
+            const int vs = pit % kVStages;
+            if (!wait_all(&sm.v_full[vs], (pit / kVStages) & 1)) return false;
+            if (!wait_all(&sm.p_full[x], pit & 1)) return false;
+            tc_fence_after();
+            const uint64_t vb = vd0 + (uint64_t)(vs * 2048);
+            const uint32_t pa = tmem + col_s(x);
+            if (leader) {
                 umma_ts(tmem + col_o(x), pa, vb, kIdescPV, pj > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 1; kk < kKT / 16; ++kk)
                     umma_ts_c<true>(tmem + col_o(x), pa + kk * 8, vb + (uint64_t)(kk * 128), kIdescPV);
                 umma_commit(smem_u32(&sm.o_done[x]));
                 if (x == 1) umma_commit(smem_u32(&sm.v_empty[vs]));   // B is the V tile's last reader
-                return true;
-            };
-            for (int r = 0; ok; ++r) {
-                const int idx = snake(r, total);
-                if (idx < 0) break;
-                const Unit t = unit_at(a, idx, qblocks);
-                if (!t.run) continue;
-                if (!(ok = wait_or_abort(smem_u32(&sm.q_full), tcount & 1, abort_flag, a.err))) break;
-                for (int j = 0; j < t.n_kt; ++j, ++it) {
-                    const int ks = it % kKStages;
-                    if (!(ok = wait_or_abort(smem_u32(&sm.k_full[ks]), (it / kKStages) & 1, abort_flag, a.err)))
-                        break;
-                    tc_fence_after();
-                    issue_s(0, ks);                                        // S_A(j)
-                    if (pend_it >= 0 && !(ok = issue_pv(1, pend_it, pend_j))) break;   // O_B, tile j-1
-                    issue_s(1, ks);                                        // S_B(j)
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int r = 0; ok; ++r) {
+            const int idx = snake(r, total);
+            if (idx < 0) break;
+            const Unit t = unit_at(a, idx, qblocks);
+            if (!t.run) continue;
+            if (!(ok = wait_all(&sm.q_full, tcount & 1))) break;
+            for (int j = 0; j < t.n_kt; ++j, ++it) {
+                const int ks = it % kKStages;
+                if (!(ok = wait_all(&sm.k_full[ks], (it / kKStages) & 1))) break;
+                tc_fence_after();
+                issue_s(0, ks);                                        // S_A(j)
+                if (pend_it >= 0 && !(ok = issue_pv(1, pend_it, pend_j))) break;   // O_B, tile j-1
+                issue_s(1, ks);                                        // S_B(j)
+                if (leader) {
                     umma_commit(smem_u32(&sm.k_empty[ks]));
                     if (j == t.n_kt - 1) umma_commit(smem_u32(&sm.q_empty));
-                    if (!(ok = issue_pv(0, it, j))) break;                 // O_A, tile j
-                    pend_it = it;
-                    pend_j = j;
                 }
-                ++tcount;
+                __syncwarp();
+                if (!(ok = issue_pv(0, it, j))) break;                 // O_A, tile j
+                pend_it = it;
+                pend_j = j;
             }
-            if (ok && pend_it >= 0) issue_pv(1, pend_it, pend_j);
-            // Every MMA issued must have finished before tensor memory is released.
-            umma_commit(smem_u32(&sm.mma_idle));
-            mbar_wait(smem_u32(&sm.mma_idle), 0);
+            ++tcount;
         }
+        if (ok && pend_it >= 0) issue_pv(1, pend_it, pend_j);
+        // Every MMA issued must have finished before tensor memory is released.
+        if (leader) umma_commit(smem_u32(&sm.mma_idle));
+        __syncwarp();
+        mbar_wait(smem_u32(&sm.mma_idle), 0);
     } else {
         // ---------------------------------------------------------------- softmax warps
         // Warpgroup x (= warp / 4) owns query tile x; thread = one row = one TMEM lane.
@@ -364,32 +379,48 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                         for (int e = 0; e < 32; ++e)
                             if ((j * kKT + c * 32 + e) > pos) s[c][e] = __float_as_uint(-INFINITY);
                 }
-                float rmax = -INFINITY;
+                // independent partial maxima (one per 32-column chunk) keep the dependency
+                // chain short: floating-point max/add are not reassociated by the compiler
+                float cmax[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 4; ++c) {
+                    // r0 over columns 0-15, r1 over columns 16-31
+                    float r0 = fmaxf(__uint_as_float(s[c][0]), __uint_as_float(s[c][1]));
+                    float r1 = fmaxf(__uint_as_float(s[c][16]), __uint_as_float(s[c][17]));
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2)
-                        rmax = fmax3(rmax, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
+                    for (int e = 2; e < 16; e += 2) {
+                        r0 = fmax3(r0, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
+                        r1 = fmax3(r1, __uint_as_float(s[c][e + 16]), __uint_as_float(s[c][e + 17]));
+                    }
+                    cmax[c] = fmaxf(r0, r1);
+                }
+                const float rmax = fmaxf(fmaxf(cmax[0], cmax[1]), fmaxf(cmax[2], cmax[3]));
                 const float m_new = fmaxf(m, rmax * sl2);
                 const bool rescale = m_new > m + kRescaleThreshold;   // also when m == -inf
                 const float m_use = rescale ? m_new : m;
                 const float alpha = rescale ? fast_exp2(m - m_new) : 1.f;
                 // a row with every key so far masked keeps m = -inf; its weights are 0
                 const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-                float rsum = 0.f;
-                uint32_t pk[2][32];
+                float part[4] = {0.f, 0.f, 0.f, 0.f};   // 4 partial row sums
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float p0 = fast_exp2(fmaf(__uint_as_float(s[c][e]), sl2, -m_sub));
-                        const float p1 = fast_exp2(fmaf(__uint_as_float(s[c][e + 1]), sl2, -m_sub));
-                        const uint32_t pp = pack_bf16x2(p0, p1);
+                        float x0, x1;
+                        ffma2(x0, x1, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]), sl2, sl2,
+                              -m_sub, -m_sub);
+                        const uint32_t pp = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
                         // the row sum uses the same bf16-rounded weights the PV product uses
-                        rsum += bf16_lo(pp) + bf16_hi(pp);
-                        pk[c >> 1][(c & 1) * 16 + e / 2] = pp;
+                        const int k = (e >> 1) & 1;
+                        part[2 * k] = add_bf16_lo(pp, part[2 * k]);
+                        part[2 * k + 1] = add_bf16_hi(pp, part[2 * k + 1]);
+                        pk[e / 2] = pp;
                     }
+                    // P columns 16c..16c+15 go over S columns already read into registers
+                    tmem_st16(lane_base + s_col + 16 * c, pk);
                 }
+                const float rsum = (part[0] + part[1]) + (part[2] + part[3]);
                 l = l * alpha + rsum;
                 m = m_use;
 
@@ -428,8 +459,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                     }
                     fence_proxy_async_smem();   // generic writes -> visible to the MMA's reads
                 }
-                tmem_st32(lane_base + s_col, pk[0]);
-                tmem_st32(lane_base + s_col + 32, pk[1]);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
