@@ -59,6 +59,7 @@ constexpr int kHalf = kRows * 128;            // 128 rows x 64 dims x 2 B = 16 K
 constexpr uint32_t kTileBytes = 2 * kHalf;    // a full 128 x 128 bf16 tile
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
+constexpr uint32_t kParkNs = 20000;           // longest hardware park per wait attempt
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when the max grows > 2^8
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr uint32_t kIdescQK = idesc_bf16(kRows, kKT, false);  // B = K tile, K-major
@@ -75,7 +76,7 @@ struct PrefillSmem {
     uint64_t q_full, q_empty;
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t v_full[kVStages], v_empty[kVStages];
-    uint64_t s_full[2], p_full[2], o_done[2];   // per query tile
+    uint64_t s_full[2], p_half[2][2], o_done[2];   // per query tile (P in two key halves)
     uint64_t mma_idle;
     uint32_t tmem_base;
     int abort;
@@ -136,7 +137,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_parked(bar, parity, kParkNs)) return true;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
@@ -171,7 +172,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(smem_u32(&sm.s_full[x]), 1);
-            mbar_init(smem_u32(&sm.p_full[x]), 4);   // the 4 warps of the tile's softmax
+            mbar_init(smem_u32(&sm.p_half[x][0]), 4);   // the 4 warps of the tile's softmax
+            mbar_init(smem_u32(&sm.p_half[x][1]), 4);
             mbar_init(smem_u32(&sm.o_done[x]), 1);
         }
         mbar_init(smem_u32(&sm.mma_idle), 1);
@@ -190,70 +192,80 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     if (warp == kProducerWarp || warp == kVProducerWarp) {
         // ---------------------------------------------------------------- TMA producers
         // Two independent producers, so a K tile is requested as soon as its slot is
-        // free, never behind a V tile waiting for its own slot.
-        if (lane == 0) {
-            const bool qk = (warp == kProducerWarp);
+        // free, never behind a V tile waiting for its own slot.  As in the MMA warp, the
+        // whole warp runs the loop and one elected lane issues the copies.
+        const bool leader = elect_one();
+        const bool qk = (warp == kProducerWarp);
+        if (leader) {
             if (qk) {
                 tma_prefetch_map(&q_map);
                 tma_prefetch_map(&k_map);
             } else {
                 tma_prefetch_map(&v_map);
             }
-            // The pools may be written by the kernel just before this one on the stream
-            // (kv_append lets us launch early): wait for it before the first load.
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            uint64_t *full = qk ? sm.k_full : sm.v_full;
-            uint64_t *empty = qk ? sm.k_empty : sm.v_empty;
-            const int ns = qk ? kKStages : kVStages;
-            const CUtensorMap *map = qk ? &k_map : &v_map;
-            int tcount = 0, it = 0;              // units / key tiles started
-            int q_issued = 0, kv_issued = 0;
-            bool ok = true;
-            for (int r = 0; ok; ++r) {
-                const int idx = snake(r, total);
-                if (idx < 0) break;
-                const Unit t = unit_at(a, idx, qblocks);
-                if (qk && t.error) record_error(a.err, kErrDevice | kErrQLen);
-                if (!t.run) continue;
-                if (qk) {
-                    if (tcount >= 1 &&
-                        !(ok = wait_or_abort(smem_u32(&sm.q_empty), (tcount - 1) & 1, abort_flag, a.err)))
-                        break;
+        }
+        // The pools may be written by the kernel just before this one on the stream
+        // (kv_append lets us launch early): wait for it before the first load.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        uint64_t *full = qk ? sm.k_full : sm.v_full;
+        uint64_t *empty = qk ? sm.k_empty : sm.v_empty;
+        const int ns = qk ? kKStages : kVStages;
+        const CUtensorMap *map = qk ? &k_map : &v_map;
+        int tcount = 0, it = 0;              // units / key tiles started
+        int q_issued = 0, kv_issued = 0;
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+            const int idx = snake(r, total);
+            if (idx < 0) break;
+            const Unit t = unit_at(a, idx, qblocks);
+            if (qk && leader && t.error) record_error(a.err, kErrDevice | kErrQLen);
+            if (!t.run) continue;
+            if (qk) {
+                if (tcount >= 1 &&
+                    !(ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&sm.q_empty), (tcount - 1) & 1,
+                                                                abort_flag, a.err))))
+                    break;
+                if (leader) {
                     const uint32_t qbar = smem_u32(&sm.q_full);
                     mbar_arrive_expect_tx(qbar, 2 * kTileBytes);
                     for (int x = 0; x < 2; ++x) {
                         tma_load_3d(smem_u32(sm.q[x][0]), &q_map, qbar, 0, t.g * kGroup, t.tok0 + x * kTilePos);
                         tma_load_3d(smem_u32(sm.q[x][1]), &q_map, qbar, 64, t.g * kGroup, t.tok0 + x * kTilePos);
                     }
-                    ++q_issued;
                 }
-                const int32_t *bt = a.block_table + (size_t)t.s * a.max_blocks_per_seq;
-                for (int j = 0; j < t.n_kt; ++j, ++it) {
-                    const int st = it % ns;
-                    int blk = __ldg(bt + (j >> 1));
-                    if (blk < 0 || blk >= a.num_blocks) {
-                        if (qk) record_error(a.err, kErrDevice | kErrBadBlock);
-                        blk = 0;   // stay inside the pool; the result is flagged as invalid
-                    }
-                    const int off = (j & 1) * kKT;
-                    if (it >= ns &&
-                        !(ok = wait_or_abort(smem_u32(&empty[st]), ((it / ns) - 1) & 1, abort_flag, a.err)))
-                        break;
+                __syncwarp();
+                ++q_issued;
+            }
+            const int32_t *bt = a.block_table + (size_t)t.s * a.max_blocks_per_seq;
+            for (int j = 0; j < t.n_kt; ++j, ++it) {
+                const int st = it % ns;
+                int blk = __ldg(bt + (j >> 1));
+                if (blk < 0 || blk >= a.num_blocks) {
+                    if (qk && leader) record_error(a.err, kErrDevice | kErrBadBlock);
+                    blk = 0;   // stay inside the pool; the result is flagged as invalid
+                }
+                const int off = (j & 1) * kKT;
+                if (it >= ns &&
+                    !(ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&empty[st]), ((it / ns) - 1) & 1,
+                                                                abort_flag, a.err))))
+                    break;
+                if (leader) {
                     const uint32_t bar = smem_u32(&full[st]);
                     uint8_t (*dst)[kHalf] = qk ? sm.k[st] : sm.v[st];
                     mbar_arrive_expect_tx(bar, kTileBytes);
                     tma_load_4d(smem_u32(dst[0]), map, bar, 0, t.g, off, blk);
                     tma_load_4d(smem_u32(dst[1]), map, bar, 64, t.g, off, blk);
-                    ++kv_issued;
                 }
-                ++tcount;
+                __syncwarp();
+                ++kv_issued;
             }
-            // Drain: no TMA copy may still be landing when the CTA exits.  In the normal
-            // path every load has been consumed and these waits return at once.
-            if (q_issued > 0) mbar_wait(smem_u32(&sm.q_full), (q_issued - 1) & 1);
-            for (int i = max(0, kv_issued - ns); i < kv_issued; ++i)
-                mbar_wait(smem_u32(&full[i % ns]), (i / ns) & 1);
+            ++tcount;
         }
+        // Drain: no TMA copy may still be landing when the CTA exits.  In the normal
+        // path every load has been consumed and these waits return at once.
+        if (q_issued > 0) mbar_wait(smem_u32(&sm.q_full), (q_issued - 1) & 1);
+        for (int i = max(0, kv_issued - ns); i < kv_issued; ++i)
+            mbar_wait(smem_u32(&full[i % ns]), (i / ns) & 1);
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
         // The whole warp runs the loop and the waits, so the descriptors and counters are
@@ -295,14 +307,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         auto issue_pv = [&](int x, int pit, int pj) -> bool {
             const int vs = pit % kVStages;
             if (!wait_all(&sm.v_full[vs], (pit / kVStages) & 1)) return false;
-            if (!wait_all(&sm.p_full[x], pit & 1)) return false;
-            tc_fence_after();
             const uint64_t vb = vd0 + (uint64_t)(vs * 2048);
             const uint32_t pa = tmem + col_s(x);
+            // keys 0-63 as soon as their P is stored, keys 64-127 when the rest is
+            if (!wait_all(&sm.p_half[x][0], pit & 1)) return false;
+            tc_fence_after();
             if (leader) {
                 umma_ts(tmem + col_o(x), pa, vb, kIdescPV, pj > 0 ? 1u : 0u);
 #pragma unroll
-                for (int kk = 1; kk < kKT / 16; ++kk)
+                for (int kk = 1; kk < kKT / 32; ++kk)
+                    umma_ts_c<true>(tmem + col_o(x), pa + kk * 8, vb + (uint64_t)(kk * 128), kIdescPV);
+            }
+            __syncwarp();
+            if (!wait_all(&sm.p_half[x][1], pit & 1)) return false;
+            tc_fence_after();
+            if (leader) {
+#pragma unroll
+                for (int kk = kKT / 32; kk < kKT / 16; ++kk)
                     umma_ts_c<true>(tmem + col_o(x), pa + kk * 8, vb + (uint64_t)(kk * 128), kIdescPV);
                 umma_commit(smem_u32(&sm.o_done[x]));
                 if (x == 1) umma_commit(smem_u32(&sm.v_empty[vs]));   // B is the V tile's last reader
@@ -401,43 +422,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                 const float alpha = rescale ? fast_exp2(m - m_new) : 1.f;
                 // a row with every key so far masked keeps m = -inf; its weights are 0
                 const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-                float part[4] = {0.f, 0.f, 0.f, 0.f};   // 4 partial row sums
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float x0, x1;
-                        ffma2(x0, x1, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]), sl2, sl2,
-                              -m_sub, -m_sub);
-                        const uint32_t pp = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
-                        // the row sum uses the same bf16-rounded weights the PV product uses
-                        const int k = (e >> 1) & 1;
-                        part[2 * k] = add_bf16_lo(pp, part[2 * k]);
-                        part[2 * k + 1] = add_bf16_hi(pp, part[2 * k + 1]);
-                        pk[e / 2] = pp;
-                    }
-                    // P columns 16c..16c+15 go over S columns already read into registers
-                    tmem_st16(lane_base + s_col + 16 * c, pk);
-                }
-                const float rsum = (part[0] + part[1]) + (part[2] + part[3]);
-                l = l * alpha + rsum;
-                m = m_use;
-
+                // The O rescale and the zeroing of V rows below both precede the release
+                // of the first half of P.
                 if (j > 0 && __any_sync(0xffffffffu, rescale)) {
                     // O must hold O += P V of the previous tile before it is rescaled (that
                     // product was issued before this tile's S, so it has completed).
                     ok = wait_or_abort(smem_u32(&sm.o_done[x]), (it - 1) & 1, abort_flag, a.err);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     tc_fence_after();
+                    // 8 columns at a time: the scores of this tile are still live in registers
+#pragma unroll 1
+                    for (int c = 0; c < 16; ++c) {
+                        uint32_t o[8];
+                        tmem_ld8(lane_base + o_col + c * 8, o);
+                        tmem_wait_ld8(o);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(lane_base + o_col + c * 32, o);
-                        tmem_wait_ld(o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(lane_base + o_col + c * 32, o);
+                        for (int e = 0; e < 8; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st8(lane_base + o_col + c * 8, o);
                     }
                 }
                 // V rows past the end of the context (the tail of the last block) may hold
@@ -459,10 +460,36 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                     }
                     fence_proxy_async_smem();   // generic writes -> visible to the MMA's reads
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[x]));
+                float part[4] = {0.f, 0.f, 0.f, 0.f};   // 4 partial row sums
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int c = 2 * h; c < 2 * h + 2; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float x0, x1;
+                            ffma2(x0, x1, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]), sl2, sl2,
+                                  -m_sub, -m_sub);
+                            const uint32_t pp = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
+                            // the row sum uses the same bf16-rounded weights the PV product uses
+                            const int k = (e >> 1) & 1;
+                            part[2 * k] = add_bf16_lo(pp, part[2 * k]);
+                            part[2 * k + 1] = add_bf16_hi(pp, part[2 * k + 1]);
+                            pk[e / 2] = pp;
+                        }
+                        // P columns 16c..16c+15 go over S columns already read into registers
+                        tmem_st16(lane_base + s_col + 16 * c, pk);
+                    }
+                    // P of keys 64h..64h+63 is in tensor memory: release that half of O += P V
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sm.p_half[x][h]));
+                }
+                const float rsum = (part[0] + part[1]) + (part[2] + part[3]);
+                l = l * alpha + rsum;
+                m = m_use;
             }
             if (!ok) break;
 
