@@ -50,12 +50,12 @@ HEAD_START_CYCLES = 200_000      # ~0.1 ms spin so a step's launches are all que
 # capture, keyed by kernel, with the hash of the sources it was taken on.  A kernel
 # whose sources changed since reports traffic null.
 TRAFFIC = {
-    # batched decode (32 sequences, 243.9 MB of K/V): profiles/decode_kernel_batched_decode.md
-    "decode": {"bytes_per_launch": 249581056 + 4862720, "sources": ("decode.cu", "common.cuh"),
-               "sha": "bb1d673b2f9d8bed"},
-    # causal prefill of 4096 tokens: profiles/prefill_kernel_causal_prefill.md
-    "prefill": {"bytes_per_launch": 50701568 + 1832704, "sources": ("prefill.cu", "common.cuh"),
-                "sha": "84c2860de6739000"},
+    # one ncu capture of the batched decode step (32 sequences, 243.9 MB of K/V)
+    "decode": {"bytes_per_launch": 249672960 + 4535552, "sources": ("decode.cu", "common.cuh"),
+               "sha": "fc9df4d86f33d1fd"},
+    # one ncu capture of the causal prefill of 4096 tokens
+    "prefill": {"bytes_per_launch": 50719232 + 1658624, "sources": ("prefill.cu", "common.cuh"),
+                "sha": "bc95774cb225c06a"},
 }
 
 
