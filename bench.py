@@ -66,7 +66,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default="batched_decode",
                    choices=["single_decode", "batched_decode", "causal_prefill", "mixed_batch",
-                            "prefix_shared_decode"])
+                            "prefix_shared_decode", "layered_decode"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -329,6 +329,69 @@ def mixed_measure(batch, steps, warmup, flush_buf, stream, clocks):
             "dec": dec, "pre": pre}
 
 
+def layered_measure(layers, steps, warmup, flush_buf, stream, clocks):
+    """The decode step over all layers: one replay of the captured CUDA graph
+    (pa_decode_graph_launch) against the same layers launched one call at a time."""
+    import torch
+
+    from paged_gqa_attention_gb300 import ops
+
+    b0 = layers.base
+    ws = ops.make_workspace(b0.num_seqs, b0.max_blocks_per_seq)
+    out = torch.empty_like(layers.q)
+    g = ops.decode_graph(layers.q, layers.k_new, layers.v_new, layers.k_pool, layers.v_pool,
+                         b0.block_table, b0.seq_lens, ws, out=out)
+
+    def graph_step(tm):
+        if tm: tm.record(0)
+        g.launch()
+        if tm: tm.record(1)
+
+    def eager_step(tm):
+        if tm: tm.record(0)
+        for l in range(layers.layers):
+            ops.paged_attn_decode_append(layers.q[l], layers.k_new[l], layers.v_new[l], layers.k_pool[l],
+                                         layers.v_pool[l], b0.block_table, b0.seq_lens, ws, out=out[l])
+        if tm: tm.record(1)
+
+    spans, wall = run_timed(graph_step, 2, steps, warmup, flush_buf, stream, clocks)
+    spans2, _ = run_timed(eager_step, 2, max(10, min(steps, 200)), warmup, flush_buf, stream)
+    ops.check_error(ws)
+    return {"graph_ms": mean([x[0] for x in spans]), "eager_ms": mean([x[0] for x in spans2]),
+            "graph": g, "ws": ws, "out": out, "launches": steps * layers.layers}
+
+
+def e2e_layered_measure(layers, graph, out, steps, warmup, stream):
+    """The graph step through the public API from pinned host memory: every step copies the
+    layers' q / k_new / v_new in, replays the graph and copies the outputs back."""
+    import torch
+
+    host = {k: getattr(layers, k).cpu().pin_memory() for k in ("q", "k_new", "v_new")}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for k, t in host.items():
+            getattr(layers, k).copy_(t, non_blocking=True)
+        graph.launch()
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return {"step_ms": mean(times), "h2d": h2d, "d2h": d2h}
+
+
 def e2e_decode_measure(batch, steps, warmup, stream):
     """The decode step through the C ABI with host buffers (pa_decode_step_host): pinned
     host inputs copied in, fused append + decode, output copied back, every step."""
@@ -498,7 +561,10 @@ def reference_arm(args, world, rank):
     from paged_gqa_attention_gb300 import workloads as wl
 
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    batch = wl.WORKLOADS[args.workload](device=dev)
+    if args.workload == "layered_decode":
+        batch = wl.layered_decode(device=dev).base     # GB/s of one layer: the same per layer
+    else:
+        batch = wl.WORKLOADS[args.workload](device=dev)
     kind = "decode" if "decode" in args.workload else "prefill"
     if args.workload == "mixed_batch":
         kind = "decode"
@@ -522,7 +588,7 @@ def reference_arm(args, world, rank):
 def rows_cap_for(workload):
     """Bound on the (token, head) rows of one oracle pass (keeps a pass to seconds)."""
     return {"single_decode": None, "batched_decode": None, "mixed_batch": 1024,
-            "causal_prefill": 2048, "prefix_shared_decode": 256}[workload]
+            "causal_prefill": 2048, "prefix_shared_decode": 256, "layered_decode": None}[workload]
 
 
 def roofline(achieved, peak, unit, bound, traffic):
@@ -559,12 +625,14 @@ def main():
     clocks.start()
 
     wname = args.workload
-    batch = wl.WORKLOADS[wname](device="cuda")
+    layers = wl.layered_decode(device="cuda") if wname == "layered_decode" else None
+    batch = layers.base if layers is not None else wl.WORKLOADS[wname](device="cuda")
     dist_barrier(world)
     line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic"}
     cfg = {"workload": wname, **batch.info, "heads": "32 q / 8 kv x 128", "block_tokens": 256,
+           **({"layers": layers.layers} if layers is not None else {}),
            "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write + read)",
            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
@@ -595,6 +663,30 @@ def main():
         line["e2e"] = {"value": world * kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                        "ms_per_step": e_ms}
+        kind = "decode"
+    elif wname == "layered_decode":
+        r = layered_measure(layers, args.steps, args.warmup, flush_buf, stream, clocks)
+        kv_bytes = layers.kv_bytes()
+        io_bytes = layers.layers * (batch.num_seqs * 32 * 128 * 2 * 2 +
+                                    batch.num_seqs * (batch.max_blocks_per_seq + 1) * 4)
+        step_ms = dist_max(r["graph_ms"], world)
+        line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
+        line["roofline"] = roofline((kv_bytes + io_bytes) / (step_ms * 1e-3) / 1e9, peaks["hbm_gbs"],
+                                    "GB/s", "hbm", traffic_for("decode"))
+        line["roofline"]["kernel"] = "decode_kernel"
+        line["roofline"]["algorithmic_bytes_per_launch"] = (kv_bytes + io_bytes) // layers.layers
+        line["kernels"] = {"layers": layers.layers, "graph_step_us": r["graph_ms"] * 1e3,
+                           "graph_us_per_layer": r["graph_ms"] * 1e3 / layers.layers,
+                           "one_call_per_layer_step_us": r["eager_ms"] * 1e3,
+                           "one_call_per_layer_us_per_layer": r["eager_ms"] * 1e3 / layers.layers,
+                           "kv_bytes_per_step": kv_bytes}
+        line["gpu_launches"] = r["launches"]
+        e = e2e_layered_measure(layers, r["graph"], r["out"], max(20, min(args.steps, 200)), 5, stream)
+        e_ms = dist_max(e["step_ms"], world)
+        line["e2e"] = {"value": world * kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                       "ms_per_step": e_ms}
+        r["graph"].close()
         kind = "decode"
     elif wname == "causal_prefill":
         r = prefill_measure(batch, args.steps, args.warmup, flush_buf, stream, clocks)
@@ -663,7 +755,7 @@ def main():
     line["clocks"] = clocks.stop()
     line["peaks"] = peaks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        src = wl.WORKLOADS[wname](device="cuda") if wname != batch.name else batch
+        src = batch if wname in ("layered_decode", batch.name) else wl.WORKLOADS[wname](device="cuda")
         line["cpu_baseline"] = cpu_baseline(src, kind, args.cpu_seconds, rows_cap_for(wname))
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -40,7 +40,12 @@
  * paged_attn_decode_static, which uses a fixed array of its own instead).
  *
  * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
- * are asynchronous and stream-ordered; PA_OK means "validated and launched".
+ * are asynchronous and stream-ordered; PA_OK means "validated and launched".  The
+ * decode and prefill kernels are launched as programmatic dependents of the kernel
+ * before them on the stream: they may start before it has finished, and wait for it
+ * before touching q, k_new, v_new, the pools, out or lse.  block_table, seq_lens and
+ * cu_q_lens may be read earlier, so a kernel that writes them immediately before a
+ * call must not let its dependents start early (griddepcontrol.launch_dependents).
  *
  * Errors.  Scalar arguments and pointers are checked on the host (PA_ERR_INVALID_ARG,
  * PA_ERR_UNSUPPORTED) before anything is launched.  Device arrays the host does not
@@ -188,6 +193,43 @@ pa_status pa_decode_step_host(pa_shape shape, void *out_host, float *lse_host,
                               void *v_pool, int32_t num_blocks, float scale, void *staging,
                               size_t staging_bytes, void *workspace, size_t workspace_bytes,
                               void *stream);
+
+/*
+ * A decode step over several layers captured once as a CUDA graph and replayed per
+ * step: the launch-gap remedy the pages name for a GPU kept idle between kernel
+ * launches [P2 §4.2 troubleshooting table: "use CUDA Graph"], decode being dominated by
+ * many small launches [P1 §2.2].  Each replay runs, for layer l = 0 .. layers-1 in
+ * order, paged_attn_decode_append on layer l's slices of layer-major tensors:
+ *   q, out          bf16 [layers][batch][32][128]
+ *   k_new, v_new    bf16 [layers][batch][8][128]
+ *   lse             fp32 [layers][batch][32], or NULL
+ *   k_pool, v_pool  bf16 [layers][num_blocks][256][8][128]
+ * with one block_table / seq_lens shared by all layers (the sequences are the same in
+ * every layer) and one workspace (the layers run one after another).  The graph holds
+ * the pointers given here: between replays the caller updates the contents in place
+ * (new q / k_new / v_new, seq_lens + 1, grown tables), never the pointers.  Results
+ * are those of the same calls made one by one.
+ *
+ * pa_decode_graph_create  validates as paged_attn_decode_append does, captures the
+ *                         layers on a private stream (nothing runs) and instantiates
+ *                         the graph; *graph receives a handle (NULL on failure).
+ *                         batch must be >= 1; the graph is tied to the current device.
+ * pa_decode_graph_launch  enqueues one replay on `stream`.
+ * pa_decode_graph_destroy releases the handle (NULL is accepted).
+ */
+typedef struct pa_decode_graph pa_decode_graph;
+
+pa_status pa_decode_graph_create(pa_shape shape, int32_t layers, void *out, float *lse,
+                                 const void *q, const void *k_new, const void *v_new,
+                                 void *k_pool, void *v_pool, const int32_t *block_table,
+                                 int32_t max_blocks_per_seq, int32_t num_blocks,
+                                 const int32_t *seq_lens, int32_t batch, float scale,
+                                 void *workspace, size_t workspace_bytes,
+                                 pa_decode_graph **graph);
+
+pa_status pa_decode_graph_launch(pa_decode_graph *graph, void *stream);
+
+pa_status pa_decode_graph_destroy(pa_decode_graph *graph);
 
 /*
  * paged_attn_decode_static: paged_attn_decode for callers that cannot allocate device

@@ -3,12 +3,21 @@
 #include <atomic>
 #include <cmath>
 #include <mutex>
+#include <new>
 
 #include <cudaTypedefs.h>
 
 #include "pagedattn.h"
 #include "common.cuh"
 #include "launch.h"
+
+// Handle of pa_decode_graph_create: the captured graph, its executable form and the
+// device it was captured on.
+struct pa_decode_graph {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    int device = -1;
+};
 
 namespace {
 
@@ -467,6 +476,83 @@ pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *
     return launch_prefill(a, q_map, k_map, v_map, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
+}
+
+pa_status pa_decode_graph_create(pa_shape shape, int32_t layers, void *out, float *lse, const void *q,
+                                 const void *k_new, const void *v_new, void *k_pool, void *v_pool,
+                                 const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
+                                 const int32_t *seq_lens, int32_t batch, float scale, void *workspace,
+                                 size_t workspace_bytes, pa_decode_graph **graph) {
+    if (!graph) return PA_ERR_INVALID_ARG;
+    *graph = nullptr;
+    if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
+    if (layers < 1 || batch < 1 || num_blocks < 1 || !k_new || !v_new || !out || !q || !k_pool || !v_pool)
+        return PA_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    // Everything that is not a launch happens before the capture: kernel attributes,
+    // the SM count and the tensor-map encoder are set up once here.
+    if (configure_decode() != cudaSuccess || sm_count() <= 0 || !get_encoder()) return PA_ERR_CUDA;
+
+    const size_t q_bytes = (size_t)batch * kHq * kD * sizeof(__nv_bfloat16);     // per layer
+    const size_t kv_bytes = (size_t)batch * kHkv * kD * sizeof(__nv_bfloat16);
+    const size_t lse_floats = (size_t)batch * kHq;
+    const size_t pool_bytes = (size_t)num_blocks * kBlock * kHkv * kD * sizeof(__nv_bfloat16);
+    cudaStream_t cs = nullptr;
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaStreamDestroy(cs);
+        return PA_ERR_CUDA;
+    }
+    pa_status st = PA_OK;
+    for (int32_t l = 0; l < layers && st == PA_OK; ++l) {
+        st = decode_impl(shape, static_cast<char *>(out) + l * q_bytes, lse ? lse + l * lse_floats : nullptr,
+                         static_cast<const char *>(q) + l * q_bytes, static_cast<const char *>(k_new) + l * kv_bytes,
+                         static_cast<const char *>(v_new) + l * kv_bytes, static_cast<char *>(k_pool) + l * pool_bytes,
+                         static_cast<char *>(v_pool) + l * pool_bytes, block_table, max_blocks_per_seq, num_blocks,
+                         seq_lens, batch, scale, 0, workspace, workspace_bytes, cs);
+    }
+    cudaGraph_t g = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(cs, &g);
+    cudaStreamDestroy(cs);
+    if (st != PA_OK || ce != cudaSuccess || !g) {
+        if (g) cudaGraphDestroy(g);
+        cudaGetLastError();
+        return st != PA_OK ? st : PA_ERR_CUDA;
+    }
+    cudaGraphExec_t x = nullptr;
+    if (cudaGraphInstantiate(&x, g, 0) != cudaSuccess) {
+        cudaGraphDestroy(g);
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    pa_decode_graph *h = new (std::nothrow) pa_decode_graph;
+    if (!h) {
+        cudaGraphExecDestroy(x);
+        cudaGraphDestroy(g);
+        return PA_ERR_CUDA;
+    }
+    h->graph = g;
+    h->exec = x;
+    h->device = dev;
+    *graph = h;
+    return PA_OK;
+}
+
+pa_status pa_decode_graph_launch(pa_decode_graph *graph, void *stream) {
+    if (!graph || !graph->exec) return PA_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (dev != graph->device) return PA_ERR_INVALID_ARG;
+    return cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_decode_graph_destroy(pa_decode_graph *graph) {
+    if (!graph) return PA_OK;
+    const bool ok = (!graph->exec || cudaGraphExecDestroy(graph->exec) == cudaSuccess) &
+                    (!graph->graph || cudaGraphDestroy(graph->graph) == cudaSuccess);
+    delete graph;
+    return ok ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_selftest_wait_timeout(void *workspace, size_t workspace_bytes, uint32_t timeout_us, void *stream) {

@@ -28,6 +28,7 @@
 // recorded in the error word and makes the (sequence, KV head)'s output NaN.
 // The kernel is launched as a programmatic dependent of the previous kernel on the
 // stream, so its launch and prologue overlap e.g. the kv_append that precedes it.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -118,6 +119,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         if (lane == 0) {
             // The pools may be written by the kernel just before this one on the stream
             // (kv_append lets us launch early): wait for it before the first pool read.
+            // The consumer warps wait too, before reading q or k_new / v_new.
             asm volatile("griddepcontrol.wait;" ::: "memory");
             int issued = 0;
             for (int i = 0; i < n_tiles; ++i) {
@@ -156,6 +158,11 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     const int tq = lane & 3;    // fragment column pair
     const int mi = lane >> 3;   // ldmatrix: which 8x8 matrix this lane addresses
     const int ri = lane & 7;    // ldmatrix: row within it
+
+    // q, k_new and v_new may come from the kernel just before this one on the stream, and
+    // the pools may still be read by it: wait for it before the first access to any of them
+    // (only block_table and seq_lens are read earlier).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Q^T as the B operand of S^T = K Q^T: [k = 16 dims] x [n = 8 heads], heads 4..7 zero.
     uint32_t qb[8][2];
@@ -389,19 +396,25 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
 
 }  // namespace
 
+cudaError_t configure_decode() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::atomic<bool> configured[64] = {};
+    if (dev < 0 || dev >= 64 || !configured[dev].load()) {
+        e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev].store(true);
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
                           int num_sms, cudaStream_t stream) {
     (void)num_sms;
     if (a.batch == 0) return cudaSuccess;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = configure_decode();
     if (e != cudaSuccess) return e;
-    static bool configured[64] = {};
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = true;
-    }
     // Programmatic dependent launch: the prologue may overlap the previous kernel on the
     // stream; the producer waits for it (griddepcontrol.wait) before reading the pools.
     cudaLaunchConfig_t cfg = {};

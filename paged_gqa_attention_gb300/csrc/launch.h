@@ -65,6 +65,10 @@ struct PrefillArgs {
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
 
 // k_map / v_map: 4-D tensor maps over the pools (see api.cu for the boxes).
+// One-time per-device kernel setup (dynamic shared memory size) of the decode kernel;
+// launch_decode does it on first use, callers about to capture launches do it first.
+cudaError_t configure_decode();
+
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
                           const CUtensorMap &v_map, int num_sms, cudaStream_t stream);
 

@@ -88,6 +88,13 @@ def load() -> ctypes.CDLL:
     lib.pa_decode_step_host.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, f32,
                                         vp, sz, vp, sz, vp]
     lib.pa_decode_step_host.restype = ctypes.c_int
+    lib.pa_decode_graph_create.argtypes = [pa_shape, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp,
+                                           i32, f32, vp, sz, ctypes.POINTER(vp)]
+    lib.pa_decode_graph_create.restype = ctypes.c_int
+    lib.pa_decode_graph_launch.argtypes = [vp, vp]
+    lib.pa_decode_graph_launch.restype = ctypes.c_int
+    lib.pa_decode_graph_destroy.argtypes = [vp]
+    lib.pa_decode_graph_destroy.restype = ctypes.c_int
     lib.pa_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint32, vp]
     lib.pa_selftest_wait_timeout.restype = ctypes.c_int
     _lib = lib
@@ -240,6 +247,65 @@ def paged_attn_decode_append(q, k_new, v_new, k_pool, v_pool, block_table, seq_l
                                          _stream(stream))
     _check("paged_attn_decode_append", st)
     return out
+
+
+class DecodeGraph:
+    """A decode step over several layers captured as one CUDA graph (pa_decode_graph_*).
+
+    The graph holds the tensors' device pointers: update their contents in place between
+    launches (new q / k_new / v_new, seq_lens + 1, grown block tables), never rebind them.
+    The tensors are kept alive for as long as the handle is."""
+
+    def __init__(self, handle: int, tensors: tuple):
+        self._handle = handle
+        self._tensors = tensors
+
+    def launch(self, stream=None) -> None:
+        if not self._handle:
+            raise RuntimeError("DecodeGraph is closed")
+        _check("pa_decode_graph_launch", load().pa_decode_graph_launch(self._handle, _stream(stream)))
+
+    def close(self) -> None:
+        if self._handle:
+            h, self._handle = self._handle, None
+            _check("pa_decode_graph_destroy", load().pa_decode_graph_destroy(h))
+        self._tensors = ()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def decode_graph(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, workspace, *,
+                 out, lse=None, scale: float = DEFAULT_SCALE) -> DecodeGraph:
+    """Capture paged_attn_decode_append over L layers as one CUDA graph.  Layer-major
+    tensors: q / out [L, B, 32, 128], k_new / v_new [L, B, 8, 128], pools
+    [L, N, 256, 8, 128], lse [L, B, 32] or None; block_table [B, W] and seq_lens [B]
+    are shared by every layer."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (None, None, NUM_Q_HEADS, HEAD_DIM), dev)
+    layers, batch = q.shape[0], q.shape[1]
+    _need(k_new, "k_new", torch.bfloat16, (layers, batch, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_new, "v_new", torch.bfloat16, (layers, batch, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(k_pool, "k_pool", torch.bfloat16, (layers, None, BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_pool, "v_pool", torch.bfloat16, tuple(k_pool.shape), dev)
+    _need(out, "out", torch.bfloat16, tuple(q.shape), dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (layers, batch, NUM_Q_HEADS), dev)
+    _need(block_table, "block_table", torch.int32, (batch, None), dev)
+    _need(seq_lens, "seq_lens", torch.int32, (batch,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    handle = ctypes.c_void_p(0)
+    st = load().pa_decode_graph_create(SHAPE, layers, out.data_ptr(), _ptr(lse), q.data_ptr(),
+                                       k_new.data_ptr(), v_new.data_ptr(), k_pool.data_ptr(),
+                                       v_pool.data_ptr(), block_table.data_ptr(), block_table.shape[1],
+                                       k_pool.shape[1], seq_lens.data_ptr(), batch, float(scale),
+                                       workspace.data_ptr(), workspace.numel(), ctypes.byref(handle))
+    _check("pa_decode_graph_create", st)
+    return DecodeGraph(handle.value, (q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, workspace,
+                                      out, lse))
 
 
 def paged_attn_prefill(q, k_pool, v_pool, block_table, cu_q_lens, seq_lens, max_q_len: int,

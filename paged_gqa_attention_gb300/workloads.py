@@ -22,7 +22,7 @@ Config names:
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 
 import torch
 
@@ -278,6 +278,57 @@ def prefix_shared_decode(device="cpu", seed: int = 4, batch: int = 128, context:
                        num_blocks=num_blocks, device=device, shared_prefix_blocks=shared_blocks,
                        info={"batch": batch, "context": context, "shared_blocks": shared_blocks,
                              "pool_blocks": num_blocks})
+
+
+@dataclass
+class Layers:
+    """A decode batch repeated over L layers, layer-major: q [L, B, Hq, D], k_new / v_new
+    [L, B, Hkv, D], k_pool / v_pool [L, N, 256, Hkv, D]; block_table and seq_lens are
+    shared by every layer (the batch's own).  Layer 0 holds the batch's values; the other
+    layers hold fresh values in the same pool slots (unowned slots stay sentinels)."""
+
+    base: Batch
+    q: torch.Tensor
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+    k_pool: torch.Tensor
+    v_pool: torch.Tensor
+
+    @property
+    def layers(self) -> int:
+        return int(self.q.shape[0])
+
+    def layer(self, l: int) -> Batch:
+        """Layer l as a Batch (views into the layer-major tensors)."""
+        return replace(self.base, name=f"{self.base.name}[{l}]", q=self.q[l], k_new=self.k_new[l],
+                       v_new=self.v_new[l], k_pool=self.k_pool[l], v_pool=self.v_pool[l])
+
+    def kv_bytes(self) -> int:
+        return self.layers * self.base.kv_bytes()
+
+
+def layered(batch: Batch, layers: int, seed: int) -> Layers:
+    """Stack `layers` copies of a decode batch (one new token per sequence) with fresh
+    seeded values per layer, for the multi-layer decode step."""
+    assert all(ql == 1 for ql in batch.q_lens_host), "a decode batch (one new token per sequence)"
+    dev = batch.q.device
+    gen = _gen(seed, dev)
+    qs, kns, vns, kps, vps = [batch.q], [batch.k_new], [batch.v_new], [batch.k_pool], [batch.v_pool]
+    owned = ~torch.isnan(batch.k_pool.float())
+    for _ in range(1, layers):
+        qs.append(_randn_bf16(tuple(batch.q.shape), gen, dev))
+        kns.append(_randn_bf16(tuple(batch.k_new.shape), gen, dev))
+        vns.append(_randn_bf16(tuple(batch.v_new.shape), gen, dev))
+        kps.append(torch.where(owned, _randn_bf16(tuple(batch.k_pool.shape), gen, dev), batch.k_pool))
+        vps.append(torch.where(owned, _randn_bf16(tuple(batch.v_pool.shape), gen, dev), batch.v_pool))
+    return Layers(batch, torch.stack(qs), torch.stack(kns), torch.stack(vns), torch.stack(kps),
+                  torch.stack(vps))
+
+
+def layered_decode(device="cpu", seed: int = 5, layers: int = 36) -> Layers:
+    """The single-sequence decode (context 512, 8-block pool) over the 36 layers of the
+    model: the launch-bound case the multi-layer CUDA graph serves."""
+    return layered(single_decode(device=device), layers, seed)
 
 
 WORKLOADS = {
