@@ -6,11 +6,14 @@ no code with the CUDA path: the arithmetic lives in ``oracle.c`` (plain C,
 double precision, the textbook definition written out loop by loop).
 
 Functions take CPU tensors (torch or numpy) holding the same bf16 bit patterns the
-GPU sees and return float64 results.
+GPU sees and return float64 results.  The 8-bit KV cache (E4M3 codes, one fp32 scale per
+(token, KV head) row) has its own append and attention: ``kv_append_fp8``,
+``attention_fp8``, with the codec ``e4m3_encode`` / ``e4m3_decode``.
 
 Parity status: every function here is pinned by the CPU tests in
-``tests/test_oracle_pins.py`` (closed forms, a library routine on tiny cases,
-invariants and a high-precision brute force).
+``tests/test_oracle_pins.py`` and ``tests/test_oracle_fp8.py`` (closed forms, library
+routines on tiny cases -- torch SDPA, torch's float8_e4m3fn -- invariants, the format's
+error bound and a high-precision brute force).
 """
 from __future__ import annotations
 
@@ -56,6 +59,18 @@ def load_library(path: str):
     lib.oracle_paged_attention.restype = ci
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ci
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_e4m3_encode.argtypes = [f32p, u8p, ctypes.c_long]
+    lib.oracle_e4m3_encode.restype = None
+    lib.oracle_e4m3_decode.argtypes = [u8p, f64p, ctypes.c_long]
+    lib.oracle_e4m3_decode.restype = None
+    lib.oracle_kv_append_fp8.argtypes = [u8p, u8p, f32p, f32p, u16p, u16p, i32p, ci, ci, i32p, i32p,
+                                         ci, ci, ci, ci]
+    lib.oracle_kv_append_fp8.restype = ci
+    lib.oracle_paged_attention_fp8.argtypes = [f64p, f64p, u16p, u8p, u8p, f32p, f32p, i32p, ci, ci,
+                                               i32p, i32p, ci, ci, ci, ci, ci, ctypes.c_double, ci]
+    lib.oracle_paged_attention_fp8.restype = ci
     return lib
 
 
@@ -155,4 +170,80 @@ def attention(q, k_pool, v_pool, block_table, cu_q_lens, seq_lens, *, scale: flo
                                        float(scale), int(num_threads))
     if rc:
         raise ValueError(f"oracle attention rejected its input (code {rc})")
+    return out, lse
+
+
+# ------------------------------------------------------------------ 8-bit KV cache
+
+def _u8(x) -> np.ndarray:
+    if not isinstance(x, np.ndarray):
+        x = x.cpu().numpy()
+    assert x.dtype == np.uint8
+    return np.ascontiguousarray(x)
+
+
+def _f32(x) -> np.ndarray:
+    if not isinstance(x, np.ndarray):
+        x = x.cpu().numpy()
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def e4m3_encode(x, *, lib=None) -> np.ndarray:
+    """float32 values -> E4M3 codes (round to nearest even, |x| > 448 -> +-448)."""
+    xf = _f32(np.asarray(x, dtype=np.float32))
+    out = np.zeros(xf.shape, np.uint8)
+    (lib or _load()).oracle_e4m3_encode(_p(xf, ctypes.c_float), _p(out, ctypes.c_uint8), xf.size)
+    return out
+
+
+def e4m3_decode(c, *, lib=None) -> np.ndarray:
+    """E4M3 codes -> float64 values."""
+    cu = _u8(np.asarray(c, dtype=np.uint8))
+    out = np.zeros(cu.shape, np.float64)
+    (lib or _load()).oracle_e4m3_decode(_p(cu, ctypes.c_uint8), _p(out, ctypes.c_double), cu.size)
+    return out
+
+
+def kv_append_fp8(k_codes, v_codes, k_scale, v_scale, k_new, v_new, block_table, cu_q_lens,
+                  seq_lens, *, block_size: int = 256, lib=None):
+    """Return (k_codes', v_codes', k_scale', v_scale'): the 8-bit cache after quantising and
+    appending the new rows.  codes: uint8 [num_blocks, block_size, Hkv, D]; scales: float32
+    [num_blocks, Hkv, block_size]; k_new/v_new: bf16 [total_tokens, Hkv, D]."""
+    kc, vc = _u8(k_codes).copy(), _u8(v_codes).copy()
+    ks, vs = _f32(k_scale).copy(), _f32(v_scale).copy()
+    kn, vn = _bits(k_new), _bits(v_new)
+    bt, cu, sl = _i32(block_table), _i32(cu_q_lens), _i32(seq_lens)
+    num_blocks, bs, hkv, d = kc.shape
+    assert bs == block_size and ks.shape == (num_blocks, hkv, bs)
+    rc = (lib or _load()).oracle_kv_append_fp8(
+        _p(kc, ctypes.c_uint8), _p(vc, ctypes.c_uint8), _p(ks, ctypes.c_float), _p(vs, ctypes.c_float),
+        _p(kn, ctypes.c_uint16), _p(vn, ctypes.c_uint16), _p(bt, ctypes.c_int32), bt.shape[1],
+        num_blocks, _p(cu, ctypes.c_int32), _p(sl, ctypes.c_int32), len(sl), hkv, d, bs)
+    if rc:
+        raise ValueError(f"oracle_kv_append_fp8 rejected its input (code {rc})")
+    return kc, vc, ks, vs
+
+
+def attention_fp8(q, k_codes, v_codes, k_scale, v_scale, block_table, cu_q_lens, seq_lens, *,
+                  scale: float, num_threads: int = 0, lib=None):
+    """Paged causal GQA attention in fp64 over the 8-bit cache (K/V = code * row scale).
+    Returns (out [T, Hq, D], lse [T, Hq]) float64."""
+    qb = _bits(q)
+    kc, vc, ks, vs = _u8(k_codes), _u8(v_codes), _f32(k_scale), _f32(v_scale)
+    bt, cu, sl = _i32(block_table), _i32(cu_q_lens), _i32(seq_lens)
+    t, hq, d = qb.shape
+    num_blocks, bs, hkv, d2 = kc.shape
+    assert d == d2 and vc.shape == kc.shape and ks.shape == (num_blocks, hkv, bs) == vs.shape
+    if bt.ndim == 1:
+        bt = bt.reshape(len(sl), -1)
+    out = np.zeros((t, hq, d), np.float64)
+    lse = np.zeros((t, hq), np.float64)
+    if t:
+        rc = (lib or _load()).oracle_paged_attention_fp8(
+            _p(out, ctypes.c_double), _p(lse, ctypes.c_double), _p(qb, ctypes.c_uint16),
+            _p(kc, ctypes.c_uint8), _p(vc, ctypes.c_uint8), _p(ks, ctypes.c_float), _p(vs, ctypes.c_float),
+            _p(bt, ctypes.c_int32), bt.shape[1], num_blocks, _p(cu, ctypes.c_int32), _p(sl, ctypes.c_int32),
+            len(sl), hq, hkv, d, bs, float(scale), int(num_threads))
+        if rc:
+            raise ValueError(f"oracle attention_fp8 rejected its input (code {rc})")
     return out, lse

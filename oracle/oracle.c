@@ -37,6 +37,10 @@
  *   out      [total_tokens][Hq][D]                 double
  *   lse      [total_tokens][Hq]                    double (natural log)
  *   block_table [num_seqs][max_blocks_per_seq]     int32
+ * The 8-bit cache (E4M3 codes with one fp32 scale per row; its definition is given at
+ * oracle_kv_append_fp8 below):
+ *   k_codes  [num_blocks][block_size][Hkv][D]      uint8, v_codes likewise
+ *   k_scale  [num_blocks][Hkv][block_size]         float, v_scale likewise
  *
  * Functions return 0 on success and a negative code on inconsistent input.
  */
@@ -123,16 +127,50 @@ int oracle_kv_append(uint16_t *k_pool, uint16_t *v_pool,
 }
 
 /*
+ * The KV cache an attention call reads: the bf16 pools, or the 8-bit cache (codes and
+ * row scales, see below).  Exactly one of the two pairs is set.
+ */
+typedef struct {
+    const uint16_t *k_pool, *v_pool;     /* bf16 [num_blocks][block_size][Hkv][D] */
+    const uint8_t *k_codes, *v_codes;    /* E4M3 [num_blocks][block_size][Hkv][D] */
+    const float *k_scale, *v_scale;      /* [num_blocks][Hkv][block_size] */
+    int num_kv_heads, head_dim, block_size;
+} kv_cache;
+
+static double e4m3_to_double(uint8_t c);
+
+/* Element offset of the row of KV head g for token j (block bt[j/bs], slot j%bs). */
+static size_t kv_row(const kv_cache *c, const int32_t *bt, int j, int g)
+{
+    return (((size_t)bt[j / c->block_size] * c->block_size + j % c->block_size) * c->num_kv_heads + g)
+           * c->head_dim;
+}
+
+/* The row's scale in the 8-bit cache; the bf16 cache has none (1). */
+static double kv_row_scale(const kv_cache *c, const float *scales, const int32_t *bt, int j, int g)
+{
+    if (!scales) return 1.0;
+    return (double)scales[((size_t)bt[j / c->block_size] * c->num_kv_heads + g) * c->block_size
+                          + (size_t)(j % c->block_size)];
+}
+
+/* Element d of the row at offset base: the bf16 value, or code * row scale. */
+static double kv_elem(const uint16_t *pool, const uint8_t *codes, size_t base, int d, double row_scale)
+{
+    return pool ? bf16_to_double(pool[base + d]) : e4m3_to_double(codes[base + d]) * row_scale;
+}
+
+/*
  * One output row: query token t, query head h.  Writes out_row[0..D) and *lse_out.
  * scores: caller-provided scratch of at least (p + 1) doubles.
  */
 static void attend_one(double *out_row, double *lse_out, double *scores,
-                       const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                       const uint16_t *q, const kv_cache *c,
                        const int32_t *block_table, int max_blocks_per_seq,
                        const int32_t *cu_q_lens, const int32_t *seq_lens, int num_seqs,
-                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                       double scale, int t, int h)
+                       int num_q_heads, double scale, int t, int h)
 {
+    const int num_kv_heads = c->num_kv_heads, head_dim = c->head_dim;
     int s = owner_sequence(cu_q_lens, num_seqs, t);
     int q_len = cu_q_lens[s + 1] - cu_q_lens[s];
     int i = t - cu_q_lens[s];
@@ -144,11 +182,11 @@ static void attend_one(double *out_row, double *lse_out, double *scores,
     /* x_j = scale * <q, k_j> for every visible key j <= p (causal, diagonal included) */
     double m = -INFINITY;
     for (int j = 0; j <= p; ++j) {
-        size_t base = (((size_t)bt[j / block_size] * block_size + j % block_size) * num_kv_heads + g)
-                      * head_dim;
+        size_t base = kv_row(c, bt, j, g);
+        double ks = kv_row_scale(c, c->k_scale, bt, j, g);
         double dot = 0.0;
         for (int d = 0; d < head_dim; ++d)
-            dot += bf16_to_double(qrow[d]) * bf16_to_double(k_pool[base + d]);
+            dot += bf16_to_double(qrow[d]) * kv_elem(c->k_pool, c->k_codes, base, d, ks);
         scores[j] = scale * dot;
         if (scores[j] > m) m = scores[j];
     }
@@ -160,31 +198,25 @@ static void attend_one(double *out_row, double *lse_out, double *scores,
     }
     for (int d = 0; d < head_dim; ++d) out_row[d] = 0.0;
     for (int j = 0; j <= p; ++j) {
-        size_t base = (((size_t)bt[j / block_size] * block_size + j % block_size) * num_kv_heads + g)
-                      * head_dim;
+        size_t base = kv_row(c, bt, j, g);
+        double vs = kv_row_scale(c, c->v_scale, bt, j, g);
         double w = scores[j];
-        for (int d = 0; d < head_dim; ++d) out_row[d] += w * bf16_to_double(v_pool[base + d]);
+        for (int d = 0; d < head_dim; ++d) out_row[d] += w * kv_elem(c->v_pool, c->v_codes, base, d, vs);
     }
     for (int d = 0; d < head_dim; ++d) out_row[d] /= denom;
     *lse_out = m + log(denom);
 }
 
-/*
- * Attention for a list of (token, head) output rows.  out: [n][D], lse: [n].
- * The rows are independent; they are distributed over OpenMP threads when
- * num_threads > 0 (0 = the OpenMP default).
- */
-int oracle_attention_rows(double *out, double *lse,
-                          const int32_t *row_tokens, const int32_t *row_heads, int n,
-                          const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+/* Rows (token, head) over either cache, spread over OpenMP threads. */
+static int attention_rows(double *out, double *lse, const int32_t *row_tokens, const int32_t *row_heads,
+                          int n, const uint16_t *q, const kv_cache *c,
                           const int32_t *block_table, int max_blocks_per_seq, int num_blocks,
                           const int32_t *cu_q_lens, const int32_t *seq_lens, int num_seqs,
-                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                          double scale, int num_threads)
+                          int num_q_heads, double scale, int num_threads)
 {
-    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return -10;
+    if (num_q_heads <= 0 || c->num_kv_heads <= 0 || num_q_heads % c->num_kv_heads) return -10;
     int rc = check_common(block_table, max_blocks_per_seq, num_blocks, cu_q_lens, seq_lens,
-                          num_seqs, block_size);
+                          num_seqs, c->block_size);
     if (rc) return rc;
     int total_tokens = num_seqs > 0 ? cu_q_lens[num_seqs] : 0;
     int max_ctx = 1;
@@ -213,9 +245,8 @@ int oracle_attention_rows(double *out, double *lse,
 #endif
         for (int r = 0; r < n; ++r) {
             if (!scores) continue;
-            attend_one(out + (size_t)r * head_dim, lse + r, scores, q, k_pool, v_pool,
-                       block_table, max_blocks_per_seq, cu_q_lens, seq_lens, num_seqs,
-                       num_q_heads, num_kv_heads, head_dim, block_size, scale,
+            attend_one(out + (size_t)r * c->head_dim, lse + r, scores, q, c, block_table,
+                       max_blocks_per_seq, cu_q_lens, seq_lens, num_seqs, num_q_heads, scale,
                        row_tokens[r], row_heads[r]);
         }
         free(scores);
@@ -224,12 +255,10 @@ int oracle_attention_rows(double *out, double *lse,
 }
 
 /* Every row of every new token: out [total_tokens][Hq][D], lse [total_tokens][Hq]. */
-int oracle_paged_attention(double *out, double *lse,
-                           const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
-                           const int32_t *block_table, int max_blocks_per_seq, int num_blocks,
-                           const int32_t *cu_q_lens, const int32_t *seq_lens, int num_seqs,
-                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                           double scale, int num_threads)
+static int attention_all(double *out, double *lse, const uint16_t *q, const kv_cache *c,
+                         const int32_t *block_table, int max_blocks_per_seq, int num_blocks,
+                         const int32_t *cu_q_lens, const int32_t *seq_lens, int num_seqs,
+                         int num_q_heads, double scale, int num_threads)
 {
     int total_tokens = num_seqs > 0 ? cu_q_lens[num_seqs] : 0;
     int n = total_tokens * num_q_heads;
@@ -238,13 +267,172 @@ int oracle_paged_attention(double *out, double *lse,
     int32_t *hd = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
     if (!tok || !hd) { free(tok); free(hd); return -12; }
     for (int r = 0; r < n; ++r) { tok[r] = r / num_q_heads; hd[r] = r % num_q_heads; }
-    int rc = oracle_attention_rows(out, lse, tok, hd, n, q, k_pool, v_pool, block_table,
-                                   max_blocks_per_seq, num_blocks, cu_q_lens, seq_lens, num_seqs,
-                                   num_q_heads, num_kv_heads, head_dim, block_size, scale,
-                                   num_threads);
+    int rc = attention_rows(out, lse, tok, hd, n, q, c, block_table, max_blocks_per_seq, num_blocks,
+                            cu_q_lens, seq_lens, num_seqs, num_q_heads, scale, num_threads);
     free(tok);
     free(hd);
     return rc;
+}
+
+/*
+ * Attention for a list of (token, head) output rows over the bf16 cache.
+ * out: [n][D], lse: [n].  num_threads > 0 fixes the OpenMP thread count (0 = default).
+ */
+int oracle_attention_rows(double *out, double *lse,
+                          const int32_t *row_tokens, const int32_t *row_heads, int n,
+                          const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                          const int32_t *block_table, int max_blocks_per_seq, int num_blocks,
+                          const int32_t *cu_q_lens, const int32_t *seq_lens, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          double scale, int num_threads)
+{
+    kv_cache c = {k_pool, v_pool, NULL, NULL, NULL, NULL, num_kv_heads, head_dim, block_size};
+    return attention_rows(out, lse, row_tokens, row_heads, n, q, &c, block_table, max_blocks_per_seq,
+                          num_blocks, cu_q_lens, seq_lens, num_seqs, num_q_heads, scale, num_threads);
+}
+
+/* Every row of every new token over the bf16 cache. */
+int oracle_paged_attention(double *out, double *lse,
+                           const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                           const int32_t *block_table, int max_blocks_per_seq, int num_blocks,
+                           const int32_t *cu_q_lens, const int32_t *seq_lens, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           double scale, int num_threads)
+{
+    kv_cache c = {k_pool, v_pool, NULL, NULL, NULL, NULL, num_kv_heads, head_dim, block_size};
+    return attention_all(out, lse, q, &c, block_table, max_blocks_per_seq, num_blocks, cu_q_lens,
+                         seq_lens, num_seqs, num_q_heads, scale, num_threads);
+}
+
+/* ======================================================================== 8-bit KV cache
+ *
+ * [P3 §3.2]: keeping the KV cache in 8 bits instead of 16 halves its memory (the page
+ * quantises to INT8 and warns that the error accumulates over decode steps).  Reading
+ * taken here: the 8-bit code is the E4M3 float of the OCP FP8 format, with one fp32
+ * scale per (token, KV head) row.
+ *
+ * E4M3: bit 7 sign, bits 6..3 exponent field e (bias 7), bits 2..0 mantissa m.
+ *   e = 0:            value (-1)^s * m * 2^-9          (zero and subnormals)
+ *   1 <= e <= 15:     value (-1)^s * (1 + m/8) * 2^(e-7)
+ *   e = 15, m = 7:    NaN (there is no infinity); the largest finite value is 448.
+ * Quantising a row x[0..D) of new K (or V) for one KV head:
+ *   amax  = max_d |x_d|                                   (exact)
+ *   scale = amax / 448 in fp32 (round to nearest even), or 1 when amax == 0
+ *   c_d   = E4M3(x_d / scale): the fp32 quotient rounded to the nearest E4M3 value
+ *           (ties to even mantissa); magnitudes beyond 448 become 448
+ * and the stored row stands for c_d * scale.
+ *
+ * Layouts: codes  [num_blocks][block_size][Hkv][D] uint8 (as the bf16 pools)
+ *          scales [num_blocks][Hkv][block_size] float (one row of scales per block and head)
+ */
+static double e4m3_to_double(uint8_t c)
+{
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+static uint8_t e4m3_from_float(float x)
+{
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a > 448.0) return sign | 0x7E;                    /* saturate to the largest finite */
+    if (a < ldexp(1.0, -6)) {                             /* subnormal range: quantum 2^-9 */
+        double m = nearbyint(a * 512.0);                  /* ties to even (default mode) */
+        return sign | (uint8_t)m;                         /* m = 8 is 2^-6, code 0x08: correct */
+    }
+    int k;
+    frexp(a, &k);                                         /* a = f * 2^k, f in [0.5, 1) */
+    int e = k - 1;                                        /* a in [2^e, 2^(e+1)) */
+    double m = nearbyint(ldexp(a, 3 - e));                /* 8 <= m <= 16, exact scaling */
+    if (m == 16.0) { m = 8.0; e += 1; }
+    if (e > 8 || (e == 8 && m > 14.0)) return sign | 0x7E;
+    return sign | (uint8_t)(((e + 7) << 3) | ((int)m - 8));
+}
+
+/* Element-wise codec, exposed for the oracle's own pins. */
+void oracle_e4m3_encode(const float *x, uint8_t *c, long n)
+{
+    for (long i = 0; i < n; ++i) c[i] = e4m3_from_float(x[i]);
+}
+
+void oracle_e4m3_decode(const uint8_t *c, double *x, long n)
+{
+    for (long i = 0; i < n; ++i) x[i] = e4m3_to_double(c[i]);
+}
+
+static float bf16_to_float(uint16_t bits)
+{
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return f;
+}
+
+/* Quantise one row of D bf16 values into D codes and its scale. */
+static void quantise_row(const uint16_t *x, int d_len, uint8_t *codes, float *scale_out)
+{
+    float amax = 0.0f;
+    for (int d = 0; d < d_len; ++d) {
+        float v = fabsf(bf16_to_float(x[d]));
+        if (v > amax) amax = v;
+    }
+    float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int d = 0; d < d_len; ++d) {
+        float q = bf16_to_float(x[d]) / scale;
+        codes[d] = e4m3_from_float(q);
+    }
+    *scale_out = scale;
+}
+
+/*
+ * Append into the 8-bit cache: the placement of oracle_kv_append [P1 §4.3.1] with each
+ * (token, KV head) row quantised as above.
+ */
+int oracle_kv_append_fp8(uint8_t *k_codes, uint8_t *v_codes, float *k_scale, float *v_scale,
+                         const uint16_t *k_new, const uint16_t *v_new,
+                         const int32_t *block_table, int max_blocks_per_seq, int num_blocks,
+                         const int32_t *cu_q_lens, const int32_t *seq_lens, int num_seqs,
+                         int num_kv_heads, int head_dim, int block_size)
+{
+    int rc = check_common(block_table, max_blocks_per_seq, num_blocks, cu_q_lens, seq_lens,
+                          num_seqs, block_size);
+    if (rc) return rc;
+    for (int s = 0; s < num_seqs; ++s) {
+        int q_len = cu_q_lens[s + 1] - cu_q_lens[s];
+        for (int i = 0; i < q_len; ++i) {
+            int t = cu_q_lens[s] + i;
+            int p = seq_lens[s] - q_len + i;
+            int blk = block_table[(size_t)s * max_blocks_per_seq + p / block_size];
+            int slot = p % block_size;
+            for (int g = 0; g < num_kv_heads; ++g) {
+                size_t src = ((size_t)t * num_kv_heads + g) * head_dim;
+                size_t dst = (((size_t)blk * block_size + slot) * num_kv_heads + g) * head_dim;
+                size_t sc = ((size_t)blk * num_kv_heads + g) * block_size + slot;
+                quantise_row(k_new + src, head_dim, k_codes + dst, k_scale + sc);
+                quantise_row(v_new + src, head_dim, v_codes + dst, v_scale + sc);
+            }
+        }
+    }
+    return 0;
+}
+
+/* Every row of every new token over the 8-bit cache (K/V element = code * row scale). */
+int oracle_paged_attention_fp8(double *out, double *lse,
+                               const uint16_t *q, const uint8_t *k_codes, const uint8_t *v_codes,
+                               const float *k_scale, const float *v_scale,
+                               const int32_t *block_table, int max_blocks_per_seq, int num_blocks,
+                               const int32_t *cu_q_lens, const int32_t *seq_lens, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                               double scale, int num_threads)
+{
+    kv_cache c = {NULL, NULL, k_codes, v_codes, k_scale, v_scale, num_kv_heads, head_dim, block_size};
+    return attention_all(out, lse, q, &c, block_table, max_blocks_per_seq, num_blocks, cu_q_lens,
+                         seq_lens, num_seqs, num_q_heads, scale, num_threads);
 }
 
 /* Threads the OpenMP runtime would use (1 without OpenMP). */

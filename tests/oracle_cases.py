@@ -145,4 +145,147 @@ def pin_battery(lib):
         return np.array_equal(kp, ek) and np.array_equal(vp, ev)
 
     check("kv_append_placement", append)
+
+    # ---- the 8-bit cache: codec against torch's float8_e4m3fn, quantisation, attention
+    def e4m3_decode():
+        codes = np.arange(256, dtype=np.uint8)
+        ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+        return np.array_equal(oracle.e4m3_decode(codes, lib=lib), ref, equal_nan=True)
+
+    def e4m3_encode():
+        x = e4m3_probe_values()
+        ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        return np.array_equal(oracle.e4m3_encode(x, lib=lib), ref)
+
+    def fp8_append():
+        c = fp8_append_case(seed=21)
+        kc, vc, ks, vs = oracle.kv_append_fp8(c["kc"], c["vc"], c["ks"], c["vs"], c["kn"], c["vn"],
+                                              c["bt"], c["cu"], c["sl"], block_size=c["bs"], lib=lib)
+        return fp8_append_ok(c, kc, vc, ks, vs)
+
+    def fp8_attention():
+        c = fp8_attention_case(seed=22)
+        out, lse = oracle.attention_fp8(c["q"], c["kc"], c["vc"], c["ks"], c["vs"], c["bt"], c["cu"],
+                                        c["sl"], scale=c["scale"], lib=lib)
+        ref_out, ref_lse = fp8_sdpa_reference(c)
+        return np.allclose(out, ref_out, rtol=0, atol=1e-12) and np.allclose(lse, ref_lse, rtol=1e-13,
+                                                                             atol=1e-12)
+
+    check("e4m3_decode_torch", e4m3_decode)
+    check("e4m3_encode_torch", e4m3_encode)
+    check("fp8_append_quantisation", fp8_append)
+    check("fp8_attention_sdpa", fp8_attention)
     return failed
+
+
+# ------------------------------------------------------------------ 8-bit cache cases
+
+def e4m3_probe_values(seed=5, n=4000):
+    """float32 values spread over E4M3's range (|x| <= 448): normals, subnormals, exact
+    ties between neighbouring codes, zeros of both signs."""
+    g = np.random.default_rng(seed)
+    mags = np.exp2(g.uniform(-12.0, np.log2(448.0), n))
+    x = (mags * g.choice([-1.0, 1.0], n)).astype(np.float32)
+    codes = np.arange(256, dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    fin = np.sort(np.unique(vals[np.isfinite(vals)]))
+    ties = ((fin[:-1] + fin[1:]) / 2).astype(np.float32)         # midpoints are exact in fp32
+    return np.concatenate([x, ties, -ties, fin.astype(np.float32),
+                           np.array([0.0, -0.0, 448.0, -448.0], np.float32)])
+
+
+def fp8_append_case(seed, bs=4, hkv=2, d=16):
+    """Empty 8-bit cache (NaN codes and scales) and an append of 7 rows into 2 sequences."""
+    g = torch.Generator().manual_seed(seed)
+    nb = 6
+    kc = np.full((nb, bs, hkv, d), 0x7F, np.uint8)
+    vc = kc.copy()
+    ks = np.full((nb, hkv, bs), np.nan, np.float32)
+    vs = ks.copy()
+    kn = (torch.randn(7, hkv, d, generator=g) * torch.exp2(torch.randint(-8, 9, (7, hkv, 1), generator=g))
+          ).to(torch.bfloat16)
+    vn = (torch.randn(7, hkv, d, generator=g) * 3).to(torch.bfloat16)
+    kn[2, 1] = 0.0                                   # an all-zero row (scale 1, codes 0)
+    bt = torch.tensor([[5, 2, 0], [3, 1, -1]], dtype=torch.int32)
+    cu = torch.tensor([0, 6, 7], dtype=torch.int32)
+    sl = torch.tensor([9, 5], dtype=torch.int32)
+    # (block, slot) of each new row: positions 3..8 of sequence 0, position 4 of sequence 1
+    where = [(5, 3), (2, 0), (2, 1), (2, 2), (2, 3), (0, 0), (1, 0)]
+    return dict(kc=kc, vc=vc, ks=ks, vs=vs, kn=kn, vn=vn, bt=bt, cu=cu, sl=sl, bs=bs, where=where)
+
+
+def fp8_append_ok(c, kc, vc, ks, vs):
+    """Every new row sits at its slot with codes/scale meaning the row within E4M3's
+    rounding error, its largest element coded as +-448; no other slot changed."""
+    written = np.zeros(kc.shape[:2], bool)
+    dec = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    for t, (b, sl) in enumerate(c["where"]):
+        written[b, sl] = True
+        for codes, scales, new in ((kc, ks, c["kn"]), (vc, vs, c["vn"])):
+            for h in range(codes.shape[2]):
+                x = new[t, h].double().numpy()
+                amax = np.abs(x).max()
+                s = float(scales[b, h, sl])
+                vals = dec[codes[b, sl, h]] * s
+                if amax == 0.0:
+                    if s != 1.0 or np.any(vals != 0.0):
+                        return False
+                    continue
+                if abs(s * 448.0 - amax) > amax * 2.0 ** -23:           # scale = amax / 448 (fp32)
+                    return False
+                if not np.any((codes[b, sl, h] & 0x7F) == 0x7E):          # the max maps to +-448
+                    return False
+                # E4M3 keeps 3 mantissa bits: |err| <= 2^-4 |x| in the normal range,
+                # <= 2^-10 * scale (half the subnormal step) below it (plus fp32 division error)
+                bound = np.maximum(np.abs(x) * 2.0 ** -4, s * 2.0 ** -10) * (1 + 2.0 ** -20)
+                if np.any(np.abs(vals - x) > bound):
+                    return False
+    untouched = ~written
+    return (np.all(kc[untouched] == 0x7F) and np.all(vc[untouched] == 0x7F) and
+            np.all(np.isnan(ks.transpose(0, 2, 1)[untouched])) and
+            np.all(np.isnan(vs.transpose(0, 2, 1)[untouched])))
+
+
+def fp8_attention_case(seed, seq_lens=(13, 6, 21), q_lens=(1, 6, 4), hq=4, hkv=2, d=16, bs=4):
+    """Random codes and positive scales in a paged 8-bit cache (block table as make_case)."""
+    g = np.random.default_rng(seed)
+    base = make_case(list(seq_lens), list(q_lens), hq=hq, hkv=hkv, d=d, bs=bs, seed=seed)
+    nb = base["k_pool"].shape[0]
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    kc = g.choice(finite, size=(nb, bs, hkv, d)).astype(np.uint8)
+    vc = g.choice(finite, size=(nb, bs, hkv, d)).astype(np.uint8)
+    ks = np.exp2(g.uniform(-9, -4, size=(nb, hkv, bs))).astype(np.float32)
+    vs = np.exp2(g.uniform(-9, -4, size=(nb, hkv, bs))).astype(np.float32)
+    return dict(q=base["q"], kc=kc, vc=vc, ks=ks, vs=vs, bt=base["bt"], cu=base["cu"],
+                sl=base["seq_lens"], q_lens=list(q_lens), hq=hq, hkv=hkv, d=d, bs=bs,
+                scale=1.0 / math.sqrt(d))
+
+
+def fp8_sdpa_reference(c):
+    """torch SDPA (float64) on K/V decoded by torch's float8_e4m3fn and scaled by their rows'
+    scales (cache layout: codes [blk][slot][head][d], scales [blk][head][slot])."""
+    dec = lambda codes: torch.from_numpy(codes).view(torch.float8_e4m3fn).double()
+    kd = dec(c["kc"]) * torch.from_numpy(c["ks"]).double().permute(0, 2, 1).unsqueeze(-1)
+    vd = dec(c["vc"]) * torch.from_numpy(c["vs"]).double().permute(0, 2, 1).unsqueeze(-1)
+    outs, lses = [], []
+    t0 = 0
+    rep = c["hq"] // c["hkv"]
+    for s, ql in enumerate(c["q_lens"]):
+        sl = int(c["sl"][s])
+        idx = [(int(c["bt"][s, j // c["bs"]]), j % c["bs"]) for j in range(sl)]
+        k = torch.stack([kd[b, o] for b, o in idx])                       # [sl, Hkv, D]
+        v = torch.stack([vd[b, o] for b, o in idx])
+        q = c["q"][t0:t0 + ql].double()
+        qh = q.permute(1, 0, 2).unsqueeze(0)
+        kh = k.permute(1, 0, 2).repeat_interleave(rep, 0).unsqueeze(0)
+        vh = v.permute(1, 0, 2).repeat_interleave(rep, 0).unsqueeze(0)
+        i = torch.arange(ql).unsqueeze(1)
+        j = torch.arange(sl).unsqueeze(0)
+        mask = j <= (sl - ql + i)
+        outs.append(F.scaled_dot_product_attention(qh, kh, vh, attn_mask=mask, scale=c["scale"])[0]
+                    .permute(1, 0, 2))
+        sc = torch.einsum("ihd,jhd->hij", q, k.repeat_interleave(rep, 1)) * c["scale"]
+        sc = sc.masked_fill(~mask, float("-inf"))
+        lses.append(torch.logsumexp(sc, dim=-1).permute(1, 0))
+        t0 += ql
+    return torch.cat(outs).numpy(), torch.cat(lses).numpy()

@@ -33,20 +33,32 @@ MUTANTS = {
     # lse missing its log-sum term
     "lse_no_log": ("*lse_out = m + log(denom);", "*lse_out = m;"),
     # V gathered from the K pool (swapped operand)
-    "v_from_k": ("out_row[d] += w * bf16_to_double(v_pool[base + d]);",
-                 "out_row[d] += w * bf16_to_double(k_pool[base + d]);"),
+    "v_from_k": ("out_row[d] += w * kv_elem(c->v_pool, c->v_codes, base, d, vs);",
+                 "out_row[d] += w * kv_elem(c->k_pool, c->k_codes, base, d, vs);"),
     # pool read as [blocks][heads][slots][dim] instead of [blocks][slots][heads][dim]
     "pool_layout_transposed": (
-        "size_t base = (((size_t)bt[j / block_size] * block_size + j % block_size) * num_kv_heads + g)\n"
-        "                      * head_dim;\n        double dot",
-        "size_t base = (((size_t)bt[j / block_size] * num_kv_heads + g) * block_size + j % block_size)\n"
-        "                      * head_dim;\n        double dot"),
+        "return (((size_t)bt[j / c->block_size] * c->block_size + j % c->block_size) * c->num_kv_heads + g)",
+        "return (((size_t)bt[j / c->block_size] * c->num_kv_heads + g) * c->block_size + j % c->block_size)"),
     # keys reversed inside a block
     "slot_reversed": (
-        "size_t base = (((size_t)bt[j / block_size] * block_size + j % block_size) * num_kv_heads + g)\n"
-        "                      * head_dim;\n        double dot",
-        "size_t base = (((size_t)bt[j / block_size] * block_size + (block_size - 1 - j % block_size)) * num_kv_heads + g)\n"
-        "                      * head_dim;\n        double dot"),
+        "return (((size_t)bt[j / c->block_size] * c->block_size + j % c->block_size) * c->num_kv_heads + g)",
+        "return (((size_t)bt[j / c->block_size] * c->block_size + (c->block_size - 1 - j % c->block_size))"
+        " * c->num_kv_heads + g)"),
+    # E4M3 exponent bias 8 instead of 7
+    "e4m3_bias": ("else v = ldexp(1.0 + m / 8.0, e - 7);", "else v = ldexp(1.0 + m / 8.0, e - 8);"),
+    # E4M3 rounding by truncation instead of to nearest even
+    "e4m3_truncate": ("double m = nearbyint(ldexp(a, 3 - e));", "double m = floor(ldexp(a, 3 - e));"),
+    # 8-bit row scale for an int8-style range (127) instead of E4M3's 448
+    "fp8_scale_range": ("float scale = amax > 0.0f ? amax / 448.0f : 1.0f;",
+                        "float scale = amax > 0.0f ? amax / 127.0f : 1.0f;"),
+    # scales read slot-major instead of [block][head][slot]
+    "fp8_scale_layout": (
+        "return (double)scales[((size_t)bt[j / c->block_size] * c->num_kv_heads + g) * c->block_size\n"
+        "                          + (size_t)(j % c->block_size)];",
+        "return (double)scales[((size_t)bt[j / c->block_size] * c->block_size + (size_t)(j % c->block_size))\n"
+        "                          * c->num_kv_heads + g];"),
+    # 8-bit append at the chunk-relative position
+    "fp8_append_relative": ("int p = seq_lens[s] - q_len + i;\n            int blk", "int p = i;\n            int blk"),
     # append writes at the chunk-relative position
     "append_relative_position": ("int p = seq_lens[s] - q_len + i;            /* absolute position */",
                                  "int p = i;            /* absolute position */"),
