@@ -66,7 +66,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default="batched_decode",
                    choices=["single_decode", "batched_decode", "causal_prefill", "mixed_batch",
-                            "prefix_shared_decode", "layered_decode"])
+                            "prefix_shared_decode", "layered_decode", "batched_decode_fp8"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -392,6 +392,117 @@ def e2e_layered_measure(layers, graph, out, steps, warmup, stream):
     return {"step_ms": mean(times), "h2d": h2d, "d2h": d2h}
 
 
+FP8_ROW_BYTES = 2 * (128 + 4)       # one token of one KV head in the 8-bit cache: K and V codes + scales
+
+
+def fp8_prepare(batch):
+    """Bench input: the 8-bit cache holding every sequence's context before its new token,
+    quantised on the GPU (kv_append_fp8) from the batch's bf16 context rows."""
+    from paged_gqa_attention_gb300 import ops
+    from paged_gqa_attention_gb300 import workloads as wl
+
+    ws = ops.make_workspace(batch.num_seqs, batch.max_blocks_per_seq)
+    k_rows, v_rows, cu, lens = wl.context_rows(batch, drop_last=1)
+    cache = ops.fp8_cache(batch.num_blocks)
+    ops.kv_append_fp8(*cache, k_rows, v_rows, batch.block_table, cu, lens, ws)
+    ops.check_error(ws)
+    return cache
+
+
+def fp8_decode_measure(batch, cache, steps, warmup, flush_buf, stream, clocks):
+    """One decode step over the 8-bit cache: kv_append_fp8 of every sequence's new token,
+    then paged_attn_decode_fp8."""
+    import torch
+
+    from paged_gqa_attention_gb300 import ops
+
+    ws = ops.make_workspace(batch.num_seqs, batch.max_blocks_per_seq)
+    out = torch.empty_like(batch.q)
+
+    def step(tm):
+        if tm: tm.record(0)
+        ops.kv_append_fp8(*cache, batch.k_new, batch.v_new, batch.block_table, batch.cu_q_lens,
+                          batch.seq_lens, ws)
+        if tm: tm.record(1)
+        ops.paged_attn_decode_fp8(batch.q, *cache, batch.block_table, batch.seq_lens, ws, out=out)
+        if tm: tm.record(2)
+
+    spans, wall = run_timed(step, 3, steps, warmup, flush_buf, stream, clocks)
+    ops.check_error(ws)
+    return {"append_ms": mean([x[0] for x in spans]), "decode_ms": mean([x[1] for x in spans]),
+            "step_ms": mean([x[0] + x[1] for x in spans]), "wall_s": wall, "launches": 2 * steps}
+
+
+def e2e_fp8_measure(batch, cache, steps, warmup, stream):
+    """The 8-bit decode step through the public API with pinned host inputs and a host result."""
+    import torch
+
+    from paged_gqa_attention_gb300 import ops
+
+    host = {k: getattr(batch, k).cpu().pin_memory()
+            for k in ("q", "k_new", "v_new", "block_table", "seq_lens", "cu_q_lens")}
+    dev = {k: torch.empty_like(getattr(batch, k)) for k in host}
+    out_host = torch.empty(batch.q.shape, dtype=batch.q.dtype).pin_memory()
+    out_dev = torch.empty_like(batch.q)
+    ws = ops.make_workspace(batch.num_seqs, batch.max_blocks_per_seq)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for k, t in host.items():
+            dev[k].copy_(t, non_blocking=True)
+        ops.kv_append_fp8(*cache, dev["k_new"], dev["v_new"], dev["block_table"], dev["cu_q_lens"],
+                          dev["seq_lens"], ws)
+        ops.paged_attn_decode_fp8(dev["q"], *cache, dev["block_table"], dev["seq_lens"], ws, out=out_dev)
+        out_host.copy_(out_dev, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ops.check_error(ws)
+    return {"step_ms": mean(times), "h2d": h2d, "d2h": d2h}
+
+
+def cpu_baseline_fp8(batch, target_s):
+    """The oracle's 8-bit attention (as it stands) over the whole batch, on a cache the
+    oracle quantised itself from the batch's bf16 context, repeated for about target_s."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from paged_gqa_attention_gb300 import ops
+    from paged_gqa_attention_gb300 import workloads as wl
+
+    kp, vp = oracle.kv_append(batch.k_pool.cpu(), batch.v_pool.cpu(), batch.k_new.cpu(), batch.v_new.cpu(),
+                              batch.block_table.cpu(), batch.cu_q_lens.cpu(), batch.seq_lens.cpu())
+    as_bf16 = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    k_rows, v_rows, cu_all, lens = wl.context_rows(batch, as_bf16(kp), as_bf16(vp))
+    empty = [t.numpy() for t in ops.fp8_cache(batch.num_blocks, device="cpu")]
+    cache = oracle.kv_append_fp8(*empty, k_rows, v_rows, batch.block_table.cpu(), cu_all, lens)
+    q, bt, cu, sl = batch.q.cpu(), batch.block_table.cpu(), batch.cu_q_lens.cpu(), batch.seq_lens.cpu()
+    reps = 0
+    t0 = time.time()
+    while True:
+        oracle.attention_fp8(q, *cache, bt, cu, sl, scale=wl.SCALE)
+        reps += 1
+        if time.time() - t0 >= target_s:
+            break
+    dt = time.time() - t0
+    nbytes = sum(batch.seq_lens_host) * 8 * FP8_ROW_BYTES
+    return {"value": reps * nbytes / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"the whole batch ({batch.num_seqs} sequences x 32 heads), {reps} pass(es), {dt:.1f} s, "
+                      f"fp64 C oracle over the 8-bit cache with OpenMP"}
+
+
 def e2e_decode_measure(batch, steps, warmup, stream):
     """The decode step through the C ABI with host buffers (pa_decode_step_host): pinned
     host inputs copied in, fused append + decode, output copied back, every step."""
@@ -561,6 +672,19 @@ def reference_arm(args, world, rank):
     from paged_gqa_attention_gb300 import workloads as wl
 
     dev = "cuda" if torch.cuda.is_available() else "cpu"
+    if args.workload == "batched_decode_fp8":
+        res = [cpu_baseline_fp8(wl.batched_decode(device=dev), max(args.cpu_seconds / max(args.steps, 1), 0.05))
+               for _ in range(args.steps)]
+        value = mean([r["value"] for r in res])
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": {"workload": args.workload},
+                          "cpu_baseline": {"value": value, "unit": "GB/s", "cores": res[0]["cores"],
+                                           "kind": "oracle", "sample": res[0]["sample"]},
+                          "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
     if args.workload == "layered_decode":
         batch = wl.layered_decode(device=dev).base     # GB/s of one layer: the same per layer
     else:
@@ -626,7 +750,12 @@ def main():
 
     wname = args.workload
     layers = wl.layered_decode(device="cuda") if wname == "layered_decode" else None
-    batch = layers.base if layers is not None else wl.WORKLOADS[wname](device="cuda")
+    if layers is not None:
+        batch = layers.base
+    elif wname == "batched_decode_fp8":
+        batch = wl.batched_decode(device="cuda")
+    else:
+        batch = wl.WORKLOADS[wname](device="cuda")
     dist_barrier(world)
     line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -688,6 +817,31 @@ def main():
                        "ms_per_step": e_ms}
         r["graph"].close()
         kind = "decode"
+    elif wname == "batched_decode_fp8":
+        cache = fp8_prepare(batch)
+        r = fp8_decode_measure(batch, cache, args.steps, args.warmup, flush_buf, stream, clocks)
+        ntok = sum(batch.seq_lens_host)
+        kv_bytes = ntok * 8 * FP8_ROW_BYTES
+        bf16_bytes = batch.kv_bytes()
+        io_bytes = batch.num_seqs * 32 * 128 * 2 * 2 + batch.num_seqs * (batch.max_blocks_per_seq + 1) * 4
+        step_ms = dist_max(r["step_ms"], world)
+        dec_ms = dist_max(r["decode_ms"], world)
+        line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
+        line["roofline"] = roofline((kv_bytes + io_bytes) / (dec_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
+                                    "hbm", traffic_for("decode_fp8"))
+        line["roofline"]["kernel"] = "decode_fp8_kernel"
+        line["roofline"]["algorithmic_bytes_per_launch"] = kv_bytes + io_bytes
+        line["kernels"] = {"kv_append_fp8_us": r["append_ms"] * 1e3, "decode_fp8_us": r["decode_ms"] * 1e3,
+                           "fp8_kv_bytes_per_step": kv_bytes, "bf16_kv_bytes_per_step": bf16_bytes,
+                           "bf16_equivalent_gbs": world * bf16_bytes / (step_ms * 1e-3) / 1e9}
+        line["gpu_launches"] = r["launches"]
+        e = e2e_fp8_measure(batch, cache, max(20, min(args.steps, 200)), 5, stream)
+        e_ms = dist_max(e["step_ms"], world)
+        line["e2e"] = {"value": world * kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"], "ms_per_step": e_ms}
+        cfg["kv_cache"] = "8-bit: E4M3 codes + one fp32 scale per token and KV head"
+        line["dtype"] = "f16 products over e4m3 codes"
+        kind = "decode_fp8"
     elif wname == "causal_prefill":
         r = prefill_measure(batch, args.steps, args.warmup, flush_buf, stream, clocks)
         flops = batch.attention_flops()
@@ -755,8 +909,11 @@ def main():
     line["clocks"] = clocks.stop()
     line["peaks"] = peaks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        src = batch if wname in ("layered_decode", batch.name) else wl.WORKLOADS[wname](device="cuda")
-        line["cpu_baseline"] = cpu_baseline(src, kind, args.cpu_seconds, rows_cap_for(wname))
+        if kind == "decode_fp8":
+            line["cpu_baseline"] = cpu_baseline_fp8(wl.batched_decode(device="cuda"), args.cpu_seconds)
+        else:
+            src = batch if wname in ("layered_decode", batch.name) else wl.WORKLOADS[wname](device="cuda")
+            line["cpu_baseline"] = cpu_baseline(src, kind, args.cpu_seconds, rows_cap_for(wname))
     if rank == 0:
         print(json.dumps(line), flush=True)
     dist_barrier(world)

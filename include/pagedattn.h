@@ -155,6 +155,37 @@ pa_status paged_attn_decode_split(pa_shape shape, void *out, float *lse, const v
                                   size_t workspace_bytes, void *stream);
 
 /*
+ * The 8-bit KV cache [P3 §3.2: storing the KV cache in 8 bits instead of 16 halves its
+ * memory].  A K or V row (one token, one KV head) is 128 E4M3 codes (sign, 4 exponent
+ * bits with bias 7, 3 mantissa bits; largest finite value 448) and one fp32 scale; the row
+ * stands for code * scale.  Layouts (device memory, 16-byte aligned):
+ *   k_codes, v_codes  uint8 [num_blocks][256][8][128]  (the bf16 pool layout, 1 byte a value)
+ *   k_scale, v_scale  fp32  [num_blocks][8][256]        (one scale per row, slots contiguous)
+ * A decode step then reads 264 bytes per token and KV head instead of 512.
+ *
+ * kv_append_fp8 quantises every new row: scale = amax / 448 in fp32 (amax = the largest
+ * magnitude of the row; 1 for an all-zero row) and code = E4M3(x / scale), the fp32
+ * quotient rounded to the nearest code (ties to even), magnitudes beyond 448 clamped to
+ * 448.  Placement, arguments and errors are those of kv_append.
+ * paged_attn_decode_fp8 is paged_attn_decode over the 8-bit cache.  Its tensor-core
+ * products run in f16 (the codes convert exactly), so q must stay within f16's range
+ * (|q| < 65504); outputs are bf16 as for paged_attn_decode.
+ */
+pa_status kv_append_fp8(pa_shape shape, void *k_codes, void *v_codes, float *k_scale,
+                        float *v_scale, const void *k_new, const void *v_new,
+                        const int32_t *block_table, int32_t max_blocks_per_seq,
+                        int32_t num_blocks, const int32_t *cu_q_lens, const int32_t *seq_lens,
+                        int32_t num_seqs, int32_t total_tokens, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+pa_status paged_attn_decode_fp8(pa_shape shape, void *out, float *lse, const void *q,
+                                const void *k_codes, const void *v_codes, const float *k_scale,
+                                const float *v_scale, const int32_t *block_table,
+                                int32_t max_blocks_per_seq, int32_t num_blocks,
+                                const int32_t *seq_lens, int32_t batch, float scale,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * paged_attn_decode_append: kv_append of one new token per sequence followed by
  * paged_attn_decode, in one kernel [P1 §4.3.1 append, §4.4.2 decode; P3 §4.2 "append,
  * then attend"].  Row b of k_new / v_new ([batch][8][128] bf16) is written to position

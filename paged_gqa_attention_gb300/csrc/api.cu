@@ -61,6 +61,18 @@ bool encode_pool_map(CUtensorMap *map, const void *pool, int num_blocks, int row
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An 8-bit code pool [num_blocks][256][8][128] uint8 as a 4-D tensor (dim, head, slot,
+// block), box {128, 1, rows, 1}: one 128-byte row per token, 128-byte swizzle.
+bool encode_code_map(CUtensorMap *map, const void *codes, int num_blocks, int rows) {
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kHkv, (cuuint64_t)kBlock, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD, (cuuint64_t)kD * kHkv, (cuuint64_t)kD * kHkv * kBlock};
+    const cuuint32_t box[4] = {(cuuint32_t)kD, 1, (cuuint32_t)rows, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(codes), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // q [tokens][32][128] bf16 as a 3-D tensor (dim, head, token), box {64, 4, 32}.
 bool encode_q_map(CUtensorMap *map, const void *q, int tokens) {
     const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kHq, (cuuint64_t)tokens};
@@ -198,6 +210,8 @@ pa_status decode_impl(pa_shape shape, void *out, float *lse, const void *q, cons
     a.split_tokens = split;
     a.nsplit = (int)nsplit;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.k_scale = nullptr;
+    a.v_scale = nullptr;
     a.counters = reinterpret_cast<int32_t *>(ws + kCounterOffset);
     a.part_o = reinterpret_cast<float *>(ws + kPartialOffset);
     a.part_ml = reinterpret_cast<float *>(ws + kPartialOffset + entries * kPartialOBytes);
@@ -268,6 +282,8 @@ pa_status kv_append(pa_shape shape, void *k_pool, void *v_pool, const void *k_ne
     AppendArgs a;
     a.k_pool = k_pool;
     a.v_pool = v_pool;
+    a.k_scale = nullptr;
+    a.v_scale = nullptr;
     a.k_new = k_new;
     a.v_new = v_new;
     a.block_table = block_table;
@@ -279,6 +295,98 @@ pa_status kv_append(pa_shape shape, void *k_pool, void *v_pool, const void *k_ne
     a.total_tokens = total_tokens;
     a.err = static_cast<uint32_t *>(workspace);
     return launch_kv_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status kv_append_fp8(pa_shape shape, void *k_codes, void *v_codes, float *k_scale, float *v_scale,
+                        const void *k_new, const void *v_new, const int32_t *block_table,
+                        int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t *cu_q_lens,
+                        const int32_t *seq_lens, int32_t num_seqs, int32_t total_tokens, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+        (num_seqs == 0 && total_tokens != 0))
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kHeaderBytes || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
+    if (total_tokens == 0) return PA_OK;
+    if (!k_codes || !v_codes || !k_scale || !v_scale || !k_new || !v_new || !block_table || !cu_q_lens ||
+        !seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scale) || !aligned16(v_scale) ||
+        !aligned16(k_new) || !aligned16(v_new) || !aligned4(block_table) || !aligned4(cu_q_lens) ||
+        !aligned4(seq_lens))
+        return PA_ERR_INVALID_ARG;
+    AppendArgs a;
+    a.k_pool = k_codes;
+    a.v_pool = v_codes;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.block_table = block_table;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.cu_q_lens = cu_q_lens;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.total_tokens = total_tokens;
+    a.err = static_cast<uint32_t *>(workspace);
+    return launch_kv_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status paged_attn_decode_fp8(pa_shape shape, void *out, float *lse, const void *q, const void *k_codes,
+                                const void *v_codes, const float *k_scale, const float *v_scale,
+                                const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
+                                const int32_t *seq_lens, int32_t batch, float scale, void *workspace,
+                                size_t workspace_bytes, void *stream) {
+    if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
+    if (batch < 0 || batch > kMaxBatch || max_blocks_per_seq < 1 || num_blocks < 1 || !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kPartialOffset || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
+    if (batch == 0) return PA_OK;
+    if (!out || !q || !k_codes || !v_codes || !k_scale || !v_scale || !block_table || !seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scale) ||
+        !aligned16(v_scale) || !aligned4(block_table) || !aligned4(seq_lens) || (lse && !aligned4(lse)))
+        return PA_ERR_INVALID_ARG;
+    if ((long long)max_blocks_per_seq * kBlock > (1ll << 30)) return PA_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms <= 0) return PA_ERR_CUDA;
+    if (!get_encoder()) return PA_ERR_CUDA;
+    const int split = auto_split_tokens(batch, max_blocks_per_seq, sms);
+    const long long max_tokens = (long long)max_blocks_per_seq * kBlock;
+    const long long nsplit = (max_tokens + split - 1) / split;
+    if (nsplit > 65535) return PA_ERR_INVALID_ARG;
+    const size_t entries = (size_t)batch * kHkv * (size_t)nsplit;
+    if (workspace_bytes_for(entries) > workspace_bytes) return PA_ERR_WORKSPACE;
+    CUtensorMap k_map, v_map;
+    if (!encode_code_map(&k_map, k_codes, num_blocks, kDecodeTileTokens) ||
+        !encode_code_map(&v_map, v_codes, num_blocks, kDecodeTileTokens))
+        return PA_ERR_INVALID_ARG;
+    char *ws = static_cast<char *>(workspace);
+    DecodeArgs a;
+    a.out = out;
+    a.lse = lse;
+    a.q = q;
+    a.k_new = nullptr;
+    a.v_new = nullptr;
+    a.k_pool_w = const_cast<void *>(k_codes);
+    a.v_pool_w = const_cast<void *>(v_codes);
+    a.block_table = block_table;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.split_tokens = split;
+    a.nsplit = (int)nsplit;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.counters = reinterpret_cast<int32_t *>(ws + kCounterOffset);
+    a.part_o = reinterpret_cast<float *>(ws + kPartialOffset);
+    a.part_ml = reinterpret_cast<float *>(ws + kPartialOffset + entries * kPartialOBytes);
+    a.err = reinterpret_cast<uint32_t *>(ws);
+    return launch_decode_fp8(a, k_map, v_map, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                             : PA_ERR_CUDA;
 }
 
 pa_status paged_attn_decode(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
@@ -427,6 +535,8 @@ pa_status paged_attn_decode_static(pa_shape shape, void *out, float *lse, const 
     a.split_tokens = split;
     a.nsplit = (int)nsplit;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.k_scale = nullptr;
+    a.v_scale = nullptr;
     a.counters = reinterpret_cast<int32_t *>(ws + kCounterOffset);
     a.part_o = reinterpret_cast<float *>(ws + kPartialOffset);
     a.part_ml = reinterpret_cast<float *>(ws + kPartialOffset + entries * kPartialOBytes);

@@ -3,11 +3,18 @@
 // Page "扔掉 vLLM！从零构建 Qwen3-8B 推理引擎，C++/CUDA 实现性能追平 98%" §4.3.1
 // (KVBlockManager::append): tokens fill a sequence's last 256-token block in order,
 // a new block is taken when it is full.  Here the host has already extended the
-// block table; the kernel only moves bytes.  New token i of sequence s lands at
+// block table; the bf16 kernel only moves bytes.  New token i of sequence s lands at
 // absolute position p = seq_lens[s] - q_len + i, slot p % 256 of block
 // block_table[s][p / 256].  In the pool layout [block][slot][kv_head][dim] one
 // token's K (or V) for all 8 KV heads is 2 KiB contiguous, so each copy is one
 // contiguous 2 KiB move: one warp per (token, K|V), 16-byte vector accesses.
+//
+// The 8-bit cache variant (k_scale set) quantises instead of copying: each (token, KV
+// head) row of 128 values gets scale = amax / 448 (fp32, 1 for an all-zero row) and codes
+// E4M3(x / scale) (fp32 division, round to nearest even, saturating at 448), one half-
+// warp per row; the codes keep the pool layout (128 bytes per row) and the scale goes to
+// [block][head][slot].  Page "从零搭建AI工程能力：手写KV Cache与动态批处理实战" §3.2: an 8-bit
+// KV cache halves its memory.
 //
 // The kernel is a chain of dependent loads (which sequence owns the token, its
 // length, its block id, then the data), so its time is latency: the owner is first
@@ -39,6 +46,7 @@ __device__ __forceinline__ int warp_find_sequence(const int32_t *cu, int n, int 
     return lo;
 }
 
+template <bool kFp8>
 __global__ void __launch_bounds__(kWarps * 32) kv_append_kernel(AppendArgs a) {
     // The pools are this kernel's only output: a dependent kernel may launch now and
     // run its prologue; it waits for our completion before touching the pools.
@@ -82,14 +90,46 @@ __global__ void __launch_bounds__(kWarps * 32) kv_append_kernel(AppendArgs a) {
     }
     const uint4 *src = reinterpret_cast<const uint4 *>(
         static_cast<const char *>(is_v ? a.v_new : a.k_new) + (size_t)t * kTokenBytes);
-    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<char *>(is_v ? a.v_pool : a.k_pool) +
-                                           ((size_t)blk * kBlock + (p % kBlock)) * kTokenBytes);
     // 2 KiB = 128 x 16 B: four 16-byte vectors per lane, all loads issued first
     uint4 v[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) v[k] = __ldg(src + lane + 32 * k);
+    const int slot = p % kBlock;
+    if constexpr (!kFp8) {
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<char *>(is_v ? a.v_pool : a.k_pool) +
+                                               ((size_t)blk * kBlock + slot) * kTokenBytes);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) dst[lane + 32 * k] = v[k];
+        for (int k = 0; k < 4; ++k) dst[lane + 32 * k] = v[k];
+    } else {
+        // vector k of lane l: KV head 2k + l/16, dims 8 (l%16) .. 8 (l%16) + 7
+        uint8_t *codes = static_cast<uint8_t *>(is_v ? a.v_pool : a.k_pool) +
+                         ((size_t)blk * kBlock + slot) * (kHkv * kD);
+        float *scales = is_v ? a.v_scale : a.k_scale;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[2 * e] = bf16_lo(w[e]);
+                x[2 * e + 1] = bf16_hi(w[e]);
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+            uint2 c;
+            c.x = f32x2_to_e4m3x2(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale)) |
+                  f32x2_to_e4m3x2(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale)) << 16;
+            c.y = f32x2_to_e4m3x2(__fdiv_rn(x[4], scale), __fdiv_rn(x[5], scale)) |
+                  f32x2_to_e4m3x2(__fdiv_rn(x[6], scale), __fdiv_rn(x[7], scale)) << 16;
+            const int head = 2 * k + (lane >> 4), chunk = lane & 15;
+            *reinterpret_cast<uint2 *>(codes + head * kD + chunk * 8) = c;
+            if (chunk == 0) scales[((size_t)blk * kHkv + head) * kBlock + slot] = scale;
+        }
+    }
 }
 
 }  // namespace
@@ -98,7 +138,10 @@ cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream) {
     if (a.total_tokens == 0) return cudaSuccess;
     const int tokens_per_cta = kWarps / 2;
     const int grid = (a.total_tokens + tokens_per_cta - 1) / tokens_per_cta;
-    kv_append_kernel<<<grid, kWarps * 32, 0, stream>>>(a);
+    if (a.k_scale)
+        kv_append_kernel<true><<<grid, kWarps * 32, 0, stream>>>(a);
+    else
+        kv_append_kernel<false><<<grid, kWarps * 32, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

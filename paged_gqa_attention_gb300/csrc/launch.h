@@ -9,8 +9,10 @@
 namespace pa {
 
 struct AppendArgs {
-    void *k_pool;
+    void *k_pool;          // bf16 pools, or the 8-bit code pools when k_scale is set
     void *v_pool;
+    float *k_scale;        // 8-bit cache only: [num_blocks][8][256] row scales (else null)
+    float *v_scale;
     const void *k_new;
     const void *v_new;
     const int32_t *block_table;
@@ -41,6 +43,8 @@ struct DecodeArgs {
     int32_t split_tokens;  // context tokens per CTA (multiple of 64)
     int32_t nsplit;        // splits per (sequence, KV head) at the maximum context
     float scale_log2;      // softmax scale * log2(e)
+    const float *k_scale;  // 8-bit cache only: row scales [num_blocks][8][256]
+    const float *v_scale;
     int32_t *counters;     // [batch * 8], zero on entry, zero again on exit
     float *part_o;         // [batch * 8 * nsplit][4][128]
     float *part_ml;        // [batch * 8 * nsplit][4][2]
@@ -73,6 +77,10 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
                           const CUtensorMap &v_map, int num_sms, cudaStream_t stream);
 
 // q_map: 3-D map over q; k_map / v_map: 4-D maps over the pools.
+// Decode over the 8-bit cache (code pools as k_map / v_map, scales in the args).
+cudaError_t launch_decode_fp8(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
+                              cudaStream_t stream);
+
 cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
                            const CUtensorMap &k_map, const CUtensorMap &v_map, int num_sms,
                            cudaStream_t stream);

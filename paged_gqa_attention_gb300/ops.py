@@ -88,6 +88,12 @@ def load() -> ctypes.CDLL:
     lib.pa_decode_step_host.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, f32,
                                         vp, sz, vp, sz, vp]
     lib.pa_decode_step_host.restype = ctypes.c_int
+    lib.kv_append_fp8.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32, vp,
+                                  sz, vp]
+    lib.kv_append_fp8.restype = ctypes.c_int
+    lib.paged_attn_decode_fp8.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, f32,
+                                          vp, sz, vp]
+    lib.paged_attn_decode_fp8.restype = ctypes.c_int
     lib.pa_decode_graph_create.argtypes = [pa_shape, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp,
                                            i32, f32, vp, sz, ctypes.POINTER(vp)]
     lib.pa_decode_graph_create.restype = ctypes.c_int
@@ -246,6 +252,68 @@ def paged_attn_decode_append(q, k_new, v_new, k_pool, v_pool, block_table, seq_l
                                          batch, float(scale), workspace.data_ptr(), workspace.numel(),
                                          _stream(stream))
     _check("paged_attn_decode_append", st)
+    return out
+
+
+def fp8_cache(num_blocks: int, device=None):
+    """An empty 8-bit KV cache: (k_codes, v_codes) uint8 [N, 256, 8, 128] holding the NaN code
+    0x7F and (k_scale, v_scale) float32 [N, 8, 256] holding NaN, so a slot that was never
+    written shows up as NaN wherever it is read."""
+    dev = device or "cuda"
+    codes = torch.full((num_blocks, BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), 0x7F, dtype=torch.uint8, device=dev)
+    scales = torch.full((num_blocks, NUM_KV_HEADS, BLOCK_SIZE), float("nan"), dtype=torch.float32, device=dev)
+    return codes, codes.clone(), scales, scales.clone()
+
+
+def _need_fp8_cache(k_codes, v_codes, k_scale, v_scale, dev):
+    _need(k_codes, "k_codes", torch.uint8, (None, BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_codes, "v_codes", torch.uint8, tuple(k_codes.shape), dev)
+    n = k_codes.shape[0]
+    _need(k_scale, "k_scale", torch.float32, (n, NUM_KV_HEADS, BLOCK_SIZE), dev)
+    _need(v_scale, "v_scale", torch.float32, (n, NUM_KV_HEADS, BLOCK_SIZE), dev)
+
+
+def kv_append_fp8(k_codes, v_codes, k_scale, v_scale, k_new, v_new, block_table, cu_q_lens, seq_lens,
+                  workspace, stream=None) -> None:
+    """Quantise the new tokens' K/V rows into the 8-bit cache (in place)."""
+    dev = k_new.device
+    _need_fp8_cache(k_codes, v_codes, k_scale, v_scale, dev)
+    _need(k_new, "k_new", torch.bfloat16, (None, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_new, "v_new", torch.bfloat16, tuple(k_new.shape), dev)
+    _need(block_table, "block_table", torch.int32, (None, None), dev)
+    num_seqs = block_table.shape[0]
+    _need(cu_q_lens, "cu_q_lens", torch.int32, (num_seqs + 1,), dev)
+    _need(seq_lens, "seq_lens", torch.int32, (num_seqs,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    st = load().kv_append_fp8(SHAPE, k_codes.data_ptr(), v_codes.data_ptr(), k_scale.data_ptr(),
+                              v_scale.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), block_table.data_ptr(),
+                              block_table.shape[1], k_codes.shape[0], cu_q_lens.data_ptr(),
+                              seq_lens.data_ptr(), num_seqs, k_new.shape[0], workspace.data_ptr(),
+                              workspace.numel(), _stream(stream))
+    _check("kv_append_fp8", st)
+
+
+def paged_attn_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens, workspace, *,
+                          scale: float = DEFAULT_SCALE, out=None, lse=None, stream=None) -> torch.Tensor:
+    """One query token per sequence over the 8-bit cache; returns out [B, 32, 128] bf16."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (None, NUM_Q_HEADS, HEAD_DIM), dev)
+    batch = q.shape[0]
+    _need_fp8_cache(k_codes, v_codes, k_scale, v_scale, dev)
+    _need(block_table, "block_table", torch.int32, (batch, None), dev)
+    _need(seq_lens, "seq_lens", torch.int32, (batch,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, tuple(q.shape), dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (batch, NUM_Q_HEADS), dev)
+    st = load().paged_attn_decode_fp8(SHAPE, out.data_ptr(), _ptr(lse), q.data_ptr(), k_codes.data_ptr(),
+                                      v_codes.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(),
+                                      block_table.data_ptr(), block_table.shape[1], k_codes.shape[0],
+                                      seq_lens.data_ptr(), batch, float(scale), workspace.data_ptr(),
+                                      workspace.numel(), _stream(stream))
+    _check("paged_attn_decode_fp8", st)
     return out
 
 

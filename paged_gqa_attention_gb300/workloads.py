@@ -280,6 +280,28 @@ def prefix_shared_decode(device="cpu", seed: int = 4, batch: int = 128, context:
                              "pool_blocks": num_blocks})
 
 
+def context_rows(batch: Batch, k_pool=None, v_pool=None, drop_last: int = 0):
+    """Every context token's K/V rows gathered through the block table, as an append request
+    that rebuilds the whole context: (k_rows, v_rows [T, Hkv, D], cu [S+1], lens [S]) with
+    positions 0 .. seq_len - 1 - drop_last of each sequence (drop_last = 1 leaves out each
+    sequence's newest token).  Pure data movement; the pools default to the batch's own."""
+    kp = batch.k_pool if k_pool is None else k_pool
+    vp = batch.v_pool if v_pool is None else v_pool
+    bt = batch.block_table.cpu()
+    blks, slots, lens = [], [], []
+    for s, sl in enumerate(batch.seq_lens_host):
+        n = sl - drop_last
+        pos = torch.arange(n)
+        blks.append(bt[s, pos // BLOCK_SIZE].long())
+        slots.append(pos % BLOCK_SIZE)
+        lens.append(n)
+    blk = torch.cat(blks).to(kp.device)
+    slot = torch.cat(slots).to(kp.device)
+    cu = torch.tensor([0] + list(torch.tensor(lens).cumsum(0).tolist()), dtype=torch.int32, device=kp.device)
+    return (kp[blk, slot].contiguous(), vp[blk, slot].contiguous(), cu,
+            torch.tensor(lens, dtype=torch.int32, device=kp.device))
+
+
 @dataclass
 class Layers:
     """A decode batch repeated over L layers, layer-major: q [L, B, Hq, D], k_new / v_new

@@ -1,0 +1,149 @@
+"""The 8-bit KV cache on the GPU against the oracle: the append (codes and scales bit-exact)
+and the decode over the cache (within the bf16 output tolerance)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import (assert_close, assert_lse_close, gpu, lib_ready, oracle_appended_pools, to_cpu,
+                         workspace_for)
+from paged_gqa_attention_gb300 import ops
+from paged_gqa_attention_gb300 import workloads as wl
+
+pytestmark = gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lib_ready()
+
+
+def oracle_cache(batch: wl.Batch, drop_last: int = 0):
+    """The 8-bit cache holding the batch's context, quantised by the oracle (host arrays):
+    positions 0 .. seq_len - 1 - drop_last of every sequence."""
+    kp, vp = oracle_appended_pools(batch)            # bf16 context incl. the new tokens
+    k_rows, v_rows, cu, lens = wl.context_rows(batch, torch.from_numpy(kp.view(np.int16)).view(torch.bfloat16),
+                                               torch.from_numpy(vp.view(np.int16)).view(torch.bfloat16),
+                                               drop_last=drop_last)
+    kc, vc, ks, vs = ops.fp8_cache(batch.num_blocks, device="cpu")
+    return oracle.kv_append_fp8(kc.numpy(), vc.numpy(), ks.numpy(), vs.numpy(), k_rows, v_rows,
+                                to_cpu(batch.block_table), cu, lens)
+
+
+def upload(cache):
+    return [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in cache]
+
+
+def same_bits(gpu_t, host):
+    g = to_cpu(gpu_t).contiguous()
+    if g.dtype == torch.float32:
+        return np.array_equal(g.view(torch.int32).numpy(), np.ascontiguousarray(host).view(np.int32))
+    return np.array_equal(g.numpy(), host)
+
+
+def scaled_rows(n, seed, device="cuda"):
+    """bf16 rows whose magnitudes span many binades (per row and within a row), a zero row
+    and values that fall into E4M3's subnormal range after scaling."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn(n, 8, 128, generator=g, device=device)
+    x = x * torch.exp2(torch.randint(-12, 13, (n, 8, 1), generator=g, device=device).float())
+    x[:, :, :8] *= 2.0 ** -9                     # small elements: subnormal codes
+    x[0, 3] = 0.0
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("lens,q_lens", [([300, 40, 513], [5, 40, 1]), ([1, 256, 257, 1000], [1, 1, 1, 1])])
+def test_kv_append_fp8_is_bit_exact(lens, q_lens):
+    b = wl.build_batch("fp8_append", 51, lens, q_lens, num_blocks=sum((l + 255) // 256 for l in lens) + 2,
+                       device="cuda")
+    kn, vn = scaled_rows(b.total_tokens, 52), scaled_rows(b.total_tokens, 53)
+    kc, vc, ks, vs = ops.fp8_cache(b.num_blocks)
+    ref = oracle.kv_append_fp8(to_cpu(kc).numpy(), to_cpu(vc).numpy(), to_cpu(ks).numpy(), to_cpu(vs).numpy(),
+                               to_cpu(kn), to_cpu(vn), to_cpu(b.block_table), to_cpu(b.cu_q_lens),
+                               to_cpu(b.seq_lens))
+    ws = workspace_for(b)
+    ops.kv_append_fp8(kc, vc, ks, vs, kn, vn, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    ops.check_error(ws)
+    for got, want, name in zip((kc, vc, ks, vs), ref, ("k_codes", "v_codes", "k_scale", "v_scale")):
+        assert same_bits(got, want), f"{name} differs from the oracle"
+
+
+@pytest.mark.parametrize("lens", [[1, 63, 64, 65, 255, 256, 257, 1000], [4096, 3000, 17]])
+def test_decode_fp8_matches_oracle(lens):
+    b = wl.build_batch("fp8_decode", 54 + len(lens), lens, [1] * len(lens),
+                       num_blocks=sum((l + 255) // 256 for l in lens) + 3, device="cuda")
+    cache = oracle_cache(b)
+    kc, vc, ks, vs = upload(cache)
+    ws = workspace_for(b)
+    lse = torch.empty(b.num_seqs, ops.NUM_Q_HEADS, dtype=torch.float32, device="cuda")
+    out = ops.paged_attn_decode_fp8(b.q, kc, vc, ks, vs, b.block_table, b.seq_lens, ws, lse=lse)
+    ops.check_error(ws)
+    ref, ref_lse = oracle.attention_fp8(to_cpu(b.q), *cache, to_cpu(b.block_table), to_cpu(b.cu_q_lens),
+                                        to_cpu(b.seq_lens), scale=wl.SCALE)
+    assert_close(out, ref, f"fp8 decode {lens}")
+    assert_lse_close(lse, ref_lse, f"fp8 decode {lens}")
+
+
+def test_decode_fp8_after_gpu_append_of_the_new_tokens():
+    """The decode step over the 8-bit cache: the context before the new tokens quantised by
+    the oracle, the new tokens appended by the GPU, then the GPU decode."""
+    lens = [700, 129, 2048, 5]
+    b = wl.build_batch("fp8_step", 58, lens, [1] * len(lens), num_blocks=sum((l + 255) // 256 for l in lens) + 2,
+                       device="cuda")
+    before = oracle_cache(b, drop_last=1)
+    full = oracle_cache(b)
+    kc, vc, ks, vs = upload(before)
+    ws = workspace_for(b)
+    ops.kv_append_fp8(kc, vc, ks, vs, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    out = ops.paged_attn_decode_fp8(b.q, kc, vc, ks, vs, b.block_table, b.seq_lens, ws)
+    ops.check_error(ws)
+    for got, want in zip((kc, vc, ks, vs), full):
+        assert same_bits(got, want)
+    ref, _ = oracle.attention_fp8(to_cpu(b.q), *full, to_cpu(b.block_table), to_cpu(b.cu_q_lens),
+                                  to_cpu(b.seq_lens), scale=wl.SCALE)
+    assert_close(out, ref, "fp8 step")
+
+
+def test_decode_fp8_single_key_returns_its_row():
+    b = wl.build_batch("fp8_one", 59, [1, 1], [1, 1], num_blocks=4, device="cuda")
+    cache = oracle_cache(b)
+    kc, vc, ks, vs = upload(cache)
+    ws = workspace_for(b)
+    out = ops.paged_attn_decode_fp8(b.q, kc, vc, ks, vs, b.block_table, b.seq_lens, ws)
+    ops.check_error(ws)
+    ref, _ = oracle.attention_fp8(to_cpu(b.q), *cache, to_cpu(b.block_table), to_cpu(b.cu_q_lens),
+                                  to_cpu(b.seq_lens), scale=wl.SCALE)
+    # one key: the output is its V row (code * scale), rounded to bf16 after an fp32 product:
+    # within one bf16 step of the exact value
+    got = to_cpu(out).double().numpy()
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
+
+
+def test_decode_fp8_full_size_batched():
+    b = wl.batched_decode(device="cuda")
+    cache = oracle_cache(b)
+    kc, vc, ks, vs = upload(cache)
+    ws = workspace_for(b)
+    out = ops.paged_attn_decode_fp8(b.q, kc, vc, ks, vs, b.block_table, b.seq_lens, ws)
+    ops.check_error(ws)
+    ref, _ = oracle.attention_fp8(to_cpu(b.q), *cache, to_cpu(b.block_table), to_cpu(b.cu_q_lens),
+                                  to_cpu(b.seq_lens), scale=wl.SCALE)
+    assert_close(out, ref, "fp8 batched decode, full size")
+
+
+def test_decode_fp8_bad_block_is_reported():
+    b = wl.build_batch("fp8_bad", 60, [600, 300], [1, 1], num_blocks=6, device="cuda")
+    cache = oracle_cache(b)
+    kc, vc, ks, vs = upload(cache)
+    ws = workspace_for(b)
+    ref, _ = oracle.attention_fp8(to_cpu(b.q), *cache, to_cpu(b.block_table), to_cpu(b.cu_q_lens),
+                                  to_cpu(b.seq_lens), scale=wl.SCALE)
+    bt = b.block_table.clone()
+    bt[0, 1] = b.num_blocks + 5
+    out = ops.paged_attn_decode_fp8(b.q, kc, vc, ks, vs, bt, b.seq_lens, ws)
+    with pytest.raises(ops.PagedAttnError) as e:
+        ops.check_error(ws)
+    assert e.value.status == 4
+    assert torch.isnan(out[0].float()).any()
+    assert_close(out[1], ref[1], "unaffected sequence")
