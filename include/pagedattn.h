@@ -185,6 +185,16 @@ pa_status paged_attn_decode_fp8(pa_shape shape, void *out, float *lse, const voi
                                 const int32_t *seq_lens, int32_t batch, float scale,
                                 void *workspace, size_t workspace_bytes, void *stream);
 
+/* As paged_attn_decode_fp8 with the split length fixed by the caller: a positive multiple
+ * of 128 tokens (the kernel's stage), or 0 for the library's choice. */
+pa_status paged_attn_decode_fp8_split(pa_shape shape, void *out, float *lse, const void *q,
+                                      const void *k_codes, const void *v_codes,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *block_table, int32_t max_blocks_per_seq,
+                                      int32_t num_blocks, const int32_t *seq_lens, int32_t batch,
+                                      float scale, int32_t split_tokens, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
 /*
  * paged_attn_decode_append: kv_append of one new token per sequence followed by
  * paged_attn_decode, in one kernel [P1 §4.3.1 append, §4.4.2 decode; P3 §4.2 "append,

@@ -333,13 +333,14 @@ pa_status kv_append_fp8(pa_shape shape, void *k_codes, void *v_codes, float *k_s
     return launch_kv_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-pa_status paged_attn_decode_fp8(pa_shape shape, void *out, float *lse, const void *q, const void *k_codes,
-                                const void *v_codes, const float *k_scale, const float *v_scale,
-                                const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
-                                const int32_t *seq_lens, int32_t batch, float scale, void *workspace,
-                                size_t workspace_bytes, void *stream) {
+pa_status paged_attn_decode_fp8_split(pa_shape shape, void *out, float *lse, const void *q, const void *k_codes,
+                                      const void *v_codes, const float *k_scale, const float *v_scale,
+                                      const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
+                                      const int32_t *seq_lens, int32_t batch, float scale, int32_t split_tokens,
+                                      void *workspace, size_t workspace_bytes, void *stream) {
     if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
-    if (batch < 0 || batch > kMaxBatch || max_blocks_per_seq < 1 || num_blocks < 1 || !std::isfinite(scale))
+    if (batch < 0 || batch > kMaxBatch || max_blocks_per_seq < 1 || num_blocks < 1 || !std::isfinite(scale) ||
+        split_tokens < 0 || split_tokens % kDecodeFp8TileTokens != 0)
         return PA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < kPartialOffset || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
     if (batch == 0) return PA_OK;
@@ -352,15 +353,18 @@ pa_status paged_attn_decode_fp8(pa_shape shape, void *out, float *lse, const voi
     const int sms = sm_count();
     if (sms <= 0) return PA_ERR_CUDA;
     if (!get_encoder()) return PA_ERR_CUDA;
-    const int split = auto_split_tokens(batch, max_blocks_per_seq, sms);
+    // the library's split rounded up to whole 128-token stages
+    const int split = split_tokens ? split_tokens
+                                   : (auto_split_tokens(batch, max_blocks_per_seq, sms) + kDecodeFp8TileTokens - 1) /
+                                         kDecodeFp8TileTokens * kDecodeFp8TileTokens;
     const long long max_tokens = (long long)max_blocks_per_seq * kBlock;
     const long long nsplit = (max_tokens + split - 1) / split;
     if (nsplit > 65535) return PA_ERR_INVALID_ARG;
     const size_t entries = (size_t)batch * kHkv * (size_t)nsplit;
     if (workspace_bytes_for(entries) > workspace_bytes) return PA_ERR_WORKSPACE;
     CUtensorMap k_map, v_map;
-    if (!encode_code_map(&k_map, k_codes, num_blocks, kDecodeTileTokens) ||
-        !encode_code_map(&v_map, v_codes, num_blocks, kDecodeTileTokens))
+    if (!encode_code_map(&k_map, k_codes, num_blocks, kDecodeFp8TileTokens) ||
+        !encode_code_map(&v_map, v_codes, num_blocks, kDecodeFp8TileTokens))
         return PA_ERR_INVALID_ARG;
     char *ws = static_cast<char *>(workspace);
     DecodeArgs a;
@@ -387,6 +391,16 @@ pa_status paged_attn_decode_fp8(pa_shape shape, void *out, float *lse, const voi
     a.err = reinterpret_cast<uint32_t *>(ws);
     return launch_decode_fp8(a, k_map, v_map, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
                                                                                              : PA_ERR_CUDA;
+}
+
+pa_status paged_attn_decode_fp8(pa_shape shape, void *out, float *lse, const void *q, const void *k_codes,
+                                const void *v_codes, const float *k_scale, const float *v_scale,
+                                const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
+                                const int32_t *seq_lens, int32_t batch, float scale, void *workspace,
+                                size_t workspace_bytes, void *stream) {
+    return paged_attn_decode_fp8_split(shape, out, lse, q, k_codes, v_codes, k_scale, v_scale, block_table,
+                                       max_blocks_per_seq, num_blocks, seq_lens, batch, scale, 0, workspace,
+                                       workspace_bytes, stream);
 }
 
 pa_status paged_attn_decode(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,

@@ -7,8 +7,11 @@
 // "扔掉 vLLM！从零构建 Qwen3-8B 推理引擎，C++/CUDA 实现性能追平 98%" §4.4.2: the four query
 // heads of a group share every KV read; split-K over the context with a log-sum-exp
 // merge), with these differences:
-//   * a stage is 64 tokens of K codes and V codes (8 KiB each, TMA, 128-byte swizzle)
-//     and their 64 + 64 scales (256-byte bulk copies); six stages, two CTAs per SM;
+//   * a stage is 128 tokens of K codes and V codes (16 KiB each, TMA, 128-byte swizzle)
+//     and their 128 + 128 scales (512-byte bulk copies), consumed by 8 warps of 16 tokens;
+//     three stages, two CTAs per SM.  A consumer warp's work per stage is one dependent
+//     chain (S, softmax, PV) of about 0.8 us whatever the data type, so a stage of half-
+//     size rows needs twice the tokens to move the bytes a bf16 stage moves;
 //   * the tensor-core products run in f16 (the GPU converts E4M3 pairs to f16 pairs
 //     exactly): ldmatrix on the code bytes gives each lane four consecutive codes of a
 //     row, which become the A fragments of two k16 steps once Q is loaded in the
@@ -29,22 +32,29 @@
 namespace pa {
 namespace {
 
-constexpr int kTile = kDecodeTileTokens;      // 64 tokens per stage
-constexpr int kStages = 6;
-constexpr int kConsumerWarps = kTile / 16;    // 4
+constexpr int kTile = kDecodeFp8TileTokens;   // 128 tokens per stage (half a cache block)
+constexpr int kStages = 3;
+constexpr int kCtasPerSm = 2;
+constexpr int kConsumerWarps = kTile / 16;    // 8
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kCodeBytes = kTile * kD;        // 64 tokens x 128 codes = 8 KiB
-constexpr int kScaleBytes = kTile * 4;        // 256 B
+constexpr int kCodeBytes = kTile * kD;        // 128 tokens x 128 codes = 16 KiB
+constexpr int kScaleBytes = kTile * 4;        // 512 B
 constexpr uint32_t kStageTx = 2 * kCodeBytes + 2 * kScaleBytes;
 constexpr float kLn2 = 0.693147180559945309f;
 
-struct DecodeFp8Smem {
-    uint8_t codes[kStages][2][kCodeBytes];    // [stage][K, V], each 1 KiB aligned
-    float scales[kStages][2][kTile];          // [stage][K, V]
+struct MergeArrays {                          // the warps' partial results, after the stages
     float o[kConsumerWarps][kGroup][kD];
     float m[kConsumerWarps][kGroup];
     float l[kConsumerWarps][kGroup];
     float sigma[kConsumerWarps];
+};
+
+struct DecodeFp8Smem {
+    union {
+        uint8_t codes[kStages][2][kCodeBytes];  // [stage][K, V], each 1 KiB aligned
+        MergeArrays mg;                         // reused once every stage is consumed
+    };
+    float scales[kStages][2][kTile];          // [stage][K, V]
     uint64_t full[kStages];
     uint64_t empty[kStages];
     int last_cta;
@@ -66,7 +76,7 @@ __device__ __forceinline__ void v_pairs(uint32_t r, uint32_t &lo, uint32_t &hi) 
     e4m3x4_to_f16x2x2(__byte_perm(r, 0u, 0x3120), lo, hi);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                   const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -192,8 +202,9 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_consta
             const float *ksc = sm.scales[st][0] + w * 16;
             const float *vsc = sm.scales[st][1] + w * 16;
 
-            // S^T[16 tokens x 8 heads] = K[16 x 128] . Q^T, 32 dims per ldmatrix
-            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            // S^T[16 tokens x 8 heads] = K[16 x 128] . Q^T, 32 dims per ldmatrix, as two
+            // independent accumulations (even / odd k16 steps) to halve the dependent chain
+            float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 uint32_t r[4], af[4], bf[4];
@@ -203,8 +214,10 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_consta
                 mma_16816_f16(s, af, qb[2 * j][0], qb[2 * j][1]);
                 e4m3x4_to_f16x2x2(r[2], bf[0], bf[2]);
                 e4m3x4_to_f16x2x2(r[3], bf[1], bf[3]);
-                mma_16816_f16(s, bf, qb[2 * j + 1][0], qb[2 * j + 1][1]);
+                mma_16816_f16(s2, bf, qb[2 * j + 1][0], qb[2 * j + 1][1]);
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[e] += s2[e];
             // s[0]: (token gq, head 2tq)   s[1]: (token gq, head 2tq+1)
             // s[2]: (token gq+8, head 2tq) s[3]: (token gq+8, head 2tq+1)
             const bool v_lo_ok = gq < my_valid;
@@ -290,46 +303,57 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_consta
         if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
     }
 
-    // ------------------------------------------------------------ merge the 4 warps
+    // ------------------------------------------------------------ merge the warps
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, o);
         l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
+    // the merge arrays overlay the stages: every consumer warp must be done with them
+    named_barrier(1, kConsumerWarps * 32);
     if (tq < 2) {
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
             const int d = mt * 16 + 2 * gq;      // accumulator rows gq, gq+8 = dims 2gq, 2gq+1
-            sm.o[w][2 * tq][d] = acc[mt][0];
-            sm.o[w][2 * tq + 1][d] = acc[mt][1];
-            sm.o[w][2 * tq][d + 1] = acc[mt][2];
-            sm.o[w][2 * tq + 1][d + 1] = acc[mt][3];
+            sm.mg.o[w][2 * tq][d] = acc[mt][0];
+            sm.mg.o[w][2 * tq + 1][d] = acc[mt][1];
+            sm.mg.o[w][2 * tq][d + 1] = acc[mt][2];
+            sm.mg.o[w][2 * tq + 1][d + 1] = acc[mt][3];
         }
         if (gq == 0) {
-            sm.m[w][2 * tq] = m0;
-            sm.m[w][2 * tq + 1] = m1;
-            sm.l[w][2 * tq] = l0;
-            sm.l[w][2 * tq + 1] = l1;
+            sm.mg.m[w][2 * tq] = m0;
+            sm.mg.m[w][2 * tq + 1] = m1;
+            sm.mg.l[w][2 * tq] = l0;
+            sm.mg.l[w][2 * tq + 1] = l1;
         }
     }
-    if (lane == 0) sm.sigma[w] = sigma;
+    if (lane == 0) sm.mg.sigma[w] = sigma;
     named_barrier(1, kConsumerWarps * 32);
     const bool bad = *reinterpret_cast<volatile int *>(&sm.poison) != 0;
 
-    const int c = threadIdx.x;          // 0..127
+    // the first 128 consumer threads merge (4 heads x 32 threads x 4 dims)
+    const int c = threadIdx.x;
+    if (c >= kGroup * 32) {
+        // the others only take part in the partials' barriers below
+        if (nsplit_b > 1) {
+            named_barrier(2, kConsumerWarps * 32);
+            named_barrier(2, kConsumerWarps * 32);
+        }
+        return;
+    }
     const int h = c >> 5;               // query head within the group
     const int d0 = (c & 31) * 4;        // 4 dims per thread
     float M = -INFINITY;
 #pragma unroll
-    for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, sm.m[ww][h]);
+    for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, sm.mg.m[ww][h]);
     float L = 0.f, o4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ww = 0; ww < kConsumerWarps; ++ww) {
-        const float e = fast_exp2(sm.m[ww][h] - M);
-        L += sm.l[ww][h] * e;
-        const float eo = e * sm.sigma[ww];
+        const float e = fast_exp2(sm.mg.m[ww][h] - M);
+        L += sm.mg.l[ww][h] * e;
+        const float eo = e * sm.mg.sigma[ww];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) o4[k] += sm.o[ww][h][d0 + k] * eo;
+        for (int k = 0; k < 4; ++k) o4[k] += sm.mg.o[ww][h][d0 + k] * eo;
     }
     if (bad) {
         M = L = __int_as_float(0x7fc00000);
@@ -354,12 +378,12 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_consta
         a.part_ml[(entry * kGroup + h) * 2 + 1] = L;
     }
     __threadfence();
-    named_barrier(1, kConsumerWarps * 32);
+    named_barrier(2, kConsumerWarps * 32);
     if (c == 0) {
         const int prev = atomicAdd(a.counters + pair, 1);
         sm.last_cta = (prev == nsplit_b - 1);
     }
-    named_barrier(1, kConsumerWarps * 32);
+    named_barrier(2, kConsumerWarps * 32);
     if (!sm.last_cta) return;
 
     // The last CTA of this (sequence, KV head) merges every split by log-sum-exp.

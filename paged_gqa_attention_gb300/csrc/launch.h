@@ -77,6 +77,9 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
                           const CUtensorMap &v_map, int num_sms, cudaStream_t stream);
 
 // q_map: 3-D map over q; k_map / v_map: 4-D maps over the pools.
+// Decode over the 8-bit cache (code pools as k_map / v_map, scales in the args); its
+// stages are 128 tokens, so its split length is a multiple of 128.
+constexpr int kDecodeFp8TileTokens = 128;
 // Decode over the 8-bit cache (code pools as k_map / v_map, scales in the args).
 cudaError_t launch_decode_fp8(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
                               cudaStream_t stream);

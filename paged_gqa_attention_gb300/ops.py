@@ -94,6 +94,9 @@ def load() -> ctypes.CDLL:
     lib.paged_attn_decode_fp8.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, f32,
                                           vp, sz, vp]
     lib.paged_attn_decode_fp8.restype = ctypes.c_int
+    lib.paged_attn_decode_fp8_split.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32,
+                                                f32, i32, vp, sz, vp]
+    lib.paged_attn_decode_fp8_split.restype = ctypes.c_int
     lib.pa_decode_graph_create.argtypes = [pa_shape, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp,
                                            i32, f32, vp, sz, ctypes.POINTER(vp)]
     lib.pa_decode_graph_create.restype = ctypes.c_int
@@ -294,8 +297,10 @@ def kv_append_fp8(k_codes, v_codes, k_scale, v_scale, k_new, v_new, block_table,
 
 
 def paged_attn_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens, workspace, *,
-                          scale: float = DEFAULT_SCALE, out=None, lse=None, stream=None) -> torch.Tensor:
-    """One query token per sequence over the 8-bit cache; returns out [B, 32, 128] bf16."""
+                          scale: float = DEFAULT_SCALE, out=None, lse=None, stream=None,
+                          split_tokens: int = 0) -> torch.Tensor:
+    """One query token per sequence over the 8-bit cache; returns out [B, 32, 128] bf16.
+    split_tokens: context tokens per CTA (multiple of 64), 0 for the library's choice."""
     dev = q.device
     _need(q, "q", torch.bfloat16, (None, NUM_Q_HEADS, HEAD_DIM), dev)
     batch = q.shape[0]
@@ -308,11 +313,11 @@ def paged_attn_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_table, se
     _need(out, "out", torch.bfloat16, tuple(q.shape), dev)
     if lse is not None:
         _need(lse, "lse", torch.float32, (batch, NUM_Q_HEADS), dev)
-    st = load().paged_attn_decode_fp8(SHAPE, out.data_ptr(), _ptr(lse), q.data_ptr(), k_codes.data_ptr(),
-                                      v_codes.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(),
-                                      block_table.data_ptr(), block_table.shape[1], k_codes.shape[0],
-                                      seq_lens.data_ptr(), batch, float(scale), workspace.data_ptr(),
-                                      workspace.numel(), _stream(stream))
+    st = load().paged_attn_decode_fp8_split(SHAPE, out.data_ptr(), _ptr(lse), q.data_ptr(), k_codes.data_ptr(),
+                                            v_codes.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(),
+                                            block_table.data_ptr(), block_table.shape[1], k_codes.shape[0],
+                                            seq_lens.data_ptr(), batch, float(scale), int(split_tokens),
+                                            workspace.data_ptr(), workspace.numel(), _stream(stream))
     _check("paged_attn_decode_fp8", st)
     return out
 
