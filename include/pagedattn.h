@@ -185,6 +185,17 @@ pa_status paged_attn_decode_fp8(pa_shape shape, void *out, float *lse, const voi
                                 const int32_t *seq_lens, int32_t batch, float scale,
                                 void *workspace, size_t workspace_bytes, void *stream);
 
+/* The decode step over the 8-bit cache in one kernel: kv_append_fp8 of each sequence's new
+ * token (row b of k_new / v_new [batch][8][128] bf16, at position seq_lens[b] - 1) fused
+ * with paged_attn_decode_fp8.  Caches and outputs are those of the two separate calls. */
+pa_status paged_attn_decode_append_fp8(pa_shape shape, void *out, float *lse, const void *q,
+                                       const void *k_new, const void *v_new, void *k_codes,
+                                       void *v_codes, float *k_scale, float *v_scale,
+                                       const int32_t *block_table, int32_t max_blocks_per_seq,
+                                       int32_t num_blocks, const int32_t *seq_lens, int32_t batch,
+                                       float scale, void *workspace, size_t workspace_bytes,
+                                       void *stream);
+
 /* As paged_attn_decode_fp8 with the split length fixed by the caller: a positive multiple
  * of 128 tokens (the kernel's stage), or 0 for the library's choice. */
 pa_status paged_attn_decode_fp8_split(pa_shape shape, void *out, float *lse, const void *q,

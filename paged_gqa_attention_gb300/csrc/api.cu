@@ -333,11 +333,13 @@ pa_status kv_append_fp8(pa_shape shape, void *k_codes, void *v_codes, float *k_s
     return launch_kv_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-pa_status paged_attn_decode_fp8_split(pa_shape shape, void *out, float *lse, const void *q, const void *k_codes,
-                                      const void *v_codes, const float *k_scale, const float *v_scale,
-                                      const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
-                                      const int32_t *seq_lens, int32_t batch, float scale, int32_t split_tokens,
-                                      void *workspace, size_t workspace_bytes, void *stream) {
+static pa_status decode_fp8_impl(pa_shape shape, void *out, float *lse, const void *q, const void *k_new, const void *v_new,
+                          const void *k_codes, const void *v_codes, const float *k_scale, const float *v_scale,
+                          const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
+                          const int32_t *seq_lens, int32_t batch, float scale, int32_t split_tokens,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+    if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+        return PA_ERR_INVALID_ARG;
     if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
     if (batch < 0 || batch > kMaxBatch || max_blocks_per_seq < 1 || num_blocks < 1 || !std::isfinite(scale) ||
         split_tokens < 0 || split_tokens % kDecodeFp8TileTokens != 0)
@@ -371,8 +373,8 @@ pa_status paged_attn_decode_fp8_split(pa_shape shape, void *out, float *lse, con
     a.out = out;
     a.lse = lse;
     a.q = q;
-    a.k_new = nullptr;
-    a.v_new = nullptr;
+    a.k_new = k_new;
+    a.v_new = v_new;
     a.k_pool_w = const_cast<void *>(k_codes);
     a.v_pool_w = const_cast<void *>(v_codes);
     a.block_table = block_table;
@@ -393,14 +395,35 @@ pa_status paged_attn_decode_fp8_split(pa_shape shape, void *out, float *lse, con
                                                                                              : PA_ERR_CUDA;
 }
 
+pa_status paged_attn_decode_fp8_split(pa_shape shape, void *out, float *lse, const void *q, const void *k_codes,
+                                      const void *v_codes, const float *k_scale, const float *v_scale,
+                                      const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
+                                      const int32_t *seq_lens, int32_t batch, float scale, int32_t split_tokens,
+                                      void *workspace, size_t workspace_bytes, void *stream) {
+    return decode_fp8_impl(shape, out, lse, q, nullptr, nullptr, k_codes, v_codes, k_scale, v_scale, block_table,
+                           max_blocks_per_seq, num_blocks, seq_lens, batch, scale, split_tokens, workspace,
+                           workspace_bytes, stream);
+}
+
 pa_status paged_attn_decode_fp8(pa_shape shape, void *out, float *lse, const void *q, const void *k_codes,
                                 const void *v_codes, const float *k_scale, const float *v_scale,
                                 const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
                                 const int32_t *seq_lens, int32_t batch, float scale, void *workspace,
                                 size_t workspace_bytes, void *stream) {
-    return paged_attn_decode_fp8_split(shape, out, lse, q, k_codes, v_codes, k_scale, v_scale, block_table,
-                                       max_blocks_per_seq, num_blocks, seq_lens, batch, scale, 0, workspace,
-                                       workspace_bytes, stream);
+    return decode_fp8_impl(shape, out, lse, q, nullptr, nullptr, k_codes, v_codes, k_scale, v_scale, block_table,
+                           max_blocks_per_seq, num_blocks, seq_lens, batch, scale, 0, workspace, workspace_bytes,
+                           stream);
+}
+
+pa_status paged_attn_decode_append_fp8(pa_shape shape, void *out, float *lse, const void *q, const void *k_new,
+                                       const void *v_new, void *k_codes, void *v_codes, float *k_scale,
+                                       float *v_scale, const int32_t *block_table, int32_t max_blocks_per_seq,
+                                       int32_t num_blocks, const int32_t *seq_lens, int32_t batch, float scale,
+                                       void *workspace, size_t workspace_bytes, void *stream) {
+    if (batch > 0 && (!k_new || !v_new)) return PA_ERR_INVALID_ARG;
+    return decode_fp8_impl(shape, out, lse, q, k_new, v_new, k_codes, v_codes, k_scale, v_scale, block_table,
+                           max_blocks_per_seq, num_blocks, seq_lens, batch, scale, 0, workspace, workspace_bytes,
+                           stream);
 }
 
 pa_status paged_attn_decode(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,

@@ -20,6 +20,9 @@
 //   * for O^T += V^T P^T the transposed ldmatrix gives a lane the codes of two tokens for
 //     two dimensions; one byte permute pairs them by dimension, so accumulator row r of
 //     a 16-dim tile holds dimension 2r (r < 8) or 2(r-8)+1;
+//   * fused append (k_new / v_new given): the warp whose 16 rows hold each sequence's new
+//     token quantises the token's K and V rows of its KV head (kv_append_fp8's rule),
+//     writes codes and scales to the cache and patches them into the landed stage;
 //   * the V scale enters through P: each warp keeps a running reference sigma (the
 //     largest V scale it has seen), accumulates P * (s_v / sigma) in f16 and rescales
 //     its accumulator when sigma grows, as the online softmax does for its maximum; the
@@ -189,11 +192,62 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_consta
 
     const int row = w * 16 + ri + ((mi & 1) << 3);   // token row addressed by this lane
 
+    // Fused append: the CTA whose range ends the context owns the new token at position
+    // seq_len - 1; the warp whose rows hold it quantises the token's K (lanes 0-15) and V
+    // (lanes 16-31) row of this KV head, 8 values a lane, stores codes and scale into the
+    // cache and patches them over the stale row of the landed stage before using it.
+    const int p_new = seq_len - 1;
+    const int i_new = (a.k_new && t_end == seq_len) ? (p_new - t_begin) / kTile : -1;
+    const int r_new = (p_new - t_begin) % kTile;        // row within that stage
+    const bool new_here = i_new >= 0 && (r_new >> 4) == w;
+    uint2 new_codes = make_uint2(0u, 0u);
+    float new_scale = 0.f;
+    if (new_here) {
+        const int kv = lane >> 4, chunk = lane & 15;
+        const uint4 src = __ldg(reinterpret_cast<const uint4 *>(
+            static_cast<const char *>(kv ? a.v_new : a.k_new) + ((size_t)b * kHkv + g) * kRowBytes) + chunk);
+        const uint32_t wv[4] = {src.x, src.y, src.z, src.w};
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[2 * e] = bf16_lo(wv[e]);
+            x[2 * e + 1] = bf16_hi(wv[e]);
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        new_scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+        new_codes.x = f32x2_to_e4m3x2(__fdiv_rn(x[0], new_scale), __fdiv_rn(x[1], new_scale)) |
+                      f32x2_to_e4m3x2(__fdiv_rn(x[2], new_scale), __fdiv_rn(x[3], new_scale)) << 16;
+        new_codes.y = f32x2_to_e4m3x2(__fdiv_rn(x[4], new_scale), __fdiv_rn(x[5], new_scale)) |
+                      f32x2_to_e4m3x2(__fdiv_rn(x[6], new_scale), __fdiv_rn(x[7], new_scale)) << 16;
+        const int blk = __ldg(bt + p_new / kBlock);
+        if (blk >= 0 && blk < a.num_blocks) {
+            const int slot = p_new % kBlock;
+            uint8_t *dst = static_cast<uint8_t *>(kv ? a.v_pool_w : a.k_pool_w) +
+                           (((size_t)blk * kBlock + slot) * kHkv + g) * kD + chunk * 8;
+            *reinterpret_cast<uint2 *>(dst) = new_codes;
+            if (chunk == 0)
+                const_cast<float *>(kv ? a.v_scale : a.k_scale)[((size_t)blk * kHkv + g) * kBlock + slot] = new_scale;
+        }   // a bad block id is reported by the producer and poisons the result
+    }
+
     for (int i = 0; i < n_tiles; ++i) {
         const int st = i % kStages;
         if (!mbar_wait(smem_u32(&sm.full[st]), (i / kStages) & 1)) {
             if (lane == 0) record_error(a.err, kErrTimeout);
             break;
+        }
+        if (new_here && i == i_new) {
+            // the new token's row: lane (kv, chunk) holds codes of dims 8 chunk .. 8 chunk + 7,
+            // half (chunk % 2) of swizzled 16-byte chunk chunk / 2 of row r_new
+            const int kv = lane >> 4, chunk = lane & 15;
+            *reinterpret_cast<uint2 *>(sm.codes[st][kv] + sw128(r_new, chunk >> 1) + (chunk & 1) * 8) = new_codes;
+            if (chunk == 0) sm.scales[st][kv][r_new] = new_scale;
+            fence_proxy_async_smem();   // generic writes before the stage is refilled by TMA
+            __syncwarp();
         }
         const int my_valid = min(max(t_end - (t_begin + i * kTile) - w * 16, 0), 16);
         if (my_valid > 0) {

@@ -94,6 +94,9 @@ def load() -> ctypes.CDLL:
     lib.paged_attn_decode_fp8.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, f32,
                                           vp, sz, vp]
     lib.paged_attn_decode_fp8.restype = ctypes.c_int
+    lib.paged_attn_decode_append_fp8.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                                 vp, i32, f32, vp, sz, vp]
+    lib.paged_attn_decode_append_fp8.restype = ctypes.c_int
     lib.paged_attn_decode_fp8_split.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32,
                                                 f32, i32, vp, sz, vp]
     lib.paged_attn_decode_fp8_split.restype = ctypes.c_int
@@ -319,6 +322,35 @@ def paged_attn_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_table, se
                                             seq_lens.data_ptr(), batch, float(scale), int(split_tokens),
                                             workspace.data_ptr(), workspace.numel(), _stream(stream))
     _check("paged_attn_decode_fp8", st)
+    return out
+
+
+def paged_attn_decode_append_fp8(q, k_new, v_new, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens,
+                                 workspace, *, scale: float = DEFAULT_SCALE, out=None, lse=None,
+                                 stream=None) -> torch.Tensor:
+    """kv_append_fp8 of one new token per sequence (k_new/v_new [B, 8, 128], written at
+    position seq_lens[b]-1) fused with paged_attn_decode_fp8: returns out [B, 32, 128]."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (None, NUM_Q_HEADS, HEAD_DIM), dev)
+    batch = q.shape[0]
+    _need(k_new, "k_new", torch.bfloat16, (batch, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_new, "v_new", torch.bfloat16, (batch, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need_fp8_cache(k_codes, v_codes, k_scale, v_scale, dev)
+    _need(block_table, "block_table", torch.int32, (batch, None), dev)
+    _need(seq_lens, "seq_lens", torch.int32, (batch,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, tuple(q.shape), dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (batch, NUM_Q_HEADS), dev)
+    st = load().paged_attn_decode_append_fp8(SHAPE, out.data_ptr(), _ptr(lse), q.data_ptr(), k_new.data_ptr(),
+                                             v_new.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
+                                             k_scale.data_ptr(), v_scale.data_ptr(), block_table.data_ptr(),
+                                             block_table.shape[1], k_codes.shape[0], seq_lens.data_ptr(), batch,
+                                             float(scale), workspace.data_ptr(), workspace.numel(),
+                                             _stream(stream))
+    _check("paged_attn_decode_append_fp8", st)
     return out
 
 

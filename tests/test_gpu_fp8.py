@@ -147,3 +147,28 @@ def test_decode_fp8_bad_block_is_reported():
     assert e.value.status == 4
     assert torch.isnan(out[0].float()).any()
     assert_close(out[1], ref[1], "unaffected sequence")
+
+
+@pytest.mark.parametrize("lens", [[700, 129, 2048, 5, 1, 128, 256, 257], [4096, 3000, 17]])
+def test_fused_append_fp8_equals_the_two_calls(lens):
+    b = wl.build_batch("fp8_fused", 61 + len(lens), lens, [1] * len(lens),
+                       num_blocks=sum((l + 255) // 256 for l in lens) + 2, device="cuda")
+    before = oracle_cache(b, drop_last=1)
+    full = oracle_cache(b)
+    ws = workspace_for(b)
+    c2 = upload(before)
+    ops.kv_append_fp8(*c2, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    lse2 = torch.empty(b.num_seqs, ops.NUM_Q_HEADS, dtype=torch.float32, device="cuda")
+    out2 = ops.paged_attn_decode_fp8(b.q, *c2, b.block_table, b.seq_lens, ws, lse=lse2)
+    c1 = upload(before)
+    lse1 = torch.empty_like(lse2)
+    out1 = ops.paged_attn_decode_append_fp8(b.q, b.k_new, b.v_new, *c1, b.block_table, b.seq_lens, ws, lse=lse1)
+    ops.check_error(ws)
+    for got, want in zip(c1, full):
+        assert same_bits(got, want)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1.view(torch.int32), lse2.view(torch.int32))
+    ref, ref_lse = oracle.attention_fp8(to_cpu(b.q), *full, to_cpu(b.block_table), to_cpu(b.cu_q_lens),
+                                        to_cpu(b.seq_lens), scale=wl.SCALE)
+    assert_close(out1, ref, f"fused fp8 step {lens}")
+    assert_lse_close(lse1, ref_lse, f"fused fp8 step {lens}")
