@@ -53,6 +53,9 @@ TRAFFIC = {
     # one ncu capture of the batched decode step (32 sequences, 243.9 MB of K/V)
     "decode": {"bytes_per_launch": 249672960 + 4535552, "sources": ("decode.cu", "common.cuh"),
                "sha": "fc9df4d86f33d1fd"},
+    # one ncu capture of the fused 8-bit decode step (batch 32, 126 MB of 8-bit K/V)
+    "decode_fp8": {"bytes_per_launch": 131062016 + 3815424, "sources": ("decode_fp8.cu", "common.cuh"),
+                   "sha": "26995a847bf72584"},
     # one ncu capture of the causal prefill of 4096 tokens
     "prefill": {"bytes_per_launch": 50719232 + 1658624, "sources": ("prefill.cu", "common.cuh"),
                 "sha": "bc95774cb225c06a"},
