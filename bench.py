@@ -69,7 +69,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default="batched_decode",
                    choices=["single_decode", "batched_decode", "causal_prefill", "mixed_batch",
-                            "prefix_shared_decode", "layered_decode", "batched_decode_fp8"])
+                            "prefix_shared_decode", "layered_decode", "batched_decode_fp8",
+                            "prefix_shared_decode_cascade"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -514,6 +515,34 @@ def cpu_baseline_fp8(batch, target_s):
                       f"fp64 C oracle over the 8-bit cache with OpenMP"}
 
 
+def cascade_measure(batch, shared_blocks, steps, warmup, flush_buf, stream, clocks):
+    """The decode step of a batch sharing a prefix, as a cascade: kv_append of the new tokens,
+    then paged_attn_decode_cascade (the shared prefix for every query on the tensor cores,
+    then each private suffix with the LSE merge)."""
+    import torch
+
+    from paged_gqa_attention_gb300 import ops
+
+    ws = ops.make_workspace(batch.num_seqs, batch.max_blocks_per_seq)
+    cws = ops.make_cascade_workspace(batch.num_seqs, batch.max_blocks_per_seq, shared_blocks)
+    out = torch.empty_like(batch.q)
+
+    def step(tm):
+        if tm: tm.record(0)
+        ops.kv_append(batch.k_pool, batch.v_pool, batch.k_new, batch.v_new, batch.block_table, batch.cu_q_lens,
+                      batch.seq_lens, ws)
+        if tm: tm.record(1)
+        ops.paged_attn_decode_cascade(batch.q, batch.k_pool, batch.v_pool, batch.block_table, batch.seq_lens,
+                                      shared_blocks, cws, out=out)
+        if tm: tm.record(2)
+
+    spans, wall = run_timed(step, 3, steps, warmup, flush_buf, stream, clocks)
+    ops.check_error(ws)
+    ops.check_error(cws)
+    return {"append_ms": mean([x[0] for x in spans]), "cascade_ms": mean([x[1] for x in spans]),
+            "step_ms": mean([x[0] + x[1] for x in spans]), "wall_s": wall, "launches": 3 * steps}
+
+
 def e2e_decode_measure(batch, steps, warmup, stream):
     """The decode step through the C ABI with host buffers (pa_decode_step_host): pinned
     host inputs copied in, fused append + decode, output copied back, every step."""
@@ -565,6 +594,9 @@ def e2e_measure(batch, kind, steps, warmup, stream):
     d2h = out_host.numel() * out_host.element_size()
     n_dec = batch.info.get("n_decode", 0)
     t_dec = n_dec          # decode tokens come first in a mixed batch (one per sequence)
+    shared = batch.info.get("shared_blocks", 0)
+    cws = (ops.make_cascade_workspace(batch.num_seqs, batch.max_blocks_per_seq, shared)
+           if kind == "cascade" else None)
 
     def step():
         for k in host:
@@ -576,6 +608,9 @@ def e2e_measure(batch, kind, steps, warmup, stream):
             ops.paged_attn_decode_append(dev["q"], dev["k_new"], dev["v_new"], batch.k_pool,
                                          batch.v_pool, dev["block_table"], dev["seq_lens"], ws,
                                          out=out_dev)
+        elif kind == "cascade":
+            ops.paged_attn_decode_cascade(dev["q"], batch.k_pool, batch.v_pool, dev["block_table"],
+                                          dev["seq_lens"], shared, cws, out=out_dev)
         elif kind == "prefill":
             ops.paged_attn_prefill(dev["q"], batch.k_pool, batch.v_pool, dev["block_table"],
                                    dev["cu_q_lens"], dev["seq_lens"], batch.max_q_len, ws,
@@ -698,6 +733,8 @@ def reference_arm(args, world, rank):
         return
     if args.workload == "layered_decode":
         batch = wl.layered_decode(device=dev).base     # GB/s of one layer: the same per layer
+    elif args.workload == "prefix_shared_decode_cascade":
+        batch = wl.prefix_shared_decode(device=dev)    # the cascade computes the same attention
     else:
         batch = wl.WORKLOADS[args.workload](device=dev)
     kind = "decode" if "decode" in args.workload else "prefill"
@@ -723,7 +760,8 @@ def reference_arm(args, world, rank):
 def rows_cap_for(workload):
     """Bound on the (token, head) rows of one oracle pass (keeps a pass to seconds)."""
     return {"single_decode": None, "batched_decode": None, "mixed_batch": 1024,
-            "causal_prefill": 2048, "prefix_shared_decode": 256, "layered_decode": None}[workload]
+            "causal_prefill": 2048, "prefix_shared_decode": 256, "layered_decode": None,
+            "prefix_shared_decode_cascade": 256}[workload]
 
 
 def roofline(achieved, peak, unit, bound, traffic):
@@ -765,6 +803,8 @@ def main():
         batch = layers.base
     elif wname == "batched_decode_fp8":
         batch = wl.batched_decode(device="cuda")
+    elif wname == "prefix_shared_decode_cascade":
+        batch = wl.prefix_shared_decode(device="cuda")
     else:
         batch = wl.WORKLOADS[wname](device="cuda")
     dist_barrier(world)
@@ -827,6 +867,27 @@ def main():
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                        "ms_per_step": e_ms}
         r["graph"].close()
+        kind = "decode"
+    elif wname == "prefix_shared_decode_cascade":
+        shared = batch.info["shared_blocks"]
+        r = cascade_measure(batch, shared, args.steps, args.warmup, flush_buf, stream, clocks)
+        kv_bytes = batch.kv_bytes()
+        uniq = wl.unique_kv_bytes(batch)
+        step_ms = dist_max(r["step_ms"], world)
+        casc_ms = dist_max(r["cascade_ms"], world)
+        line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
+        line["roofline"] = roofline(uniq / (casc_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s", "hbm", None)
+        line["roofline"]["kernel"] = "cascade (prefix pass on prefill_kernel + suffix decode_kernel)"
+        line["roofline"]["algorithmic_bytes_per_launch"] = uniq
+        line["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "cascade_us": r["cascade_ms"] * 1e3,
+                           "kv_bytes_per_step": kv_bytes, "unique_kv_bytes": uniq,
+                           "unique_kv_gbs": uniq / (casc_ms * 1e-3) / 1e9}
+        line["gpu_launches"] = r["launches"]
+        cfg["cascade"] = f"{shared} shared blocks attended once per KV head, then the private suffixes"
+        e = e2e_measure(batch, "cascade", max(10, min(args.steps, 50)), 3, stream)
+        e_ms = dist_max(e["step_ms"], world)
+        line["e2e"] = {"value": world * kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"], "ms_per_step": e_ms}
         kind = "decode"
     elif wname == "batched_decode_fp8":
         cache = fp8_prepare(batch)
@@ -925,7 +986,8 @@ def main():
         if kind == "decode_fp8":
             line["cpu_baseline"] = cpu_baseline_fp8(wl.batched_decode(device="cuda"), args.cpu_seconds)
         else:
-            src = batch if wname in ("layered_decode", batch.name) else wl.WORKLOADS[wname](device="cuda")
+            src = (batch if wname in ("layered_decode", "prefix_shared_decode_cascade", batch.name)
+                   else wl.WORKLOADS[wname](device="cuda"))
             line["cpu_baseline"] = cpu_baseline(src, kind, args.cpu_seconds, rows_cap_for(wname))
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -247,6 +247,29 @@ pa_status pa_decode_step_host(pa_shape shape, void *out_host, float *lse_host,
                               void *stream);
 
 /*
+ * paged_attn_decode_cascade: paged_attn_decode for a batch whose sequences share a prefix
+ * [P1 §2.3 prefix cache: requests with the same prefix reuse its KV state].  The first
+ * shared_blocks entries of every sequence's block table are the same physical blocks
+ * (checked on the device: a sequence whose entries differ from row 0's gets a NaN output
+ * and PA_ERR_DEVICE).  The result is that of paged_attn_decode; the work is split in two:
+ * all batch x 32 queries attend to the shared prefix at once on the tensor cores (the
+ * prefix is read once per KV head instead of once per sequence, split over keys), then
+ * the decode kernel attends each sequence's private suffix and merges the two by
+ * log-sum-exp.  Every seq_lens[b] must exceed shared_blocks * 256 (else PA_ERR_DEVICE).
+ * 1 <= shared_blocks < max_blocks_per_seq.  workspace: pa_cascade_workspace_bytes() bytes,
+ * zeroed once like any workspace.
+ */
+size_t pa_cascade_workspace_bytes(pa_shape shape, int32_t max_batch, int32_t max_blocks_per_seq,
+                                  int32_t shared_blocks);
+
+pa_status paged_attn_decode_cascade(pa_shape shape, void *out, float *lse, const void *q,
+                                    const void *k_pool, const void *v_pool,
+                                    const int32_t *block_table, int32_t max_blocks_per_seq,
+                                    int32_t num_blocks, const int32_t *seq_lens, int32_t batch,
+                                    int32_t shared_blocks, float scale, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/*
  * A decode step over several layers captured once as a CUDA graph and replayed per
  * step: the launch-gap remedy the pages name for a GPU kept idle between kernel
  * launches [P2 §4.2 troubleshooting table: "use CUDA Graph"], decode being dominated by

@@ -161,10 +161,21 @@ HostStepLayout host_step_layout(int batch, int max_blocks_per_seq) {
     return L;
 }
 
+// Cascade extras of a decode over a shared prefix (see DecodeArgs): the first attended
+// token, the prefix partials and the number of shared table entries.
+struct CascadeExtras {
+    int32_t kv_begin;
+    const float *pre_o;
+    const float *pre_lse;
+    int32_t pre_n;
+    int32_t shared_blocks;
+};
+
 pa_status decode_impl(pa_shape shape, void *out, float *lse, const void *q, const void *k_new,
                       const void *v_new, const void *k_pool, const void *v_pool, const int32_t *block_table,
                       int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t *seq_lens, int32_t batch,
-                      float scale, int32_t split_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+                      float scale, int32_t split_tokens, void *workspace, size_t workspace_bytes, void *stream,
+                      const CascadeExtras *cx = nullptr) {
     if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
     if (batch < 0 || batch > kMaxBatch || max_blocks_per_seq < 1 || num_blocks < 1 || !std::isfinite(scale) ||
         split_tokens < 0 || split_tokens % kDecodeTileTokens != 0)
@@ -181,8 +192,9 @@ pa_status decode_impl(pa_shape shape, void *out, float *lse, const void *q, cons
     const int sms = sm_count();
     if (sms <= 0) return PA_ERR_CUDA;
     if (!get_encoder()) return PA_ERR_CUDA;
-    const int split = split_tokens ? split_tokens : auto_split_tokens(batch, max_blocks_per_seq, sms);
-    const long long max_tokens = (long long)max_blocks_per_seq * kBlock;
+    const int skip_blocks = cx ? cx->kv_begin / kBlock : 0;   // a cascade splits only the suffix
+    const int split = split_tokens ? split_tokens : auto_split_tokens(batch, max_blocks_per_seq - skip_blocks, sms);
+    const long long max_tokens = (long long)(max_blocks_per_seq - skip_blocks) * kBlock;
     const long long nsplit = (max_tokens + split - 1) / split;
     if (nsplit > 65535) return PA_ERR_INVALID_ARG;
     const size_t entries = (size_t)batch * kHkv * (size_t)nsplit;
@@ -212,12 +224,41 @@ pa_status decode_impl(pa_shape shape, void *out, float *lse, const void *q, cons
     a.scale_log2 = scale * 1.4426950408889634f;
     a.k_scale = nullptr;
     a.v_scale = nullptr;
+    a.kv_begin = cx ? cx->kv_begin : 0;
+    a.pre_o = cx ? cx->pre_o : nullptr;
+    a.pre_lse = cx ? cx->pre_lse : nullptr;
+    a.pre_n = cx ? cx->pre_n : 0;
+    a.shared_blocks = cx ? cx->shared_blocks : 0;
     a.counters = reinterpret_cast<int32_t *>(ws + kCounterOffset);
     a.part_o = reinterpret_cast<float *>(ws + kPartialOffset);
     a.part_ml = reinterpret_cast<float *>(ws + kPartialOffset + entries * kPartialOBytes);
     a.err = reinterpret_cast<uint32_t *>(ws);
     return launch_decode(a, k_map, v_map, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
                                                                                                  : PA_ERR_CUDA;
+}
+
+// Cascade plan for batch B over tables max_blocks_per_seq wide with shared_blocks shared
+// entries: the prefix keys split into n_kv_splits ranges of kv_split_tiles 128-key tiles
+// (about one prefill unit per SM), and the workspace carved as [decode part | pre_o |
+// pre_lse], each part 256-byte aligned.
+struct CascadePlan {
+    int kv_split_tiles, n_kv_splits;
+    size_t decode_bytes, pre_o_offset, pre_lse_offset, total;
+};
+
+CascadePlan cascade_plan(int batch, int max_blocks_per_seq, int shared_blocks, int sms) {
+    CascadePlan p;
+    const int tiles = shared_blocks * (kBlock / kPrefillKvTile);
+    const int qblocks = (batch + 2 * kPrefillQPositions - 1) / (2 * kPrefillQPositions);
+    int nks = (sms + kHkv * qblocks / 2) / (kHkv * qblocks);
+    nks = nks < 1 ? 1 : (nks > tiles ? tiles : nks);
+    p.kv_split_tiles = (tiles + nks - 1) / nks;
+    p.n_kv_splits = (tiles + p.kv_split_tiles - 1) / p.kv_split_tiles;
+    p.decode_bytes = round256(workspace_bytes_for(partial_entries_bound(batch, max_blocks_per_seq - shared_blocks)));
+    p.pre_o_offset = p.decode_bytes;
+    p.pre_lse_offset = p.pre_o_offset + round256((size_t)p.n_kv_splits * batch * kHq * kD * sizeof(float));
+    p.total = p.pre_lse_offset + round256((size_t)p.n_kv_splits * batch * kHq * sizeof(float));
+    return p;
 }
 
 }  // namespace
@@ -387,6 +428,11 @@ static pa_status decode_fp8_impl(pa_shape shape, void *out, float *lse, const vo
     a.scale_log2 = scale * 1.4426950408889634f;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
+    a.kv_begin = 0;
+    a.pre_o = nullptr;
+    a.pre_lse = nullptr;
+    a.pre_n = 0;
+    a.shared_blocks = 0;
     a.counters = reinterpret_cast<int32_t *>(ws + kCounterOffset);
     a.part_o = reinterpret_cast<float *>(ws + kPartialOffset);
     a.part_ml = reinterpret_cast<float *>(ws + kPartialOffset + entries * kPartialOBytes);
@@ -620,6 +666,9 @@ pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *
     a.max_q_len = max_q_len;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.err = static_cast<uint32_t *>(workspace);
+    a.prefix_len = 0;
+    a.kv_split_tiles = 0;
+    a.n_kv_splits = 1;
     return launch_prefill(a, q_map, k_map, v_map, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
@@ -700,6 +749,69 @@ pa_status pa_decode_graph_destroy(pa_decode_graph *graph) {
                     (!graph->graph || cudaGraphDestroy(graph->graph) == cudaSuccess);
     delete graph;
     return ok ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_cascade_workspace_bytes(pa_shape shape, int32_t max_batch, int32_t max_blocks_per_seq,
+                                  int32_t shared_blocks) {
+    if (!shape_ok(shape) || max_batch < 1 || max_batch > kMaxBatch || shared_blocks < 1 ||
+        shared_blocks >= max_blocks_per_seq)
+        return 0;
+    const int sms = sm_count();
+    if (sms <= 0) return 0;
+    return cascade_plan(max_batch, max_blocks_per_seq, shared_blocks, sms).total;
+}
+
+pa_status paged_attn_decode_cascade(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
+                                    const void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
+                                    int32_t num_blocks, const int32_t *seq_lens, int32_t batch,
+                                    int32_t shared_blocks, float scale, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+    if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
+    if (batch < 0 || batch > kMaxBatch || max_blocks_per_seq < 2 || num_blocks < 1 || shared_blocks < 1 ||
+        shared_blocks >= max_blocks_per_seq || !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kPartialOffset || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
+    if (batch == 0) return PA_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_table || !seq_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned4(block_table) ||
+        !aligned4(seq_lens) || (lse && !aligned4(lse)))
+        return PA_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms <= 0 || !get_encoder()) return PA_ERR_CUDA;
+    const CascadePlan plan = cascade_plan(batch, max_blocks_per_seq, shared_blocks, sms);
+    if (workspace_bytes < plan.total) return PA_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    float *pre_o = reinterpret_cast<float *>(ws + plan.pre_o_offset);
+    float *pre_lse = reinterpret_cast<float *>(ws + plan.pre_lse_offset);
+
+    // 1. every query over the shared prefix (block_table row 0), split over keys, on the
+    //    tensor cores: normalised fp32 partials and their lse
+    CUtensorMap q_map, kp_map, vp_map;
+    if (!encode_q_map(&q_map, q, batch) || !encode_pool_map(&kp_map, k_pool, num_blocks, kPrefillKvTile) ||
+        !encode_pool_map(&vp_map, v_pool, num_blocks, kPrefillKvTile))
+        return PA_ERR_INVALID_ARG;
+    PrefillArgs p;
+    p.out = pre_o;
+    p.lse = pre_lse;
+    p.block_table = block_table;
+    p.max_blocks_per_seq = shared_blocks;
+    p.num_blocks = num_blocks;
+    p.cu_q_lens = nullptr;
+    p.seq_lens = nullptr;
+    p.num_seqs = 1;
+    p.total_tokens = batch;
+    p.max_q_len = batch;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = reinterpret_cast<uint32_t *>(ws);
+    p.prefix_len = shared_blocks * kBlock;
+    p.kv_split_tiles = plan.kv_split_tiles;
+    p.n_kv_splits = plan.n_kv_splits;
+    if (launch_prefill_prefix(p, q_map, kp_map, vp_map, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PA_ERR_CUDA;
+    // 2. each sequence's private suffix, merged with the prefix partials
+    const CascadeExtras cx = {shared_blocks * kBlock, pre_o, pre_lse, plan.n_kv_splits, shared_blocks};
+    return decode_impl(shape, out, lse, q, nullptr, nullptr, k_pool, v_pool, block_table, max_blocks_per_seq,
+                       num_blocks, seq_lens, batch, scale, 0, workspace, plan.decode_bytes, stream, &cx);
 }
 
 pa_status pa_selftest_wait_timeout(void *workspace, size_t workspace_bytes, uint32_t timeout_us, void *stream) {

@@ -61,6 +61,33 @@ struct DecodeSmem {
 
 constexpr size_t kSmemBytes = sizeof(DecodeSmem) + 1024;  // + alignment slack
 
+// Fold the shared-prefix partials of output row (b, qh) into (M, L, o): M in log2 units,
+// o unnormalised; each partial is a normalised output with weight e^lse.
+__device__ __forceinline__ void fold_prefix(const DecodeArgs &a, int b, int qh, int d0, float &M, float &L,
+                                            float (&o)[4]) {
+    for (int k = 0; k < a.pre_n; ++k) {
+        const size_t row = ((size_t)k * a.batch + b) * kHq + qh;
+        const float mk = __ldcg(a.pre_lse + row) * 1.4426950408889634f;
+        const float4 ok = __ldcg(reinterpret_cast<const float4 *>(a.pre_o + row * kD + d0));
+        const float mn = fmaxf(M, mk);
+        const float e_old = fast_exp2(M - mn), e_k = fast_exp2(mk - mn);
+        L = L * e_old + e_k;
+        o[0] = o[0] * e_old + ok.x * e_k;
+        o[1] = o[1] * e_old + ok.y * e_k;
+        o[2] = o[2] * e_old + ok.z * e_k;
+        o[3] = o[3] * e_old + ok.w * e_k;
+        M = mn;
+    }
+}
+
+// A cascade is only valid if this sequence's first shared_blocks table entries are row 0's
+// (the prefix partials were computed from row 0): checked by each warp writing an output.
+__device__ __forceinline__ bool shared_table_mismatch(const DecodeArgs &a, const int32_t *bt, int lane) {
+    bool bad = false;
+    for (int j = lane; j < a.shared_blocks; j += 32) bad |= __ldg(bt + j) != __ldg(a.block_table + j);
+    return __any_sync(0xffffffffu, bad);
+}
+
 __device__ __forceinline__ void store_out4(__nv_bfloat16 *dst, const float (&v)[4], float inv) {
     uint2 w;
     w.x = pack_bf16x2(v[0] * inv, v[1] * inv);
@@ -90,17 +117,18 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     if (warp == kConsumerWarps && lane == 0) {
         tma_prefetch_map(&k_map);
         tma_prefetch_map(&v_map);
-        blk0 = __ldg(bt + (split * a.split_tokens) / kBlock);   // < max_blocks_per_seq
+        blk0 = __ldg(bt + (a.kv_begin + split * a.split_tokens) / kBlock);   // < max_blocks_per_seq
     }
     const int seq_len = __ldg(a.seq_lens + b);
-    if (seq_len < 1 || seq_len > a.max_blocks_per_seq * kBlock) {
+    // (a cascade attends only past the shared prefix: the context must extend beyond it)
+    if (seq_len < 1 || seq_len > a.max_blocks_per_seq * kBlock || seq_len <= a.kv_begin) {
         if (split == 0 && g == 0 && threadIdx.x == 0) record_error(a.err, kErrDevice | kErrBadSeqLen);
         return;  // every CTA of this sequence takes the same exit: counters untouched
     }
-    const int t_begin = split * a.split_tokens;
+    const int t_begin = a.kv_begin + split * a.split_tokens;
     if (t_begin >= seq_len) return;       // this split lies past the context
     const int t_end = min(t_begin + a.split_tokens, seq_len);
-    const int nsplit_b = (seq_len + a.split_tokens - 1) / a.split_tokens;
+    const int nsplit_b = (seq_len - a.kv_begin + a.split_tokens - 1) / a.split_tokens;
     const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
 
     if (threadIdx.x == 0) {
@@ -350,6 +378,13 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + ((size_t)b * kHq + qh) * kD + d0;
 
     if (nsplit_b == 1) {
+        if (a.pre_n > 0) {
+            fold_prefix(a, b, qh, d0, M, L, o4);
+            if (shared_table_mismatch(a, bt, c & 31)) {
+                if ((c & 31) == 0) record_error(a.err, kErrDevice | kErrBadBlock);
+                M = L = __int_as_float(0x7fc00000);
+            }
+        }
         store_out4(out, o4, 1.f / L);
         if (a.lse && (c & 31) == 0) a.lse[(size_t)b * kHq + qh] = (M + __log2f(L)) * kLn2;
         return;
@@ -389,6 +424,13 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         go[1] += ok.y * e;
         go[2] += ok.z * e;
         go[3] += ok.w * e;
+    }
+    if (a.pre_n > 0) {
+        fold_prefix(a, b, qh, d0, GM, GL, go);
+        if (shared_table_mismatch(a, bt, c & 31)) {
+            if ((c & 31) == 0) record_error(a.err, kErrDevice | kErrBadBlock);
+            GM = GL = __int_as_float(0x7fc00000);
+        }
     }
     store_out4(out, go, 1.f / GL);
     if (a.lse && (c & 31) == 0) a.lse[(size_t)b * kHq + qh] = (GM + __log2f(GL)) * kLn2;

@@ -45,6 +45,16 @@ struct DecodeArgs {
     float scale_log2;      // softmax scale * log2(e)
     const float *k_scale;  // 8-bit cache only: row scales [num_blocks][8][256]
     const float *v_scale;
+    // Cascade over a shared prefix (decode kernel only): attend to tokens kv_begin ..
+    // seq_len-1 and fold in pre_n partials of the prefix, pre_o [k][batch][32][128] fp32
+    // normalised and pre_lse [k][batch][32] (natural log); the first shared_blocks table
+    // entries of every sequence must equal row 0's.  kv_begin = pre_n = shared_blocks = 0
+    // otherwise.
+    int32_t kv_begin;
+    const float *pre_o;
+    const float *pre_lse;
+    int32_t pre_n;
+    int32_t shared_blocks;
     int32_t *counters;     // [batch * 8], zero on entry, zero again on exit
     float *part_o;         // [batch * 8 * nsplit][4][128]
     float *part_ml;        // [batch * 8 * nsplit][4][2]
@@ -64,6 +74,13 @@ struct PrefillArgs {
     int32_t max_q_len;
     float scale_log2;
     uint32_t *err;
+    // Shared-prefix mode (launch_prefill_prefix): the total_tokens queries all attend to
+    // keys 0 .. prefix_len-1 of block_table row 0 (no causal mask), split over keys into
+    // n_kv_splits ranges of kv_split_tiles 128-key tiles; out receives fp32 normalised
+    // partial outputs [split][token][32][128] and lse [split][token][32] (natural log).
+    int32_t prefix_len;
+    int32_t kv_split_tiles;
+    int32_t n_kv_splits;
 };
 
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
@@ -83,6 +100,9 @@ constexpr int kDecodeFp8TileTokens = 128;
 // Decode over the 8-bit cache (code pools as k_map / v_map, scales in the args).
 cudaError_t launch_decode_fp8(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
                               cudaStream_t stream);
+
+cudaError_t launch_prefill_prefix(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
+                                  const CUtensorMap &v_map, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
                            const CUtensorMap &k_map, const CUtensorMap &v_map, int num_sms,

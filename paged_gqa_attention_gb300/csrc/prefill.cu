@@ -92,7 +92,9 @@ struct Unit {
     int positions;  // real positions in this unit (1..64)
     int pos0;       // absolute position of the unit's first query
     int seq_len;    // context length (keys 0 .. seq_len-1 exist)
-    int n_kt;       // key tiles to visit: 0 .. (last position) / 128
+    int kt0;        // first key tile visited (0 unless the keys are split)
+    int n_kt;       // key tiles to visit: kt0 .. kt0 + n_kt - 1
+    int ks;         // key split of the unit (shared-prefix mode)
 };
 
 __device__ __forceinline__ Unit unit_at(const PrefillArgs &a, int idx, int qblocks) {
@@ -119,8 +121,38 @@ __device__ __forceinline__ Unit unit_at(const PrefillArgs &a, int idx, int qbloc
     t.positions = min(kUnitPos, q_len - qb * kUnitPos);
     t.pos0 = seq_len - q_len + qb * kUnitPos;
     t.seq_len = seq_len;
+    t.kt0 = 0;
     t.n_kt = (t.pos0 + t.positions - 1) / kKT + 1;
+    t.ks = 0;
     return t;
+}
+
+// Shared-prefix mode: unit idx = ((query block) x 8 + KV head) x n_kv_splits + key split;
+// every query sees keys 0 .. prefix_len-1 of table row 0.
+__device__ __forceinline__ Unit unit_at_prefix(const PrefillArgs &a, int idx, int qblocks) {
+    Unit t;
+    const int ks = idx % a.n_kv_splits;
+    const int rest = idx / a.n_kv_splits;
+    const int qb = qblocks - 1 - rest / kHkv;
+    t.s = 0;
+    t.g = rest % kHkv;
+    t.error = false;
+    t.run = qb * kUnitPos < a.total_tokens;
+    t.tok0 = qb * kUnitPos;
+    t.positions = min(kUnitPos, a.total_tokens - qb * kUnitPos);
+    t.pos0 = 0;
+    t.seq_len = a.prefix_len;
+    t.kt0 = ks * a.kv_split_tiles;
+    t.n_kt = min(a.kv_split_tiles, (a.prefix_len + kKT - 1) / kKT - t.kt0);
+    t.ks = ks;
+    if (t.n_kt <= 0) t.run = false;
+    return t;
+}
+
+template <bool kPrefix>
+__device__ __forceinline__ Unit unit_for(const PrefillArgs &a, int idx, int qblocks) {
+    if constexpr (kPrefix) return unit_at_prefix(a, idx, qblocks);
+    else return unit_at(a, idx, qblocks);
 }
 
 // Index of this CTA's r-th unit in the snake order (or -1 past the end).
@@ -147,6 +179,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     }
 }
 
+template <bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                const __grid_constant__ CUtensorMap v_map, const PrefillArgs a) {
@@ -157,7 +190,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int qblocks = (a.max_q_len + kUnitPos - 1) / kUnitPos;
-    const int total = a.num_seqs * kHkv * qblocks;
+    const int total = kPrefix ? kHkv * qblocks * a.n_kv_splits : a.num_seqs * kHkv * qblocks;
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&sm.q_full), 1);
@@ -217,7 +250,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         for (int r = 0; ok; ++r) {
             const int idx = snake(r, total);
             if (idx < 0) break;
-            const Unit t = unit_at(a, idx, qblocks);
+            const Unit t = unit_for<kPrefix>(a, idx, qblocks);
             if (qk && leader && t.error) record_error(a.err, kErrDevice | kErrQLen);
             if (!t.run) continue;
             if (qk) {
@@ -239,12 +272,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             const int32_t *bt = a.block_table + (size_t)t.s * a.max_blocks_per_seq;
             for (int j = 0; j < t.n_kt; ++j, ++it) {
                 const int st = it % ns;
-                int blk = __ldg(bt + (j >> 1));
+                const int jg = t.kt0 + j;              // key tile within the context
+                int blk = __ldg(bt + (jg >> 1));
                 if (blk < 0 || blk >= a.num_blocks) {
                     if (qk && leader) record_error(a.err, kErrDevice | kErrBadBlock);
                     blk = 0;   // stay inside the pool; the result is flagged as invalid
                 }
-                const int off = (j & 1) * kKT;
+                const int off = (jg & 1) * kKT;
                 if (it >= ns &&
                     !(ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&empty[st]), ((it / ns) - 1) & 1,
                                                                 abort_flag, a.err))))
@@ -334,7 +368,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         for (int r = 0; ok; ++r) {
             const int idx = snake(r, total);
             if (idx < 0) break;
-            const Unit t = unit_at(a, idx, qblocks);
+            const Unit t = unit_for<kPrefix>(a, idx, qblocks);
             if (!t.run) continue;
             if (!(ok = wait_all(&sm.q_full, tcount & 1))) break;
             for (int j = 0; j < t.n_kt; ++j, ++it) {
@@ -375,10 +409,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         for (int r = 0; ok; ++r) {
             const int idx = snake(r, total);
             if (idx < 0) break;
-            const Unit t = unit_at(a, idx, qblocks);
+            const Unit t = unit_for<kPrefix>(a, idx, qblocks);
             if (!t.run) continue;
-            const int pos_first = t.pos0 + x * kTilePos;   // first query position of this tile
-            const int pos = pos_first + pl;
+            // the last key each row may see: its own position (causal), or the whole prefix
+            const int pos_first = kPrefix ? t.seq_len - 1 : t.pos0 + x * kTilePos;
+            const int pos = kPrefix ? t.seq_len - 1 : pos_first + pl;
             float m = -INFINITY;                   // running max, log2 units (scaled)
             float l = 0.f;                         // running sum of the bf16 weights
             for (int j = 0; j < t.n_kt; ++j, ++it) {
@@ -391,14 +426,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tmem_wait_ld(s[c]);
 
-                // causal mask (only on tiles reaching past the tile's first query position)
-                // and the row maximum of the raw scores
-                if ((j * kKT + kKT - 1) > pos_first) {
+                // mask of the keys past each row's last visible key (only on tiles reaching
+                // past the tile's first such key) and the row maximum of the raw scores
+                const int jg = t.kt0 + j;                  // key tile within the context
+                if ((jg * kKT + kKT - 1) > pos_first) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            if ((j * kKT + c * 32 + e) > pos) s[c][e] = __float_as_uint(-INFINITY);
+                            if ((jg * kKT + c * 32 + e) > pos) s[c][e] = __float_as_uint(-INFINITY);
                 }
                 // independent partial maxima (one per 32-column chunk) keep the dependency
                 // chain short: floating-point max/add are not reassociated by the compiler
@@ -444,7 +480,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                 // V rows past the end of the context (the tail of the last block) may hold
                 // anything, NaN included; P is 0 there but 0 * NaN is not, so tile A (the
                 // V tile's first reader) zeroes them.
-                const int kv_valid = t.seq_len - j * kKT;
+                const int kv_valid = t.seq_len - jg * kKT;
                 if (x == 0 && kv_valid < kKT) {
                     const int vs = it % kVStages;
                     ok = wait_or_abort(smem_u32(&sm.v_full[vs]), (it / kVStages) & 1, abort_flag, a.err);
@@ -499,25 +535,37 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             tc_fence_after();
             const float inv_l = 1.f / l;
             const bool row_ok = x * kTilePos + pl < t.positions;
-            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
-                                 ((size_t)(t.tok0 + x * kTilePos + pl) * kHq + t.g * kGroup + hl) * kD;
+            // shared-prefix mode: fp32 partials of key split ks, [ks][token][32][128]
+            const size_t orow = (size_t)t.ks * a.total_tokens * kHq +
+                                (size_t)(t.tok0 + x * kTilePos + pl) * kHq + t.g * kGroup + hl;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
                 tmem_ld32(lane_base + o_col + c * 32, o);
                 tmem_wait_ld(o);
-                uint32_t w[16];
+                if constexpr (kPrefix) {
+                    if (row_ok) {
+                        float4 *d4 = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + orow * kD + c * 32);
 #pragma unroll
-                for (int e = 0; e < 32; e += 2)
-                    w[e / 2] = pack_bf16x2(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
-                if (row_ok) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+                        for (int v = 0; v < 8; ++v)
+                            d4[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                                __uint_as_float(o[4 * v + 2]) * inv_l,
+                                                __uint_as_float(o[4 * v + 3]) * inv_l);
+                    }
+                } else {
+                    uint32_t w[16];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+                    for (int e = 0; e < 32; e += 2)
+                        w[e / 2] = pack_bf16x2(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
+                    if (row_ok) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * kD + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+                    }
                 }
             }
-            if (row_ok && a.lse)
-                a.lse[(size_t)(t.tok0 + x * kTilePos + pl) * kHq + t.g * kGroup + hl] = (m + __log2f(l)) * kLn2;
+            if (row_ok && a.lse) a.lse[orow] = (m + __log2f(l)) * kLn2;
             tc_fence_before();
         }
     }
@@ -542,21 +590,22 @@ __global__ void wait_selftest_kernel(uint32_t *err, uint64_t limit_ns) {
     if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, limit_ns)) record_error(err, kErrTimeout);
 }
 
-}  // namespace
-
-cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
-                           const CUtensorMap &v_map, int num_sms, cudaStream_t stream) {
+template <bool kPrefix>
+cudaError_t launch_prefill_mode(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
+                                const CUtensorMap &v_map, int num_sms, cudaStream_t stream) {
     if (a.num_seqs == 0 || a.max_q_len == 0 || a.total_tokens == 0) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     static bool configured[64] = {};
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        e = cudaFuncSetAttribute(prefill_kernel<kPrefix>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
-    const long long units = (long long)a.num_seqs * kHkv * ((a.max_q_len + kUnitPos - 1) / kUnitPos);
+    const long long qblocks = (a.max_q_len + kUnitPos - 1) / kUnitPos;
+    const long long units = kPrefix ? kHkv * qblocks * a.n_kv_splits : (long long)a.num_seqs * kHkv * qblocks;
     const int grid = (int)(units < num_sms ? units : num_sms);
     // Programmatic dependent launch: the producers wait (griddepcontrol.wait) before their
     // first load, so the launch and prologue may overlap the previous kernel on the stream.
@@ -570,7 +619,19 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel, q_map, k_map, v_map, a);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<kPrefix>, q_map, k_map, v_map, a);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
+                           const CUtensorMap &v_map, int num_sms, cudaStream_t stream) {
+    return launch_prefill_mode<false>(a, q_map, k_map, v_map, num_sms, stream);
+}
+
+cudaError_t launch_prefill_prefix(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
+                                  const CUtensorMap &v_map, int num_sms, cudaStream_t stream) {
+    return launch_prefill_mode<true>(a, q_map, k_map, v_map, num_sms, stream);
 }
 
 cudaError_t launch_wait_selftest(uint32_t *err, uint64_t limit_ns, cudaStream_t stream) {

@@ -100,6 +100,11 @@ def load() -> ctypes.CDLL:
     lib.paged_attn_decode_fp8_split.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32,
                                                 f32, i32, vp, sz, vp]
     lib.paged_attn_decode_fp8_split.restype = ctypes.c_int
+    lib.pa_cascade_workspace_bytes.argtypes = [pa_shape, i32, i32, i32]
+    lib.pa_cascade_workspace_bytes.restype = sz
+    lib.paged_attn_decode_cascade.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, i32, f32,
+                                              vp, sz, vp]
+    lib.paged_attn_decode_cascade.restype = ctypes.c_int
     lib.pa_decode_graph_create.argtypes = [pa_shape, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp,
                                            i32, f32, vp, sz, ctypes.POINTER(vp)]
     lib.pa_decode_graph_create.restype = ctypes.c_int
@@ -351,6 +356,42 @@ def paged_attn_decode_append_fp8(q, k_new, v_new, k_codes, v_codes, k_scale, v_s
                                              float(scale), workspace.data_ptr(), workspace.numel(),
                                              _stream(stream))
     _check("paged_attn_decode_append_fp8", st)
+    return out
+
+
+def make_cascade_workspace(max_batch: int, max_blocks_per_seq: int, shared_blocks: int, device=None,
+                           stream=None) -> torch.Tensor:
+    """Allocate and zero a workspace for paged_attn_decode_cascade."""
+    n = load().pa_cascade_workspace_bytes(SHAPE, max_batch, max_blocks_per_seq, shared_blocks)
+    if n == 0:
+        raise ValueError("invalid cascade workspace request")
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    _check("pa_workspace_init", load().pa_workspace_init(ws.data_ptr(), n, _stream(stream)))
+    return ws
+
+
+def paged_attn_decode_cascade(q, k_pool, v_pool, block_table, seq_lens, shared_blocks: int, workspace, *,
+                              scale: float = DEFAULT_SCALE, out=None, lse=None, stream=None) -> torch.Tensor:
+    """paged_attn_decode for sequences whose first shared_blocks table entries are the same
+    blocks: the shared prefix attended once for all queries, then each private suffix."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (None, NUM_Q_HEADS, HEAD_DIM), dev)
+    batch = q.shape[0]
+    _need(k_pool, "k_pool", torch.bfloat16, (None, BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_pool, "v_pool", torch.bfloat16, tuple(k_pool.shape), dev)
+    _need(block_table, "block_table", torch.int32, (batch, None), dev)
+    _need(seq_lens, "seq_lens", torch.int32, (batch,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, tuple(q.shape), dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (batch, NUM_Q_HEADS), dev)
+    st = load().paged_attn_decode_cascade(SHAPE, out.data_ptr(), _ptr(lse), q.data_ptr(), k_pool.data_ptr(),
+                                          v_pool.data_ptr(), block_table.data_ptr(), block_table.shape[1],
+                                          k_pool.shape[0], seq_lens.data_ptr(), batch, int(shared_blocks),
+                                          float(scale), workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check("paged_attn_decode_cascade", st)
     return out
 
 
