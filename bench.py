@@ -51,14 +51,14 @@ HEAD_START_CYCLES = 200_000      # ~0.1 ms spin so a step's launches are all que
 # whose sources changed since reports traffic null.
 TRAFFIC = {
     # one ncu capture of the batched decode step (32 sequences, 243.9 MB of K/V)
-    "decode": {"bytes_per_launch": 249672960 + 4535552, "sources": ("decode.cu", "common.cuh"),
-               "sha": "fc9df4d86f33d1fd"},
+    "decode": {"bytes_per_launch": 249187840 + 4330240, "sources": ("decode.cu", "common.cuh"),
+               "sha": "fd3ceb8afb829cfe"},
     # one ncu capture of the fused 8-bit decode step (batch 32, 126 MB of 8-bit K/V)
     "decode_fp8": {"bytes_per_launch": 131062016 + 3815424, "sources": ("decode_fp8.cu", "common.cuh"),
                    "sha": "26995a847bf72584"},
     # one ncu capture of the causal prefill of 4096 tokens
-    "prefill": {"bytes_per_launch": 50719232 + 1658624, "sources": ("prefill.cu", "common.cuh"),
-                "sha": "bc95774cb225c06a"},
+    "prefill": {"bytes_per_launch": 50702336 + 1554432, "sources": ("prefill.cu", "common.cuh"),
+                "sha": "a19e7418e23e9cb9"},
 }
 
 
