@@ -341,6 +341,11 @@ pa_status paged_attn_decode_static(pa_shape shape, void *out, float *lse, const 
  * p = seq_lens[s] - q_len + i and attends to context positions 0..p (its own key
  * included).  A sequence with q_len 0 is skipped.  max_q_len must bound every
  * q_len (checked on the device).  lse may be NULL.
+ * The workspace needs only its error word (256 bytes).  With several sequences and a
+ * workspace of pa_workspace_bytes() size, a planning kernel first sorts the work
+ * units (64 positions x one KV head) by the number of key tiles they visit, into the
+ * workspace's split-K area, so that the longest are started first; a workspace too
+ * small for that list gets the natural order.  Results do not depend on the order.
  */
 pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *q,
                              const void *k_pool, const void *v_pool,

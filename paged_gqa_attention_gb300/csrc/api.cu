@@ -206,7 +206,7 @@ pa_status decode_impl(pa_shape shape, void *out, float *lse, const void *q, cons
         return PA_ERR_INVALID_ARG;
 
     char *ws = static_cast<char *>(workspace);
-    DecodeArgs a;
+    DecodeArgs a = {};
     a.out = out;
     a.lse = lse;
     a.q = q;
@@ -320,7 +320,7 @@ pa_status kv_append(pa_shape shape, void *k_pool, void *v_pool, const void *k_ne
     if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new) ||
         !aligned4(block_table) || !aligned4(cu_q_lens) || !aligned4(seq_lens))
         return PA_ERR_INVALID_ARG;
-    AppendArgs a;
+    AppendArgs a = {};
     a.k_pool = k_pool;
     a.v_pool = v_pool;
     a.k_scale = nullptr;
@@ -356,7 +356,7 @@ pa_status kv_append_fp8(pa_shape shape, void *k_codes, void *v_codes, float *k_s
         !aligned16(k_new) || !aligned16(v_new) || !aligned4(block_table) || !aligned4(cu_q_lens) ||
         !aligned4(seq_lens))
         return PA_ERR_INVALID_ARG;
-    AppendArgs a;
+    AppendArgs a = {};
     a.k_pool = k_codes;
     a.v_pool = v_codes;
     a.k_scale = k_scale;
@@ -410,7 +410,7 @@ static pa_status decode_fp8_impl(pa_shape shape, void *out, float *lse, const vo
         !encode_code_map(&v_map, v_codes, num_blocks, kDecodeFp8TileTokens))
         return PA_ERR_INVALID_ARG;
     char *ws = static_cast<char *>(workspace);
-    DecodeArgs a;
+    DecodeArgs a = {};
     a.out = out;
     a.lse = lse;
     a.q = q;
@@ -602,7 +602,7 @@ pa_status paged_attn_decode_static(pa_shape shape, void *out, float *lse, const 
     if (!encode_pool_map(&k_map, k_pool, num_blocks, kDecodeTileTokens) ||
         !encode_pool_map(&v_map, v_pool, num_blocks, kDecodeTileTokens))
         return PA_ERR_INVALID_ARG;
-    DecodeArgs a;
+    DecodeArgs a = {};
     a.out = out;
     a.lse = lse;
     a.q = q;
@@ -620,6 +620,11 @@ pa_status paged_attn_decode_static(pa_shape shape, void *out, float *lse, const 
     a.scale_log2 = scale * 1.4426950408889634f;
     a.k_scale = nullptr;
     a.v_scale = nullptr;
+    a.kv_begin = 0;        // no shared prefix: the whole context, no partials to fold in
+    a.pre_o = nullptr;
+    a.pre_lse = nullptr;
+    a.pre_n = 0;
+    a.shared_blocks = 0;
     a.counters = reinterpret_cast<int32_t *>(ws + kCounterOffset);
     a.part_o = reinterpret_cast<float *>(ws + kPartialOffset);
     a.part_ml = reinterpret_cast<float *>(ws + kPartialOffset + entries * kPartialOBytes);
@@ -653,7 +658,7 @@ pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *
     if (!encode_q_map(&q_map, q, total_tokens) || !encode_pool_map(&k_map, k_pool, num_blocks, kPrefillKvTile) ||
         !encode_pool_map(&v_map, v_pool, num_blocks, kPrefillKvTile))
         return PA_ERR_INVALID_ARG;
-    PrefillArgs a;
+    PrefillArgs a = {};
     a.out = out;
     a.lse = lse;
     a.block_table = block_table;
@@ -669,6 +674,12 @@ pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *
     a.prefix_len = 0;
     a.kv_split_tiles = 0;
     a.n_kv_splits = 1;
+    // Several sequences: the units are sorted by work first, into the workspace's partial
+    // area (decode scratch, unused by the prefill) when it is large enough.
+    a.order = nullptr;
+    const long long plan_units = prefill_plan_units(a);
+    if (plan_units > 0 && workspace_bytes >= kPartialOffset + (size_t)plan_units * sizeof(int32_t))
+        a.order = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + kPartialOffset);
     return launch_prefill(a, q_map, k_map, v_map, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
@@ -790,7 +801,7 @@ pa_status paged_attn_decode_cascade(pa_shape shape, void *out, float *lse, const
     if (!encode_q_map(&q_map, q, batch) || !encode_pool_map(&kp_map, k_pool, num_blocks, kPrefillKvTile) ||
         !encode_pool_map(&vp_map, v_pool, num_blocks, kPrefillKvTile))
         return PA_ERR_INVALID_ARG;
-    PrefillArgs p;
+    PrefillArgs p = {};
     p.out = pre_o;
     p.lse = pre_lse;
     p.block_table = block_table;
@@ -806,6 +817,7 @@ pa_status paged_attn_decode_cascade(pa_shape shape, void *out, float *lse, const
     p.prefix_len = shared_blocks * kBlock;
     p.kv_split_tiles = plan.kv_split_tiles;
     p.n_kv_splits = plan.n_kv_splits;
+    p.order = nullptr;
     if (launch_prefill_prefix(p, q_map, kp_map, vp_map, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PA_ERR_CUDA;
     // 2. each sequence's private suffix, merged with the prefix partials

@@ -81,6 +81,10 @@ struct PrefillArgs {
     int32_t prefix_len;
     int32_t kv_split_tiles;
     int32_t n_kv_splits;
+    // Several sequences: order[rank] = unit dealt at rank (units sorted by key tiles, most
+    // first), written by a planning kernel launched just before the prefill; nullptr: the
+    // units are dealt in their natural order (latest query blocks first).
+    int32_t *order;
 };
 
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
@@ -103,6 +107,10 @@ cudaError_t launch_decode_fp8(const DecodeArgs &a, const CUtensorMap &k_map, con
 
 cudaError_t launch_prefill_prefix(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
                                   const CUtensorMap &v_map, int num_sms, cudaStream_t stream);
+
+// Units the planning kernel orders (several sequences), 0 when the natural order is
+// used; a non-null PrefillArgs::order must hold this many int32 entries.
+long long prefill_plan_units(const PrefillArgs &a);
 
 cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
                            const CUtensorMap &k_map, const CUtensorMap &v_map, int num_sms,

@@ -21,8 +21,9 @@
 // score block; at 128 rows per K/V tile the L2-to-SM delivery (not the tensor core) was
 // the limit.
 //
-// CTA = 11 warps, persistent (one per SM), units dealt in a snake order, latest query
-// blocks (most keys) first:
+// CTA = 11 warps, persistent (one per SM), units dealt in a snake order, most key tiles
+// first (one sequence: latest query blocks first; several: in the order a planning
+// kernel sorts them into, longest processing time first):
 //   warps 0-3   softmax + epilogue of tile A; thread = one row (= TMEM lane) of A
 //   warps 4-7   softmax + epilogue of tile B
 //   warp 8      TMA producer of Q and K (ring of 2 slots)
@@ -149,10 +150,80 @@ __device__ __forceinline__ Unit unit_at_prefix(const PrefillArgs &a, int idx, in
     return t;
 }
 
-template <bool kPrefix>
+template <bool kPrefix, bool kPlanned>
 __device__ __forceinline__ Unit unit_for(const PrefillArgs &a, int idx, int qblocks) {
     if constexpr (kPrefix) return unit_at_prefix(a, idx, qblocks);
+    else if constexpr (kPlanned) return unit_at(a, __ldg(a.order + idx), qblocks);
     else return unit_at(a, idx, qblocks);
+}
+
+// Key tiles of unit idx (the unit_at rule; 0 for a unit without work, which sorts last).
+__device__ __forceinline__ int plan_key(const PrefillArgs &a, int idx, int qblocks) {
+    const Unit t = unit_at(a, idx, qblocks);
+    return t.run ? t.n_kt : 0;
+}
+
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanMaxKeys = 12288;   // histogram buckets in shared memory (48 KiB)
+// key buckets: a unit visits at most 2 * max_blocks_per_seq key tiles
+inline int plan_keys(const PrefillArgs &a) { return 2 * a.max_blocks_per_seq + 2; }
+
+// Planning kernel for several sequences: a counting sort of the units by key tiles, most
+// first (longest processing time first), written as order[rank] = unit.  Units with equal
+// keys take their ranks in whatever order the atomics resolve; every unit is computed by
+// one CTA on its own, so the outputs do not depend on that order.  nk = key buckets.
+__global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const PrefillArgs a, int qblocks, int total,
+                                                                       int nk) {
+    __shared__ int hist[kPlanMaxKeys];
+    __shared__ int warp_sum[kPlanThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int k = tid; k < nk; k += kPlanThreads) hist[k] = 0;
+    __syncthreads();
+    for (int idx = tid; idx < total; idx += kPlanThreads)
+        atomicAdd(&hist[min(plan_key(a, idx, qblocks), nk - 1)], 1);
+    __syncthreads();
+    // hist[k] <- first rank of key k = number of units with more key tiles.  Thread t owns
+    // the keys hi, hi - 1, ..., hi - per + 1 counted from the top.
+    const int per = (nk + kPlanThreads - 1) / kPlanThreads;
+    const int hi = nk - 1 - tid * per;
+    int sum = 0;
+    for (int i = 0; i < per; ++i)
+        if (hi - i >= 0) sum += hist[hi - i];
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += n;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sum[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, w, d);
+            if (lane >= d) w += n;
+        }
+        warp_sum[lane] = w;   // inclusive over warps
+    }
+    __syncthreads();
+    int run = incl - sum + (warp > 0 ? warp_sum[warp - 1] : 0);
+    for (int i = 0; i < per; ++i) {
+        const int k = hi - i;
+        if (k >= 0) {
+            const int v = hist[k];
+            hist[k] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < total; idx += kPlanThreads) {
+        const int rank = atomicAdd(&hist[min(plan_key(a, idx, qblocks), nk - 1)], 1);
+        a.order[rank] = idx;
+    }
+    // Complete only after the kernel before this one on the stream (kv_append lets its
+    // dependents start early): the prefill launched after this kernel relies on it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Index of this CTA's r-th unit in the snake order (or -1 past the end).
@@ -179,7 +250,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     }
 }
 
-template <bool kPrefix>
+template <bool kPrefix, bool kPlanned>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                const __grid_constant__ CUtensorMap v_map, const PrefillArgs a) {
@@ -250,7 +321,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         for (int r = 0; ok; ++r) {
             const int idx = snake(r, total);
             if (idx < 0) break;
-            const Unit t = unit_for<kPrefix>(a, idx, qblocks);
+            const Unit t = unit_for<kPrefix, kPlanned>(a, idx, qblocks);
             if (qk && leader && t.error) record_error(a.err, kErrDevice | kErrQLen);
             if (!t.run) continue;
             if (qk) {
@@ -307,6 +378,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         // single-lane branch, the same stream competed for issue slots with the softmax
         // warps of its sub-partition and fed the tensor core at about half its rate.
         const bool leader = elect_one();
+        // The unit order is written by the planning kernel just before this one.
+        if constexpr (kPlanned) asm volatile("griddepcontrol.wait;" ::: "memory");
         // Matrix descriptors are built once; per MMA only a constant is added to the
         // start-address field (units of 16 bytes): +2 per 16 dims along a 128-byte row,
         // +1024 per 64-dim half (16 KiB), +2048 per tile or ring slot (32 KiB), +128 per
@@ -368,7 +441,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         for (int r = 0; ok; ++r) {
             const int idx = snake(r, total);
             if (idx < 0) break;
-            const Unit t = unit_for<kPrefix>(a, idx, qblocks);
+            const Unit t = unit_for<kPrefix, kPlanned>(a, idx, qblocks);
             if (!t.run) continue;
             if (!(ok = wait_all(&sm.q_full, tcount & 1))) break;
             for (int j = 0; j < t.n_kt; ++j, ++it) {
@@ -397,6 +470,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     } else {
         // ---------------------------------------------------------------- softmax warps
         // Warpgroup x (= warp / 4) owns query tile x; thread = one row = one TMEM lane.
+        if constexpr (kPlanned) asm volatile("griddepcontrol.wait;" ::: "memory");
         const int x = warp >> 2;
         const int row = (warp & 3) * 32 + lane;    // MMA row == TMEM lane
         const int pl = row >> 2;                   // query position within the tile
@@ -409,7 +483,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         for (int r = 0; ok; ++r) {
             const int idx = snake(r, total);
             if (idx < 0) break;
-            const Unit t = unit_for<kPrefix>(a, idx, qblocks);
+            const Unit t = unit_for<kPrefix, kPlanned>(a, idx, qblocks);
             if (!t.run) continue;
             // the last key each row may see: its own position (causal), or the whole prefix
             const int pos_first = kPrefix ? t.seq_len - 1 : t.pos0 + x * kTilePos;
@@ -590,16 +664,15 @@ __global__ void wait_selftest_kernel(uint32_t *err, uint64_t limit_ns) {
     if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, limit_ns)) record_error(err, kErrTimeout);
 }
 
-template <bool kPrefix>
+template <bool kPrefix, bool kPlanned>
 cudaError_t launch_prefill_mode(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
                                 const CUtensorMap &v_map, int num_sms, cudaStream_t stream) {
-    if (a.num_seqs == 0 || a.max_q_len == 0 || a.total_tokens == 0) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     static bool configured[64] = {};
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(prefill_kernel<kPrefix>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(prefill_kernel<kPrefix, kPlanned>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
@@ -609,29 +682,44 @@ cudaError_t launch_prefill_mode(const PrefillArgs &a, const CUtensorMap &q_map, 
     const int grid = (int)(units < num_sms ? units : num_sms);
     // Programmatic dependent launch: the producers wait (griddepcontrol.wait) before their
     // first load, so the launch and prologue may overlap the previous kernel on the stream.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<kPrefix>, q_map, k_map, v_map, a);
+    if constexpr (kPlanned) {
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(kPlanThreads);
+        cfg.dynamicSmemBytes = 0;
+        e = cudaLaunchKernelEx(&cfg, prefill_plan_kernel, a, (int)qblocks, (int)units, plan_keys(a));
+        if (e != cudaSuccess) return e;
+    }
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<kPrefix, kPlanned>, q_map, k_map, v_map, a);
 }
 
 }  // namespace
 
+long long prefill_plan_units(const PrefillArgs &a) {
+    if (a.num_seqs <= 1 || plan_keys(a) > kPlanMaxKeys) return 0;
+    return (long long)a.num_seqs * kHkv * ((a.max_q_len + kUnitPos - 1) / kUnitPos);
+}
+
 cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
                            const CUtensorMap &v_map, int num_sms, cudaStream_t stream) {
-    return launch_prefill_mode<false>(a, q_map, k_map, v_map, num_sms, stream);
+    if (a.num_seqs == 0 || a.max_q_len == 0 || a.total_tokens == 0) return cudaSuccess;
+    if (a.order) return launch_prefill_mode<false, true>(a, q_map, k_map, v_map, num_sms, stream);
+    return launch_prefill_mode<false, false>(a, q_map, k_map, v_map, num_sms, stream);
 }
 
 cudaError_t launch_prefill_prefix(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
                                   const CUtensorMap &v_map, int num_sms, cudaStream_t stream) {
-    return launch_prefill_mode<true>(a, q_map, k_map, v_map, num_sms, stream);
+    if (a.num_seqs == 0 || a.max_q_len == 0 || a.total_tokens == 0) return cudaSuccess;
+    return launch_prefill_mode<true, false>(a, q_map, k_map, v_map, num_sms, stream);
 }
 
 cudaError_t launch_wait_selftest(uint32_t *err, uint64_t limit_ns, cudaStream_t stream) {

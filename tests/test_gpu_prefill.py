@@ -143,3 +143,29 @@ def test_empty_sequences_are_skipped():
     out, _ = append_and_prefill(b)
     ref, _ = oracle_attention(b, kp, vp)
     assert_close(out, ref, "empty sequences")
+
+
+def test_work_plan_leaves_results_unchanged():
+    """Several sequences: the units are first sorted by work (a planning kernel writing into
+    the workspace).  A workspace holding only the error word leaves no room for that order,
+    so the units go in their natural order; both runs must agree bit for bit (each unit is
+    computed by one CTA on its own), and with the oracle."""
+    ctx_and_q = [(0, 300), (700, 64), (33, 1), (2000, 129), (0, 5), (511, 200)]
+    b = small_batch(ctx_and_q, seed=91)
+    kp, vp = oracle_appended_pools(b)
+    ws = workspace_for(b)
+    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    ops.check_error(ws)
+    runs = []
+    for w in (ws, torch.zeros(256, dtype=torch.uint8, device="cuda")):
+        lse = torch.empty(b.total_tokens, 32, dtype=torch.float32, device="cuda")
+        out = ops.paged_attn_prefill(b.q, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens,
+                                     b.max_q_len, w, lse=lse)
+        ops.check_error(w)
+        runs.append((out, lse))
+    (o1, l1), (o2, l2) = runs
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+    ref, ref_lse = oracle_attention(b, kp, vp)
+    assert_close(o1, ref, "planned prefill")
+    assert_lse_close(l1, ref_lse, "planned prefill")
