@@ -109,15 +109,22 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // The first block id of this split does not depend on the context length: the
-    // producer fetches it (and the tensor maps) while everyone fetches seq_len, so the
-    // first tile load is one memory round trip closer to the kernel's start.
+    // A sequence's n context tokens are cut into nsplit_b = ceil(n / split_tokens) splits
+    // of equal length (rounded up to the tile), so the CTAs of one wave end at different
+    // times and no split is a small remainder.  Each split starts at or after
+    // split * split_tokens / 2 (for nsplit_b >= 2 the length exceeds split_tokens / 2):
+    // the producer warp fetches the 32 block-table entries from there on (and the tensor
+    // maps) while everyone fetches seq_len, so the first tile load is usually one memory
+    // round trip from the kernel's start.
     const int32_t *bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
-    int blk0 = 0;
-    if (warp == kConsumerWarps && lane == 0) {
-        tma_prefetch_map(&k_map);
-        tma_prefetch_map(&v_map);
-        blk0 = __ldg(bt + (a.kv_begin + split * a.split_tokens) / kBlock);   // < max_blocks_per_seq
+    const int wlo = (a.kv_begin + split * (a.split_tokens >> 1)) / kBlock;
+    int bwin = 0;
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            tma_prefetch_map(&k_map);
+            tma_prefetch_map(&v_map);
+        }
+        if (wlo + lane < a.max_blocks_per_seq) bwin = __ldg(bt + wlo + lane);
     }
     const int seq_len = __ldg(a.seq_lens + b);
     // (a cascade attends only past the shared prefix: the context must extend beyond it)
@@ -125,10 +132,12 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         if (split == 0 && g == 0 && threadIdx.x == 0) record_error(a.err, kErrDevice | kErrBadSeqLen);
         return;  // every CTA of this sequence takes the same exit: counters untouched
     }
-    const int t_begin = a.kv_begin + split * a.split_tokens;
-    if (t_begin >= seq_len) return;       // this split lies past the context
-    const int t_end = min(t_begin + a.split_tokens, seq_len);
-    const int nsplit_b = (seq_len - a.kv_begin + a.split_tokens - 1) / a.split_tokens;
+    const int n_ctx = seq_len - a.kv_begin;
+    const int nsplit_b = (n_ctx + a.split_tokens - 1) / a.split_tokens;
+    if (split >= nsplit_b) return;        // this split lies past the context
+    const int len_b = ((n_ctx + nsplit_b - 1) / nsplit_b + kTile - 1) / kTile * kTile;
+    const int t_begin = a.kv_begin + split * len_b;
+    const int t_end = min(t_begin + len_b, seq_len);
     const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
 
     if (threadIdx.x == 0) {
@@ -144,6 +153,9 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ TMA producer
+        const int wi = t_begin / kBlock - wlo;   // >= 0; beyond the window: fetch it now
+        int blk0 = __shfl_sync(0xffffffffu, bwin, wi & 31);
+        if (wi < 0 || wi >= 32) blk0 = __ldg(bt + t_begin / kBlock);
         if (lane == 0) {
             // The pools may be written by the kernel just before this one on the stream
             // (kv_append lets us launch early): wait for it before the first pool read.
@@ -398,32 +410,52 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         a.part_ml[(entry * kGroup + h) * 2 + 0] = M;
         a.part_ml[(entry * kGroup + h) * 2 + 1] = L;
     }
-    __threadfence();
+    // Count this split in with one release/acquire atomic: the barrier orders every
+    // thread's partial stores before thread 0's release, and the acquire of the CTA that
+    // counts last (then the barrier) orders its loads of the others' partials after them.
     named_barrier(1, kConsumerWarps * 32);
     if (c == 0) {
-        const int prev = atomicAdd(a.counters + pair, 1);
+        int prev;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(a.counters + pair) : "memory");
         sm.last_cta = (prev == nsplit_b - 1);
     }
     named_barrier(1, kConsumerWarps * 32);
     if (!sm.last_cta) return;
 
-    // The last CTA of this (sequence, KV head) merges every split by log-sum-exp.
-    __threadfence();
+    // The last CTA of this (sequence, KV head) merges every split by log-sum-exp, in split
+    // order whichever CTA it is (its own split from registers: the same values), with the
+    // loads of four splits issued together.
     if (c == 0) a.counters[pair] = 0;   // ready for the next call
     const size_t e0 = (size_t)pair * a.nsplit;
-    float GM = -INFINITY;
-    for (int k = 0; k < nsplit_b; ++k) GM = fmaxf(GM, __ldcg(a.part_ml + ((e0 + k) * kGroup + h) * 2));
-    float GL = 0.f, go[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k = 0; k < nsplit_b; ++k) {
-        const float mk = __ldcg(a.part_ml + ((e0 + k) * kGroup + h) * 2);
-        const float lk = __ldcg(a.part_ml + ((e0 + k) * kGroup + h) * 2 + 1);
-        const float e = fast_exp2(mk - GM);
-        const float4 ok = __ldcg(reinterpret_cast<const float4 *>(a.part_o + ((e0 + k) * kGroup + h) * kD + d0));
-        GL += lk * e;
-        go[0] += ok.x * e;
-        go[1] += ok.y * e;
-        go[2] += ok.z * e;
-        go[3] += ok.w * e;
+    float GM = -INFINITY, GL = 0.f, go[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < nsplit_b; k0 += 4) {
+        float mk[4], lk[4];
+        float4 ok[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int k = k0 + u;
+            if (k == split) {
+                mk[u] = M;
+                lk[u] = L;
+                ok[u] = make_float4(o4[0], o4[1], o4[2], o4[3]);
+            } else if (k < nsplit_b) {
+                mk[u] = __ldcg(a.part_ml + ((e0 + k) * kGroup + h) * 2);
+                lk[u] = __ldcg(a.part_ml + ((e0 + k) * kGroup + h) * 2 + 1);
+                ok[u] = __ldcg(reinterpret_cast<const float4 *>(a.part_o + ((e0 + k) * kGroup + h) * kD + d0));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (k0 + u >= nsplit_b) break;
+            const float mn = fmaxf(GM, mk[u]);
+            const float e_old = fast_exp2(GM - mn), e_k = fast_exp2(mk[u] - mn);
+            GL = GL * e_old + lk[u] * e_k;
+            go[0] = go[0] * e_old + ok[u].x * e_k;
+            go[1] = go[1] * e_old + ok[u].y * e_k;
+            go[2] = go[2] * e_old + ok[u].z * e_k;
+            go[3] = go[3] * e_old + ok[u].w * e_k;
+            GM = mn;
+        }
     }
     if (a.pre_n > 0) {
         fold_prefix(a, b, qh, d0, GM, GL, go);
