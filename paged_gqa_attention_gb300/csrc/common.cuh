@@ -277,6 +277,13 @@ __device__ __forceinline__ float add_bf16_hi(uint32_t v, float c) {
     return d;
 }
 
+// Approximate reciprocal (rcp.approx, subnormal inputs kept).
+__device__ __forceinline__ float fast_rcp(float x) {
+    float y;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

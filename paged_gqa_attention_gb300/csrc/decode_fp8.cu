@@ -184,6 +184,7 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_consta
     float m0 = -INFINITY, m1 = -INFINITY;   // running max (log2 units) of heads 2tq, 2tq+1
     float l0 = 0.f, l1 = 0.f;               // this thread's share of the running sums
     float sigma = 0.f;                      // reference V scale of the accumulator
+    float inv_sigma = 0.f;                  // its reciprocal
     float acc[8][4];                        // O^T tiles, in units of sigma
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
@@ -293,8 +294,11 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_consta
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
             }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float alpha0 = fast_exp2(m0 - mn0), alpha1 = fast_exp2(m1 - mn1);
+            // lazy rescaling: the running max moves only when the tile's max exceeds it by
+            // more than 2^8 (weights stay <= 2^8, far inside f16), so most tiles rescale nothing
+            const bool up0 = mx0 > m0 + 8.f, up1 = mx1 > m1 + 8.f;   // also when m == -inf
+            const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
+            const float alpha0 = up0 ? fast_exp2(m0 - mn0) : 1.f, alpha1 = up1 ? fast_exp2(m1 - mn1) : 1.f;
             m0 = mn0;
             m1 = mn1;
             const float p0 = fast_exp2(x0 - m0), p1 = fast_exp2(x1 - m1);
@@ -303,26 +307,36 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_consta
             l1 = l1 * alpha1 + p1 + p3;
 
             // V scales of this warp's tokens (0 past the context end: scale slots there
-            // may hold anything) and the accumulator's reference scale
+            // may hold anything) and their maximum
             const float sv_lo = v_lo_ok ? vsc[gq] : 0.f;
             const float sv_hi = v_hi_ok ? vsc[gq + 8] : 0.f;
             float svm = fmaxf(sv_lo, sv_hi);
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, o));
-            const float sigma_new = fmaxf(sigma, svm) > 0.f ? fmaxf(sigma, svm) : 1.f;
-            const float grow = sigma / sigma_new;          // 0 on the first tile (acc is 0)
-            const float inv = 1.f / sigma_new;
-            sigma = sigma_new;
-            const float r_lo = sv_lo * inv, r_hi = sv_hi * inv;
+            // the accumulator's reference V scale grows with the largest scale seen; its
+            // reciprocal is recomputed only then (an approximate reciprocal: the factor it
+            // introduces is undone exactly by the same values in grow and the final sigma)
+            // (floored at 2^-100 so that the reciprocal stays finite: a V row whose scale is
+            // below it contributes less than the output's bf16 resolution near zero)
+            float grow = 1.f;
+            const float svr = fmaxf(svm, 0x1p-100f);
+            if (svr > sigma) {
+                inv_sigma = fast_rcp(svr);
+                grow = sigma * inv_sigma;                  // 0 on the first tile (acc is 0)
+                sigma = svr;
+            }
+            const float r_lo = sv_lo * inv_sigma, r_hi = sv_hi * inv_sigma;
             const uint32_t pp_lo = pack_f16x2(p0 * r_lo, p1 * r_lo);   // token gq:   heads 2tq, 2tq+1
             const uint32_t pp_hi = pack_f16x2(p2 * r_hi, p3 * r_hi);   // token gq+8: heads 2tq, 2tq+1
             const float f0 = alpha0 * grow, f1 = alpha1 * grow;
+            if (__any_sync(0xffffffffu, f0 != 1.f || f1 != 1.f)) {
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                acc[mt][0] *= f0;
-                acc[mt][1] *= f1;
-                acc[mt][2] *= f0;
-                acc[mt][3] *= f1;
+                for (int mt = 0; mt < 8; ++mt) {
+                    acc[mt][0] *= f0;
+                    acc[mt][1] *= f1;
+                    acc[mt][2] *= f0;
+                    acc[mt][3] *= f1;
+                }
             }
             // P^T as the B operand of O^T += V^T P^T: transpose the 8x8 16-bit blocks.
             const uint32_t pb0 = movmatrix_trans(pp_lo);
