@@ -1,0 +1,31 @@
+"""bench.py's command line on the CPU: it parses, lists every workload and keeps the
+per-launch traffic table consistent with the sources it was measured on."""
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+WORKLOADS = ["single_decode", "batched_decode", "causal_prefill", "mixed_batch", "prefix_shared_decode",
+             "layered_decode", "batched_decode_fp8", "prefix_shared_decode_cascade"]
+
+
+def test_help_lists_every_workload():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--help"], capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0, r.stderr
+    for w in WORKLOADS:
+        assert w in r.stdout
+
+
+def test_traffic_entries_name_existing_sources():
+    for name, entry in bench.TRAFFIC.items():
+        assert entry["bytes_per_launch"] > 0
+        for src in entry["sources"]:
+            assert os.path.exists(os.path.join(ROOT, "paged_gqa_attention_gb300", "csrc", src)), (name, src)
+        # a stale entry reports null rather than a number taken on other sources
+        fresh = bench.source_hash(*entry["sources"]) == entry["sha"]
+        assert (bench.traffic_for(name) is not None) == fresh
