@@ -59,6 +59,9 @@ TRAFFIC = {
     # one ncu capture of the causal prefill of 4096 tokens
     "prefill": {"bytes_per_launch": 50676480 + 1682944, "sources": ("prefill.cu", "common.cuh"),
                 "sha": "b0aea3dbb3034acb"},
+    # one ncu capture of the merged Q/K/V projection of 4096 tokens (hidden 4096)
+    "qkv": {"bytes_per_launch": 136257792 + 34989312, "sources": ("qkv.cu", "common.cuh"),
+            "sha": "a31217bec3438add"},
 }
 
 
@@ -70,7 +73,7 @@ def parse_args():
     p.add_argument("--workload", default="batched_decode",
                    choices=["single_decode", "batched_decode", "causal_prefill", "mixed_batch",
                             "prefix_shared_decode", "layered_decode", "batched_decode_fp8",
-                            "prefix_shared_decode_cascade"])
+                            "prefix_shared_decode_cascade", "qkv_append"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -707,6 +710,95 @@ def cpu_baseline(batch, kind, target_s, rows_cap=None):
                       f"{dt:.1f} s, fp64 C oracle with OpenMP"}
 
 
+# ------------------------------------------------------------------ merged Q/K/V projection
+
+QKV_HIDDEN = 4096                  # Qwen3-8B's hidden size
+
+
+def qkv_inputs(tokens, seed, device="cuda"):
+    """Synthetic x [tokens, 4096] ~ N(0, 1) and stacked weights [6144, 4096] ~ N(0, 1/4096), bf16."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn(tokens, QKV_HIDDEN, generator=g, device=device).to(torch.bfloat16)
+    w = (torch.randn(6144, QKV_HIDDEN, generator=g, device=device) / 64).to(torch.bfloat16)
+    return x, w
+
+
+def qkv_measure(batch, x, w, steps, warmup, flush_buf, stream, clocks):
+    """One paged_qkv_append call (one kernel): q of every new token out, k and v into the cache."""
+    import torch
+
+    from paged_gqa_attention_gb300 import ops
+
+    ws = ops.make_workspace(batch.num_seqs, batch.max_blocks_per_seq)
+    q = torch.empty(x.shape[0], 32, 128, dtype=torch.bfloat16, device="cuda")
+
+    def step(tm):
+        if tm: tm.record(0)
+        ops.paged_qkv_append(x, w, batch.k_pool, batch.v_pool, batch.block_table, batch.cu_q_lens,
+                             batch.seq_lens, ws, q_out=q)
+        if tm: tm.record(1)
+
+    spans, wall = run_timed(step, 2, steps, warmup, flush_buf, stream, clocks)
+    ops.check_error(ws)
+    return {"step_ms": mean([sp[0] for sp in spans]), "wall_s": wall, "launches": steps}
+
+
+def e2e_qkv_measure(batch, x, w, steps, warmup, stream):
+    """End to end through the public call: x copied from pinned host memory, the projection,
+    q copied back to pinned host memory, all inside the timed region (w stays resident, as a
+    layer's weights do)."""
+    import torch
+
+    from paged_gqa_attention_gb300 import ops
+
+    ws = ops.make_workspace(batch.num_seqs, batch.max_blocks_per_seq)
+    x_host = x.cpu().pin_memory()
+    q_host = torch.empty(x.shape[0], 32, 128, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    q_dev = torch.empty(x.shape[0], 32, 128, dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        x_dev.copy_(x_host, non_blocking=True)
+        ops.paged_qkv_append(x_dev, w, batch.k_pool, batch.v_pool, batch.block_table, batch.cu_q_lens,
+                             batch.seq_lens, ws, q_out=q_dev)
+        q_host.copy_(q_dev, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ops.check_error(ws)
+    return {"step_ms": e0.elapsed_time(e1) / steps, "h2d": x_host.numel() * 2, "d2h": q_host.numel() * 2}
+
+
+def cpu_baseline_qkv(tokens, target_s):
+    """The oracle's fp64 projection on the host cores over sampled token rows of the workload."""
+    import oracle
+
+    x, w = qkv_inputs(tokens, 7, device="cpu")
+    rows = list(range(0, tokens, max(1, tokens // 16)))[:16]
+    reps = 0
+    t0 = time.time()
+    while True:
+        oracle.qkv_project(x, w, rows=rows)
+        reps += 1
+        if time.time() - t0 >= target_s:
+            break
+    dt = time.time() - t0
+    return {"value": 2.0 * len(rows) * QKV_HIDDEN * 6144 * reps / dt / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} token rows x 6144 outputs x {QKV_HIDDEN}, {reps} pass(es), {dt:.1f} s, "
+                      f"fp64 C oracle with OpenMP"}
+
+
 # ------------------------------------------------------------------ main paths
 
 def reference_arm(args, world, rank):
@@ -729,6 +821,18 @@ def reference_arm(args, world, rank):
                           "cpu_baseline": {"value": value, "unit": "GB/s", "cores": res[0]["cores"],
                                            "kind": "oracle", "sample": res[0]["sample"]},
                           "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    if args.workload == "qkv_append":
+        res = [cpu_baseline_qkv(4096, max(args.cpu_seconds / max(args.steps, 1), 0.05)) for _ in range(args.steps)]
+        value = mean([r["value"] for r in res])
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": {"workload": args.workload},
+                          "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res[0]["cores"],
+                                           "kind": "oracle", "sample": res[0]["sample"]},
+                          "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                                   "d2h_bytes_per_step": 0}}), flush=True)
         return
     if args.workload == "layered_decode":
@@ -805,6 +909,8 @@ def main():
         batch = wl.batched_decode(device="cuda")
     elif wname == "prefix_shared_decode_cascade":
         batch = wl.prefix_shared_decode(device="cuda")
+    elif wname == "qkv_append":
+        batch = wl.causal_prefill(device="cuda")      # the 4096-token prompt's new tokens
     else:
         batch = wl.WORKLOADS[wname](device="cuda")
     dist_barrier(world)
@@ -916,6 +1022,32 @@ def main():
         cfg["kv_cache"] = "8-bit: E4M3 codes + one fp32 scale per token and KV head"
         line["dtype"] = "f16 products over e4m3 codes"
         kind = "decode_fp8"
+    elif wname == "qkv_append":
+        x, w = qkv_inputs(batch.total_tokens, 7)
+        r = qkv_measure(batch, x, w, args.steps, args.warmup, flush_buf, stream, clocks)
+        flops = 2.0 * batch.total_tokens * QKV_HIDDEN * 6144
+        step_ms = dist_max(r["step_ms"], world)
+        line.update(value=world * flops / (step_ms * 1e-3) / 1e12, unit="TFLOP/s", ms_per_step=step_ms)
+        line["roofline"] = roofline(flops / (step_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s", "tensor",
+                                    traffic_for("qkv"))
+        line["roofline"]["kernel"] = "qkv_kernel"
+        line["roofline"]["algorithmic_flops_per_launch"] = flops
+        # the same call for a decode step's batch: 32 new tokens, the weights dominate the bytes
+        db = wl.batched_decode(device="cuda")
+        dx, _ = qkv_inputs(db.total_tokens, 8)
+        dr = qkv_measure(db, dx, w, max(20, min(args.steps, 200)), args.warmup, flush_buf, stream, None)
+        wbytes = 6144 * QKV_HIDDEN * 2 + db.total_tokens * (QKV_HIDDEN + 6144) * 2
+        line["kernels"] = {"qkv_us": r["step_ms"] * 1e3, "tokens": batch.total_tokens, "hidden": QKV_HIDDEN,
+                           "decode_batch": {"tokens": db.total_tokens, "qkv_us": dr["step_ms"] * 1e3,
+                                            "bytes": wbytes, "gbs": wbytes / (dr["step_ms"] * 1e-3) / 1e9,
+                                            "hbm_frac": wbytes / (dr["step_ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
+        line["gpu_launches"] = r["launches"] + dr["launches"]
+        e = e2e_qkv_measure(batch, x, w, max(10, min(args.steps, 50)), 3, stream)
+        e_ms = dist_max(e["step_ms"], world)
+        line["e2e"] = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"], "ms_per_step": e_ms}
+        cfg["projection"] = "x [4096, 4096] @ w_qkv [6144, 4096]^T; q out, k and v into their cache slots"
+        kind = "qkv"
     elif wname == "causal_prefill":
         r = prefill_measure(batch, args.steps, args.warmup, flush_buf, stream, clocks)
         flops = batch.attention_flops()
@@ -985,6 +1117,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         if kind == "decode_fp8":
             line["cpu_baseline"] = cpu_baseline_fp8(wl.batched_decode(device="cuda"), args.cpu_seconds)
+        elif kind == "qkv":
+            line["cpu_baseline"] = cpu_baseline_qkv(batch.total_tokens, args.cpu_seconds)
         else:
             src = (batch if wname in ("layered_decode", "prefix_shared_decode_cascade", batch.name)
                    else wl.WORKLOADS[wname](device="cuda"))

@@ -17,7 +17,9 @@
  *   paged_attn_prefill  causal attention of a chunk of new tokens over the earlier
  *                       context plus itself [P1 §4.4.1 flash_attn_prefill; P3 §3.3
  *                       chunked prefill]
- * All three compute softmax(Q K^T * scale) V [P2 §2.2] with the causal rule "a
+ * and, before them, paged_qkv_append computes the new tokens' q, k and v in one merged
+ * projection [P1 §4.4.3 QKV fusion] with k and v written straight into the cache.
+ * The attention calls compute softmax(Q K^T * scale) V [P2 §2.2] with the causal rule "a
  * position sees itself and earlier positions" [P2 §2.2]; the caller appends before
  * attending, so a context length always counts the new tokens [P3 §4.2].
  *
@@ -126,6 +128,31 @@ pa_status kv_append(pa_shape shape, void *k_pool, void *v_pool,
                     const int32_t *cu_q_lens, const int32_t *seq_lens, int32_t num_seqs,
                     int32_t total_tokens, void *workspace, size_t workspace_bytes,
                     void *stream);
+
+/*
+ * paged_qkv_append: the merged Q/K/V projection of the new tokens [P1 §4.4.3 QKV fusion:
+ * one matrix product with the three weights stacked, output sliced into q, k, v], with
+ * k and v written straight into their cache slots by the kv_append rule above (no
+ * round trip of K/V through memory).  For token t (row t of x):
+ *   y[n] = sum_k x[t][k] * w_qkv[n][k],  n = 0 .. 6143, fp32 accumulation, bf16 result;
+ *   columns 0..4095 -> q_out[t][n / 128][n % 128];
+ *   columns 4096..5119 -> K of KV head (n - 4096) / 128, dim n % 128, at the token's
+ *   cache slot; columns 5120..6143 -> V likewise [P1 §4.4.2: 8 KV heads].
+ * No rotary position embedding or per-head normalisation is applied (the pages define
+ * neither); a caller that needs them applies them to q_out and the cache rows itself.
+ *   x [total_tokens][hidden] bf16, hidden a multiple of 256 (4096 for Qwen3-8B);
+ *   w_qkv [6144][hidden] bf16: rows 0-4095 the q weight, 4096-5119 k, 5120-6143 v, each
+ *   [out][in] as a linear layer stores it; q_out [total_tokens][32][128] bf16.
+ * Pools, block_table, cu_q_lens, seq_lens and the workspace as for kv_append; a token
+ * whose sequence data are inconsistent or whose block id is outside the pool gets no
+ * K/V write and records PA_ERR_DEVICE (its q row is still written).
+ */
+pa_status paged_qkv_append(pa_shape shape, int32_t hidden, void *q_out, const void *x,
+                           const void *w_qkv, void *k_pool, void *v_pool,
+                           const int32_t *block_table, int32_t max_blocks_per_seq,
+                           int32_t num_blocks, const int32_t *cu_q_lens,
+                           const int32_t *seq_lens, int32_t num_seqs, int32_t total_tokens,
+                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * paged_attn_decode: one query token per sequence [P1 §4.4.2].

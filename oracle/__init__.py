@@ -10,8 +10,11 @@ GPU sees and return float64 results.  The 8-bit KV cache (E4M3 codes, one fp32 s
 (token, KV head) row) has its own append and attention: ``kv_append_fp8``,
 ``attention_fp8``, with the codec ``e4m3_encode`` / ``e4m3_decode``.
 
+The merged Q/K/V projection (page 1 §4.4.3) is ``qkv_project``; ``qkv_append`` adds the
+append of its k and v (rounded once to bf16 by ``bf16_round``) to the cache.
+
 Parity status: every function here is pinned by the CPU tests in
-``tests/test_oracle_pins.py`` and ``tests/test_oracle_fp8.py`` (closed forms, library
+``tests/test_oracle_pins.py``, ``tests/test_oracle_fp8.py`` and ``tests/test_oracle_qkv.py`` (closed forms, library
 routines on tiny cases -- torch SDPA, torch's float8_e4m3fn -- invariants, the format's
 error bound and a high-precision brute force).
 """
@@ -71,6 +74,10 @@ def load_library(path: str):
     lib.oracle_paged_attention_fp8.argtypes = [f64p, f64p, u16p, u8p, u8p, f32p, f32p, i32p, ci, ci,
                                                i32p, i32p, ci, ci, ci, ci, ci, ctypes.c_double, ci]
     lib.oracle_paged_attention_fp8.restype = ci
+    lib.oracle_qkv_project.argtypes = [f64p, u16p, u16p, i32p, ci, ci, ci, ci, ci]
+    lib.oracle_qkv_project.restype = ci
+    lib.oracle_bf16_round.argtypes = [f64p, u16p, ctypes.c_long]
+    lib.oracle_bf16_round.restype = None
     return lib
 
 
@@ -247,3 +254,52 @@ def attention_fp8(q, k_codes, v_codes, k_scale, v_scale, block_table, cu_q_lens,
         if rc:
             raise ValueError(f"oracle attention_fp8 rejected its input (code {rc})")
     return out, lse
+
+
+Q_COLS, KV_COLS = 32 * 128, 8 * 128   # q: 32 heads, k and v: 8 KV heads, 128 dims each
+
+
+def qkv_project(x, w, *, rows=None, num_threads: int = 0, lib=None) -> np.ndarray:
+    """The merged projection y = x w^T in fp64 (page 1 §4.4.3 QKV fusion).
+
+    x: [tokens, hidden] bf16; w: [n_out, hidden] bf16 (a linear layer's weight).  Returns
+    y [len(rows) or tokens, n_out] float64 for the listed token rows (default: all).
+    """
+    xb, wb = _bits(x), _bits(w)
+    tokens, hidden = xb.shape
+    n_out, hw = wb.shape
+    assert hw == hidden
+    r = None if rows is None else _i32(np.asarray(rows))
+    n_rows = tokens if r is None else len(r)
+    y = np.zeros((n_rows, n_out), dtype=np.float64)
+    lib = lib or _load()
+    rc = lib.oracle_qkv_project(_p(y, ctypes.c_double), _p(xb, ctypes.c_uint16), _p(wb, ctypes.c_uint16),
+                                None if r is None else _p(r, ctypes.c_int32), n_rows, tokens, hidden, n_out,
+                                num_threads)
+    if rc:
+        raise ValueError(f"oracle_qkv_project rejected its input (code {rc})")
+    return y
+
+
+def bf16_round(v, *, lib=None) -> np.ndarray:
+    """float64 values -> bf16 bit patterns (uint16), round to nearest, ties to even."""
+    a = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
+    out = np.zeros(a.shape, dtype=np.uint16)
+    (lib or _load()).oracle_bf16_round(_p(a, ctypes.c_double), _p(out, ctypes.c_uint16), a.size)
+    return out
+
+
+def qkv_append(x, w, k_pool, v_pool, block_table, cu_q_lens, seq_lens, *, num_threads: int = 0, lib=None):
+    """The merged projection of every new token with its k and v appended to the cache.
+
+    Returns (q [tokens, 32, 128] float64, k_pool', v_pool' uint16): q is exact; the cache
+    holds k and v rounded once to bf16 (its format), placed by ``kv_append``'s rule.
+    """
+    y = qkv_project(x, w, num_threads=num_threads, lib=lib)
+    t = y.shape[0]
+    assert y.shape[1] == Q_COLS + 2 * KV_COLS
+    q = y[:, :Q_COLS].reshape(t, 32, 128)
+    k_new = bf16_round(y[:, Q_COLS:Q_COLS + KV_COLS], lib=lib).reshape(t, 8, 128)
+    v_new = bf16_round(y[:, Q_COLS + KV_COLS:], lib=lib).reshape(t, 8, 128)
+    kp, vp = kv_append(k_pool, v_pool, k_new, v_new, block_table, cu_q_lens, seq_lens, lib=lib)
+    return q, kp, vp

@@ -42,6 +42,11 @@
  *   k_codes  [num_blocks][block_size][Hkv][D]      uint8, v_codes likewise
  *   k_scale  [num_blocks][Hkv][block_size]         float, v_scale likewise
  *
+ * The merged Q/K/V projection (its definition is given at oracle_qkv_project below):
+ *   x        [tokens][hidden]                      bf16 bit patterns
+ *   w        [n_out][hidden]                       bf16 bit patterns (a linear layer's weight)
+ *   y        [tokens][n_out]                       double
+ *
  * Functions return 0 on success and a negative code on inconsistent input.
  */
 #include <math.h>
@@ -433,6 +438,66 @@ int oracle_paged_attention_fp8(double *out, double *lse,
     kv_cache c = {NULL, NULL, k_codes, v_codes, k_scale, v_scale, num_kv_heads, head_dim, block_size};
     return attention_all(out, lse, q, &c, block_table, max_blocks_per_seq, num_blocks, cu_q_lens,
                          seq_lens, num_seqs, num_q_heads, scale, num_threads);
+}
+
+/*
+ * The merged Q/K/V projection [P1 §4.4.3 QKV fusion]: the q, k and v weights stacked
+ * into one matrix, one product, the output sliced by columns.  For each listed token
+ * row t (rows[r], or r itself when rows is NULL) and output column n:
+ *     y[r][n] = sum_k x[t][k] * w[n][k]
+ * in double precision on the exact bf16 values, summed in order of k.
+ */
+int oracle_qkv_project(double *y, const uint16_t *x, const uint16_t *w, const int32_t *rows, int n_rows,
+                       int tokens, int hidden, int n_out, int num_threads)
+{
+    if (n_rows < 0 || tokens < 0 || hidden < 1 || n_out < 1) return -1;
+    for (int r = 0; r < n_rows; ++r)
+        if (rows && (rows[r] < 0 || rows[r] >= tokens)) return -2;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (long rn = 0; rn < (long)n_rows * n_out; ++rn) {
+        const int r = (int)(rn / n_out), n = (int)(rn % n_out);
+        const int t = rows ? rows[r] : r;
+        double acc = 0.0;
+        for (int k = 0; k < hidden; ++k)
+            acc += bf16_to_double(x[(size_t)t * hidden + k]) * bf16_to_double(w[(size_t)n * hidden + k]);
+        y[(size_t)r * n_out + n] = acc;
+    }
+    return 0;
+}
+
+/*
+ * Round doubles to the nearest bf16 (ties to even), as bit patterns: a result that
+ * fits the bf16 grid exactly, with the format's subnormals and overflow to infinity.
+ * bf16 keeps 8 significant bits; a value in [2^e, 2^(e+1)) with e >= -126 is a
+ * multiple of 2^(e-7), below 2^-126 a multiple of 2^-133.
+ */
+void oracle_bf16_round(const double *v, uint16_t *out, long n)
+{
+    for (long i = 0; i < n; ++i) {
+        const double x = v[i];
+        if (isnan(x)) { out[i] = 0x7FC0; continue; }
+        const uint16_t sign = signbit(x) ? 0x8000 : 0;
+        const double a = fabs(x);
+        if (a == 0.0) { out[i] = sign; continue; }
+        int e;
+        frexp(a, &e);              /* a = m * 2^e, m in [0.5, 1): a in [2^(e-1), 2^e) */
+        int lo = e - 1;
+        if (lo < -126) lo = -126;
+        const double quantum = ldexp(1.0, lo - 7);
+        double m = floor(a / quantum);   /* a / quantum is exact: a power-of-two scaling */
+        const double frac = a / quantum - m;
+        if (frac > 0.5 || (frac == 0.5 && fmod(m, 2.0) != 0.0)) m += 1.0;
+        const double r = m * quantum;
+        if (r >= 0x1p128) { out[i] = sign | 0x7F80; continue; }   /* beyond the largest finite */
+        /* r is on the bf16 grid, hence exactly a float whose low 16 bits are zero */
+        const float f = (float)r;
+        uint32_t bits;
+        memcpy(&bits, &f, sizeof bits);
+        out[i] = sign | (uint16_t)(bits >> 16);
+    }
 }
 
 /* Threads the OpenMP runtime would use (1 without OpenMP). */

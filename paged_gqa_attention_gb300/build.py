@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libpagedattn.so")
-SOURCES = ["api.cu", "kv_append.cu", "decode.cu", "decode_fp8.cu", "prefill.cu"]
+SOURCES = ["api.cu", "kv_append.cu", "decode.cu", "decode_fp8.cu", "prefill.cu", "qkv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

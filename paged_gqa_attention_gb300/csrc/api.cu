@@ -84,6 +84,18 @@ bool encode_q_map(CUtensorMap *map, const void *q, int tokens) {
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A row-major bf16 matrix [rows][cols] as a 2-D tensor (col, row), box {64, box_rows},
+// 128-byte swizzle (cols a multiple of 8 so that the row stride is 16-byte aligned).
+bool encode_matrix_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ device facts
 std::atomic<int> g_sms[64];
 
@@ -336,6 +348,46 @@ pa_status kv_append(pa_shape shape, void *k_pool, void *v_pool, const void *k_ne
     a.total_tokens = total_tokens;
     a.err = static_cast<uint32_t *>(workspace);
     return launch_kv_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status paged_qkv_append(pa_shape shape, int32_t hidden, void *q_out, const void *x, const void *w_qkv,
+                           void *k_pool, void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
+                           int32_t num_blocks, const int32_t *cu_q_lens, const int32_t *seq_lens, int32_t num_seqs,
+                           int32_t total_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
+    if (hidden < 256 || hidden % 256 != 0 || hidden > (1 << 16)) return PA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+        (num_seqs == 0 && total_tokens != 0))
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kHeaderBytes || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
+    if (total_tokens == 0) return PA_OK;
+    if (!q_out || !x || !w_qkv || !k_pool || !v_pool || !block_table || !cu_q_lens || !seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(q_out) || !aligned16(x) || !aligned16(w_qkv) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned4(block_table) || !aligned4(cu_q_lens) || !aligned4(seq_lens))
+        return PA_ERR_INVALID_ARG;
+    if ((long long)max_blocks_per_seq * kBlock > (1ll << 30)) return PA_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms <= 0) return PA_ERR_CUDA;
+    if (!get_encoder()) return PA_ERR_CUDA;
+    CUtensorMap x_map, w_map;
+    if (!encode_matrix_map(&x_map, x, total_tokens, hidden, qkv_tile_rows_loaded(total_tokens)) ||
+        !encode_matrix_map(&w_map, w_qkv, kHq * kD + 2 * kHkv * kD, hidden, qkv_tile_cols(total_tokens)))
+        return PA_ERR_INVALID_ARG;
+    QkvArgs a = {};
+    a.q_out = q_out;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.block_table = block_table;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.cu_q_lens = cu_q_lens;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.total_tokens = total_tokens;
+    a.hidden = hidden;
+    a.err = static_cast<uint32_t *>(workspace);
+    return launch_qkv(a, x_map, w_map, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status kv_append_fp8(pa_shape shape, void *k_codes, void *v_codes, float *k_scale, float *v_scale,

@@ -87,7 +87,30 @@ struct PrefillArgs {
     int32_t *order;
 };
 
+// Merged Q/K/V projection with K and V written into the cache (qkv.cu).
+struct QkvArgs {
+    void *q_out;            // [total_tokens][32][128] bf16
+    void *k_pool;           // [num_blocks][256][8][128] bf16
+    void *v_pool;
+    const int32_t *block_table;
+    int32_t max_blocks_per_seq;
+    int32_t num_blocks;
+    const int32_t *cu_q_lens;
+    const int32_t *seq_lens;
+    int32_t num_seqs;
+    int32_t total_tokens;
+    int32_t hidden;         // a multiple of 256
+    uint32_t *err;
+};
+
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
+
+// x_map: x [total_tokens][hidden] bf16, box {64, qkv_tile_rows_loaded(total_tokens)}; w_map:
+// w [6144][hidden] bf16, box {64, qkv_tile_cols(total_tokens)}; both 128-byte swizzle.
+int qkv_tile_cols(int total_tokens);
+int qkv_tile_rows_loaded(int total_tokens);
+cudaError_t launch_qkv(const QkvArgs &a, const CUtensorMap &x_map, const CUtensorMap &w_map, int num_sms,
+                       cudaStream_t stream);
 
 // k_map / v_map: 4-D tensor maps over the pools (see api.cu for the boxes).
 // One-time per-device kernel setup (dynamic shared memory size) of the decode kernel;

@@ -1,0 +1,355 @@
+// qkv.cu -- the merged Q/K/V projection of a batch of new tokens, with K and V written
+// straight into their slots of the paged cache.
+//
+// Page "扔掉 vLLM！从零构建 Qwen3-8B 推理引擎，C++/CUDA 实现性能追平 98%":
+//   §4.4.3 QKV fusion   the three projections are one matrix product with the weights
+//                       stacked (w_qkv_merged), whose output is sliced into q, k, v;
+//   §4.4.2 GQA          k and v have the 8 KV heads (1024 columns each), q the 32 heads;
+//   §4.3.1              KV in 256-token blocks reached through a block table.
+// Page "从零搭建AI工程能力：手写KV Cache与动态批处理实战" §3.2: the new tokens' K and V are
+// appended to the cache.
+//
+// out[t][n] = sum_k x[t][k] * w[n][k]  (w stored [6144 out][hidden in], as a linear layer's
+// weight), fp32 accumulation, one bf16 rounding.  Columns 0-4095 are q (head n / 128,
+// dim n % 128) and go to q_out[t]; columns 4096-5119 are k of KV head (n - 4096) / 128 and
+// 5120-6143 v, written to the cache slot of token t (position seq_len - q_len + i of its
+// sequence, as kv_append places it), so K and V never make a round trip through memory
+// before they reach the cache.  No rotary position embedding or per-head normalisation is
+// applied: the pages define neither.
+//
+// GEMM on the 5th-generation tensor cores: a tile is 128 tokens x BN output columns (BN
+// 256, or 64 when there are few tokens and the weights dominate the bytes), the hidden
+// dimension in steps of 64 through a TMA ring; two accumulators in tensor memory, so the
+// epilogue of one tile overlaps the products of the next.  With at most 32 tokens only 32
+// rows of x are loaded per stage (BMA = 32): the ring then holds twice the weight bytes in
+// flight.  The MMA still reads 128 rows; rows 32-127 come from the neighbouring shared
+// memory, their results are discarded.  CTA = 6 warps, persistent:
+//   warps 0-3  epilogue: thread = one token row = TMEM lane
+//   warp 4     TMA producer (x and w tiles, 128-byte swizzle)
+//   warp 5     TMEM allocator and the tcgen05.mma issuer
+// Every wait is bounded; on expiry the CTA records PA_ERR_TIMEOUT and unwinds.
+#include "common.cuh"
+#include "launch.h"
+
+namespace pa {
+namespace {
+
+constexpr int kQCols = kHq * kD;               // 4096
+constexpr int kKVCols = kHkv * kD;             // 1024
+constexpr int kBM = 128;                       // tokens per tile (MMA M)
+constexpr int kBK = 64;                        // hidden elements per sub-tile (one 128-byte row)
+constexpr int kEpiWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 6 * 32;
+constexpr uint32_t kParkNs = 20000;
+constexpr uint32_t kRingBytes = 192 * 1024;    // the TMA ring's share of shared memory
+
+// BN output columns per tile, BMA rows of x loaded per stage (128, or 32 for <= 32 tokens).
+// A stage covers kSub adjacent sub-tiles of 64 hidden elements: with few tokens the weights
+// come from DRAM once, and 4 sub-tiles make each weight row's share of a stage 512
+// contiguous bytes instead of 128 (one DRAM page opened per 128 bytes held reads of the
+// weights at a third of the bandwidth).
+template <int BN, int BMA>
+struct QkvCfg {
+    static constexpr int kSub = BN == 256 ? 1 : 4;
+    static constexpr uint32_t kASub = BMA * kBK * 2;
+    static constexpr uint32_t kBSub = BN * kBK * 2;
+    static constexpr uint32_t kABytes = kSub * kASub;
+    static constexpr uint32_t kBBytes = kSub * kBSub;
+    static constexpr int kStages = (int)(kRingBytes / (kABytes + kBBytes));
+    static constexpr uint32_t kTmemCols = BN == 256 ? 512 : 128;   // two accumulators
+    static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, false);   // both operands K-major
+};
+
+template <int BN, int BMA>
+struct QkvSmem {
+    // the A stages first: an MMA over a 32-row stage reads 96 more rows after it, which
+    // stay inside this struct (the next stages, then the B ring)
+    uint8_t a[QkvCfg<BN, BMA>::kStages][QkvCfg<BN, BMA>::kABytes];
+    uint8_t b[QkvCfg<BN, BMA>::kStages][QkvCfg<BN, BMA>::kBBytes];
+    uint64_t full[QkvCfg<BN, BMA>::kStages], empty[QkvCfg<BN, BMA>::kStages];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t mma_idle;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int BN, int BMA>
+constexpr size_t qkv_smem_bytes() { return sizeof(QkvSmem<BN, BMA>) + 1024; }
+static_assert(qkv_smem_bytes<256, 128>() <= 232448 && qkv_smem_bytes<64, 128>() <= 232448 &&
+              qkv_smem_bytes<64, 32>() <= 232448, "shared memory");
+// the 128-row MMA reads of the last 32-row A stage end inside the B ring
+static_assert(QkvCfg<64, 32>::kStages * QkvCfg<64, 32>::kABytes + QkvCfg<64, 32>::kBBytes * QkvCfg<64, 32>::kStages >=
+              QkvCfg<64, 32>::kStages * QkvCfg<64, 32>::kABytes - QkvCfg<64, 32>::kASub + kBM * kBK * 2,
+              "A over-read");
+
+// 2-D tiled TMA load (col, row) completing its bytes on the mbarrier
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              uint32_t *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait_parked(bar, parity, kParkNs)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            record_error(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Cache slot of token t (the kv_append rule): element offset of (slot, KV head 0, dim 0) in
+// a pool, or -1 when the token's sequence data are inconsistent or its block id is outside
+// the pool (recorded in the error word).
+__device__ __forceinline__ long long cache_row(const QkvArgs &a, int t) {
+    int lo = 0, hi = a.num_seqs - 1;   // the sequence s with cu_q_lens[s] <= t < cu_q_lens[s + 1]
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.cu_q_lens + mid) <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    const int s = lo;
+    const int c0 = __ldg(a.cu_q_lens + s), c1 = __ldg(a.cu_q_lens + s + 1);
+    const int seq_len = __ldg(a.seq_lens + s);
+    const int q_len = c1 - c0;
+    if (c0 > t || t >= c1 || q_len > seq_len || seq_len > a.max_blocks_per_seq * kBlock) {
+        record_error(a.err, kErrDevice | kErrBadCuQ);
+        return -1;
+    }
+    const int p = seq_len - q_len + (t - c0);
+    const int blk = __ldg(a.block_table + (size_t)s * a.max_blocks_per_seq + p / kBlock);
+    if (blk < 0 || blk >= a.num_blocks) {
+        record_error(a.err, kErrDevice | kErrBadBlock);
+        return -1;
+    }
+    return ((long long)blk * kBlock + p % kBlock) * kHkv * kD;
+}
+
+template <int BN, int BMA>
+__global__ void __launch_bounds__(kThreads, 1)
+qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map, const QkvArgs a) {
+    using Cfg = QkvCfg<BN, BMA>;
+    constexpr int kStages = Cfg::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    QkvSmem<BN, BMA> &sm = *reinterpret_cast<QkvSmem<BN, BMA> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    volatile int *abort_flag = &sm.abort;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n_tiles = (kQCols + 2 * kKVCols) / BN;
+    const int m_tiles = (a.total_tokens + kBM - 1) / kBM;
+    const int total = m_tiles * n_tiles;
+    const int ksteps = a.hidden / (kBK * Cfg::kSub);   // stages per tile
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(smem_u32(&sm.full[i]), 1);
+            mbar_init(smem_u32(&sm.empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&sm.acc_full[i]), 1);
+            mbar_init(smem_u32(&sm.acc_empty[i]), kEpiWarps);
+        }
+        mbar_init(smem_u32(&sm.mma_idle), 1);
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(&sm.tmem_base), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == kProducerWarp) {
+        // ---------------------------------------------------------------- TMA producer
+        const bool leader = elect_one();
+        if (leader) {
+            tma_prefetch_map(&x_map);
+            tma_prefetch_map(&w_map);
+        }
+        // x may be written by the kernel just before this one on the stream
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        int it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const int mt = t / n_tiles, nt = t - (t / n_tiles) * n_tiles;
+            for (int kc = 0; kc < ksteps; ++kc, ++it) {
+                const int s = it % kStages;
+                if (it >= kStages &&
+                    !(ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&sm.empty[s]), ((it / kStages) - 1) & 1,
+                                                                abort_flag, a.err))))
+                    break;
+                if (leader) {
+                    const uint32_t bar = smem_u32(&sm.full[s]);
+                    mbar_arrive_expect_tx(bar, Cfg::kABytes + Cfg::kBBytes);
+#pragma unroll
+                    for (int j = 0; j < Cfg::kSub; ++j) {
+                        const int k0 = (kc * Cfg::kSub + j) * kBK;
+                        tma_load_2d(smem_u32(sm.a[s] + j * Cfg::kASub), &x_map, bar, k0, mt * kBM);
+                        tma_load_2d(smem_u32(sm.b[s] + j * Cfg::kBSub), &w_map, bar, k0, nt * BN);
+                    }
+                }
+                __syncwarp();
+            }
+        }
+        // no copy may still be landing when the CTA exits
+        for (int i = max(0, it - kStages); i < it; ++i) mbar_wait(smem_u32(&sm.full[i % kStages]), (i / kStages) & 1);
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issuer
+        const bool leader = elect_one();
+        const uint64_t ad0 = sdesc_sw128(smem_u32(sm.a[0]), 16, 1024);
+        const uint64_t bd0 = sdesc_sw128(smem_u32(sm.b[0]), 16, 1024);
+        int it = 0, lt = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
+            const int acc = lt & 1;
+            if (lt >= 2 && !(ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&sm.acc_empty[acc]),
+                                                                         ((lt >> 1) - 1) & 1, abort_flag, a.err))))
+                break;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * BN);
+            for (int kc = 0; kc < ksteps; ++kc, ++it) {
+                const int s = it % kStages;
+                if (!(ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&sm.full[s]), (it / kStages) & 1,
+                                                                abort_flag, a.err))))
+                    break;
+                tc_fence_after();
+                // +2 per 16 elements along the 128-byte row; a stage is BMA / BN rows of 128 B
+                const uint64_t ad = ad0 + (uint64_t)(s * (Cfg::kABytes >> 4));
+                const uint64_t bd = bd0 + (uint64_t)(s * (Cfg::kBBytes >> 4));
+                if (leader) {
+#pragma unroll
+                    for (int j = 0; j < Cfg::kSub; ++j) {
+                        const uint64_t adj = ad + (uint64_t)(j * (Cfg::kASub >> 4));
+                        const uint64_t bdj = bd + (uint64_t)(j * (Cfg::kBSub >> 4));
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            if (kc == 0 && j == 0 && kk == 0) umma_ss_c<false>(d, adj, bdj, Cfg::kIdesc);
+                            else umma_ss_c<true>(d, adj + (uint64_t)(kk * 2), bdj + (uint64_t)(kk * 2), Cfg::kIdesc);
+                        }
+                    }
+                    umma_commit(smem_u32(&sm.empty[s]));
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (leader) umma_commit(smem_u32(&sm.acc_full[acc]));
+            __syncwarp();
+        }
+        // every MMA issued must have finished before tensor memory is released
+        if (leader) umma_commit(smem_u32(&sm.mma_idle));
+        __syncwarp();
+        mbar_wait(smem_u32(&sm.mma_idle), 0);
+    } else {
+        // ---------------------------------------------------------------- epilogue warps
+        // q_out and the pools may still be read by the kernel before this one on the stream
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        const int row = warp * 32 + lane;                       // token row = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        int lt = 0, cached_mt = -1;
+        long long dst_row = -1;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+            const int mt = t / n_tiles, nt = t - (t / n_tiles) * n_tiles;
+            const int acc = lt & 1;
+            const int tok = mt * kBM + row;
+            const bool live = tok < a.total_tokens;
+            const int col0 = nt * BN;
+            if (col0 >= kQCols && mt != cached_mt) {   // K/V columns: this token's cache slot
+                dst_row = live ? cache_row(a, tok) : -1;
+                cached_mt = mt;
+            }
+            const bool ok = wait_or_abort(smem_u32(&sm.acc_full[acc]), (lt >> 1) & 1, abort_flag, a.err);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(lane_base + (uint32_t)(acc * BN + c * 32), v);
+                tmem_wait_ld(v);
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) w[e / 2] = pack_bf16x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+                const int col = col0 + c * 32;
+                __nv_bfloat16 *dst = nullptr;
+                if (col < kQCols) {
+                    if (live) dst = static_cast<__nv_bfloat16 *>(a.q_out) + (size_t)tok * kQCols + col;
+                } else if (dst_row >= 0) {
+                    const bool is_k = col < kQCols + kKVCols;
+                    const int kvc = col - kQCols - (is_k ? 0 : kKVCols);   // KV head * 128 + dim
+                    dst = static_cast<__nv_bfloat16 *>(is_k ? a.k_pool : a.v_pool) + dst_row + kvc;
+                }
+                if (dst) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[acc]));
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+}
+
+template <int BN, int BMA>
+cudaError_t launch_qkv_bn(const QkvArgs &a, const CUtensorMap &x_map, const CUtensorMap &w_map, int num_sms,
+                          cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool configured[64] = {};
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(qkv_kernel<BN, BMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)qkv_smem_bytes<BN, BMA>());
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    const long long tiles = (long long)((a.total_tokens + kBM - 1) / kBM) * ((kQCols + 2 * kKVCols) / BN);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles < num_sms ? tiles : num_sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = qkv_smem_bytes<BN, BMA>();
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qkv_kernel<BN, BMA>, x_map, w_map, a);
+}
+
+}  // namespace
+
+int qkv_tile_cols(int total_tokens) { return total_tokens <= 2 * kBM ? 64 : 256; }
+int qkv_tile_rows_loaded(int total_tokens) { return total_tokens <= 32 ? 32 : kBM; }
+
+cudaError_t launch_qkv(const QkvArgs &a, const CUtensorMap &x_map, const CUtensorMap &w_map, int num_sms,
+                       cudaStream_t stream) {
+    if (a.total_tokens == 0) return cudaSuccess;
+    if (qkv_tile_rows_loaded(a.total_tokens) == 32) return launch_qkv_bn<64, 32>(a, x_map, w_map, num_sms, stream);
+    if (qkv_tile_cols(a.total_tokens) == 64) return launch_qkv_bn<64, 128>(a, x_map, w_map, num_sms, stream);
+    return launch_qkv_bn<256, 128>(a, x_map, w_map, num_sms, stream);
+}
+
+}  // namespace pa

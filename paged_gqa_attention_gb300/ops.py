@@ -71,6 +71,9 @@ def load() -> ctypes.CDLL:
     lib.pa_check_error.restype = ctypes.c_int
     lib.kv_append.argtypes = [pa_shape, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32, vp, sz, vp]
     lib.kv_append.restype = ctypes.c_int
+    lib.paged_qkv_append.argtypes = [pa_shape, i32, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32, vp, sz,
+                                     vp]
+    lib.paged_qkv_append.restype = ctypes.c_int
     lib.paged_attn_decode.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, f32, vp,
                                       sz, vp]
     lib.paged_attn_decode.restype = ctypes.c_int
@@ -197,6 +200,36 @@ def kv_append(k_pool, v_pool, k_new, v_new, block_table, cu_q_lens, seq_lens, wo
                           k_pool.shape[0], cu_q_lens.data_ptr(), seq_lens.data_ptr(), num_seqs,
                           k_new.shape[0], workspace.data_ptr(), workspace.numel(), _stream(stream))
     _check("kv_append", st)
+
+
+QKV_COLS = NUM_Q_HEADS * HEAD_DIM + 2 * NUM_KV_HEADS * HEAD_DIM   # 6144
+
+
+def paged_qkv_append(x, w_qkv, k_pool, v_pool, block_table, cu_q_lens, seq_lens, workspace, *,
+                     q_out=None, stream=None) -> torch.Tensor:
+    """Merged Q/K/V projection of the new tokens: x [T, hidden] @ w_qkv[6144, hidden]^T; returns
+    q [T, 32, 128] and writes k and v into the pools at each sequence's tail positions."""
+    dev = x.device
+    _need(x, "x", torch.bfloat16, (None, None), dev)
+    hidden = x.shape[1]
+    _need(w_qkv, "w_qkv", torch.bfloat16, (QKV_COLS, hidden), dev)
+    _need(k_pool, "k_pool", torch.bfloat16, (None, BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_pool, "v_pool", torch.bfloat16, tuple(k_pool.shape), dev)
+    _need(block_table, "block_table", torch.int32, (None, None), dev)
+    num_seqs = block_table.shape[0]
+    _need(cu_q_lens, "cu_q_lens", torch.int32, (num_seqs + 1,), dev)
+    _need(seq_lens, "seq_lens", torch.int32, (num_seqs,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    if q_out is None:
+        q_out = torch.empty(x.shape[0], NUM_Q_HEADS, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    _need(q_out, "q_out", torch.bfloat16, (x.shape[0], NUM_Q_HEADS, HEAD_DIM), dev)
+    st = load().paged_qkv_append(SHAPE, hidden, q_out.data_ptr(), x.data_ptr(), w_qkv.data_ptr(),
+                                 k_pool.data_ptr(), v_pool.data_ptr(), block_table.data_ptr(),
+                                 block_table.shape[1], k_pool.shape[0], cu_q_lens.data_ptr(),
+                                 seq_lens.data_ptr(), num_seqs, x.shape[0], workspace.data_ptr(),
+                                 workspace.numel(), _stream(stream))
+    _check("paged_qkv_append", st)
+    return q_out
 
 
 def paged_attn_decode(q, k_pool, v_pool, block_table, seq_lens, workspace, *,

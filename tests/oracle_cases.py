@@ -175,7 +175,82 @@ def pin_battery(lib):
     check("e4m3_encode_torch", e4m3_encode)
     check("fp8_append_quantisation", fp8_append)
     check("fp8_attention_sdpa", fp8_attention)
+
+    # ---- the merged Q/K/V projection and the bf16 rounding of its k and v
+    def qkv_integer():
+        x, w = qkv_integer_case(seed=31)
+        y = oracle.qkv_project(x, w, lib=lib)
+        xi = x.double().numpy().astype(np.int64)
+        wi = w.double().numpy().astype(np.int64)
+        return np.array_equal(y, (xi @ wi.T).astype(np.float64))
+
+    def qkv_rows():
+        x, w = qkv_integer_case(seed=32)
+        full = oracle.qkv_project(x, w, lib=lib)
+        part = oracle.qkv_project(x, w, rows=[4, 0, 2], lib=lib)
+        return np.array_equal(part, full[[4, 0, 2]])
+
+    def bf16_torch():
+        v = bf16_probe_values()
+        ref = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        return np.array_equal(oracle.bf16_round(v, lib=lib), ref)
+
+    def bf16_nearest():
+        v = np.random.default_rng(33).standard_normal(2000) * np.exp2(np.random.default_rng(34).uniform(-140, 120, 2000))
+        return bf16_is_nearest_even(v, oracle.bf16_round(v, lib=lib))
+
+    check("qkv_integer_exact", qkv_integer)
+    check("qkv_row_subset", qkv_rows)
+    check("bf16_round_torch", bf16_torch)
+    check("bf16_round_nearest_even", bf16_nearest)
     return failed
+
+
+# ------------------------------------------------------------------ Q/K/V projection cases
+
+def qkv_integer_case(seed, tokens=6, hidden=64, n_out=40):
+    """bf16 x [tokens, hidden] and w [n_out, hidden] with small integer values: every product
+    and partial sum is an exact integer, so integer arithmetic gives the exact result."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randint(-4, 5, (tokens, hidden), generator=g).to(torch.bfloat16)
+    w = torch.randint(-4, 5, (n_out, hidden), generator=g).to(torch.bfloat16)
+    return x, w
+
+
+def bf16_probe_values(seed=35, n=3000):
+    """float32-representable values for the bf16 rounding: normals over the range, bf16
+    subnormals, exact midpoints between neighbouring bf16 values (ties), the largest finite
+    bf16 and values past it, zeros of both signs."""
+    g = np.random.default_rng(seed)
+    x = (g.standard_normal(n) * np.exp2(g.uniform(-120, 120, n))).astype(np.float32)
+    sub = (g.standard_normal(200) * 2.0 ** -130).astype(np.float32)          # bf16 subnormal range
+    base = torch.from_numpy(g.standard_normal(500).astype(np.float32)).to(torch.bfloat16)
+    bits = base.view(torch.int16).numpy().view(np.uint16).astype(np.uint32)
+    lo = (bits << 16).view(np.float32)
+    hi = ((bits + 1) << 16).view(np.float32)
+    ties = ((lo.astype(np.float64) + hi.astype(np.float64)) / 2).astype(np.float32)   # exact in fp32
+    big = np.array([3.3895314e38, 3.3961e38, 3.4e38, -3.4e38, 0.0, -0.0], dtype=np.float32)
+    return np.concatenate([x, sub, ties, big]).astype(np.float64)
+
+
+def bf16_is_nearest_even(v, bits):
+    """Brute force: each bf16 result is at least as close to its input as the neighbouring
+    bf16 values on either side, and on a tie its last mantissa bit is even."""
+    def dec(b):
+        f = (b.astype(np.uint32) << 16).view(np.float32)
+        with np.errstate(invalid="ignore"):            # neighbours past the ends are NaN patterns
+            return f.astype(np.float64)
+    r = dec(bits)
+    ok = np.isfinite(r) | (np.abs(v) >= 3.3895313892515355e38)
+    fin = np.isfinite(r) & (np.abs(r) > 0)
+    up, down = dec(bits + 1), dec(bits - 1)
+    d0 = np.abs(r - v)
+    for nb in (up, down):
+        m = fin & np.isfinite(nb) & (np.sign(nb) == np.sign(r))
+        ok &= ~m | (d0 <= np.abs(nb - v))
+        tie = m & (d0 == np.abs(nb - v))
+        ok &= ~tie | ((bits & 1) == 0)
+    return bool(ok.all())
 
 
 # ------------------------------------------------------------------ 8-bit cache cases

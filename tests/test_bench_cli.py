@@ -10,7 +10,7 @@ sys.path.insert(0, ROOT)
 import bench  # noqa: E402
 
 WORKLOADS = ["single_decode", "batched_decode", "causal_prefill", "mixed_batch", "prefix_shared_decode",
-             "layered_decode", "batched_decode_fp8", "prefix_shared_decode_cascade"]
+             "layered_decode", "batched_decode_fp8", "prefix_shared_decode_cascade", "qkv_append"]
 
 
 def test_help_lists_every_workload():

@@ -1,0 +1,186 @@
+"""paged_qkv_append (merged Q/K/V projection with K and V written into the cache) against the
+oracle.
+
+Tolerance: each output is one bf16 rounding of a dot product accumulated in fp32 by the
+tensor cores, so every element of q and of the appended K/V rows must lie within one bf16
+step of the exact fp64 value (2^-8 relative) plus the accumulation error, which scales with
+the sum of the absolute products rather than with the (possibly cancelled) result: we allow
+2^-16 * sum_k |x_k w_k| (about 256 fp32 roundings of that sum).  The whole q must also be
+within rel-RMS 5e-3.  Every pool byte outside the new tokens' slots must be unchanged
+(bit-exact).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import gpu, lib_ready, workspace_for
+from paged_gqa_attention_gb300 import ops
+from paged_gqa_attention_gb300 import workloads as wl
+
+pytestmark = gpu
+
+HIDDEN = 4096
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lib_ready()
+
+
+def weights(seed, hidden=HIDDEN):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return (torch.randn(ops.QKV_COLS, hidden, generator=g, device="cuda") / np.sqrt(hidden)).to(torch.bfloat16)
+
+
+def inputs(seed, tokens, hidden=HIDDEN):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return torch.randn(tokens, hidden, generator=g, device="cuda").to(torch.bfloat16)
+
+
+def batch_for(ctx_and_q, seed):
+    seq_lens = [c + q for c, q in ctx_and_q]
+    q_lens = [q for _, q in ctx_and_q]
+    return wl.build_batch("qkv_case", seed, seq_lens, q_lens, num_blocks=sum((s + 255) // 256 for s in seq_lens) + 3,
+                          device="cuda")
+
+
+def abs_sums(x, w, rows=None):
+    """sum_k |x[t][k] w[n][k]| for the listed token rows (the scale of the accumulation error)."""
+    xa = x.cpu().double().abs().numpy()
+    if rows is not None:
+        xa = xa[rows]
+    return xa @ w.cpu().double().abs().numpy().T
+
+
+def within_tol(got, exact, abs_sum, what):
+    got = np.asarray(got, dtype=np.float64)
+    tol = np.abs(exact) * 2.0 ** -8 + abs_sum * 2.0 ** -16
+    err = np.abs(got - exact)
+    i = np.unravel_index(np.argmax(err / tol), err.shape)
+    assert (err <= tol).all(), (f"{what}: worst element {i}: got {got[i]!r} exact {exact[i]!r} "
+                                f"tolerance {tol[i]!r} ({(err > tol).sum()} elements beyond it)")
+
+
+def new_slots(b):
+    """(block, slot) of every new token, in token order."""
+    bt, cu, sl = b.block_table.cpu(), b.cu_q_lens.cpu(), b.seq_lens.cpu()
+    out = []
+    for s in range(b.num_seqs):
+        q_len = int(cu[s + 1] - cu[s])
+        for i in range(q_len):
+            p = int(sl[s]) - q_len + i
+            out.append((int(bt[s, p // 256]), p % 256))
+    return out
+
+
+def check_case(b, x, w):
+    kp0 = b.k_pool.view(torch.int16).cpu().numpy().view(np.uint16).copy()
+    vp0 = b.v_pool.view(torch.int16).cpu().numpy().view(np.uint16).copy()
+    ws = workspace_for(b)
+    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    ops.check_error(ws)
+    y = oracle.qkv_project(x.cpu(), w.cpu())
+    a = abs_sums(x, w)
+    qg = q.float().cpu().numpy().astype(np.float64).reshape(x.shape[0], -1)
+    within_tol(qg, y[:, :4096], a[:, :4096], "q")
+    rel = np.sqrt(((qg - y[:, :4096]) ** 2).sum() / (y[:, :4096] ** 2).sum())
+    assert rel <= 5e-3, rel
+    kp = b.k_pool.view(torch.int16).cpu().numpy().view(np.uint16)
+    vp = b.v_pool.view(torch.int16).cpu().numpy().view(np.uint16)
+    touched = np.zeros(kp.shape[:2], dtype=bool)
+    for t, (blk, slot) in enumerate(new_slots(b)):
+        touched[blk, slot] = True
+        kf = torch.from_numpy(kp[blk, slot].copy()).view(torch.bfloat16).double().numpy().reshape(-1)
+        vf = torch.from_numpy(vp[blk, slot].copy()).view(torch.bfloat16).double().numpy().reshape(-1)
+        within_tol(kf, y[t, 4096:5120], a[t, 4096:5120], f"k row of token {t}")
+        within_tol(vf, y[t, 5120:], a[t, 5120:], f"v row of token {t}")
+    assert np.array_equal(kp[~touched], kp0[~touched]), "k pool written outside the new slots"
+    assert np.array_equal(vp[~touched], vp0[~touched]), "v pool written outside the new slots"
+
+
+@pytest.mark.parametrize("ctx_and_q", [
+    [(0, 1)],
+    [(0, 37)],                                  # few tokens: 64-column tiles
+    [(200, 100), (0, 64), (511, 1)],            # chunks after context, a decode-like row
+    [(0, 300)],                                 # many tokens: 256-column tiles, a ragged last tile
+    [(37, 130), (1000, 0), (255, 200)],         # a sequence with no new token
+])
+def test_qkv_append_matches_oracle(ctx_and_q):
+    b = batch_for(ctx_and_q, seed=60 + len(ctx_and_q))
+    x = inputs(61, b.total_tokens)
+    w = weights(62)
+    check_case(b, x, w)
+
+
+def test_decode_batch_one_token_per_sequence():
+    b = wl.batched_decode(device="cuda", seed=63, batch=32, hi=2000, num_blocks=300)
+    check_case(b, inputs(64, b.total_tokens), weights(65))
+
+
+def test_full_prefill_chunk_sampled_rows():
+    """4096 new tokens (the causal prefill workload's prompt): sampled rows of q and of the
+    cache against the oracle, every other cache row untouched is not re-checked here."""
+    b = wl.causal_prefill(device="cuda")
+    x = inputs(66, b.total_tokens)
+    w = weights(67)
+    ws = workspace_for(b)
+    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    ops.check_error(ws)
+    rows = [0, 1, 127, 128, 2047, 2048, 4000, 4095]
+    y = oracle.qkv_project(x.cpu(), w.cpu(), rows=rows)
+    a = abs_sums(x, w, rows)
+    slots = new_slots(b)
+    qg = q.float().cpu().numpy().astype(np.float64).reshape(b.total_tokens, -1)
+    for r, t in enumerate(rows):
+        within_tol(qg[t], y[r, :4096], a[r, :4096], f"q row {t}")
+        blk, slot = slots[t]
+        kf = b.k_pool[blk, slot].double().cpu().numpy().reshape(-1)
+        vf = b.v_pool[blk, slot].double().cpu().numpy().reshape(-1)
+        within_tol(kf, y[r, 4096:5120], a[r, 4096:5120], f"k row {t}")
+        within_tol(vf, y[r, 5120:], a[r, 5120:], f"v row {t}")
+
+
+def test_bad_block_writes_no_kv_but_keeps_q():
+    b = batch_for([(0, 40), (100, 20)], seed=68)
+    x = inputs(69, b.total_tokens)
+    w = weights(70)
+    bt = b.block_table.clone()
+    bt[1, 0] = b.num_blocks + 7                 # sequence 1's only block is outside the pool
+    kp0 = b.k_pool.clone()
+    ws = workspace_for(b)
+    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, bt, b.cu_q_lens, b.seq_lens, ws)
+    with pytest.raises(ops.PagedAttnError) as e:
+        ops.check_error(ws)
+    assert e.value.status == 4
+    y = oracle.qkv_project(x.cpu(), w.cpu())
+    qg = q.float().cpu().numpy().astype(np.float64).reshape(b.total_tokens, -1)
+    within_tol(qg, y[:, :4096], abs_sums(x, w)[:, :4096], "q")
+    # sequence 0's rows are appended, nothing of sequence 1 is written anywhere
+    touched = np.zeros((b.num_blocks, 256), dtype=bool)
+    for t, (blk, slot) in enumerate(new_slots(b)[:40]):
+        touched[blk, slot] = True
+    a = b.k_pool.view(torch.int16).cpu().numpy()
+    o = kp0.view(torch.int16).cpu().numpy()
+    assert np.array_equal(a[~touched], o[~touched])
+
+
+def test_fused_append_feeds_the_decode():
+    """The fused projection + append followed by the decode equals the decode over the
+    oracle's appended cache (within the attention tolerance)."""
+    from gpu_helpers import assert_close
+    b = wl.batched_decode(device="cuda", seed=71, batch=8, hi=1500, num_blocks=64)
+    x = inputs(72, b.total_tokens)
+    w = weights(73)
+    q_ref, kp, vp = oracle.qkv_append(x.cpu(), w.cpu(), b.k_pool.cpu(), b.v_pool.cpu(), b.block_table.cpu(),
+                                      b.cu_q_lens.cpu(), b.seq_lens.cpu())
+    ws = workspace_for(b)
+    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    out = ops.paged_attn_decode(q, b.k_pool, b.v_pool, b.block_table, b.seq_lens, ws)
+    ops.check_error(ws)
+    # the oracle attends with the GPU's q (its own q is exact fp64, the GPU's is bf16)
+    ref, _ = oracle.attention(q.cpu(), kp, vp, b.block_table.cpu(), b.cu_q_lens.cpu(), b.seq_lens.cpu(),
+                              scale=wl.SCALE)
+    assert_close(out, ref, "decode after the fused projection")

@@ -59,6 +59,20 @@ MUTANTS = {
         "                          * c->num_kv_heads + g];"),
     # 8-bit append at the chunk-relative position
     "fp8_append_relative": ("int p = seq_lens[s] - q_len + i;\n            int blk", "int p = i;\n            int blk"),
+    # projection with the weight read transposed ([hidden][n_out] instead of [n_out][hidden])
+    "qkv_weight_transposed": ("bf16_to_double(w[(size_t)n * hidden + k]);",
+                              "bf16_to_double(w[(size_t)k * n_out + n]);"),
+    # projection ignores the requested rows
+    "qkv_rows_ignored": ("const int t = rows ? rows[r] : r;", "const int t = r;"),
+    # projection drops the last input element
+    "qkv_dropped_term": ("for (int k = 0; k < hidden; ++k)\n            acc +=",
+                         "for (int k = 0; k < hidden - 1; ++k)\n            acc +="),
+    # bf16 rounding by truncation
+    "bf16_truncate": ("if (frac > 0.5 || (frac == 0.5 && fmod(m, 2.0) != 0.0)) m += 1.0;", ""),
+    # bf16 ties rounded away from zero instead of to even
+    "bf16_ties_away": ("(frac == 0.5 && fmod(m, 2.0) != 0.0)", "(frac == 0.5)"),
+    # bf16 subnormals with the normal quantum (8 significant bits all the way down)
+    "bf16_no_subnormals": ("if (lo < -126) lo = -126;", ""),
     # append writes at the chunk-relative position
     "append_relative_position": ("int p = seq_lens[s] - q_len + i;            /* absolute position */",
                                  "int p = i;            /* absolute position */"),
