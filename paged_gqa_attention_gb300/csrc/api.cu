@@ -372,7 +372,7 @@ pa_status paged_qkv_append(pa_shape shape, int32_t hidden, void *q_out, const vo
     if (!get_encoder()) return PA_ERR_CUDA;
     CUtensorMap x_map, w_map;
     if (!encode_matrix_map(&x_map, x, total_tokens, hidden, qkv_tile_rows_loaded(total_tokens)) ||
-        !encode_matrix_map(&w_map, w_qkv, kHq * kD + 2 * kHkv * kD, hidden, qkv_tile_cols(total_tokens)))
+        !encode_matrix_map(&w_map, w_qkv, kHq * kD + 2 * kHkv * kD, hidden, qkv_weight_box_rows(total_tokens)))
         return PA_ERR_INVALID_ARG;
     QkvArgs a = {};
     a.q_out = q_out;

@@ -106,8 +106,9 @@ struct QkvArgs {
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
 
 // x_map: x [total_tokens][hidden] bf16, box {64, qkv_tile_rows_loaded(total_tokens)}; w_map:
-// w [6144][hidden] bf16, box {64, qkv_tile_cols(total_tokens)}; both 128-byte swizzle.
+// w [6144][hidden] bf16, box {64, qkv_weight_box_rows(total_tokens)}; both 128-byte swizzle.
 int qkv_tile_cols(int total_tokens);
+int qkv_weight_box_rows(int total_tokens);
 int qkv_tile_rows_loaded(int total_tokens);
 cudaError_t launch_qkv(const QkvArgs &a, const CUtensorMap &x_map, const CUtensorMap &w_map, int num_sms,
                        cudaStream_t stream);

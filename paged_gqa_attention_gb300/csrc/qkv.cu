@@ -60,7 +60,43 @@ struct QkvCfg {
     static constexpr int kStages = (int)(kRingBytes / (kABytes + kBBytes));
     static constexpr uint32_t kTmemCols = BN == 256 ? 512 : 128;   // two accumulators
     static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, false);   // both operands K-major
+    static constexpr uint32_t kIdescHalf = idesc_bf16(kBM, BN / 2, false);
+    static constexpr int kWBox = BN > 128 ? 128 : BN;                // weight rows per TMA box
 };
+
+// A CTA's work item: 128 tokens (tile row mt) x `width` output columns from col0; width 0
+// past the end.  Tiles of BN columns are dealt round-robin over the grid.  When the last
+// round would keep at most half of the CTAs busy and the tiles are 256 wide, each of its
+// tiles is split into two 128-column halves for twice as many CTAs, so that round takes
+// about half as long (4096 tokens: 768 tiles on 152 CTAs leave 8 for a sixth round).
+struct QkvItem {
+    int mt, col0, width;
+};
+
+template <int BN>
+__device__ __forceinline__ QkvItem qkv_item(int k, int m_tiles) {
+    constexpr int n_tiles = (kQCols + 2 * kKVCols) / BN;
+    const int total = m_tiles * n_tiles;
+    const int g = (int)gridDim.x, c = (int)blockIdx.x;
+    const int rounds = (total + g - 1) / g;
+    const int last = total - (rounds - 1) * g;          // tiles of the last round
+    const bool split = BN == 256 && rounds >= 2 && 2 * last <= g;
+    QkvItem w = {0, 0, 0};
+    if (!split || k < rounds - 1) {
+        const int t = c + k * g;
+        if (t >= total) return w;
+        w.mt = t / n_tiles;
+        w.col0 = (t - w.mt * n_tiles) * BN;
+        w.width = BN;
+        return w;
+    }
+    if (k > rounds - 1 || c >= 2 * last) return w;
+    const int t = (rounds - 1) * g + (c >> 1);
+    w.mt = t / n_tiles;
+    w.col0 = (t - w.mt * n_tiles) * BN + (c & 1) * (BN / 2);
+    w.width = BN / 2;
+    return w;
+}
 
 template <int BN, int BMA>
 struct QkvSmem {
@@ -146,9 +182,7 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
     volatile int *abort_flag = &sm.abort;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n_tiles = (kQCols + 2 * kKVCols) / BN;
     const int m_tiles = (a.total_tokens + kBM - 1) / kBM;
-    const int total = m_tiles * n_tiles;
     const int ksteps = a.hidden / (kBK * Cfg::kSub);   // stages per tile
 
     if (threadIdx.x == 0) {
@@ -184,8 +218,10 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
         asm volatile("griddepcontrol.wait;" ::: "memory");
         int it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const int mt = t / n_tiles, nt = t - (t / n_tiles) * n_tiles;
+        for (int k = 0; ok; ++k) {
+            const QkvItem w = qkv_item<BN>(k, m_tiles);
+            if (!w.width) break;
+            const uint32_t b_bytes = Cfg::kBBytes / (BN / w.width);
             for (int kc = 0; kc < ksteps; ++kc, ++it) {
                 const int s = it % kStages;
                 if (it >= kStages &&
@@ -194,12 +230,15 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
                     break;
                 if (leader) {
                     const uint32_t bar = smem_u32(&sm.full[s]);
-                    mbar_arrive_expect_tx(bar, Cfg::kABytes + Cfg::kBBytes);
+                    mbar_arrive_expect_tx(bar, Cfg::kABytes + b_bytes);
 #pragma unroll
                     for (int j = 0; j < Cfg::kSub; ++j) {
                         const int k0 = (kc * Cfg::kSub + j) * kBK;
-                        tma_load_2d(smem_u32(sm.a[s] + j * Cfg::kASub), &x_map, bar, k0, mt * kBM);
-                        tma_load_2d(smem_u32(sm.b[s] + j * Cfg::kBSub), &w_map, bar, k0, nt * BN);
+                        tma_load_2d(smem_u32(sm.a[s] + j * Cfg::kASub), &x_map, bar, k0, w.mt * kBM);
+                        // the weight rows in boxes of kWBox rows (128 B each), stacked
+                        for (int r = 0; r < w.width / Cfg::kWBox; ++r)
+                            tma_load_2d(smem_u32(sm.b[s] + j * Cfg::kBSub + r * Cfg::kWBox * 128), &w_map, bar, k0,
+                                        w.col0 + r * Cfg::kWBox);
                     }
                 }
                 __syncwarp();
@@ -214,7 +253,10 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
         const uint64_t bd0 = sdesc_sw128(smem_u32(sm.b[0]), 16, 1024);
         int it = 0, lt = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
+        for (int k = 0; ok; ++k, ++lt) {
+            const QkvItem w = qkv_item<BN>(k, m_tiles);
+            if (!w.width) break;
+            const uint32_t idesc = w.width == BN ? Cfg::kIdesc : Cfg::kIdescHalf;
             const int acc = lt & 1;
             if (lt >= 2 && !(ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&sm.acc_empty[acc]),
                                                                          ((lt >> 1) - 1) & 1, abort_flag, a.err))))
@@ -237,8 +279,8 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
                         const uint64_t bdj = bd + (uint64_t)(j * (Cfg::kBSub >> 4));
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk) {
-                            if (kc == 0 && j == 0 && kk == 0) umma_ss_c<false>(d, adj, bdj, Cfg::kIdesc);
-                            else umma_ss_c<true>(d, adj + (uint64_t)(kk * 2), bdj + (uint64_t)(kk * 2), Cfg::kIdesc);
+                            if (kc == 0 && j == 0 && kk == 0) umma_ss_c<false>(d, adj, bdj, idesc);
+                            else umma_ss_c<true>(d, adj + (uint64_t)(kk * 2), bdj + (uint64_t)(kk * 2), idesc);
                         }
                     }
                     umma_commit(smem_u32(&sm.empty[s]));
@@ -261,12 +303,14 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         int lt = 0, cached_mt = -1;
         long long dst_row = -1;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
-            const int mt = t / n_tiles, nt = t - (t / n_tiles) * n_tiles;
+        for (int k = 0;; ++k, ++lt) {
+            const QkvItem w = qkv_item<BN>(k, m_tiles);
+            if (!w.width) break;
+            const int mt = w.mt;
             const int acc = lt & 1;
             const int tok = mt * kBM + row;
             const bool live = tok < a.total_tokens;
-            const int col0 = nt * BN;
+            const int col0 = w.col0;
             if (col0 >= kQCols && mt != cached_mt) {   // K/V columns: this token's cache slot
                 dst_row = live ? cache_row(a, tok) : -1;
                 cached_mt = mt;
@@ -275,7 +319,7 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < w.width / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(lane_base + (uint32_t)(acc * BN + c * 32), v);
                 tmem_wait_ld(v);
@@ -342,6 +386,7 @@ cudaError_t launch_qkv_bn(const QkvArgs &a, const CUtensorMap &x_map, const CUte
 }  // namespace
 
 int qkv_tile_cols(int total_tokens) { return total_tokens <= 2 * kBM ? 64 : 256; }
+int qkv_weight_box_rows(int total_tokens) { return qkv_tile_cols(total_tokens) > 128 ? 128 : qkv_tile_cols(total_tokens); }
 int qkv_tile_rows_loaded(int total_tokens) { return total_tokens <= 32 ? 32 : kBM; }
 
 cudaError_t launch_qkv(const QkvArgs &a, const CUtensorMap &x_map, const CUtensorMap &w_map, int num_sms,

@@ -107,6 +107,7 @@ def check_case(b, x, w):
     [(200, 100), (0, 64), (511, 1)],            # chunks after context, a decode-like row
     [(0, 300)],                                 # many tokens: 256-column tiles, a ragged last tile
     [(37, 130), (1000, 0), (255, 200)],         # a sequence with no new token
+    [(100, 900)],                               # 192 tiles on 152 CTAs: the last round in halves
 ])
 def test_qkv_append_matches_oracle(ctx_and_q):
     b = batch_for(ctx_and_q, seed=60 + len(ctx_and_q))
