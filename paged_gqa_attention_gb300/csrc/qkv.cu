@@ -17,16 +17,17 @@
 // before they reach the cache.  No rotary position embedding or per-head normalisation is
 // applied: the pages define neither.
 //
-// GEMM on the 5th-generation tensor cores: a tile is 128 tokens x BN output columns (BN
-// 256, or 64 when there are few tokens and the weights dominate the bytes), the hidden
-// dimension in steps of 64 through a TMA ring; two accumulators in tensor memory, so the
-// epilogue of one tile overlaps the products of the next.  With at most 32 tokens only 32
+// GEMM on the 5th-generation tensor cores: with more than 256 tokens a pair of CTAs on two
+// SMs computes 256 tokens x 256 output columns (tcgen05.mma.cta_group::2, see the pair kernel
+// below); with fewer, one CTA computes 128 tokens x 64 columns (the weights dominate the
+// bytes).  The hidden dimension goes in steps of 64 through a TMA ring; two accumulators in
+// tensor memory, so the epilogue of one tile overlaps the products of the next.  With at most 32 tokens only 32
 // rows of x are loaded per stage (BMA = 32): the ring then holds twice the weight bytes in
 // flight.  The MMA still reads 128 rows; rows 32-127 come from the neighbouring shared
-// memory, their results are discarded.  CTA = 6 warps, persistent:
+// memory, their results are discarded.  CTA = 6 warps, persistent (both kernels):
 //   warps 0-3  epilogue: thread = one token row = TMEM lane
 //   warp 4     TMA producer (x and w tiles, 128-byte swizzle)
-//   warp 5     TMEM allocator and the tcgen05.mma issuer
+//   warp 5     TMEM allocator and the tcgen05.mma issuer (in a pair: rank 0's)
 // Every wait is bounded; on expiry the CTA records PA_ERR_TIMEOUT and unwinds.
 #include "common.cuh"
 #include "launch.h"
@@ -74,10 +75,9 @@ struct QkvItem {
 };
 
 template <int BN>
-__device__ __forceinline__ QkvItem qkv_item(int k, int m_tiles) {
+__device__ __forceinline__ QkvItem qkv_item_of(int k, int m_tiles, int g, int c) {
     constexpr int n_tiles = (kQCols + 2 * kKVCols) / BN;
     const int total = m_tiles * n_tiles;
-    const int g = (int)gridDim.x, c = (int)blockIdx.x;
     const int rounds = (total + g - 1) / g;
     const int last = total - (rounds - 1) * g;          // tiles of the last round
     const bool split = BN == 256 && rounds >= 2 && 2 * last <= g;
@@ -98,6 +98,12 @@ __device__ __forceinline__ QkvItem qkv_item(int k, int m_tiles) {
     return w;
 }
 
+// The item sequence of this CTA (one CTA per tile).
+template <int BN>
+__device__ __forceinline__ QkvItem qkv_item(int k, int m_tiles) {
+    return qkv_item_of<BN>(k, m_tiles, (int)gridDim.x, (int)blockIdx.x);
+}
+
 template <int BN, int BMA>
 struct QkvSmem {
     // the A stages first: an MMA over a 32-row stage reads 96 more rows after it, which
@@ -113,7 +119,7 @@ struct QkvSmem {
 
 template <int BN, int BMA>
 constexpr size_t qkv_smem_bytes() { return sizeof(QkvSmem<BN, BMA>) + 1024; }
-static_assert(qkv_smem_bytes<256, 128>() <= 232448 && qkv_smem_bytes<64, 128>() <= 232448 &&
+static_assert(qkv_smem_bytes<64, 128>() <= 232448 &&
               qkv_smem_bytes<64, 32>() <= 232448, "shared memory");
 // the 128-row MMA reads of the last 32-row A stage end inside the B ring
 static_assert(QkvCfg<64, 32>::kStages * QkvCfg<64, 32>::kABytes + QkvCfg<64, 32>::kBBytes * QkvCfg<64, 32>::kStages >=
@@ -356,6 +362,323 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
     }
 }
 
+
+// ------------------------------------------------------------------ CTA pairs (many tokens)
+// With many tokens the 128 x 256 tile of one CTA needs ~190 GB/s of L2 -> SM traffic at the
+// full tensor rate, more than one SM receives.  A pair of CTAs on two SMs (a 2-CTA cluster)
+// computes a 256 x 256 tile with tcgen05.mma.cta_group::2 (M = 256): each SM holds its own
+// 128 token rows and loads only half of the 256 weight rows, the MMA reading the other half
+// from the peer's shared memory, so each SM needs ~128 GB/s.  Rank 0's MMA warp issues for
+// both; both halves of a stage complete on rank 0's barrier (pair-scoped TMA), rank 0's
+// commits reach both CTAs (multicast), and both CTAs' epilogue warps hand an accumulator back
+// on rank 0's barrier.  Each CTA's tensor memory holds its rows' two accumulators.
+constexpr int kPairBM = 2 * kBM;                       // tokens per pair tile
+constexpr int kPairBN = 256;
+constexpr uint32_t kPairABytes = kBM * kBK * 2;        // this CTA's 128 rows x 64: 16 KiB
+constexpr uint32_t kPairBBytes = (kPairBN / 2) * kBK * 2;   // this CTA's 128 weight rows: 16 KiB
+constexpr int kPairStages = (int)(kRingBytes / (kPairABytes + kPairBBytes));
+constexpr int kPairWBox = 64;                          // weight rows per TMA box
+constexpr uint32_t kPairIdesc = idesc_bf16(kPairBM, kPairBN, false);
+constexpr uint32_t kPairIdescHalf = idesc_bf16(kPairBM, kPairBN / 2, false);
+
+struct QkvPairSmem {
+    uint8_t a[kPairStages][kPairABytes];
+    uint8_t b[kPairStages][kPairBBytes];
+    uint64_t full[kPairStages], empty[kPairStages];    // full: rank 0's counts both CTAs' copies
+    uint64_t acc_full[2], acc_empty[2];                // acc_empty: rank 0's, both CTAs' epilogues
+    uint64_t mma_idle;
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr size_t kPairSmemBytes = sizeof(QkvPairSmem) + 1024;
+static_assert(kPairSmemBytes <= 232448, "shared memory");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+// Arrive on a barrier of either CTA of the pair (release at CTA scope: what it announces is
+// tensor memory this thread has finished reading).
+__device__ __forceinline__ void arrive_remote(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// Every thread of both CTAs.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 2-D TMA load into this CTA's shared memory completing on a barrier of either CTA
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t cluster_bar, int c0,
+                                                 int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(cluster_bar)
+        : "memory");
+}
+
+// D rows 0-127 in rank 0's tensor memory, 128-255 in rank 1's; A rows likewise from each
+// CTA's shared memory at the same address; B columns 0 .. N/2-1 from rank 0, the rest from
+// rank 1.
+template <bool kAcc>
+__device__ __forceinline__ void umma_ss_pair_c(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "n"(kAcc ? 1 : 0)
+        : "memory");
+}
+
+// Arrive on the barrier at this offset in both CTAs once every prior pair MMA has completed.
+__device__ __forceinline__ void umma_commit_both(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 ::"r"(bar), "h"((uint16_t)3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_local(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+qkv_pair_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
+                const QkvArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    QkvPairSmem &sm = *reinterpret_cast<QkvPairSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    volatile int *abort_flag = &sm.abort;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool lead = rank == 0;
+    const int m_tiles = (a.total_tokens + kPairBM - 1) / kPairBM;
+    const int clusters = (int)gridDim.x >> 1, cid = (int)blockIdx.x >> 1;
+    const int ksteps = a.hidden / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kPairStages; ++i) {
+            mbar_init(smem_u32(&sm.full[i]), 1);
+            mbar_init(smem_u32(&sm.empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&sm.acc_full[i]), 1);
+            mbar_init(smem_u32(&sm.acc_empty[i]), 2 * kEpiWarps);
+        }
+        mbar_init(smem_u32(&sm.mma_idle), 1);
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        // one warp of each CTA allocates the pair's tensor memory together
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&sm.tmem_base)),
+                     "r"(512u)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    // both CTAs' barriers and tensor memory exist before either issues anything to the other
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == kProducerWarp) {
+        // ---------------------------------------------------------------- TMA producer
+        const bool leader = elect_one();
+        if (leader) {
+            tma_prefetch_map(&x_map);
+            tma_prefetch_map(&w_map);
+        }
+        // x may be written by the kernel just before this one on the stream
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        int it = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const QkvItem w = qkv_item_of<kPairBN>(k, m_tiles, clusters, cid);
+            if (!w.width) break;
+            const int cols = w.width / 2;                  // weight rows this CTA loads
+            for (int kc = 0; kc < ksteps; ++kc, ++it) {
+                const int s = it % kPairStages;
+                if (it >= kPairStages &&
+                    !(ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&sm.empty[s]),
+                                                                ((it / kPairStages) - 1) & 1, abort_flag, a.err))))
+                    break;
+                if (leader) {
+                    const uint32_t bar = smem_u32(&sm.full[s]);
+                    if (lead) mbar_arrive_expect_tx(bar, 2 * (kPairABytes + (uint32_t)cols * 128));
+                    const uint32_t bar0 = peer_addr(bar, 0);
+                    const int k0 = kc * kBK;
+                    tma_load_2d_pair(smem_u32(sm.a[s]), &x_map, bar0, k0, w.mt * kPairBM + (int)rank * kBM);
+                    for (int r = 0; r < cols / kPairWBox; ++r)
+                        tma_load_2d_pair(smem_u32(sm.b[s] + r * kPairWBox * 128), &w_map, bar0, k0,
+                                         w.col0 + (int)rank * cols + r * kPairWBox);
+                }
+                __syncwarp();
+            }
+        }
+        // No copy may still be landing when the CTA exits: both CTAs' copies complete on rank
+        // 0's barriers, which rank 0 waits on here (the MMA warp consumed them all in the
+        // normal path); rank 1 stays until the cluster barrier below.
+        if (lead)
+            for (int i = max(0, it - kPairStages); i < it; ++i)
+                mbar_wait(smem_u32(&sm.full[i % kPairStages]), (i / kPairStages) & 1);
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issuer (rank 0)
+        if (lead) {
+            const bool leader = elect_one();
+            const uint64_t ad0 = sdesc_sw128(smem_u32(sm.a[0]), 16, 1024);
+            const uint64_t bd0 = sdesc_sw128(smem_u32(sm.b[0]), 16, 1024);
+            int it = 0, lt = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k, ++lt) {
+                const QkvItem w = qkv_item_of<kPairBN>(k, m_tiles, clusters, cid);
+                if (!w.width) break;
+                const uint32_t idesc = w.width == kPairBN ? kPairIdesc : kPairIdescHalf;
+                const int acc = lt & 1;
+                if (lt >= 2 && !(ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&sm.acc_empty[acc]),
+                                                                             ((lt >> 1) - 1) & 1, abort_flag, a.err))))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * kPairBN);
+                for (int kc = 0; kc < ksteps; ++kc, ++it) {
+                    const int s = it % kPairStages;
+                    if (!(ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&sm.full[s]), (it / kPairStages) & 1,
+                                                                    abort_flag, a.err))))
+                        break;
+                    tc_fence_after();
+                    // +2 per 16 elements along the 128-byte row; +stage size per stage
+                    const uint64_t ad = ad0 + (uint64_t)(s * (kPairABytes >> 4));
+                    const uint64_t bd = bd0 + (uint64_t)(s * (kPairBBytes >> 4));
+                    if (leader) {
+                        if (kc == 0) umma_ss_pair_c<false>(d, ad, bd, idesc);
+                        else umma_ss_pair_c<true>(d, ad, bd, idesc);
+#pragma unroll
+                        for (int kk = 1; kk < kBK / 16; ++kk)
+                            umma_ss_pair_c<true>(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc);
+                        umma_commit_both(smem_u32(&sm.empty[s]));
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (leader) umma_commit_both(smem_u32(&sm.acc_full[acc]));
+                __syncwarp();
+            }
+            // every MMA issued must have finished before tensor memory is released
+            if (leader) umma_commit_local(smem_u32(&sm.mma_idle));
+            __syncwarp();
+            mbar_wait(smem_u32(&sm.mma_idle), 0);
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue warps
+        // q_out and the pools may still be read by the kernel before this one on the stream
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        const int row = warp * 32 + lane;                       // token row = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t acc_empty0 = peer_addr(smem_u32(&sm.acc_empty[0]), 0);   // + 8 per accumulator
+        int lt = 0, cached_mt = -1;
+        long long dst_row = -1;
+        for (int k = 0;; ++k, ++lt) {
+            const QkvItem w = qkv_item_of<kPairBN>(k, m_tiles, clusters, cid);
+            if (!w.width) break;
+            const int acc = lt & 1;
+            const int tok = w.mt * kPairBM + (int)rank * kBM + row;
+            const bool live = tok < a.total_tokens;
+            if (w.col0 >= kQCols && w.mt != cached_mt) {   // K/V columns: this token's cache slot
+                dst_row = live ? cache_row(a, tok) : -1;
+                cached_mt = w.mt;
+            }
+            const bool ok = wait_or_abort(smem_u32(&sm.acc_full[acc]), (lt >> 1) & 1, abort_flag, a.err);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < w.width / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(lane_base + (uint32_t)(acc * kPairBN + c * 32), v);
+                tmem_wait_ld(v);
+                uint32_t p[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) p[e / 2] = pack_bf16x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+                const int col = w.col0 + c * 32;
+                __nv_bfloat16 *dst = nullptr;
+                if (col < kQCols) {
+                    if (live) dst = static_cast<__nv_bfloat16 *>(a.q_out) + (size_t)tok * kQCols + col;
+                } else if (dst_row >= 0) {
+                    const bool is_k = col < kQCols + kKVCols;
+                    const int kvc = col - kQCols - (is_k ? 0 : kKVCols);   // KV head * 128 + dim
+                    dst = static_cast<__nv_bfloat16 *>(is_k ? a.k_pool : a.v_pool) + dst_row + kvc;
+                }
+                if (dst) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) d4[q] = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive_remote(acc_empty0 + (uint32_t)acc * 8u);
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    // Both CTAs meet before tensor memory is released or either exits: rank 0's MMAs read the
+    // peer's shared memory and write its tensor memory until mma_idle.
+    __syncthreads();
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u) : "memory");
+    }
+}
+
+cudaError_t launch_qkv_pair(const QkvArgs &a, const CUtensorMap &x_map, const CUtensorMap &w_map, int num_sms,
+                            cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static int max_clusters[64] = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kPairSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (max_clusters[dev] == 0) {
+        e = cudaFuncSetAttribute(qkv_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmemBytes);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        cfg.gridDim = dim3(2 * (num_sms / 2));
+        e = cudaOccupancyMaxActiveClusters(&n, qkv_pair_kernel, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        max_clusters[dev] = n;
+    }
+    const long long tiles = (long long)((a.total_tokens + kPairBM - 1) / kPairBM) * ((kQCols + 2 * kKVCols) / kPairBN);
+    const int clusters = (int)(tiles < max_clusters[dev] ? tiles : max_clusters[dev]);
+    cfg.gridDim = dim3(2 * clusters);
+    return cudaLaunchKernelEx(&cfg, qkv_pair_kernel, x_map, w_map, a);
+}
+
 template <int BN, int BMA>
 cudaError_t launch_qkv_bn(const QkvArgs &a, const CUtensorMap &x_map, const CUtensorMap &w_map, int num_sms,
                           cudaStream_t stream) {
@@ -386,7 +709,7 @@ cudaError_t launch_qkv_bn(const QkvArgs &a, const CUtensorMap &x_map, const CUte
 }  // namespace
 
 int qkv_tile_cols(int total_tokens) { return total_tokens <= 2 * kBM ? 64 : 256; }
-int qkv_weight_box_rows(int total_tokens) { return qkv_tile_cols(total_tokens) > 128 ? 128 : qkv_tile_cols(total_tokens); }
+int qkv_weight_box_rows(int total_tokens) { return qkv_tile_cols(total_tokens) > 128 ? kPairWBox : qkv_tile_cols(total_tokens); }
 int qkv_tile_rows_loaded(int total_tokens) { return total_tokens <= 32 ? 32 : kBM; }
 
 cudaError_t launch_qkv(const QkvArgs &a, const CUtensorMap &x_map, const CUtensorMap &w_map, int num_sms,
@@ -394,7 +717,7 @@ cudaError_t launch_qkv(const QkvArgs &a, const CUtensorMap &x_map, const CUtenso
     if (a.total_tokens == 0) return cudaSuccess;
     if (qkv_tile_rows_loaded(a.total_tokens) == 32) return launch_qkv_bn<64, 32>(a, x_map, w_map, num_sms, stream);
     if (qkv_tile_cols(a.total_tokens) == 64) return launch_qkv_bn<64, 128>(a, x_map, w_map, num_sms, stream);
-    return launch_qkv_bn<256, 128>(a, x_map, w_map, num_sms, stream);
+    return launch_qkv_pair(a, x_map, w_map, num_sms, stream);
 }
 
 }  // namespace pa
