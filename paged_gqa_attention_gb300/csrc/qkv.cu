@@ -18,7 +18,7 @@
 // applied: the pages define neither.
 //
 // GEMM on the 5th-generation tensor cores: with more than 256 tokens a pair of CTAs on two
-// SMs computes 256 tokens x 256 output columns (tcgen05.mma.cta_group::2, see the pair kernel
+// SMs computes 256 tokens x 192 output columns (tcgen05.mma.cta_group::2, see the pair kernel
 // below); with fewer, one CTA computes 128 tokens x 64 columns (the weights dominate the
 // bytes).  The hidden dimension goes in steps of 64 through a TMA ring; two accumulators in
 // tensor memory, so the epilogue of one tile overlaps the products of the next.  With at most 32 tokens only 32
@@ -53,23 +53,19 @@ constexpr uint32_t kRingBytes = 192 * 1024;    // the TMA ring's share of shared
 // weights at a third of the bandwidth).
 template <int BN, int BMA>
 struct QkvCfg {
-    static constexpr int kSub = BN == 256 ? 1 : 4;
+    static constexpr int kSub = 4;
     static constexpr uint32_t kASub = BMA * kBK * 2;
     static constexpr uint32_t kBSub = BN * kBK * 2;
     static constexpr uint32_t kABytes = kSub * kASub;
     static constexpr uint32_t kBBytes = kSub * kBSub;
     static constexpr int kStages = (int)(kRingBytes / (kABytes + kBBytes));
-    static constexpr uint32_t kTmemCols = BN == 256 ? 512 : 128;   // two accumulators
+    static constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators
     static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, false);   // both operands K-major
-    static constexpr uint32_t kIdescHalf = idesc_bf16(kBM, BN / 2, false);
-    static constexpr int kWBox = BN > 128 ? 128 : BN;                // weight rows per TMA box
+    static constexpr int kWBox = BN;                                 // weight rows per TMA box
 };
 
-// A CTA's work item: 128 tokens (tile row mt) x `width` output columns from col0; width 0
-// past the end.  Tiles of BN columns are dealt round-robin over the grid.  When the last
-// round would keep at most half of the CTAs busy and the tiles are 256 wide, each of its
-// tiles is split into two 128-column halves for twice as many CTAs, so that round takes
-// about half as long (4096 tokens: 768 tiles on 152 CTAs leave 8 for a sixth round).
+// A work item: tile row mt (its tokens) x `width` output columns from col0; width 0 past
+// the end.  Tiles are dealt round-robin over the g workers (CTAs, or CTA pairs).
 struct QkvItem {
     int mt, col0, width;
 };
@@ -77,24 +73,12 @@ struct QkvItem {
 template <int BN>
 __device__ __forceinline__ QkvItem qkv_item_of(int k, int m_tiles, int g, int c) {
     constexpr int n_tiles = (kQCols + 2 * kKVCols) / BN;
-    const int total = m_tiles * n_tiles;
-    const int rounds = (total + g - 1) / g;
-    const int last = total - (rounds - 1) * g;          // tiles of the last round
-    const bool split = BN == 256 && rounds >= 2 && 2 * last <= g;
     QkvItem w = {0, 0, 0};
-    if (!split || k < rounds - 1) {
-        const int t = c + k * g;
-        if (t >= total) return w;
-        w.mt = t / n_tiles;
-        w.col0 = (t - w.mt * n_tiles) * BN;
-        w.width = BN;
-        return w;
-    }
-    if (k > rounds - 1 || c >= 2 * last) return w;
-    const int t = (rounds - 1) * g + (c >> 1);
+    const int t = c + k * g;
+    if (t >= m_tiles * n_tiles) return w;
     w.mt = t / n_tiles;
-    w.col0 = (t - w.mt * n_tiles) * BN + (c & 1) * (BN / 2);
-    w.width = BN / 2;
+    w.col0 = (t - w.mt * n_tiles) * BN;
+    w.width = BN;
     return w;
 }
 
@@ -227,7 +211,7 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
         for (int k = 0; ok; ++k) {
             const QkvItem w = qkv_item<BN>(k, m_tiles);
             if (!w.width) break;
-            const uint32_t b_bytes = Cfg::kBBytes / (BN / w.width);
+            const uint32_t b_bytes = Cfg::kBBytes;
             for (int kc = 0; kc < ksteps; ++kc, ++it) {
                 const int s = it % kStages;
                 if (it >= kStages &&
@@ -262,7 +246,7 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
         for (int k = 0; ok; ++k, ++lt) {
             const QkvItem w = qkv_item<BN>(k, m_tiles);
             if (!w.width) break;
-            const uint32_t idesc = w.width == BN ? Cfg::kIdesc : Cfg::kIdescHalf;
+            const uint32_t idesc = Cfg::kIdesc;
             const int acc = lt & 1;
             if (lt >= 2 && !(ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&sm.acc_empty[acc]),
                                                                          ((lt >> 1) - 1) & 1, abort_flag, a.err))))
@@ -317,7 +301,7 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
             const int tok = mt * kBM + row;
             const bool live = tok < a.total_tokens;
             const int col0 = w.col0;
-            if (col0 >= kQCols && mt != cached_mt) {   // K/V columns: this token's cache slot
+            if (col0 + w.width > kQCols && mt != cached_mt) {   // K/V columns: this token's cache slot
                 dst_row = live ? cache_row(a, tok) : -1;
                 cached_mt = mt;
             }
@@ -364,22 +348,22 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
 
 
 // ------------------------------------------------------------------ CTA pairs (many tokens)
-// With many tokens the 128 x 256 tile of one CTA needs ~190 GB/s of L2 -> SM traffic at the
+// With many tokens a 128 x 256 tile of one CTA needs ~190 GB/s of L2 -> SM traffic at the
 // full tensor rate, more than one SM receives.  A pair of CTAs on two SMs (a 2-CTA cluster)
-// computes a 256 x 256 tile with tcgen05.mma.cta_group::2 (M = 256): each SM holds its own
-// 128 token rows and loads only half of the 256 weight rows, the MMA reading the other half
-// from the peer's shared memory, so each SM needs ~128 GB/s.  Rank 0's MMA warp issues for
+// computes a 256 x 192 tile with tcgen05.mma.cta_group::2 (M = 256): each SM holds its own
+// 128 token rows and loads only half of the 192 weight rows, the MMA reading the other half
+// from the peer's shared memory (~147 GB/s per SM at the full rate; 192 rather than 256
+// columns deal 4096 tokens' 512 tiles over 76 pairs in 6.7 rounds instead of 5.05).  Rank 0's MMA warp issues for
 // both; both halves of a stage complete on rank 0's barrier (pair-scoped TMA), rank 0's
 // commits reach both CTAs (multicast), and both CTAs' epilogue warps hand an accumulator back
 // on rank 0's barrier.  Each CTA's tensor memory holds its rows' two accumulators.
 constexpr int kPairBM = 2 * kBM;                       // tokens per pair tile
-constexpr int kPairBN = 256;
+constexpr int kPairBN = 192;                           // 4096 tokens: 512 tiles, 6.7 per pair
 constexpr uint32_t kPairABytes = kBM * kBK * 2;        // this CTA's 128 rows x 64: 16 KiB
-constexpr uint32_t kPairBBytes = (kPairBN / 2) * kBK * 2;   // this CTA's 128 weight rows: 16 KiB
+constexpr uint32_t kPairBBytes = (kPairBN / 2) * kBK * 2;   // this CTA's 96 weight rows: 12 KiB
 constexpr int kPairStages = (int)(kRingBytes / (kPairABytes + kPairBBytes));
-constexpr int kPairWBox = 64;                          // weight rows per TMA box
+constexpr int kPairWBox = kPairBN / 2;                 // weight rows per TMA box (a CTA's half)
 constexpr uint32_t kPairIdesc = idesc_bf16(kPairBM, kPairBN, false);
-constexpr uint32_t kPairIdescHalf = idesc_bf16(kPairBM, kPairBN / 2, false);
 
 struct QkvPairSmem {
     uint8_t a[kPairStages][kPairABytes];
@@ -544,7 +528,7 @@ qkv_pair_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
             for (int k = 0; ok; ++k, ++lt) {
                 const QkvItem w = qkv_item_of<kPairBN>(k, m_tiles, clusters, cid);
                 if (!w.width) break;
-                const uint32_t idesc = w.width == kPairBN ? kPairIdesc : kPairIdescHalf;
+                const uint32_t idesc = kPairIdesc;
                 const int acc = lt & 1;
                 if (lt >= 2 && !(ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&sm.acc_empty[acc]),
                                                                              ((lt >> 1) - 1) & 1, abort_flag, a.err))))
@@ -594,7 +578,7 @@ qkv_pair_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
             const int acc = lt & 1;
             const int tok = w.mt * kPairBM + (int)rank * kBM + row;
             const bool live = tok < a.total_tokens;
-            if (w.col0 >= kQCols && w.mt != cached_mt) {   // K/V columns: this token's cache slot
+            if (w.col0 + w.width > kQCols && w.mt != cached_mt) {   // K/V columns: this token's cache slot
                 dst_row = live ? cache_row(a, tok) : -1;
                 cached_mt = w.mt;
             }
@@ -708,15 +692,15 @@ cudaError_t launch_qkv_bn(const QkvArgs &a, const CUtensorMap &x_map, const CUte
 
 }  // namespace
 
-int qkv_tile_cols(int total_tokens) { return total_tokens <= 2 * kBM ? 64 : 256; }
-int qkv_weight_box_rows(int total_tokens) { return qkv_tile_cols(total_tokens) > 128 ? kPairWBox : qkv_tile_cols(total_tokens); }
+int qkv_tile_cols(int total_tokens) { return total_tokens <= 2 * kBM ? 64 : kPairBN; }
+int qkv_weight_box_rows(int total_tokens) { return total_tokens <= 2 * kBM ? 64 : kPairWBox; }
 int qkv_tile_rows_loaded(int total_tokens) { return total_tokens <= 32 ? 32 : kBM; }
 
 cudaError_t launch_qkv(const QkvArgs &a, const CUtensorMap &x_map, const CUtensorMap &w_map, int num_sms,
                        cudaStream_t stream) {
     if (a.total_tokens == 0) return cudaSuccess;
     if (qkv_tile_rows_loaded(a.total_tokens) == 32) return launch_qkv_bn<64, 32>(a, x_map, w_map, num_sms, stream);
-    if (qkv_tile_cols(a.total_tokens) == 64) return launch_qkv_bn<64, 128>(a, x_map, w_map, num_sms, stream);
+    if (a.total_tokens <= 2 * kBM) return launch_qkv_bn<64, 128>(a, x_map, w_map, num_sms, stream);
     return launch_qkv_pair(a, x_map, w_map, num_sms, stream);
 }
 
