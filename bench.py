@@ -52,16 +52,16 @@ HEAD_START_CYCLES = 200_000      # ~0.1 ms spin so a step's launches are all que
 TRAFFIC = {
     # one ncu capture of the batched decode step (32 sequences, 243.9 MB of K/V)
     "decode": {"bytes_per_launch": 249313536 + 4450560, "sources": ("decode.cu", "common.cuh"),
-               "sha": "0c133841a6d23e33"},
+               "sha": "0c133841a6d23e33", "workload": "batched_decode"},
     # one ncu capture of the fused 8-bit decode step (batch 32, 126 MB of 8-bit K/V)
     "decode_fp8": {"bytes_per_launch": 131073024 + 4144384, "sources": ("decode_fp8.cu", "common.cuh"),
-                   "sha": "67c2060515e80bb8"},
+                   "sha": "67c2060515e80bb8", "workload": "batched_decode_fp8"},
     # one ncu capture of the causal prefill of 4096 tokens
     "prefill": {"bytes_per_launch": 50676480 + 1682944, "sources": ("prefill.cu", "common.cuh"),
-                "sha": "b0aea3dbb3034acb"},
+                "sha": "b0aea3dbb3034acb", "workload": "causal_prefill"},
     # one ncu capture of the merged Q/K/V projection of 4096 tokens (hidden 4096)
     "qkv": {"bytes_per_launch": 117843712 + 37423616, "sources": ("qkv.cu", "common.cuh"),
-            "sha": "3d86c5c3900fc01e"},
+            "sha": "3d86c5c3900fc01e", "workload": "qkv_append"},
 }
 
 
@@ -873,9 +873,13 @@ def roofline(achieved, peak, unit, bound, traffic):
             "frac": achieved / peak if peak else None, "traffic": traffic}
 
 
-def traffic_for(kernel):
+def traffic_for(kernel, workload=None):
+    """DRAM bytes of one launch from the committed capture, or None when the sources changed
+    since, or when the line's workload is not the one captured (a launch of another size)."""
     t = TRAFFIC.get(kernel)
     if not t or source_hash(*t["sources"]) != t["sha"]:
+        return None
+    if workload is not None and workload != t["workload"]:
         return None
     return t["bytes_per_launch"]
 
@@ -930,10 +934,13 @@ def main():
         attn_ms = dist_max(r["attn_ms"], world)
         line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s",
                     ms_per_step=step_ms)
-        ach = (kv_bytes + io_bytes) / (attn_ms * 1e-3) / 1e9
-        line["roofline"] = roofline(ach, peaks["hbm_gbs"], "GB/s", "hbm", traffic_for("decode"))
+        # algorithmic bytes: every distinct K/V byte once (the shared prefix of the prefix-shared
+        # workload is one set of blocks, however many sequences read it)
+        alg_bytes = wl.unique_kv_bytes(batch) + io_bytes
+        ach = alg_bytes / (attn_ms * 1e-3) / 1e9
+        line["roofline"] = roofline(ach, peaks["hbm_gbs"], "GB/s", "hbm", traffic_for("decode", wname))
         line["roofline"]["kernel"] = "decode_kernel"
-        line["roofline"]["algorithmic_bytes_per_launch"] = kv_bytes + io_bytes
+        line["roofline"]["algorithmic_bytes_per_launch"] = alg_bytes
         line["kernels"] = {"decode_append_us": r["attn_ms"] * 1e3,
                            "two_call_step": {"kv_append_us": r["two_call_append_ms"] * 1e3,
                                              "decode_us": r["two_call_decode_ms"] * 1e3},
@@ -958,7 +965,7 @@ def main():
         step_ms = dist_max(r["graph_ms"], world)
         line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
         line["roofline"] = roofline((kv_bytes + io_bytes) / (step_ms * 1e-3) / 1e9, peaks["hbm_gbs"],
-                                    "GB/s", "hbm", traffic_for("decode"))
+                                    "GB/s", "hbm", traffic_for("decode", wname))
         line["roofline"]["kernel"] = "decode_kernel"
         line["roofline"]["algorithmic_bytes_per_launch"] = (kv_bytes + io_bytes) // layers.layers
         line["kernels"] = {"layers": layers.layers, "graph_step_us": r["graph_ms"] * 1e3,
@@ -1006,7 +1013,7 @@ def main():
         dec_ms = dist_max(r["decode_ms"], world)
         line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
         line["roofline"] = roofline((kv_bytes + io_bytes) / (dec_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
-                                    "hbm", traffic_for("decode_fp8"))
+                                    "hbm", traffic_for("decode_fp8", wname))
         line["roofline"]["kernel"] = "decode_fp8_kernel"
         line["roofline"]["algorithmic_bytes_per_launch"] = kv_bytes + io_bytes
         line["kernels"] = {"decode_append_fp8_us": r["step_ms"] * 1e3,
@@ -1029,7 +1036,7 @@ def main():
         step_ms = dist_max(r["step_ms"], world)
         line.update(value=world * flops / (step_ms * 1e-3) / 1e12, unit="TFLOP/s", ms_per_step=step_ms)
         line["roofline"] = roofline(flops / (step_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s", "tensor",
-                                    traffic_for("qkv"))
+                                    traffic_for("qkv", wname))
         line["roofline"]["kernel"] = "qkv_pair_kernel"
         line["roofline"]["algorithmic_flops_per_launch"] = flops
         # the same call for a decode step's batch: 32 new tokens, the weights dominate the bytes
@@ -1056,7 +1063,7 @@ def main():
         line.update(value=world * flops / (step_ms * 1e-3) / 1e12, unit="TFLOP/s",
                     ms_per_step=step_ms)
         line["roofline"] = roofline(flops / (attn_ms * 1e-3) / 1e12, peaks["bf16_tflops"],
-                                    "TFLOP/s", "tensor", traffic_for("prefill"))
+                                    "TFLOP/s", "tensor", traffic_for("prefill", wname))
         line["roofline"]["kernel"] = "prefill_kernel"
         line["roofline"]["algorithmic_flops_per_launch"] = flops
         line["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "prefill_us": r["attn_ms"] * 1e3}
@@ -1078,7 +1085,7 @@ def main():
         line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s",
                     ms_per_step=step_ms)
         line["roofline"] = roofline(kv_bytes / (r["decode_ms"] * 1e-3) / 1e9, peaks["hbm_gbs"],
-                                    "GB/s", "hbm", traffic_for("decode"))
+                                    "GB/s", "hbm", traffic_for("decode", wname))
         line["roofline"]["kernel"] = "decode_kernel"
         line["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "decode_us": r["decode_ms"] * 1e3,
                            "prefill_us": r["prefill_ms"] * 1e3,
@@ -1107,7 +1114,7 @@ def main():
             "workload": "causal_prefill", "prompt": 4096, "steps": psteps,
             "value": world * flops / (p_step * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": p_step,
             "roofline": dict(roofline(flops / (p_attn * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s",
-                                      "tensor", traffic_for("prefill")),
+                                      "tensor", traffic_for("prefill", "causal_prefill")),
                              kernel="prefill_kernel", algorithmic_flops_per_launch=flops),
             "kv_append_us": pr["append_ms"] * 1e3, "prefill_us": pr["attn_ms"] * 1e3,
             "gpu_launches": pr["launches"]}

@@ -29,3 +29,15 @@ def test_traffic_entries_name_existing_sources():
         # a stale entry reports null rather than a number taken on other sources
         fresh = bench.source_hash(*entry["sources"]) == entry["sha"]
         assert (bench.traffic_for(name) is not None) == fresh
+
+
+def test_traffic_only_for_the_captured_workload():
+    # a capture's bytes describe a launch of the captured size: a line of another workload
+    # (another size of launch of the same kernel) reports null
+    for name, entry in bench.TRAFFIC.items():
+        assert entry["workload"] in WORKLOADS, name
+        fresh = bench.source_hash(*entry["sources"]) == entry["sha"]
+        got = bench.traffic_for(name, entry["workload"])
+        assert got == (entry["bytes_per_launch"] if fresh else None)
+        others = [w for w in WORKLOADS if w != entry["workload"]]
+        assert all(bench.traffic_for(name, w) is None for w in others)
