@@ -56,6 +56,14 @@ __global__ void __launch_bounds__(kWarps * 32) kv_append_kernel(AppendArgs a) {
     const int t = blockIdx.x * (kWarps / 2) + (warp >> 1);
     const bool is_v = warp & 1;
     if (t >= a.total_tokens) return;
+    // The row's 2 KiB does not depend on where it goes: its loads are issued first, so they
+    // overlap the chain that finds the destination.  2 KiB = 128 x 16 B: four 16-byte vectors
+    // per lane.
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+        static_cast<const char *>(is_v ? a.v_new : a.k_new) + (size_t)t * kTokenBytes);
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = __ldg(src + lane + 32 * k);
 
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         // cu_q_lens must start at 0 and end at total_tokens
@@ -88,12 +96,6 @@ __global__ void __launch_bounds__(kWarps * 32) kv_append_kernel(AppendArgs a) {
         if (lane == 0 && !is_v) record_error(a.err, kErrDevice | kErrBadBlock);
         return;
     }
-    const uint4 *src = reinterpret_cast<const uint4 *>(
-        static_cast<const char *>(is_v ? a.v_new : a.k_new) + (size_t)t * kTokenBytes);
-    // 2 KiB = 128 x 16 B: four 16-byte vectors per lane, all loads issued first
-    uint4 v[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = __ldg(src + lane + 32 * k);
     const int slot = p % kBlock;
     if constexpr (!kFp8) {
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<char *>(is_v ? a.v_pool : a.k_pool) +
