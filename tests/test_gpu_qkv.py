@@ -144,8 +144,13 @@ def test_full_prefill_chunk_sampled_rows():
         within_tol(vf, y[r, 5120:], a[r, 5120:], f"v row {t}")
 
 
-def test_bad_block_writes_no_kv_but_keeps_q():
-    b = batch_for([(0, 40), (100, 20)], seed=68)
+@pytest.mark.parametrize("ctx_and_q", [
+    [(0, 40), (100, 20)],                       # one CTA per tile
+    [(0, 300), (100, 20)],                      # CTA pairs
+])
+def test_bad_block_writes_no_kv_but_keeps_q(ctx_and_q):
+    b = batch_for(ctx_and_q, seed=68)
+    n0 = ctx_and_q[0][1]                        # sequence 0's new tokens
     x = inputs(69, b.total_tokens)
     w = weights(70)
     bt = b.block_table.clone()
@@ -161,7 +166,7 @@ def test_bad_block_writes_no_kv_but_keeps_q():
     within_tol(qg, y[:, :4096], abs_sums(x, w)[:, :4096], "q")
     # sequence 0's rows are appended, nothing of sequence 1 is written anywhere
     touched = np.zeros((b.num_blocks, 256), dtype=bool)
-    for t, (blk, slot) in enumerate(new_slots(b)[:40]):
+    for t, (blk, slot) in enumerate(new_slots(b)[:n0]):
         touched[blk, slot] = True
     a = b.k_pool.view(torch.int16).cpu().numpy()
     o = kp0.view(torch.int16).cpu().numpy()
