@@ -43,9 +43,9 @@
  *
  * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  * are asynchronous and stream-ordered; PA_OK means "validated and launched".  The
- * decode and prefill kernels are launched as programmatic dependents of the kernel
- * before them on the stream: they may start before it has finished, and wait for it
- * before touching q, k_new, v_new, the pools, out or lse.  block_table, seq_lens and
+ * decode, prefill and projection kernels are launched as programmatic dependents of the
+ * kernel before them on the stream: they may start before it has finished, and wait for
+ * it before touching q, x, k_new, v_new, the pools, out or lse.  block_table, seq_lens and
  * cu_q_lens may be read earlier, so a kernel that writes them immediately before a
  * call must not let its dependents start early (griddepcontrol.launch_dependents).
  *
