@@ -245,6 +245,15 @@ def mean(xs):
     return sum(xs) / len(xs) if xs else float("nan")
 
 
+def pcts(xs):
+    """p10 / p50 / p90 of per-step times (ms), nearest rank."""
+    if not xs:
+        return None
+    v = sorted(xs)
+    at = lambda q: v[min(len(v) - 1, int(q * len(v)))]
+    return {"p10": at(0.1), "p50": at(0.5), "p90": at(0.9)}
+
+
 # ------------------------------------------------------------------ the two measured paths
 
 def decode_measure(batch, steps, warmup, flush_buf, stream, clocks):
@@ -277,6 +286,7 @@ def decode_measure(batch, steps, warmup, flush_buf, stream, clocks):
     spans2, _ = run_timed(two_calls, 3, max(10, min(steps, 200)), warmup, flush_buf, stream)
     ops.check_error(ws)
     return {"attn_ms": mean([s[0] for s in spans]), "step_ms": mean([s[0] for s in spans]),
+            "step_pcts": pcts([s[0] for s in spans]),
             "two_call_append_ms": mean([s[0] for s in spans2]),
             "two_call_decode_ms": mean([s[1] for s in spans2]), "wall_s": wall, "launches": steps}
 
@@ -301,7 +311,8 @@ def prefill_measure(batch, steps, warmup, flush_buf, stream, clocks):
     spans, wall = run_timed(step, 3, steps, warmup, flush_buf, stream, clocks)
     ops.check_error(ws)
     return {"append_ms": mean([s[0] for s in spans]), "attn_ms": mean([s[1] for s in spans]),
-            "step_ms": mean([s[0] + s[1] for s in spans]), "wall_s": wall, "launches": 2 * steps}
+            "step_ms": mean([s[0] + s[1] for s in spans]), "step_pcts": pcts([s[0] + s[1] for s in spans]),
+            "wall_s": wall, "launches": 2 * steps}
 
 
 def mixed_measure(batch, steps, warmup, flush_buf, stream, clocks):
@@ -332,7 +343,8 @@ def mixed_measure(batch, steps, warmup, flush_buf, stream, clocks):
     ops.check_error(ws)
     return {"append_ms": mean([s[0] for s in spans]), "decode_ms": mean([s[1] for s in spans]),
             "prefill_ms": mean([s[2] for s in spans]),
-            "step_ms": mean([sum(s) for s in spans]), "wall_s": wall, "launches": 3 * steps,
+            "step_ms": mean([sum(s) for s in spans]), "step_pcts": pcts([sum(s) for s in spans]),
+            "wall_s": wall, "launches": 3 * steps,
             "dec": dec, "pre": pre}
 
 
@@ -364,7 +376,8 @@ def layered_measure(layers, steps, warmup, flush_buf, stream, clocks):
     spans, wall = run_timed(graph_step, 2, steps, warmup, flush_buf, stream, clocks)
     spans2, _ = run_timed(eager_step, 2, max(10, min(steps, 200)), warmup, flush_buf, stream)
     ops.check_error(ws)
-    return {"graph_ms": mean([x[0] for x in spans]), "eager_ms": mean([x[0] for x in spans2]),
+    return {"graph_ms": mean([x[0] for x in spans]), "step_pcts": pcts([x[0] for x in spans]),
+            "eager_ms": mean([x[0] for x in spans2]),
             "graph": g, "ws": ws, "out": out, "launches": steps * layers.layers}
 
 
@@ -445,6 +458,7 @@ def fp8_decode_measure(batch, cache, steps, warmup, flush_buf, stream, clocks):
     spans2, _ = run_timed(two_calls, 3, max(10, min(steps, 200)), warmup, flush_buf, stream)
     ops.check_error(ws)
     return {"step_ms": mean([x[0] for x in spans]), "decode_ms": mean([x[0] for x in spans]),
+            "step_pcts": pcts([x[0] for x in spans]),
             "two_call_append_ms": mean([x[0] for x in spans2]), "two_call_decode_ms": mean([x[1] for x in spans2]),
             "wall_s": wall, "launches": steps}
 
@@ -543,7 +557,8 @@ def cascade_measure(batch, shared_blocks, steps, warmup, flush_buf, stream, cloc
     ops.check_error(ws)
     ops.check_error(cws)
     return {"append_ms": mean([x[0] for x in spans]), "cascade_ms": mean([x[1] for x in spans]),
-            "step_ms": mean([x[0] + x[1] for x in spans]), "wall_s": wall, "launches": 3 * steps}
+            "step_ms": mean([x[0] + x[1] for x in spans]), "step_pcts": pcts([x[0] + x[1] for x in spans]),
+            "wall_s": wall, "launches": 3 * steps}
 
 
 def e2e_decode_measure(batch, steps, warmup, stream):
@@ -743,7 +758,8 @@ def qkv_measure(batch, x, w, steps, warmup, flush_buf, stream, clocks):
 
     spans, wall = run_timed(step, 2, steps, warmup, flush_buf, stream, clocks)
     ops.check_error(ws)
-    return {"step_ms": mean([sp[0] for sp in spans]), "wall_s": wall, "launches": steps}
+    return {"step_ms": mean([sp[0] for sp in spans]), "step_pcts": pcts([sp[0] for sp in spans]), "wall_s": wall,
+            "launches": steps}
 
 
 def e2e_qkv_measure(batch, x, w, steps, warmup, stream):
@@ -1119,6 +1135,8 @@ def main():
             "kv_append_us": pr["append_ms"] * 1e3, "prefill_us": pr["attn_ms"] * 1e3,
             "gpu_launches": pr["launches"]}
         batch = pb
+    if r.get("step_pcts"):
+        line["step_ms_percentiles"] = r["step_pcts"]   # this rank's timed steps (rank 0 prints)
     line["clocks"] = clocks.stop()
     line["peaks"] = peaks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
