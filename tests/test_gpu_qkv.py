@@ -116,6 +116,27 @@ def test_qkv_append_matches_oracle(ctx_and_q):
     check_case(b, x, w)
 
 
+@pytest.mark.parametrize("hidden", [256, 1280])
+@pytest.mark.parametrize("ctx_and_q", [[(10, 40)], [(0, 300)]])   # one CTA per tile; CTA pairs
+def test_other_hidden_sizes(hidden, ctx_and_q):
+    """hidden is any multiple of 256: 1 and 5 ring stages per tile (one CTA), 4 and 20 (pairs)."""
+    b = batch_for(ctx_and_q, seed=80 + hidden % 7)
+    x = inputs(81, b.total_tokens, hidden)
+    w = weights(82, hidden)
+    ws = workspace_for(b)
+    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    ops.check_error(ws)
+    y = oracle.qkv_project(x.cpu(), w.cpu())
+    a = abs_sums(x, w)
+    qg = q.float().cpu().numpy().astype(np.float64).reshape(x.shape[0], -1)
+    within_tol(qg, y[:, :4096], a[:, :4096], "q")
+    for t, (blk, slot) in enumerate(new_slots(b)):
+        kf = b.k_pool[blk, slot].double().cpu().numpy().reshape(-1)
+        vf = b.v_pool[blk, slot].double().cpu().numpy().reshape(-1)
+        within_tol(kf, y[t, 4096:5120], a[t, 4096:5120], f"k row of token {t}")
+        within_tol(vf, y[t, 5120:], a[t, 5120:], f"v row of token {t}")
+
+
 def test_decode_batch_one_token_per_sequence():
     b = wl.batched_decode(device="cuda", seed=63, batch=32, hi=2000, num_blocks=300)
     check_case(b, inputs(64, b.total_tokens), weights(65))
