@@ -501,9 +501,9 @@ def e2e_fp8_measure(batch, cache, steps, warmup, stream):
     return {"step_ms": mean(times), "h2d": h2d, "d2h": d2h}
 
 
-def cpu_baseline_fp8(batch, target_s):
-    """The oracle's 8-bit attention (as it stands) over the whole batch, on a cache the
-    oracle quantised itself from the batch's bf16 context, repeated for about target_s."""
+def oracle_sample_fp8(batch):
+    """The oracle's 8-bit attention (as it stands) on a cache the oracle quantised itself from
+    the batch's bf16 context; a pass covers the first n sequences (decode: one row each)."""
     import numpy as np
     import torch
 
@@ -518,18 +518,15 @@ def cpu_baseline_fp8(batch, target_s):
     empty = [t.numpy() for t in ops.fp8_cache(batch.num_blocks, device="cpu")]
     cache = oracle.kv_append_fp8(*empty, k_rows, v_rows, batch.block_table.cpu(), cu_all, lens)
     q, bt, cu, sl = batch.q.cpu(), batch.block_table.cpu(), batch.cu_q_lens.cpu(), batch.seq_lens.cpu()
-    reps = 0
-    t0 = time.time()
-    while True:
-        oracle.attention_fp8(q, *cache, bt, cu, sl, scale=wl.SCALE)
-        reps += 1
-        if time.time() - t0 >= target_s:
-            break
-    dt = time.time() - t0
-    nbytes = sum(batch.seq_lens_host) * 8 * FP8_ROW_BYTES
-    return {"value": reps * nbytes / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"the whole batch ({batch.num_seqs} sequences x 32 heads), {reps} pass(es), {dt:.1f} s, "
-                      f"fp64 C oracle over the 8-bit cache with OpenMP"}
+    seq_bytes = [n * 8 * FP8_ROW_BYTES for n in batch.seq_lens_host]
+
+    def run(n):
+        t0 = time.time()
+        oracle.attention_fp8(q[:n], *cache, bt[:n], cu[:n + 1], sl[:n], scale=wl.SCALE)
+        return time.time() - t0, float(sum(seq_bytes[:n]))
+
+    return {"run": run, "units": batch.num_seqs, "unit": "GB/s", "scale": 1e9,
+            "what": "sequences x 32 heads of the batch", "how": "fp64 C oracle over the 8-bit cache with OpenMP"}
 
 
 def cascade_measure(batch, shared_blocks, steps, warmup, flush_buf, stream, clocks):
@@ -661,13 +658,10 @@ def e2e_measure(batch, kind, steps, warmup, stream):
 
 # ------------------------------------------------------------------ CPU oracle
 
-def cpu_baseline(batch, kind, target_s, rows_cap=None):
-    """Time the oracle (as it stands) on a bounded sample of the workload.
-
-    The sample is the first sequences of the batch whose total work fits the time
-    target (at least one sequence); the throughput is scaled to the metric's unit by
-    the sample's own bytes or flops.
-    """
+def oracle_sample_attention(batch, kind, rows_cap=None):
+    """The oracle (as it stands) on a bounded sample of the workload: (token, head) rows of the
+    first sequences (at least one; capped for prefill), each pass over n of them (evenly
+    spaced).  The throughput is scaled to the metric's unit by the rows' own bytes or flops."""
     import numpy as np
 
     import oracle
@@ -678,13 +672,8 @@ def cpu_baseline(batch, kind, target_s, rows_cap=None):
                               batch.seq_lens.cpu())
     q = batch.q.cpu()
     bt, cu, sl = batch.block_table.cpu(), batch.cu_q_lens.cpu(), batch.seq_lens.cpu()
-    cores = oracle.max_threads()
-    # rows of the sample: all heads of the first n sequences' tokens (capped for prefill)
     toks_all = []
-    n_seq = 0
-    t_probe = time.time()
     for s in range(batch.num_seqs):
-        n_seq += 1
         lo, hi = int(cu[s]), int(cu[s + 1])
         toks_all.extend(range(lo, hi))
         if rows_cap and len(toks_all) * 32 >= rows_cap:
@@ -694,35 +683,51 @@ def cpu_baseline(batch, kind, target_s, rows_cap=None):
     if rows_cap and len(toks) > rows_cap:
         sel = np.linspace(0, len(toks) - 1, rows_cap).astype(np.int64)
         toks, heads = toks[sel], heads[sel]
-    reps = 0
-    t0 = time.time()
+    # work per row: the (query, key) pairs it attends to
+    cu_l, sl_l, ql_l = [int(x) for x in cu], batch.seq_lens_host, batch.q_lens_host
+    seqs = np.searchsorted(cu_l, toks, side="right") - 1
+    pairs = np.array([sl_l[s] - ql_l[s] + (t - cu_l[s]) + 1 for t, s in zip(toks.tolist(), seqs.tolist())],
+                     dtype=np.float64)
+    # decode: KV bytes, every (sequence, KV head) context row read once -> per query-head row
+    # the share is (p + 1) tokens x 2 (K, V) x 128 x 2 B / 4 heads; prefill: 4 x 128 flops a pair
+    per_pair = (2 * 128 * 2) / 4 if kind == "decode" else 4 * 128
+
+    def run(n):
+        pick = np.linspace(0, len(toks) - 1, n).astype(np.int64) if n < len(toks) else np.arange(len(toks))
+        t0 = time.time()
+        oracle.attention(q, kp, vp, bt, cu, sl, scale=wl.SCALE, rows=(toks[pick], heads[pick]))
+        return time.time() - t0, float(pairs[pick].sum()) * per_pair
+
+    return {"run": run, "units": len(toks), "unit": "GB/s" if kind == "decode" else "TFLOP/s",
+            "scale": 1e9 if kind == "decode" else 1e12, "what": "(token, head) rows of the workload",
+            "how": "fp64 C oracle with OpenMP"}
+
+
+def timed_oracle(sample, target_s):
+    """Full passes over the sample for about target_s (at least one): the cpu_baseline object."""
+    import oracle
+
+    reps, dt, work = 0, 0.0, 0.0
     while True:
-        oracle.attention(q, kp, vp, bt, cu, sl, scale=wl.SCALE, rows=(toks, heads))
-        reps += 1
-        if time.time() - t0 >= target_s:
+        d, w = sample["run"](sample["units"])
+        reps, dt, work = reps + 1, dt + d, work + w
+        if dt >= target_s:
             break
-    dt = time.time() - t0
-    # work of the sample
-    sl_l = batch.seq_lens_host
-    cu_l = [int(x) for x in cu]
-    ql_l = batch.q_lens_host
-    pairs = 0
-    kv_tokens = 0
-    for t, h in zip(toks.tolist(), heads.tolist()):
-        s = int(np.searchsorted(cu_l, t, side="right") - 1)
-        p = sl_l[s] - ql_l[s] + (t - cu_l[s])
-        pairs += p + 1
-    if kind == "decode":
-        # decode KV bytes: every (sequence, kv-head) context row read once -> per q-head
-        # row the share is (p + 1) tokens x 2 (K, V) x 128 x 2 B / 4 heads
-        value = pairs * (2 * 128 * 2) / 4 * reps / dt / 1e9
-        unit = "GB/s"
-    else:
-        value = pairs * 4 * 128 * reps / dt / 1e12
-        unit = "TFLOP/s"
-    return {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
-            "sample": f"{len(toks)} (token, head) rows of the workload, {reps} pass(es), "
-                      f"{dt:.1f} s, fp64 C oracle with OpenMP"}
+    return {"value": work / dt / sample["scale"], "unit": sample["unit"], "cores": oracle.max_threads(),
+            "kind": "oracle", "sample": f"{sample['units']} {sample['what']}, {reps} pass(es), {dt:.1f} s, "
+                                        f"{sample['how']}"}
+
+
+def cpu_baseline(batch, kind, target_s, rows_cap=None):
+    return timed_oracle(oracle_sample_attention(batch, kind, rows_cap), target_s)
+
+
+def cpu_baseline_fp8(batch, target_s):
+    return timed_oracle(oracle_sample_fp8(batch), target_s)
+
+
+def cpu_baseline_qkv(tokens, target_s):
+    return timed_oracle(oracle_sample_qkv(tokens), target_s)
 
 
 # ------------------------------------------------------------------ merged Q/K/V projection
@@ -795,84 +800,68 @@ def e2e_qkv_measure(batch, x, w, steps, warmup, stream):
     return {"step_ms": e0.elapsed_time(e1) / steps, "h2d": x_host.numel() * 2, "d2h": q_host.numel() * 2}
 
 
-def cpu_baseline_qkv(tokens, target_s):
-    """The oracle's fp64 projection on the host cores over sampled token rows of the workload."""
+def oracle_sample_qkv(tokens):
+    """The oracle's fp64 projection on the host cores; a pass covers n of 16 token rows spread
+    over the workload's tokens."""
     import oracle
 
     x, w = qkv_inputs(tokens, 7, device="cpu")
     rows = list(range(0, tokens, max(1, tokens // 16)))[:16]
-    reps = 0
-    t0 = time.time()
-    while True:
-        oracle.qkv_project(x, w, rows=rows)
-        reps += 1
-        if time.time() - t0 >= target_s:
-            break
-    dt = time.time() - t0
-    return {"value": 2.0 * len(rows) * QKV_HIDDEN * 6144 * reps / dt / 1e12, "unit": "TFLOP/s",
-            "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{len(rows)} token rows x 6144 outputs x {QKV_HIDDEN}, {reps} pass(es), {dt:.1f} s, "
-                      f"fp64 C oracle with OpenMP"}
+
+    def run(n):
+        t0 = time.time()
+        oracle.qkv_project(x, w, rows=rows[:n])
+        return time.time() - t0, 2.0 * n * QKV_HIDDEN * 6144
+
+    return {"run": run, "units": len(rows), "unit": "TFLOP/s", "scale": 1e12,
+            "what": f"token rows x 6144 outputs x {QKV_HIDDEN}", "how": "fp64 C oracle with OpenMP"}
 
 
 # ------------------------------------------------------------------ main paths
 
 def reference_arm(args, world, rank):
-    """--impl reference: the oracle on the host cores, rank 0 only."""
+    """--impl reference: the oracle on the host cores, rank 0 only.  The inputs are prepared
+    once; one warm-up pass over the whole sample sizes each step's share of it so that the K
+    steps together take about --cpu-seconds."""
     if rank != 0:
         return
+    import oracle
     import torch
 
     from paged_gqa_attention_gb300 import workloads as wl
 
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     if args.workload == "batched_decode_fp8":
-        res = [cpu_baseline_fp8(wl.batched_decode(device=dev), max(args.cpu_seconds / max(args.steps, 1), 0.05))
-               for _ in range(args.steps)]
-        value = mean([r["value"] for r in res])
-        print(json.dumps({"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-                          "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
-                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                          "config": {"workload": args.workload},
-                          "cpu_baseline": {"value": value, "unit": "GB/s", "cores": res[0]["cores"],
-                                           "kind": "oracle", "sample": res[0]["sample"]},
-                          "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
-                                  "d2h_bytes_per_step": 0}}), flush=True)
-        return
-    if args.workload == "qkv_append":
-        res = [cpu_baseline_qkv(4096, max(args.cpu_seconds / max(args.steps, 1), 0.05)) for _ in range(args.steps)]
-        value = mean([r["value"] for r in res])
-        print(json.dumps({"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-                          "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
-                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                          "config": {"workload": args.workload},
-                          "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res[0]["cores"],
-                                           "kind": "oracle", "sample": res[0]["sample"]},
-                          "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
-                                  "d2h_bytes_per_step": 0}}), flush=True)
-        return
-    if args.workload == "layered_decode":
-        batch = wl.layered_decode(device=dev).base     # GB/s of one layer: the same per layer
-    elif args.workload == "prefix_shared_decode_cascade":
-        batch = wl.prefix_shared_decode(device=dev)    # the cascade computes the same attention
+        sample = oracle_sample_fp8(wl.batched_decode(device=dev))
+    elif args.workload == "qkv_append":
+        sample = oracle_sample_qkv(4096)
     else:
-        batch = wl.WORKLOADS[args.workload](device=dev)
-    kind = "decode" if "decode" in args.workload else "prefill"
-    if args.workload == "mixed_batch":
-        kind = "decode"
-    per_step_s = max(args.cpu_seconds / max(args.steps, 1), 0.05)
-    rows_cap = rows_cap_for(args.workload)
-    for _ in range(min(args.warmup, 1)):
-        cpu_baseline(batch, kind, 0.0, rows_cap)
-    res = [cpu_baseline(batch, kind, per_step_s, rows_cap) for _ in range(args.steps)]
-    value = mean([r["value"] for r in res])
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": res[0]["unit"],
+        if args.workload == "layered_decode":
+            batch = wl.layered_decode(device=dev).base     # GB/s of one layer: the same per layer
+        elif args.workload == "prefix_shared_decode_cascade":
+            batch = wl.prefix_shared_decode(device=dev)    # the cascade computes the same attention
+        else:
+            batch = wl.WORKLOADS[args.workload](device=dev)
+        kind = "decode" if "decode" in args.workload or args.workload == "mixed_batch" else "prefill"
+        sample = oracle_sample_attention(batch, kind, rows_cap_for(args.workload))
+    steps = max(args.steps, 1)
+    d_full, _ = sample["run"](sample["units"])                      # warm-up, sizes the steps
+    per_step = args.cpu_seconds / steps
+    n = max(1, min(sample["units"], int(sample["units"] * per_step / max(d_full, 1e-9))))
+    vals, secs = [], 0.0
+    for _ in range(steps):
+        d, w = sample["run"](n)
+        secs += d
+        vals.append(w / d / sample["scale"])
+    value = mean(vals)
+    cpu = {"value": value, "unit": sample["unit"], "cores": oracle.max_threads(), "kind": "oracle",
+           "sample": f"{n} of {sample['units']} {sample['what']} per step, {steps} steps, {secs:.1f} s, "
+                     f"{sample['how']}"}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": sample["unit"],
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.workload},
-            "cpu_baseline": {"value": value, "unit": res[0]["unit"], "cores": res[0]["cores"],
-                             "kind": "oracle", "sample": res[0]["sample"]},
-            "e2e": {"value": value, "unit": res[0]["unit"], "h2d_bytes_per_step": 0,
+            "data": "synthetic", "config": {"workload": args.workload}, "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": sample["unit"], "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
