@@ -891,10 +891,11 @@ def traffic_for(kernel, workload=None):
 
 def main():
     args = parse_args()
-    world, rank, local = dist_setup()
     if args.impl == "reference":
-        reference_arm(args, world, rank)
+        # host-only: rank 0 runs the oracle, the other ranks exit at once (no process group)
+        reference_arm(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return
+    world, rank, local = dist_setup()
     import torch
 
     from paged_gqa_attention_gb300 import build as pa_build

@@ -41,3 +41,22 @@ def test_traffic_only_for_the_captured_workload():
         assert got == (entry["bytes_per_launch"] if fresh else None)
         others = [w for w in WORKLOADS if w != entry["workload"]]
         assert all(bench.traffic_for(name, w) is None for w in others)
+
+
+def _reference_run(rank, world):
+    env = dict(os.environ, RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                           "--workload", "single_decode", "--steps", "3", "--warmup", "1",
+                           "--cpu-seconds", "0.3"], capture_output=True, text=True, env=env, timeout=600)
+
+
+def test_reference_arm_rank0_prints_other_ranks_exit():
+    import json
+    r0 = _reference_run(0, 2)
+    assert r0.returncode == 0, r0.stderr[-2000:]
+    line = json.loads(r0.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    r1 = _reference_run(1, 2)
+    assert r1.returncode == 0, r1.stderr[-2000:]
+    assert r1.stdout.strip() == ""
