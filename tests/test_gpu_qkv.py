@@ -211,3 +211,20 @@ def test_fused_append_feeds_the_decode():
     ref, _ = oracle.attention(q.cpu(), kp, vp, b.block_table.cpu(), b.cu_q_lens.cpu(), b.seq_lens.cpu(),
                               scale=wl.SCALE)
     assert_close(out, ref, "decode after the fused projection")
+
+
+@pytest.mark.parametrize("ctx_and_q", [[(0, 300)], [(0, 4096)]])
+def test_repeated_calls_are_bit_identical(ctx_and_q):
+    """The CTA-pair path is deterministic: q and the appended cache rows repeat bit for bit."""
+    b = batch_for(ctx_and_q, seed=90)
+    x = inputs(91, b.total_tokens)
+    w = weights(92)
+    ws = workspace_for(b)
+    q1 = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws).clone()
+    k1, v1 = b.k_pool.clone(), b.v_pool.clone()
+    for _ in range(3):
+        q2 = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+        ops.check_error(ws)
+        assert torch.equal(q1.view(torch.int16), q2.view(torch.int16))
+        assert torch.equal(k1.view(torch.int16), b.k_pool.view(torch.int16))
+        assert torch.equal(v1.view(torch.int16), b.v_pool.view(torch.int16))
