@@ -245,6 +245,9 @@ pa_status decode_impl(pa_shape shape, void *out, float *lse, const void *q, cons
     a.part_o = reinterpret_cast<float *>(ws + kPartialOffset);
     a.part_ml = reinterpret_cast<float *>(ws + kPartialOffset + entries * kPartialOBytes);
     a.err = reinterpret_cast<uint32_t *>(ws);
+    // A grid that fits in one wave (two CTAs per SM) with at most 8 splits a pair: the splits
+    // of a pair merge as a cluster, through its shared memory.
+    a.cluster_merge = nsplit > 1 && nsplit <= 8 && (long long)batch * kHkv * nsplit <= 2LL * sms ? 1 : 0;
     return launch_decode(a, k_map, v_map, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
                                                                                                  : PA_ERR_CUDA;
 }

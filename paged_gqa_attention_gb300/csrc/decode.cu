@@ -57,9 +57,23 @@ struct DecodeSmem {
     uint64_t empty[kStages];
     int last_cta;
     int poison;                                // a block id of this split was out of range
+    float cl_ml[kGroup][2];                    // cluster merge: this split's (m, l) per head
 };
 
 constexpr size_t kSmemBytes = sizeof(DecodeSmem) + 1024;  // + alignment slack
+
+// One log-sum-exp merge step: fold a split's (m, l, o) into the running (M, L, o4).  Written
+// once, with explicit fused multiply-adds, so that every merge path rounds identically.
+__device__ __forceinline__ void merge_split(float &M, float &L, float (&o)[4], float mk, float lk, float4 ok) {
+    const float mn = fmaxf(M, mk);
+    const float e_old = fast_exp2(M - mn), e_k = fast_exp2(mk - mn);
+    L = __fmaf_rn(lk, e_k, L * e_old);
+    o[0] = __fmaf_rn(ok.x, e_k, o[0] * e_old);
+    o[1] = __fmaf_rn(ok.y, e_k, o[1] * e_old);
+    o[2] = __fmaf_rn(ok.z, e_k, o[2] * e_old);
+    o[3] = __fmaf_rn(ok.w, e_k, o[3] * e_old);
+    M = mn;
+}
 
 // Fold the shared-prefix partials of output row (b, qh) into (M, L, o): M in log2 units,
 // o unnormalised; each partial is a normalised output with weight e^lse.
@@ -69,14 +83,7 @@ __device__ __forceinline__ void fold_prefix(const DecodeArgs &a, int b, int qh, 
         const size_t row = ((size_t)k * a.batch + b) * kHq + qh;
         const float mk = __ldcg(a.pre_lse + row) * 1.4426950408889634f;
         const float4 ok = __ldcg(reinterpret_cast<const float4 *>(a.pre_o + row * kD + d0));
-        const float mn = fmaxf(M, mk);
-        const float e_old = fast_exp2(M - mn), e_k = fast_exp2(mk - mn);
-        L = L * e_old + e_k;
-        o[0] = o[0] * e_old + ok.x * e_k;
-        o[1] = o[1] * e_old + ok.y * e_k;
-        o[2] = o[2] * e_old + ok.z * e_k;
-        o[3] = o[3] * e_old + ok.w * e_k;
-        M = mn;
+        merge_split(M, L, o, mk, 1.f, ok);   // a normalised partial: weight e^lse
     }
 }
 
@@ -95,6 +102,41 @@ __device__ __forceinline__ void store_out4(__nv_bfloat16 *dst, const float (&v)[
     *reinterpret_cast<uint2 *>(dst) = w;
 }
 
+// ------------------------------------------------------------------ cluster merge
+// Every thread of every CTA of the cluster (a pair's splits).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// kCluster: the splits of one (sequence, KV head) form a thread-block cluster (at most 8,
+// launched when the whole grid fits in one wave).  Split 0 merges the pair's partials straight
+// from its peers' shared memory after a cluster barrier, instead of through the workspace and
+// an atomic counter; splits past the context do no work but still meet the others at both
+// cluster barriers (so no barrier waits on a CTA that has left).  Same merge order and
+// arithmetic as the workspace path, so the results are bit-identical.
+template <bool kCluster>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
               const DecodeArgs a) {
@@ -130,11 +172,21 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     // (a cascade attends only past the shared prefix: the context must extend beyond it)
     if (seq_len < 1 || seq_len > a.max_blocks_per_seq * kBlock || seq_len <= a.kv_begin) {
         if (split == 0 && g == 0 && threadIdx.x == 0) record_error(a.err, kErrDevice | kErrBadSeqLen);
+        if constexpr (kCluster) {
+            cluster_sync_all();
+            cluster_sync_all();
+        }
         return;  // every CTA of this sequence takes the same exit: counters untouched
     }
     const int n_ctx = seq_len - a.kv_begin;
     const int nsplit_b = (n_ctx + a.split_tokens - 1) / a.split_tokens;
-    if (split >= nsplit_b) return;        // this split lies past the context
+    if (split >= nsplit_b) {              // this split lies past the context
+        if constexpr (kCluster) {
+            cluster_sync_all();
+            cluster_sync_all();
+        }
+        return;
+    }
     const int len_b = ((n_ctx + nsplit_b - 1) / nsplit_b + kTile - 1) / kTile * kTile;
     const int t_begin = a.kv_begin + split * len_b;
     const int t_end = min(t_begin + len_b, seq_len);
@@ -188,6 +240,11 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             // No copy may still be landing in shared memory when the CTA exits.
             for (int i = max(0, issued - kStages); i < issued; ++i)
                 mbar_wait(smem_u32(&sm.full[i % kStages]), (i / kStages) & 1);
+        }
+        if constexpr (kCluster) {
+            __syncwarp();
+            cluster_sync_all();
+            cluster_sync_all();
         }
         return;
     }
@@ -389,6 +446,48 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     const int qh = g * kGroup + h;      // query head
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + ((size_t)b * kHq + qh) * kD + d0;
 
+    if constexpr (kCluster) {
+        // This split's partial into its own shared memory: thread c alone read entries
+        // [.][h][d0 .. d0+3] of the merge area, so it may overwrite warp 0's without a barrier.
+        *reinterpret_cast<float4 *>(&sm.o[0][h][d0]) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+        if ((c & 31) == 0) {
+            sm.cl_ml[h][0] = M;
+            sm.cl_ml[h][1] = L;
+        }
+        cluster_sync_all();   // every split's partial is in place
+        if (split == 0) {
+            float GM = M, GL = L, go[4] = {o4[0], o4[1], o4[2], o4[3]};
+            if (nsplit_b > 1) {
+                // by log-sum-exp in split order, as the workspace merge (split 0 from registers)
+                GM = -INFINITY;
+                GL = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) go[k] = 0.f;
+                for (int k = 0; k < nsplit_b; ++k) {
+                    float mk = M, lk = L;
+                    float4 ok = make_float4(o4[0], o4[1], o4[2], o4[3]);
+                    if (k > 0) {
+                        mk = ld_cluster_f32(peer_addr(smem_u32(&sm.cl_ml[h][0]), (uint32_t)k));
+                        lk = ld_cluster_f32(peer_addr(smem_u32(&sm.cl_ml[h][1]), (uint32_t)k));
+                        ok = ld_cluster_f4(peer_addr(smem_u32(&sm.o[0][h][d0]), (uint32_t)k));
+                    }
+                    merge_split(GM, GL, go, mk, lk, ok);
+                }
+            }
+            if (a.pre_n > 0) {
+                fold_prefix(a, b, qh, d0, GM, GL, go);
+                if (shared_table_mismatch(a, bt, c & 31)) {
+                    if ((c & 31) == 0) record_error(a.err, kErrDevice | kErrBadBlock);
+                    GM = GL = __int_as_float(0x7fc00000);
+                }
+            }
+            store_out4(out, go, 1.f / GL);
+            if (a.lse && (c & 31) == 0) a.lse[(size_t)b * kHq + qh] = (GM + __log2f(GL)) * kLn2;
+        }
+        cluster_sync_all();   // the peers' shared memory stays until split 0 has read it
+        return;
+    }
+
     if (nsplit_b == 1) {
         if (a.pre_n > 0) {
             fold_prefix(a, b, qh, d0, M, L, o4);
@@ -447,14 +546,7 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             if (k0 + u >= nsplit_b) break;
-            const float mn = fmaxf(GM, mk[u]);
-            const float e_old = fast_exp2(GM - mn), e_k = fast_exp2(mk[u] - mn);
-            GL = GL * e_old + lk[u] * e_k;
-            go[0] = go[0] * e_old + ok[u].x * e_k;
-            go[1] = go[1] * e_old + ok[u].y * e_k;
-            go[2] = go[2] * e_old + ok[u].z * e_k;
-            go[3] = go[3] * e_old + ok[u].w * e_k;
-            GM = mn;
+            merge_split(GM, GL, go, mk[u], lk[u], ok[u]);
         }
     }
     if (a.pre_n > 0) {
@@ -476,7 +568,9 @@ cudaError_t configure_decode() {
     if (e != cudaSuccess) return e;
     static std::atomic<bool> configured[64] = {};
     if (dev < 0 || dev >= 64 || !configured[dev].load()) {
-        e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        e = cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev].store(true);
     }
@@ -496,12 +590,21 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const C
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel, k_map, v_map, a);
+    if (a.cluster_merge) {
+        if (a.nsplit < 1 || a.nsplit > 8) return cudaErrorInvalidValue;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 1;
+        attr[1].val.clusterDim.y = (unsigned)a.nsplit;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, decode_kernel<true>, k_map, v_map, a);
+    }
+    return cudaLaunchKernelEx(&cfg, decode_kernel<false>, k_map, v_map, a);
 }
 
 // ------------------------------------------------------------------ fixed scratch

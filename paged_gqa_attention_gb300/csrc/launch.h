@@ -59,6 +59,9 @@ struct DecodeArgs {
     float *part_o;         // [batch * 8 * nsplit][4][128]
     float *part_ml;        // [batch * 8 * nsplit][4][2]
     uint32_t *err;
+    // Decode kernel only: 1 = the splits of a (sequence, KV head) form a cluster (nsplit <= 8)
+    // and merge through its shared memory; the counters and partials are not used.
+    int32_t cluster_merge;
 };
 
 struct PrefillArgs {

@@ -262,3 +262,20 @@ def test_decode_step_from_host_buffers(pinned):
         assert_close(out_host, ref, "decode step from host buffers")
         assert_lse_close(lse_host, ref_lse, "decode step from host buffers")
     assert np.array_equal(b.k_pool.view(torch.int16).cpu().numpy().view(np.uint16), kp)
+
+
+def test_cluster_merge_with_an_invalid_length():
+    """A sequence whose length is invalid on the cluster-merge path (short contexts, one wave):
+    the error is reported, its output is left alone, the other sequence is still right."""
+    b = decode_batch([300, 200], seed=31, maxb=2)
+    ref, _ = oracle_attention(b)
+    sl = b.seq_lens.clone()
+    sl[0] = 0                                   # invalid: no context at all
+    ws = workspace_for(b)
+    out = torch.full_like(b.q, 7.0)
+    ops.paged_attn_decode(b.q, b.k_pool, b.v_pool, b.block_table, sl, ws, out=out)
+    with pytest.raises(ops.PagedAttnError) as e:
+        ops.check_error(ws)
+    assert e.value.status == 4
+    assert torch.all(out[0] == 7.0)
+    assert_close(out[1:], ref[1:], "the valid sequence")
