@@ -51,8 +51,8 @@ HEAD_START_CYCLES = 200_000      # ~0.1 ms spin so a step's launches are all que
 # whose sources changed since reports traffic null.
 TRAFFIC = {
     # one ncu capture of the batched decode step (32 sequences, 243.9 MB of K/V)
-    "decode": {"bytes_per_launch": 249313536 + 4450560, "sources": ("decode.cu", "common.cuh"),
-               "sha": "0c133841a6d23e33", "workload": "batched_decode"},
+    "decode": {"bytes_per_launch": 249330688 + 3646208, "sources": ("decode.cu", "common.cuh"),
+               "sha": "c142d4ea0a9be97f", "workload": "batched_decode"},
     # one ncu capture of the fused 8-bit decode step (batch 32, 126 MB of 8-bit K/V)
     "decode_fp8": {"bytes_per_launch": 131073024 + 4144384, "sources": ("decode_fp8.cu", "common.cuh"),
                    "sha": "67c2060515e80bb8", "workload": "batched_decode_fp8"},
