@@ -347,8 +347,9 @@ pa_status pa_decode_graph_destroy(pa_decode_graph *graph);
  * PA_ERR_WORKSPACE and launches nothing.
  *
  * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before any
- * stream capture.  Every call shares the one array and first clears, on `stream`, the
+ * (cudaGetSymbolAddress) with that device current, and looks it up again if the device's
+ * context has been destroyed and created anew since (cudaDeviceReset); make that first
+ * call before any stream capture.  Every call shares the one array and first clears, on `stream`, the
  * parts that must start at zero; calls whose executions may overlap on the GPU (other
  * streams, other host threads) race on it and must be serialised by the caller.
  *

@@ -1,8 +1,8 @@
 // decode.cu -- batched single-token GQA attention over the paged KV cache.
 //
 // Page "扔掉 vLLM！从零构建 Qwen3-8B 推理引擎，C++/CUDA 实现性能追平 98%":
-//   §4.4.2 gqa_decode_attn  the query heads of one group share one KV read
-//                           (head_idx = g * heads_per_group + h);
+//   §4.4.2 gqa_decode_attn  the query heads of one group share one KV read: the 4
+//                           query heads of KV group g are 4g .. 4g + 3;
 //   §4.3.1                  KV in 256-token blocks reached through a block table.
 // Page "从零手搓AI推理引擎：避开调包陷阱的工程实践指南" §2.2: softmax(QK^T/sqrt(d))V with
 // the maximum subtracted first.
@@ -30,6 +30,8 @@
 // stream, so its launch and prologue overlap e.g. the kv_append that precedes it.
 #include <atomic>
 #include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "launch.h"
@@ -602,7 +604,15 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const C
         attr[1].val.clusterDim.y = (unsigned)a.nsplit;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
-        return cudaLaunchKernelEx(&cfg, decode_kernel<true>, k_map, v_map, a);
+        e = cudaLaunchKernelEx(&cfg, decode_kernel<true>, k_map, v_map, a);
+        if (e != cudaErrorLaunchOutOfResources && e != cudaErrorInvalidClusterSize && e != cudaErrorNotSupported &&
+            e != cudaErrorCooperativeLaunchTooLarge)
+            return e;
+        // The cluster was refused (e.g. SMs partitioned or shared with other work): clear the
+        // launch error and merge through the workspace and counters instead, which gives the
+        // same bits (both merges run the same steps in the same order).
+        cudaGetLastError();
+        cfg.numAttrs = 1;
     }
     return cudaLaunchKernelEx(&cfg, decode_kernel<false>, k_map, v_map, a);
 }
@@ -615,12 +625,44 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map, const C
 // until the process exits, and all calls share them.
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
+// Unique ID of the context current on this thread (0 if none is current or the driver
+// cannot say).  The driver entry points are looked up once through the runtime, so the
+// library needs no link-time dependency on libcuda.
+static unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
 void *static_scratch_address(cudaError_t *status) {
     // In host code g_static_scratch names a host-side stand-in, not device memory: the
-    // device address comes from cudaGetSymbolAddress, looked up once per device while
-    // that device is current, and cached.
+    // device address comes from cudaGetSymbolAddress, looked up while the device is
+    // current.  The address belongs to the context the module was loaded into, so it is
+    // cached per context (a context torn down and created again, e.g. after
+    // cudaDeviceReset, gets a fresh lookup); where the context cannot be identified it is
+    // looked up on every call (the lookup allocates nothing).
     static std::mutex mu;
-    static void *cached[64] = {};
+    struct Entry {
+        unsigned long long ctx;
+        void *ptr;
+    };
+    static Entry cache[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= 64) {
@@ -628,17 +670,22 @@ void *static_scratch_address(cudaError_t *status) {
         return nullptr;
     }
     std::lock_guard<std::mutex> lock(mu);
-    if (!cached[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (e != cudaSuccess) {
-            *status = e;
-            return nullptr;
-        }
-        cached[dev] = p;
+    unsigned long long ctx = current_context_id();
+    if (ctx != 0 && cache[dev].ctx == ctx && cache[dev].ptr) {
+        *status = cudaSuccess;
+        return cache[dev].ptr;
     }
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);   // also creates the context if needed
+    if (e != cudaSuccess) {
+        *status = e;
+        return nullptr;
+    }
+    if (ctx == 0) ctx = current_context_id();
+    cache[dev].ctx = ctx;
+    cache[dev].ptr = ctx != 0 ? p : nullptr;
     *status = cudaSuccess;
-    return cached[dev];
+    return p;
 }
 
 }  // namespace pa

@@ -146,7 +146,8 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
 cudaError_t launch_wait_selftest(uint32_t *err, uint64_t limit_ns, cudaStream_t stream);
 
 // Device address of the file-scope scratch of paged_attn_decode_static on the current
-// device (looked up on the first call per device); nullptr and *status set on failure.
+// device (looked up on the first call per device and context); nullptr and *status set on
+// failure.
 void *static_scratch_address(cudaError_t *status);
 
 // Tile sizes the tensor maps must be encoded with.

@@ -169,33 +169,6 @@ def test_empty_batch_is_a_no_op():
     assert out.shape[0] == 0
 
 
-def test_prefix_shared_decode_full_size_sampled():
-    """Batch 128 x 32768 with the first 64 blocks shared by every table: all rows of a few
-    sequences against the oracle.  Only the blocks those sequences use are copied to the
-    host (a compact pool with re-numbered tables), before the GPU append; the oracle
-    applies its own append to that copy."""
-    import oracle
-    b = wl.prefix_shared_decode(device="cuda")
-    seqs = [0, 77, 127]
-    rows = b.block_table[seqs]                              # [3, 128]
-    used = torch.unique(rows[rows >= 0])
-    remap = torch.full((b.num_blocks,), -1, dtype=torch.int64, device="cuda")
-    remap[used] = torch.arange(used.numel(), device="cuda")
-    small_bt = remap[rows.long()].to(torch.int32).cpu()
-    cu = torch.arange(len(seqs) + 1, dtype=torch.int32)
-    kp, vp = oracle.kv_append(b.k_pool.index_select(0, used).cpu(), b.v_pool.index_select(0, used).cpu(),
-                              b.k_new[seqs].cpu(), b.v_new[seqs].cpu(), small_bt, cu,
-                              b.seq_lens[seqs].cpu())
-    ref, ref_lse = oracle.attention(b.q[seqs].cpu(), kp, vp, small_bt, cu, b.seq_lens[seqs].cpu(),
-                                    scale=wl.SCALE)
-    ws = workspace_for(b)
-    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
-    out, lse = run_decode(b, ws)
-    assert torch.isfinite(out.float()).all()
-    assert_close(out[seqs], ref, "prefix-shared decode (sampled sequences)")
-    assert_lse_close(lse[seqs], ref_lse, "prefix-shared decode (sampled sequences)")
-
-
 @pytest.mark.parametrize("seed", [1, 3])
 def test_fused_append_decode_equals_the_two_calls(seed):
     """paged_attn_decode_append == kv_append followed by paged_attn_decode: identical pools
@@ -279,3 +252,31 @@ def test_cluster_merge_with_an_invalid_length():
     assert e.value.status == 4
     assert torch.all(out[0] == 7.0)
     assert_close(out[1:], ref[1:], "the valid sequence")
+
+
+@pytest.mark.parametrize("lens", [[512, 100, 1, 300], [65, 512, 257, 2]])
+def test_fused_append_decode_on_the_cluster_merge_path(lens):
+    """Short contexts of mixed lengths (tables 2 blocks wide, at most 4 sequences): the grid
+    fits in one wave with 8 splits of 64 tokens a pair, so the splits merge as a cluster;
+    sequences shorter than 512 leave splits idle (they only meet the others at the cluster
+    barriers).  The fused append + decode must match the oracle, leave the pools bit-identical
+    to kv_append's, and give the same bits as kv_append followed by paged_attn_decode."""
+    b = wl.build_batch("cluster_fused", 41 + len(lens), lens, [1] * len(lens), num_blocks=12,
+                       device="cuda", max_blocks_per_seq=2)
+    kp, vp = oracle_appended_pools(b)
+    ref, ref_lse = oracle_attention(b, kp, vp)
+    ws = workspace_for(b)
+    k2, v2 = b.k_pool.clone(), b.v_pool.clone()
+    lse = torch.empty(b.num_seqs, 32, dtype=torch.float32, device="cuda")
+    out = ops.paged_attn_decode_append(b.q, b.k_new, b.v_new, k2, v2, b.block_table, b.seq_lens, ws, lse=lse)
+    ops.check_error(ws)
+    assert np.array_equal(k2.view(torch.int16).cpu().numpy().view(np.uint16), kp)
+    assert np.array_equal(v2.view(torch.int16).cpu().numpy().view(np.uint16), vp)
+    assert_close(out, ref, f"fused cluster path {lens}")
+    assert_lse_close(lse, ref_lse, f"fused cluster path {lens}")
+    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    lse2 = torch.empty_like(lse)
+    out2 = ops.paged_attn_decode(b.q, b.k_pool, b.v_pool, b.block_table, b.seq_lens, ws, lse=lse2)
+    ops.check_error(ws)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse, lse2)
