@@ -25,3 +25,18 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With PA_PARITY_REPORT set to a path, write the realised error of every GPU-vs-oracle
+    comparison of the run there (JSON), so the margin left under each bar can be read."""
+    path = os.environ.get("PA_PARITY_REPORT")
+    if not path:
+        return
+    helpers = sys.modules.get("gpu_helpers")
+    if helpers is None:
+        return
+    import json
+    with open(path, "w") as f:
+        json.dump({"bars": {"max_abs": helpers.MAX_ABS, "rel_rms": helpers.REL_RMS, "lse_abs": helpers.LSE_ABS},
+                   "comparisons": helpers.REPORT}, f, indent=1)

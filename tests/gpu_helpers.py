@@ -37,9 +37,16 @@ def errors(gpu_out: torch.Tensor, ref: np.ndarray):
     return max_abs, rel
 
 
+# Realised errors of every comparison made in this process, in order: (what, kind, values).
+# The session hook in conftest.py writes them out when PA_PARITY_REPORT names a file.
+REPORT = []
+
+
 def assert_close(gpu_out, ref, what=""):
     assert np.isfinite(gpu_out.detach().float().cpu().numpy()).all(), f"{what}: non-finite output"
     max_abs, rel = errors(gpu_out, ref)
+    REPORT.append({"what": what, "kind": "out", "max_abs": max_abs, "rel_rms": rel,
+                   "elements": int(np.asarray(ref).size)})
     assert max_abs <= MAX_ABS and rel <= REL_RMS, f"{what}: max_abs={max_abs:.3e} rel_rms={rel:.3e}"
     return max_abs, rel
 
@@ -47,6 +54,7 @@ def assert_close(gpu_out, ref, what=""):
 def assert_lse_close(gpu_lse, ref, what=""):
     g = gpu_lse.detach().double().cpu().numpy()
     err = float(np.max(np.abs(g - ref))) if g.size else 0.0
+    REPORT.append({"what": what, "kind": "lse", "max_abs": err, "elements": int(np.asarray(ref).size)})
     assert err <= LSE_ABS, f"{what}: lse max_abs={err:.3e}"
 
 

@@ -64,29 +64,6 @@ def test_cascade_repeated_calls_on_one_workspace():
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
 
 
-def test_cascade_full_size_prefix_shared_sampled():
-    """Batch 128 x 32768 with 64 shared blocks: every row of three sequences against the
-    oracle (a compact host copy of the blocks they use, as in the plain decode's test)."""
-    b = wl.prefix_shared_decode(device="cuda")
-    seqs = [0, 64, 127]
-    rows = b.block_table[seqs]
-    used = torch.unique(rows[rows >= 0])
-    remap = torch.full((b.num_blocks,), -1, dtype=torch.int64, device="cuda")
-    remap[used] = torch.arange(used.numel(), device="cuda")
-    small_bt = remap[rows.long()].to(torch.int32).cpu()
-    cu = torch.arange(len(seqs) + 1, dtype=torch.int32)
-    kp, vp = oracle.kv_append(b.k_pool.index_select(0, used).cpu(), b.v_pool.index_select(0, used).cpu(),
-                              b.k_new[seqs].cpu(), b.v_new[seqs].cpu(), small_bt, cu, b.seq_lens[seqs].cpu())
-    ref, ref_lse = oracle.attention(b.q[seqs].cpu(), kp, vp, small_bt, cu, b.seq_lens[seqs].cpu(), scale=wl.SCALE)
-    ws = workspace_for(b)
-    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
-    out, lse, cws = run_cascade(b, b.info["shared_blocks"])
-    ops.check_error(cws)
-    assert torch.isfinite(out.float()).all()
-    assert_close(out[seqs], ref, "cascade, prefix-shared full size (sampled sequences)")
-    assert_lse_close(lse[seqs], ref_lse, "cascade, prefix-shared full size (sampled sequences)")
-
-
 def test_cascade_rejects_a_table_that_does_not_share_the_prefix():
     b = shared_case([700, 900, 1100], 2, seed=76)
     kp, vp = oracle_appended_pools(b)

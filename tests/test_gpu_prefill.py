@@ -53,44 +53,6 @@ def test_prefill_matches_oracle(ctx_and_q):
     assert_lse_close(lse, ref_lse, f"prefill {ctx_and_q}")
 
 
-def test_causal_prefill_4096_sampled():
-    """The 4096-token causal prefill at full size, checked on sampled rows."""
-    b = wl.causal_prefill(device="cuda")
-    kp, vp = oracle_appended_pools(b)
-    out, lse = append_and_prefill(b)
-    g = np.random.default_rng(0)
-    toks = np.concatenate([np.arange(0, 40), np.arange(4056, 4096), g.integers(0, 4096, 176)])
-    heads = g.integers(0, 32, len(toks))
-    ref, ref_lse = oracle_attention(b, kp, vp, rows=(toks, heads))
-    sel = out[torch.as_tensor(toks, device="cuda"), torch.as_tensor(heads, device="cuda")]
-    assert_close(sel, ref, "causal_prefill sampled rows")
-    sel_lse = lse[torch.as_tensor(toks, device="cuda"), torch.as_tensor(heads, device="cuda")]
-    assert_lse_close(sel_lse, ref_lse, "causal_prefill sampled lse")
-    assert torch.isfinite(out.float()).all()
-
-
-def test_mixed_batch_full_size():
-    """One append for 120 decode tokens + 8 chunks of 512, then decode and prefill."""
-    b = wl.mixed_batch(device="cuda")
-    kp, vp = oracle_appended_pools(b)
-    ws = workspace_for(b)
-    ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
-    dec = b.select(slice(0, 120))
-    pre = b.select(slice(120, 128))
-    out_d = ops.paged_attn_decode(dec.q, dec.k_pool, dec.v_pool, dec.block_table, dec.seq_lens, ws)
-    out_p = ops.paged_attn_prefill(pre.q, pre.k_pool, pre.v_pool, pre.block_table, pre.cu_q_lens,
-                                   pre.seq_lens, pre.max_q_len, ws)
-    ops.check_error(ws)
-    ref_d, _ = oracle_attention(dec, kp, vp)
-    assert_close(out_d, ref_d, "mixed: decode part")
-    g = np.random.default_rng(1)
-    toks = g.integers(0, pre.total_tokens, 256)
-    heads = g.integers(0, 32, 256)
-    ref_p, _ = oracle_attention(pre, kp, vp, rows=(toks, heads))
-    sel = out_p[torch.as_tensor(toks, device="cuda"), torch.as_tensor(heads, device="cuda")]
-    assert_close(sel, ref_p, "mixed: prefill part (sampled)")
-
-
 def test_decode_equals_last_prefill_row():
     b = small_batch([(0, 700)], seed=21)
     out, _ = append_and_prefill(b)
