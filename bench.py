@@ -76,6 +76,8 @@ def parse_args():
                             "prefix_shared_decode_cascade", "qkv_append"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement")
+    p.add_argument("--only-main", action="store_true",
+                   help="measure only the named workload (no sub-objects for the other configurations)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target duration of the CPU oracle sample")
@@ -658,33 +660,57 @@ def e2e_measure(batch, kind, steps, warmup, stream):
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_sample_attention(batch, kind, rows_cap=None):
+def compact_subset(batch, n_seqs):
+    """Host copy of the first n_seqs sequences of a batch with only the pool blocks they use
+    (tables renumbered to a compact pool): input preparation for the oracle's sample, so that
+    a sample of a large workload does not copy its whole pools.  Pure data movement."""
+    import torch
+
+    from paged_gqa_attention_gb300 import workloads as wl
+
+    sub = batch.select(slice(0, n_seqs))
+    rows = sub.block_table
+    used = torch.unique(rows[rows >= 0])
+    remap = torch.full((batch.num_blocks,), -1, dtype=torch.int64, device=rows.device)
+    remap[used] = torch.arange(used.numel(), device=rows.device)
+    bt = torch.where(rows >= 0, remap[rows.clamp(min=0).long()], torch.full_like(rows.long(), -1))
+    return wl.Batch(name=sub.name, q=sub.q.cpu(), k_new=sub.k_new.cpu(), v_new=sub.v_new.cpu(),
+                    k_pool=batch.k_pool.index_select(0, used).cpu(),
+                    v_pool=batch.v_pool.index_select(0, used).cpu(),
+                    block_table=bt.to(torch.int32).cpu(), seq_lens=sub.seq_lens.cpu(),
+                    cu_q_lens=sub.cu_q_lens.cpu(), max_q_len=sub.max_q_len,
+                    seq_lens_host=list(sub.seq_lens_host), q_lens_host=list(sub.q_lens_host),
+                    info=dict(sub.info))
+
+
+def oracle_sample_attention(batch, kind, rows_cap=None, threads=0):
     """The oracle (as it stands) on a bounded sample of the workload: (token, head) rows of the
     first sequences (at least one; capped for prefill), each pass over n of them (evenly
-    spaced).  The throughput is scaled to the metric's unit by the rows' own bytes or flops."""
+    spaced).  The throughput is scaled to the metric's unit by the rows' own bytes or flops.
+    threads: OpenMP threads of the oracle (0 = every core)."""
     import numpy as np
 
     import oracle
     from paged_gqa_attention_gb300 import workloads as wl
 
-    kp, vp = oracle.kv_append(batch.k_pool.cpu(), batch.v_pool.cpu(), batch.k_new.cpu(),
-                              batch.v_new.cpu(), batch.block_table.cpu(), batch.cu_q_lens.cpu(),
-                              batch.seq_lens.cpu())
-    q = batch.q.cpu()
-    bt, cu, sl = batch.block_table.cpu(), batch.cu_q_lens.cpu(), batch.seq_lens.cpu()
-    toks_all = []
-    for s in range(batch.num_seqs):
-        lo, hi = int(cu[s]), int(cu[s + 1])
-        toks_all.extend(range(lo, hi))
-        if rows_cap and len(toks_all) * 32 >= rows_cap:
+    n_seqs, rows_so_far = 0, 0
+    for ql in batch.q_lens_host:
+        n_seqs += 1
+        rows_so_far += ql * 32
+        if rows_cap and rows_so_far >= rows_cap:
             break
+    sb = compact_subset(batch, n_seqs)
+    kp, vp = oracle.kv_append(sb.k_pool, sb.v_pool, sb.k_new, sb.v_new, sb.block_table, sb.cu_q_lens,
+                              sb.seq_lens)
+    q, bt, cu, sl = sb.q, sb.block_table, sb.cu_q_lens, sb.seq_lens
+    toks_all = list(range(int(cu[-1])))
     toks = np.repeat(np.array(toks_all, dtype=np.int32), 32)
     heads = np.tile(np.arange(32, dtype=np.int32), len(toks_all))
     if rows_cap and len(toks) > rows_cap:
         sel = np.linspace(0, len(toks) - 1, rows_cap).astype(np.int64)
         toks, heads = toks[sel], heads[sel]
     # work per row: the (query, key) pairs it attends to
-    cu_l, sl_l, ql_l = [int(x) for x in cu], batch.seq_lens_host, batch.q_lens_host
+    cu_l, sl_l, ql_l = [int(x) for x in cu], sb.seq_lens_host, sb.q_lens_host
     seqs = np.searchsorted(cu_l, toks, side="right") - 1
     pairs = np.array([sl_l[s] - ql_l[s] + (t - cu_l[s]) + 1 for t, s in zip(toks.tolist(), seqs.tolist())],
                      dtype=np.float64)
@@ -695,12 +721,33 @@ def oracle_sample_attention(batch, kind, rows_cap=None):
     def run(n):
         pick = np.linspace(0, len(toks) - 1, n).astype(np.int64) if n < len(toks) else np.arange(len(toks))
         t0 = time.time()
-        oracle.attention(q, kp, vp, bt, cu, sl, scale=wl.SCALE, rows=(toks[pick], heads[pick]))
+        oracle.attention(q, kp, vp, bt, cu, sl, scale=wl.SCALE, rows=(toks[pick], heads[pick]),
+                         num_threads=threads)
         return time.time() - t0, float(pairs[pick].sum()) * per_pair
 
     return {"run": run, "units": len(toks), "unit": "GB/s" if kind == "decode" else "TFLOP/s",
-            "scale": 1e9 if kind == "decode" else 1e12, "what": "(token, head) rows of the workload",
-            "how": "fp64 C oracle with OpenMP"}
+            "scale": 1e9 if kind == "decode" else 1e12,
+            "what": f"(token, head) rows of the first {n_seqs} sequence(s) of the workload",
+            "how": "fp64 C oracle with OpenMP", "threads": threads}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 def timed_oracle(sample, target_s):
@@ -713,13 +760,15 @@ def timed_oracle(sample, target_s):
         reps, dt, work = reps + 1, dt + d, work + w
         if dt >= target_s:
             break
-    return {"value": work / dt / sample["scale"], "unit": sample["unit"], "cores": oracle.max_threads(),
-            "kind": "oracle", "sample": f"{sample['units']} {sample['what']}, {reps} pass(es), {dt:.1f} s, "
-                                        f"{sample['how']}"}
+    threads = sample.get("threads") or oracle.max_threads()
+    return {"value": work / dt / sample["scale"], "unit": sample["unit"], "cores": threads,
+            "kind": "oracle", "cpu_model": cpu_model(),
+            "sample": f"{sample['units']} {sample['what']}, {reps} pass(es), {dt:.1f} s, {sample['how']}"
+                      f" on {threads} thread(s)"}
 
 
-def cpu_baseline(batch, kind, target_s, rows_cap=None):
-    return timed_oracle(oracle_sample_attention(batch, kind, rows_cap), target_s)
+def cpu_baseline(batch, kind, target_s, rows_cap=None, threads=0):
+    return timed_oracle(oracle_sample_attention(batch, kind, rows_cap, threads), target_s)
 
 
 def cpu_baseline_fp8(batch, target_s):
@@ -889,6 +938,260 @@ def traffic_for(kernel, workload=None):
     return t["bytes_per_launch"]
 
 
+DEFAULT_SUBS = ("single_decode", "causal_prefill", "mixed_batch", "prefix_shared_decode",
+                "prefix_shared_decode_cascade", "batched_decode_fp8", "layered_decode", "qkv_append")
+
+
+def load_workload(wname):
+    """The batch (and, for the layered step, the layers) a workload measures, on the GPU."""
+    from paged_gqa_attention_gb300 import workloads as wl
+
+    layers = wl.layered_decode(device="cuda") if wname == "layered_decode" else None
+    if layers is not None:
+        return layers.base, layers
+    if wname == "batched_decode_fp8":
+        return wl.batched_decode(device="cuda"), None
+    if wname == "prefix_shared_decode_cascade":
+        return wl.prefix_shared_decode(device="cuda"), None
+    if wname == "qkv_append":
+        return wl.causal_prefill(device="cuda"), None   # the 4096-token prompt's new tokens
+    return wl.WORKLOADS[wname](device="cuda"), None
+
+
+def warm_l2_latency(batch, stream, steps=200):
+    """The fused decode step back to back with nothing flushed in between (the whole working
+    set stays in L2): mean latency of one call, in us."""
+    import torch
+
+    from paged_gqa_attention_gb300 import ops
+
+    ws = ops.make_workspace(batch.num_seqs, batch.max_blocks_per_seq)
+    out = torch.empty_like(batch.q)
+    call = lambda: ops.paged_attn_decode_append(batch.q, batch.k_new, batch.v_new, batch.k_pool, batch.v_pool,
+                                                batch.block_table, batch.seq_lens, ws, out=out)
+    for _ in range(20):
+        call()
+    torch.cuda.synchronize()
+    # every call is queued behind a device spin first, so that the events bracket device time
+    # and not the host's launch rate
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda._sleep(HEAD_START_CYCLES * max(1, steps // 2))
+    for e0, e1 in ev:
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ops.check_error(ws)
+    v = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    return {"mean_us": mean(v), "p50_us": pcts(v)["p50"], "steps": steps,
+            "how": "fused append + decode, all calls queued behind a device spin, no L2 flush between "
+                   "them (the 2 MiB context stays in L2), CUDA events around each call"}
+
+
+def measure(wname, steps, warmup, e2e_steps, peaks, flush_buf, stream, clocks, world):
+    """One workload's entry of the JSON line: value, unit, ms_per_step, roofline, kernels,
+    gpu_launches, e2e and config.  Returns (entry, kind, batch, layers)."""
+    import torch
+
+    from paged_gqa_attention_gb300 import workloads as wl
+
+    batch, layers = load_workload(wname)
+    e = {}
+    cfg = {"workload": wname, **batch.info, "heads": "32 q / 8 kv x 128", "block_tokens": 256,
+           **({"layers": layers.layers} if layers is not None else {}),
+           "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write + read)",
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+    if wname in ("single_decode", "batched_decode", "prefix_shared_decode"):
+        r = decode_measure(batch, steps, warmup, flush_buf, stream, clocks)
+        kv_bytes = batch.kv_bytes()
+        io_bytes = batch.num_seqs * 32 * 128 * 2 * 2 + batch.num_seqs * (batch.max_blocks_per_seq + 1) * 4
+        step_ms = dist_max(r["step_ms"], world)
+        attn_ms = dist_max(r["attn_ms"], world)
+        e.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
+        # algorithmic bytes: every distinct K/V byte once (the shared prefix of the prefix-shared
+        # workload is one set of blocks, however many sequences read it)
+        alg_bytes = wl.unique_kv_bytes(batch) + io_bytes
+        ach = alg_bytes / (attn_ms * 1e-3) / 1e9
+        e["roofline"] = roofline(ach, peaks["hbm_gbs"], "GB/s", "hbm", traffic_for("decode", wname))
+        e["roofline"]["kernel"] = "decode_kernel"
+        e["roofline"]["algorithmic_bytes_per_launch"] = alg_bytes
+        e["kernels"] = {"decode_append_us": r["attn_ms"] * 1e3,
+                        "two_call_step": {"kv_append_us": r["two_call_append_ms"] * 1e3,
+                                          "decode_us": r["two_call_decode_ms"] * 1e3},
+                        "kv_bytes_per_step": kv_bytes,
+                        "unique_kv_bytes": wl.unique_kv_bytes(batch)}
+        if wname == "prefix_shared_decode":
+            uniq = wl.unique_kv_bytes(batch)
+            e["kernels"]["unique_kv_gbs"] = uniq / (attn_ms * 1e-3) / 1e9
+            e["kernels"]["unique_kv_frac"] = e["kernels"]["unique_kv_gbs"] / peaks["hbm_gbs"]
+        if wname == "single_decode":
+            e["warm_l2_latency"] = warm_l2_latency(batch, stream)
+        e["gpu_launches"] = r["launches"]
+        x = e2e_decode_measure(batch, e2e_steps, 5, stream)
+        x_ms = dist_max(x["step_ms"], world)
+        e["e2e"] = {"value": world * kv_bytes / (x_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms,
+                    "via": "pa_decode_step_host (C ABI, host buffers)"}
+        kind = "decode"
+    elif wname == "layered_decode":
+        r = layered_measure(layers, steps, warmup, flush_buf, stream, clocks)
+        kv_bytes = layers.kv_bytes()
+        io_bytes = layers.layers * (batch.num_seqs * 32 * 128 * 2 * 2 +
+                                    batch.num_seqs * (batch.max_blocks_per_seq + 1) * 4)
+        step_ms = dist_max(r["graph_ms"], world)
+        e.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
+        e["roofline"] = roofline((kv_bytes + io_bytes) / (step_ms * 1e-3) / 1e9, peaks["hbm_gbs"],
+                                 "GB/s", "hbm", traffic_for("decode", wname))
+        e["roofline"]["kernel"] = "decode_kernel"
+        e["roofline"]["algorithmic_bytes_per_launch"] = (kv_bytes + io_bytes) // layers.layers
+        e["kernels"] = {"layers": layers.layers, "graph_step_us": r["graph_ms"] * 1e3,
+                        "graph_us_per_layer": r["graph_ms"] * 1e3 / layers.layers,
+                        "one_call_per_layer_step_us": r["eager_ms"] * 1e3,
+                        "one_call_per_layer_us_per_layer": r["eager_ms"] * 1e3 / layers.layers,
+                        "kv_bytes_per_step": kv_bytes}
+        e["gpu_launches"] = r["launches"]
+        x = e2e_layered_measure(layers, r["graph"], r["out"], e2e_steps, 5, stream)
+        x_ms = dist_max(x["step_ms"], world)
+        e["e2e"] = {"value": world * kv_bytes / (x_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
+        r["graph"].close()
+        kind = "decode"
+    elif wname == "prefix_shared_decode_cascade":
+        shared = batch.info["shared_blocks"]
+        r = cascade_measure(batch, shared, steps, warmup, flush_buf, stream, clocks)
+        kv_bytes = batch.kv_bytes()
+        uniq = wl.unique_kv_bytes(batch)
+        step_ms = dist_max(r["step_ms"], world)
+        casc_ms = dist_max(r["cascade_ms"], world)
+        e.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
+        e["roofline"] = roofline(uniq / (casc_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s", "hbm", None)
+        e["roofline"]["kernel"] = "cascade (prefix pass on prefill_kernel + suffix decode_kernel)"
+        e["roofline"]["algorithmic_bytes_per_launch"] = uniq
+        e["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "cascade_us": r["cascade_ms"] * 1e3,
+                        "kv_bytes_per_step": kv_bytes, "unique_kv_bytes": uniq,
+                        "unique_kv_gbs": uniq / (casc_ms * 1e-3) / 1e9}
+        e["gpu_launches"] = r["launches"]
+        cfg["cascade"] = f"{shared} shared blocks attended once per KV head, then the private suffixes"
+        x = e2e_measure(batch, "cascade", max(10, min(e2e_steps, 50)), 3, stream)
+        x_ms = dist_max(x["step_ms"], world)
+        e["e2e"] = {"value": world * kv_bytes / (x_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
+        kind = "decode"
+    elif wname == "batched_decode_fp8":
+        cache = fp8_prepare(batch)
+        r = fp8_decode_measure(batch, cache, steps, warmup, flush_buf, stream, clocks)
+        ntok = sum(batch.seq_lens_host)
+        kv_bytes = ntok * 8 * FP8_ROW_BYTES
+        bf16_bytes = batch.kv_bytes()
+        io_bytes = batch.num_seqs * 32 * 128 * 2 * 2 + batch.num_seqs * (batch.max_blocks_per_seq + 1) * 4
+        step_ms = dist_max(r["step_ms"], world)
+        dec_ms = dist_max(r["decode_ms"], world)
+        e.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
+        e["roofline"] = roofline((kv_bytes + io_bytes) / (dec_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
+                                 "hbm", traffic_for("decode_fp8", wname))
+        e["roofline"]["kernel"] = "decode_fp8_kernel"
+        e["roofline"]["algorithmic_bytes_per_launch"] = kv_bytes + io_bytes
+        e["kernels"] = {"decode_append_fp8_us": r["step_ms"] * 1e3,
+                        "two_call_step": {"kv_append_fp8_us": r["two_call_append_ms"] * 1e3,
+                                          "decode_fp8_us": r["two_call_decode_ms"] * 1e3},
+                        "fp8_kv_bytes_per_step": kv_bytes, "bf16_kv_bytes_per_step": bf16_bytes,
+                        "bf16_equivalent_gbs": world * bf16_bytes / (step_ms * 1e-3) / 1e9}
+        e["gpu_launches"] = r["launches"]
+        x = e2e_fp8_measure(batch, cache, e2e_steps, 5, stream)
+        x_ms = dist_max(x["step_ms"], world)
+        e["e2e"] = {"value": world * kv_bytes / (x_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
+        cfg["kv_cache"] = "8-bit: E4M3 codes + one fp32 scale per token and KV head"
+        e["dtype"] = "f16 products over e4m3 codes"
+        kind = "decode_fp8"
+    elif wname == "qkv_append":
+        x_in, w = qkv_inputs(batch.total_tokens, 7)
+        r = qkv_measure(batch, x_in, w, steps, warmup, flush_buf, stream, clocks)
+        flops = 2.0 * batch.total_tokens * QKV_HIDDEN * 6144
+        step_ms = dist_max(r["step_ms"], world)
+        e.update(value=world * flops / (step_ms * 1e-3) / 1e12, unit="TFLOP/s", ms_per_step=step_ms)
+        e["roofline"] = roofline(flops / (step_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s", "tensor",
+                                 traffic_for("qkv", wname))
+        e["roofline"]["kernel"] = "qkv_pair_kernel"
+        e["roofline"]["algorithmic_flops_per_launch"] = flops
+        # the same call for a decode step's batch: 32 new tokens, the weights dominate the bytes
+        db = wl.batched_decode(device="cuda")
+        dx, _ = qkv_inputs(db.total_tokens, 8)
+        dr = qkv_measure(db, dx, w, max(20, min(steps, 200)), warmup, flush_buf, stream, None)
+        wbytes = 6144 * QKV_HIDDEN * 2 + db.total_tokens * (QKV_HIDDEN + 6144) * 2
+        e["kernels"] = {"qkv_us": r["step_ms"] * 1e3, "tokens": batch.total_tokens, "hidden": QKV_HIDDEN,
+                        "decode_batch": {"tokens": db.total_tokens, "qkv_us": dr["step_ms"] * 1e3,
+                                         "bytes": wbytes, "gbs": wbytes / (dr["step_ms"] * 1e-3) / 1e9,
+                                         "hbm_frac": wbytes / (dr["step_ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
+        e["gpu_launches"] = r["launches"] + dr["launches"]
+        x = e2e_qkv_measure(batch, x_in, w, max(10, min(e2e_steps, 50)), 3, stream)
+        x_ms = dist_max(x["step_ms"], world)
+        e["e2e"] = {"value": world * flops / (x_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
+        cfg["projection"] = "x [4096, 4096] @ w_qkv [6144, 4096]^T; q out, k and v into their cache slots"
+        kind = "qkv"
+    elif wname == "causal_prefill":
+        r = prefill_measure(batch, steps, warmup, flush_buf, stream, clocks)
+        flops = batch.attention_flops()
+        step_ms = dist_max(r["step_ms"], world)
+        attn_ms = dist_max(r["attn_ms"], world)
+        e.update(value=world * flops / (step_ms * 1e-3) / 1e12, unit="TFLOP/s", ms_per_step=step_ms)
+        e["roofline"] = roofline(flops / (attn_ms * 1e-3) / 1e12, peaks["bf16_tflops"],
+                                 "TFLOP/s", "tensor", traffic_for("prefill", wname))
+        e["roofline"]["kernel"] = "prefill_kernel"
+        e["roofline"]["algorithmic_flops_per_launch"] = flops
+        e["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "prefill_us": r["attn_ms"] * 1e3}
+        e["gpu_launches"] = r["launches"]
+        x = e2e_measure(batch, "prefill", max(10, min(e2e_steps, 50)), 3, stream)
+        x_ms = dist_max(x["step_ms"], world)
+        e["e2e"] = {"value": world * flops / (x_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
+        kind = "prefill"
+    else:  # mixed_batch
+        r = mixed_measure(batch, steps, warmup, flush_buf, stream, clocks)
+        dec, pre = r["dec"], r["pre"]
+        kv_bytes = dec.kv_bytes()
+        flops = pre.attention_flops()
+        step_ms = dist_max(r["step_ms"], world)
+        t_bw = kv_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+        t_tc = flops / (peaks["bf16_tflops"] * 1e12) * 1e3
+        e.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
+        e["roofline"] = roofline(kv_bytes / (r["decode_ms"] * 1e-3) / 1e9, peaks["hbm_gbs"],
+                                 "GB/s", "hbm", traffic_for("decode", wname))
+        e["roofline"]["kernel"] = "decode_kernel"
+        e["roofline"]["algorithmic_bytes_per_launch"] = kv_bytes
+        e["prefill_roofline"] = dict(roofline(flops / (r["prefill_ms"] * 1e-3) / 1e12, peaks["bf16_tflops"],
+                                              "TFLOP/s", "tensor", traffic_for("prefill", wname)),
+                                     kernel="prefill_kernel (+ planning kernel)",
+                                     algorithmic_flops_per_launch=flops)
+        e["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "decode_us": r["decode_ms"] * 1e3,
+                        "prefill_us": r["prefill_ms"] * 1e3,
+                        "prefill_tflops": flops / (r["prefill_ms"] * 1e-3) / 1e12,
+                        "combined_roofline_frac": (t_bw + t_tc) / step_ms}
+        e["gpu_launches"] = r["launches"]
+        x = e2e_measure(batch, "mixed", max(10, min(e2e_steps, 100)), 3, stream)
+        x_ms = dist_max(x["step_ms"], world)
+        e["e2e"] = {"value": world * kv_bytes / (x_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
+        kind = "decode"
+    if r.get("step_pcts"):
+        e["step_ms_percentiles"] = r["step_pcts"]   # this rank's timed steps (rank 0 prints)
+    e["config"] = cfg
+    return e, kind, batch, layers
+
+
+def cpu_for(wname, kind, batch, seconds, threads=0):
+    """The oracle timed on the host cores over a bounded sample of the workload."""
+    from paged_gqa_attention_gb300 import workloads as wl
+
+    if kind == "decode_fp8":
+        return cpu_baseline_fp8(batch, seconds)
+    if kind == "qkv":
+        return cpu_baseline_qkv(batch.total_tokens, seconds)
+    return cpu_baseline(batch, kind, seconds, rows_cap_for(wname), threads)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -900,7 +1203,6 @@ def main():
 
     from paged_gqa_attention_gb300 import build as pa_build
     from paged_gqa_attention_gb300 import ops
-    from paged_gqa_attention_gb300 import workloads as wl
 
     torch.cuda.set_device(local)
     pa_build.build()
@@ -910,234 +1212,56 @@ def main():
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     clocks = ClockSampler(local)
     clocks.start()
-
     wname = args.workload
-    layers = wl.layered_decode(device="cuda") if wname == "layered_decode" else None
-    if layers is not None:
-        batch = layers.base
-    elif wname == "batched_decode_fp8":
-        batch = wl.batched_decode(device="cuda")
-    elif wname == "prefix_shared_decode_cascade":
-        batch = wl.prefix_shared_decode(device="cuda")
-    elif wname == "qkv_append":
-        batch = wl.causal_prefill(device="cuda")      # the 4096-token prompt's new tokens
-    else:
-        batch = wl.WORKLOADS[wname](device="cuda")
+    cpu_ok = rank == 0 and world == 1 and not args.no_cpu_baseline
     dist_barrier(world)
+
+    e2e_steps = max(20, min(args.steps, 200))
+    entry, kind, batch, layers = measure(wname, args.steps, args.warmup, e2e_steps, peaks, flush_buf, stream,
+                                         clocks, world)
     line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic"}
-    cfg = {"workload": wname, **batch.info, "heads": "32 q / 8 kv x 128", "block_tokens": 256,
-           **({"layers": layers.layers} if layers is not None else {}),
-           "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write + read)",
-           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    line.update(entry)
+    if cpu_ok:
+        line["cpu_baseline"] = cpu_for(wname, kind, batch, args.cpu_seconds)
+        if wname in ("single_decode", "batched_decode"):
+            one = cpu_for(wname, kind, batch, max(2.0, args.cpu_seconds / 4), threads=1)
+            line["cpu_baseline"]["one_core"] = {"value": one["value"], "unit": one["unit"], "cores": 1,
+                                                "sample": one["sample"]}
+    del batch, layers
+    torch.cuda.empty_cache()
 
-    if wname in ("single_decode", "batched_decode", "prefix_shared_decode"):
-        r = decode_measure(batch, args.steps, args.warmup, flush_buf, stream, clocks)
-        kv_bytes = batch.kv_bytes()
-        io_bytes = batch.num_seqs * 32 * 128 * 2 * 2 + batch.num_seqs * (batch.max_blocks_per_seq + 1) * 4
-        step_ms = dist_max(r["step_ms"], world)
-        attn_ms = dist_max(r["attn_ms"], world)
-        line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s",
-                    ms_per_step=step_ms)
-        # algorithmic bytes: every distinct K/V byte once (the shared prefix of the prefix-shared
-        # workload is one set of blocks, however many sequences read it)
-        alg_bytes = wl.unique_kv_bytes(batch) + io_bytes
-        ach = alg_bytes / (attn_ms * 1e-3) / 1e9
-        line["roofline"] = roofline(ach, peaks["hbm_gbs"], "GB/s", "hbm", traffic_for("decode", wname))
-        line["roofline"]["kernel"] = "decode_kernel"
-        line["roofline"]["algorithmic_bytes_per_launch"] = alg_bytes
-        line["kernels"] = {"decode_append_us": r["attn_ms"] * 1e3,
-                           "two_call_step": {"kv_append_us": r["two_call_append_ms"] * 1e3,
-                                             "decode_us": r["two_call_decode_ms"] * 1e3},
-                           "kv_bytes_per_step": kv_bytes,
-                           "unique_kv_bytes": wl.unique_kv_bytes(batch)}
-        if wname == "prefix_shared_decode":
-            uniq = wl.unique_kv_bytes(batch)
-            line["kernels"]["unique_kv_gbs"] = uniq / (attn_ms * 1e-3) / 1e9
-            line["kernels"]["unique_kv_frac"] = line["kernels"]["unique_kv_gbs"] / peaks["hbm_gbs"]
-        line["gpu_launches"] = r["launches"]
-        e = e2e_decode_measure(batch, max(20, min(args.steps, 200)), 5, stream)
-        e_ms = dist_max(e["step_ms"], world)
-        line["e2e"] = {"value": world * kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
-                       "ms_per_step": e_ms}
-        kind = "decode"
-    elif wname == "layered_decode":
-        r = layered_measure(layers, args.steps, args.warmup, flush_buf, stream, clocks)
-        kv_bytes = layers.kv_bytes()
-        io_bytes = layers.layers * (batch.num_seqs * 32 * 128 * 2 * 2 +
-                                    batch.num_seqs * (batch.max_blocks_per_seq + 1) * 4)
-        step_ms = dist_max(r["graph_ms"], world)
-        line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
-        line["roofline"] = roofline((kv_bytes + io_bytes) / (step_ms * 1e-3) / 1e9, peaks["hbm_gbs"],
-                                    "GB/s", "hbm", traffic_for("decode", wname))
-        line["roofline"]["kernel"] = "decode_kernel"
-        line["roofline"]["algorithmic_bytes_per_launch"] = (kv_bytes + io_bytes) // layers.layers
-        line["kernels"] = {"layers": layers.layers, "graph_step_us": r["graph_ms"] * 1e3,
-                           "graph_us_per_layer": r["graph_ms"] * 1e3 / layers.layers,
-                           "one_call_per_layer_step_us": r["eager_ms"] * 1e3,
-                           "one_call_per_layer_us_per_layer": r["eager_ms"] * 1e3 / layers.layers,
-                           "kv_bytes_per_step": kv_bytes}
-        line["gpu_launches"] = r["launches"]
-        e = e2e_layered_measure(layers, r["graph"], r["out"], max(20, min(args.steps, 200)), 5, stream)
-        e_ms = dist_max(e["step_ms"], world)
-        line["e2e"] = {"value": world * kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
-                       "ms_per_step": e_ms}
-        r["graph"].close()
-        kind = "decode"
-    elif wname == "prefix_shared_decode_cascade":
-        shared = batch.info["shared_blocks"]
-        r = cascade_measure(batch, shared, args.steps, args.warmup, flush_buf, stream, clocks)
-        kv_bytes = batch.kv_bytes()
-        uniq = wl.unique_kv_bytes(batch)
-        step_ms = dist_max(r["step_ms"], world)
-        casc_ms = dist_max(r["cascade_ms"], world)
-        line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
-        line["roofline"] = roofline(uniq / (casc_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s", "hbm", None)
-        line["roofline"]["kernel"] = "cascade (prefix pass on prefill_kernel + suffix decode_kernel)"
-        line["roofline"]["algorithmic_bytes_per_launch"] = uniq
-        line["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "cascade_us": r["cascade_ms"] * 1e3,
-                           "kv_bytes_per_step": kv_bytes, "unique_kv_bytes": uniq,
-                           "unique_kv_gbs": uniq / (casc_ms * 1e-3) / 1e9}
-        line["gpu_launches"] = r["launches"]
-        cfg["cascade"] = f"{shared} shared blocks attended once per KV head, then the private suffixes"
-        e = e2e_measure(batch, "cascade", max(10, min(args.steps, 50)), 3, stream)
-        e_ms = dist_max(e["step_ms"], world)
-        line["e2e"] = {"value": world * kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"], "ms_per_step": e_ms}
-        kind = "decode"
-    elif wname == "batched_decode_fp8":
-        cache = fp8_prepare(batch)
-        r = fp8_decode_measure(batch, cache, args.steps, args.warmup, flush_buf, stream, clocks)
-        ntok = sum(batch.seq_lens_host)
-        kv_bytes = ntok * 8 * FP8_ROW_BYTES
-        bf16_bytes = batch.kv_bytes()
-        io_bytes = batch.num_seqs * 32 * 128 * 2 * 2 + batch.num_seqs * (batch.max_blocks_per_seq + 1) * 4
-        step_ms = dist_max(r["step_ms"], world)
-        dec_ms = dist_max(r["decode_ms"], world)
-        line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
-        line["roofline"] = roofline((kv_bytes + io_bytes) / (dec_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
-                                    "hbm", traffic_for("decode_fp8", wname))
-        line["roofline"]["kernel"] = "decode_fp8_kernel"
-        line["roofline"]["algorithmic_bytes_per_launch"] = kv_bytes + io_bytes
-        line["kernels"] = {"decode_append_fp8_us": r["step_ms"] * 1e3,
-                           "two_call_step": {"kv_append_fp8_us": r["two_call_append_ms"] * 1e3,
-                                             "decode_fp8_us": r["two_call_decode_ms"] * 1e3},
-                           "fp8_kv_bytes_per_step": kv_bytes, "bf16_kv_bytes_per_step": bf16_bytes,
-                           "bf16_equivalent_gbs": world * bf16_bytes / (step_ms * 1e-3) / 1e9}
-        line["gpu_launches"] = r["launches"]
-        e = e2e_fp8_measure(batch, cache, max(20, min(args.steps, 200)), 5, stream)
-        e_ms = dist_max(e["step_ms"], world)
-        line["e2e"] = {"value": world * kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"], "ms_per_step": e_ms}
-        cfg["kv_cache"] = "8-bit: E4M3 codes + one fp32 scale per token and KV head"
-        line["dtype"] = "f16 products over e4m3 codes"
-        kind = "decode_fp8"
-    elif wname == "qkv_append":
-        x, w = qkv_inputs(batch.total_tokens, 7)
-        r = qkv_measure(batch, x, w, args.steps, args.warmup, flush_buf, stream, clocks)
-        flops = 2.0 * batch.total_tokens * QKV_HIDDEN * 6144
-        step_ms = dist_max(r["step_ms"], world)
-        line.update(value=world * flops / (step_ms * 1e-3) / 1e12, unit="TFLOP/s", ms_per_step=step_ms)
-        line["roofline"] = roofline(flops / (step_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s", "tensor",
-                                    traffic_for("qkv", wname))
-        line["roofline"]["kernel"] = "qkv_pair_kernel"
-        line["roofline"]["algorithmic_flops_per_launch"] = flops
-        # the same call for a decode step's batch: 32 new tokens, the weights dominate the bytes
-        db = wl.batched_decode(device="cuda")
-        dx, _ = qkv_inputs(db.total_tokens, 8)
-        dr = qkv_measure(db, dx, w, max(20, min(args.steps, 200)), args.warmup, flush_buf, stream, None)
-        wbytes = 6144 * QKV_HIDDEN * 2 + db.total_tokens * (QKV_HIDDEN + 6144) * 2
-        line["kernels"] = {"qkv_us": r["step_ms"] * 1e3, "tokens": batch.total_tokens, "hidden": QKV_HIDDEN,
-                           "decode_batch": {"tokens": db.total_tokens, "qkv_us": dr["step_ms"] * 1e3,
-                                            "bytes": wbytes, "gbs": wbytes / (dr["step_ms"] * 1e-3) / 1e9,
-                                            "hbm_frac": wbytes / (dr["step_ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
-        line["gpu_launches"] = r["launches"] + dr["launches"]
-        e = e2e_qkv_measure(batch, x, w, max(10, min(args.steps, 50)), 3, stream)
-        e_ms = dist_max(e["step_ms"], world)
-        line["e2e"] = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"], "ms_per_step": e_ms}
-        cfg["projection"] = "x [4096, 4096] @ w_qkv [6144, 4096]^T; q out, k and v into their cache slots"
-        kind = "qkv"
-    elif wname == "causal_prefill":
-        r = prefill_measure(batch, args.steps, args.warmup, flush_buf, stream, clocks)
-        flops = batch.attention_flops()
-        step_ms = dist_max(r["step_ms"], world)
-        attn_ms = dist_max(r["attn_ms"], world)
-        line.update(value=world * flops / (step_ms * 1e-3) / 1e12, unit="TFLOP/s",
-                    ms_per_step=step_ms)
-        line["roofline"] = roofline(flops / (attn_ms * 1e-3) / 1e12, peaks["bf16_tflops"],
-                                    "TFLOP/s", "tensor", traffic_for("prefill", wname))
-        line["roofline"]["kernel"] = "prefill_kernel"
-        line["roofline"]["algorithmic_flops_per_launch"] = flops
-        line["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "prefill_us": r["attn_ms"] * 1e3}
-        line["gpu_launches"] = r["launches"]
-        e = e2e_measure(batch, "prefill", max(10, min(args.steps, 50)), 3, stream)
-        e_ms = dist_max(e["step_ms"], world)
-        line["e2e"] = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
-                       "ms_per_step": e_ms}
-        kind = "prefill"
-    else:  # mixed_batch
-        r = mixed_measure(batch, args.steps, args.warmup, flush_buf, stream, clocks)
-        dec, pre = r["dec"], r["pre"]
-        kv_bytes = dec.kv_bytes()
-        flops = pre.attention_flops()
-        step_ms = dist_max(r["step_ms"], world)
-        t_bw = kv_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
-        t_tc = flops / (peaks["bf16_tflops"] * 1e12) * 1e3
-        line.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s",
-                    ms_per_step=step_ms)
-        line["roofline"] = roofline(kv_bytes / (r["decode_ms"] * 1e-3) / 1e9, peaks["hbm_gbs"],
-                                    "GB/s", "hbm", traffic_for("decode", wname))
-        line["roofline"]["kernel"] = "decode_kernel"
-        line["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "decode_us": r["decode_ms"] * 1e3,
-                           "prefill_us": r["prefill_ms"] * 1e3,
-                           "prefill_tflops": flops / (r["prefill_ms"] * 1e-3) / 1e12,
-                           "combined_roofline_frac": (t_bw + t_tc) / step_ms}
-        line["gpu_launches"] = r["launches"]
-        e = e2e_measure(batch, "mixed", max(10, min(args.steps, 100)), 3, stream)
-        e_ms = dist_max(e["step_ms"], world)
-        line["e2e"] = {"value": world * kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
-                       "ms_per_step": e_ms}
-        kind = "decode"
-
-    line["config"] = cfg
-    # the other half of the metric: causal prefill, in the same run
-    if wname in ("single_decode", "batched_decode", "prefix_shared_decode") and not args.no_prefill:
-        del batch
-        torch.cuda.empty_cache()
-        pb = wl.causal_prefill(device="cuda")
-        psteps = max(10, min(args.steps, 200))
-        pr = prefill_measure(pb, psteps, max(3, min(args.warmup, 10)), flush_buf, stream, clocks)
-        flops = pb.attention_flops()
-        p_step = dist_max(pr["step_ms"], world)
-        p_attn = dist_max(pr["attn_ms"], world)
-        line["prefill"] = {
-            "workload": "causal_prefill", "prompt": 4096, "steps": psteps,
-            "value": world * flops / (p_step * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": p_step,
-            "roofline": dict(roofline(flops / (p_attn * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s",
-                                      "tensor", traffic_for("prefill", "causal_prefill")),
-                             kernel="prefill_kernel", algorithmic_flops_per_launch=flops),
-            "kv_append_us": pr["append_ms"] * 1e3, "prefill_us": pr["attn_ms"] * 1e3,
-            "gpu_launches": pr["launches"]}
-        batch = pb
-    if r.get("step_pcts"):
-        line["step_ms_percentiles"] = r["step_pcts"]   # this rank's timed steps (rank 0 prints)
+    # The default run also measures every other configuration of the metric (one sub-object
+    # each, fewer steps, a shorter CPU baseline): the causal prefill as "prefill" (the other
+    # half of the metric), the rest under "configs".
+    sub_steps = max(10, min(args.steps, 200))
+    sub_warm = max(3, min(args.warmup, 10))
+    sub_cpu = max(2.0, args.cpu_seconds / 4)
+    if wname == "batched_decode" and not args.only_main:
+        subs = {}
+        for sname in DEFAULT_SUBS:
+            if sname == "causal_prefill" and args.no_prefill:
+                continue
+            se, skind, sbatch, slayers = measure(sname, sub_steps, sub_warm, max(10, min(sub_steps, 50)), peaks,
+                                                 flush_buf, stream, clocks, world)
+            se["steps"] = sub_steps
+            se["warmup"] = sub_warm
+            if cpu_ok:
+                se["cpu_baseline"] = cpu_for(sname, skind, sbatch, sub_cpu)
+                if sname == "single_decode":
+                    one = cpu_for(sname, skind, sbatch, sub_cpu, threads=1)
+                    se["cpu_baseline"]["one_core"] = {"value": one["value"], "unit": one["unit"], "cores": 1,
+                                                      "sample": one["sample"]}
+            if sname == "causal_prefill":
+                line["prefill"] = se
+            else:
+                subs[sname] = se
+            del sbatch, slayers
+            torch.cuda.empty_cache()
+        line["configs"] = subs
     line["clocks"] = clocks.stop()
     line["peaks"] = peaks
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        if kind == "decode_fp8":
-            line["cpu_baseline"] = cpu_baseline_fp8(wl.batched_decode(device="cuda"), args.cpu_seconds)
-        elif kind == "qkv":
-            line["cpu_baseline"] = cpu_baseline_qkv(batch.total_tokens, args.cpu_seconds)
-        else:
-            src = (batch if wname in ("layered_decode", "prefix_shared_decode_cascade", batch.name)
-                   else wl.WORKLOADS[wname](device="cuda"))
-            line["cpu_baseline"] = cpu_baseline(src, kind, args.cpu_seconds, rows_cap_for(wname))
     if rank == 0:
         print(json.dumps(line), flush=True)
     dist_barrier(world)

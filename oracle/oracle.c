@@ -47,6 +47,9 @@
  *   w        [n_out][hidden]                       bf16 bit patterns (a linear layer's weight)
  *   y        [tokens][n_out]                       double
  *
+ * Rotary position embedding of q and k heads (not on the pages; RoFormer's definition,
+ * given at oracle_rope below) acts on the projection's output in place.
+ *
  * Functions return 0 on success and a negative code on inconsistent input.
  */
 #include <math.h>
@@ -234,8 +237,9 @@ static int attention_rows(double *out, double *lse, const int32_t *row_tokens, c
 
     int failed = 0;
 #ifdef _OPENMP
-    if (num_threads > 0) omp_set_num_threads(num_threads);
-#pragma omp parallel
+    /* a thread count for this region only: the process-wide default stays as it was */
+    const int team = num_threads > 0 ? num_threads : omp_get_max_threads();
+#pragma omp parallel num_threads(team)
 #endif
     {
         double *scores = (double *)malloc(sizeof(double) * (size_t)max_ctx);
@@ -454,8 +458,8 @@ int oracle_qkv_project(double *y, const uint16_t *x, const uint16_t *w, const in
     for (int r = 0; r < n_rows; ++r)
         if (rows && (rows[r] < 0 || rows[r] >= tokens)) return -2;
 #ifdef _OPENMP
-    if (num_threads > 0) omp_set_num_threads(num_threads);
-#pragma omp parallel for schedule(static)
+    const int team = num_threads > 0 ? num_threads : omp_get_max_threads();
+#pragma omp parallel for schedule(static) num_threads(team)
 #endif
     for (long rn = 0; rn < (long)n_rows * n_out; ++rn) {
         const int r = (int)(rn / n_out), n = (int)(rn % n_out);
@@ -498,6 +502,56 @@ void oracle_bf16_round(const double *v, uint16_t *out, long n)
         memcpy(&bits, &f, sizeof bits);
         out[i] = sign | (uint16_t)(bits >> 16);
     }
+}
+
+/*
+ * Absolute position of every new token: new token i of sequence s sits at
+ * p = seq_lens[s] - q_len + i, the rule the append and the attention use [P1 §4.3.1;
+ * P3 §3.3 chunked prefill].  pos: [cu_q_lens[num_seqs]].
+ */
+int oracle_token_positions(int32_t *pos, const int32_t *cu_q_lens, const int32_t *seq_lens, int num_seqs)
+{
+    if (num_seqs < 0 || (num_seqs > 0 && cu_q_lens[0] != 0)) return -1;
+    for (int s = 0; s < num_seqs; ++s) {
+        int q_len = cu_q_lens[s + 1] - cu_q_lens[s];
+        if (q_len < 0 || seq_lens[s] < q_len) return -2;
+        for (int i = 0; i < q_len; ++i) pos[cu_q_lens[s] + i] = seq_lens[s] - q_len + i;
+    }
+    return 0;
+}
+
+/*
+ * Rotary position embedding.  The pages do not define it; the definition here is that of
+ * RoFormer (Su et al., 2021, "RoFormer: Enhanced Transformer with Rotary Position
+ * Embedding"), in the pairing Qwen3 and the Llama family use ("rotate half"): in a head
+ * vector of D values, dims i and i + D/2 (0 <= i < D/2) form a pair, turned by the angle
+ * p * theta^(-2i/D) at position p:
+ *     x'[i]       = x[i] cos(a) - x[i + D/2] sin(a)
+ *     x'[i + D/2] = x[i + D/2] cos(a) + x[i] sin(a),      a = p * theta^(-2i/D)
+ * (Qwen3: theta = 1 000 000).  y: [tokens][row_stride] doubles; the n_heads head vectors
+ * of head_dim values from column first_col on are rotated in place, token t at
+ * positions[t].  Double precision throughout.
+ */
+int oracle_rope(double *y, int tokens, int row_stride, int first_col, int n_heads, int head_dim,
+                const int32_t *positions, double theta)
+{
+    if (tokens < 0 || head_dim < 2 || head_dim % 2 || n_heads < 0 || first_col < 0 ||
+        first_col + n_heads * head_dim > row_stride || !(theta > 1.0))
+        return -1;
+    const int half = head_dim / 2;
+    for (int t = 0; t < tokens; ++t) {
+        for (int h = 0; h < n_heads; ++h) {
+            double *v = y + (size_t)t * row_stride + first_col + (size_t)h * head_dim;
+            for (int i = 0; i < half; ++i) {
+                const double a = (double)positions[t] * pow(theta, -2.0 * i / head_dim);
+                const double c = cos(a), s = sin(a);
+                const double lo = v[i], hi = v[i + half];
+                v[i] = lo * c - hi * s;
+                v[i + half] = hi * c + lo * s;
+            }
+        }
+    }
+    return 0;
 }
 
 /* Threads the OpenMP runtime would use (1 without OpenMP). */
