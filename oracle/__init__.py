@@ -11,10 +11,13 @@ GPU sees and return float64 results.  The 8-bit KV cache (E4M3 codes, one fp32 s
 ``attention_fp8``, with the codec ``e4m3_encode`` / ``e4m3_decode``.
 
 The merged Q/K/V projection (page 1 §4.4.3) is ``qkv_project``; ``qkv_append`` adds the
-append of its k and v (rounded once to bf16 by ``bf16_round``) to the cache.
+append of its k and v (rounded once to bf16 by ``bf16_round``) to the cache, optionally after
+the rotary position embedding of q and k (``rope``; RoFormer's definition, not on the pages)
+at each token's position (``token_positions``).
 
 Parity status: every function here is pinned by the CPU tests in
-``tests/test_oracle_pins.py``, ``tests/test_oracle_fp8.py`` and ``tests/test_oracle_qkv.py`` (closed forms, library
+``tests/test_oracle_pins.py``, ``tests/test_oracle_fp8.py``, ``tests/test_oracle_qkv.py`` and
+``tests/test_oracle_rope.py`` (closed forms, library
 routines on tiny cases -- torch SDPA, torch's float8_e4m3fn -- invariants, the format's
 error bound and a high-precision brute force).
 """
@@ -78,6 +81,10 @@ def load_library(path: str):
     lib.oracle_qkv_project.restype = ci
     lib.oracle_bf16_round.argtypes = [f64p, u16p, ctypes.c_long]
     lib.oracle_bf16_round.restype = None
+    lib.oracle_token_positions.argtypes = [i32p, i32p, i32p, ci]
+    lib.oracle_token_positions.restype = ci
+    lib.oracle_rope.argtypes = [f64p, ci, ci, ci, ci, ci, i32p, ctypes.c_double]
+    lib.oracle_rope.restype = ci
     return lib
 
 
@@ -100,6 +107,8 @@ def _bits(x) -> np.ndarray:
 
 
 def _i32(x) -> np.ndarray:
+    if isinstance(x, (list, tuple)):
+        x = np.asarray(x)
     if not isinstance(x, np.ndarray):
         x = x.cpu().numpy()
     return np.ascontiguousarray(x, dtype=np.int32)
@@ -289,15 +298,49 @@ def bf16_round(v, *, lib=None) -> np.ndarray:
     return out
 
 
-def qkv_append(x, w, k_pool, v_pool, block_table, cu_q_lens, seq_lens, *, num_threads: int = 0, lib=None):
+def token_positions(cu_q_lens, seq_lens, *, lib=None) -> np.ndarray:
+    """Absolute position of every new token (seq_len - q_len + i), int32 [total_tokens]."""
+    cu, sl = _i32(cu_q_lens), _i32(seq_lens)
+    pos = np.zeros(int(cu[-1]) if len(cu) else 0, dtype=np.int32)
+    rc = (lib or _load()).oracle_token_positions(_p(pos, ctypes.c_int32), _p(cu, ctypes.c_int32),
+                                                 _p(sl, ctypes.c_int32), len(sl))
+    if rc:
+        raise ValueError(f"oracle_token_positions rejected its input (code {rc})")
+    return pos
+
+
+def rope(y, positions, theta: float, *, first_col: int = 0, n_heads: int = 1, head_dim: int = 128,
+         lib=None) -> np.ndarray:
+    """Rotary position embedding (RoFormer, rotate-half pairing) of n_heads head vectors of
+    each row of y from column first_col on, row t at positions[t]; returns a rotated copy."""
+    out = np.array(y, dtype=np.float64, copy=True, order="C")
+    if out.ndim == 1:
+        out = out.reshape(1, -1)
+    pos = _i32(np.asarray(positions))
+    assert len(pos) == out.shape[0]
+    rc = (lib or _load()).oracle_rope(_p(out, ctypes.c_double), out.shape[0], out.shape[1], first_col, n_heads,
+                                      head_dim, _p(pos, ctypes.c_int32), float(theta))
+    if rc:
+        raise ValueError(f"oracle_rope rejected its input (code {rc})")
+    return out
+
+
+def qkv_append(x, w, k_pool, v_pool, block_table, cu_q_lens, seq_lens, *, rope_theta: float = 0.0,
+               num_threads: int = 0, lib=None):
     """The merged projection of every new token with its k and v appended to the cache.
 
     Returns (q [tokens, 32, 128] float64, k_pool', v_pool' uint16): q is exact; the cache
-    holds k and v rounded once to bf16 (its format), placed by ``kv_append``'s rule.
+    holds k and v rounded once to bf16 (its format), placed by ``kv_append``'s rule.  With
+    rope_theta > 0 the 32 q heads and the 8 k heads of each token are first rotated at the
+    token's absolute position (``rope``); v is never rotated.
     """
     y = qkv_project(x, w, num_threads=num_threads, lib=lib)
     t = y.shape[0]
     assert y.shape[1] == Q_COLS + 2 * KV_COLS
+    if rope_theta:
+        pos = token_positions(cu_q_lens, seq_lens, lib=lib)
+        y = rope(y, pos, rope_theta, first_col=0, n_heads=32, lib=lib)
+        y = rope(y, pos, rope_theta, first_col=Q_COLS, n_heads=8, lib=lib)
     q = y[:, :Q_COLS].reshape(t, 32, 128)
     k_new = bf16_round(y[:, Q_COLS:Q_COLS + KV_COLS], lib=lib).reshape(t, 8, 128)
     v_new = bf16_round(y[:, Q_COLS + KV_COLS:], lib=lib).reshape(t, 8, 128)

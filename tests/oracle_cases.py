@@ -203,6 +203,27 @@ def pin_battery(lib):
     check("qkv_row_subset", qkv_rows)
     check("bf16_round_torch", bf16_torch)
     check("bf16_round_nearest_even", bf16_nearest)
+
+    # ---- the rotary position embedding of q and k (RoFormer, rotate-half pairing)
+    def rope_complex():
+        y = np.random.default_rng(36).standard_normal((4, 256))
+        pos = np.array([0, 3, 700, 40000])
+        r = oracle.rope(y, pos, 1e6, n_heads=2, lib=lib)
+        w = 1e6 ** (-np.arange(64) / 64.0)
+        tol = 1e-14 * (1.0 + pos[:, None])
+        ok = True
+        for h in range(2):
+            z = y[:, h * 128:h * 128 + 64] + 1j * y[:, h * 128 + 64:(h + 1) * 128]
+            zr = z * np.exp(1j * pos[:, None] * w[None, :])
+            ok = ok and bool(np.all(np.abs(r[:, h * 128:h * 128 + 64] - zr.real) <= tol))
+            ok = ok and bool(np.all(np.abs(r[:, h * 128 + 64:(h + 1) * 128] - zr.imag) <= tol))
+        return ok
+
+    def rope_positions():
+        return oracle.token_positions([0, 1, 4], [9, 20], lib=lib).tolist() == [8, 17, 18, 19]
+
+    check("rope_complex_form", rope_complex)
+    check("rope_token_positions", rope_positions)
     return failed
 
 

@@ -73,6 +73,17 @@ MUTANTS = {
     "bf16_ties_away": ("(frac == 0.5 && fmod(m, 2.0) != 0.0)", "(frac == 0.5)"),
     # bf16 subnormals with the normal quantum (8 significant bits all the way down)
     "bf16_no_subnormals": ("if (lo < -126) lo = -126;", ""),
+    # rotary embedding: one sign of the rotation flipped
+    "rope_sign": ("v[i] = lo * c - hi * s;", "v[i] = lo * c + hi * s;"),
+    # rotary embedding: frequency exponent i / D instead of 2i / D
+    "rope_frequency": ("pow(theta, -2.0 * i / head_dim)", "pow(theta, -1.0 * i / head_dim)"),
+    # rotary embedding: adjacent dims paired (2i, 2i + 1) instead of (i, i + D/2)
+    "rope_interleaved": ("const double lo = v[i], hi = v[i + half];\n                v[i] = lo * c - hi * s;\n"
+                         "                v[i + half] = hi * c + lo * s;",
+                         "const double lo = v[2 * i], hi = v[2 * i + 1];\n                v[2 * i] = lo * c - hi * s;\n"
+                         "                v[2 * i + 1] = hi * c + lo * s;"),
+    # rotary embedding at the chunk-relative position
+    "rope_relative_position": ("pos[cu_q_lens[s] + i] = seq_lens[s] - q_len + i;", "pos[cu_q_lens[s] + i] = i;"),
     # append writes at the chunk-relative position
     "append_relative_position": ("int p = seq_lens[s] - q_len + i;            /* absolute position */",
                                  "int p = i;            /* absolute position */"),
