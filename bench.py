@@ -796,7 +796,8 @@ def qkv_inputs(tokens, seed, device="cuda"):
 
 
 def qkv_measure(batch, x, w, steps, warmup, flush_buf, stream, clocks):
-    """One paged_qkv_append call (one kernel): q of every new token out, k and v into the cache."""
+    """One paged_qkv_append call (one kernel): q of every new token out, k and v into the cache,
+    q and k rotated by Qwen3's rotary embedding (theta 1e6) at each token's position."""
     import torch
 
     from paged_gqa_attention_gb300 import ops
@@ -807,7 +808,7 @@ def qkv_measure(batch, x, w, steps, warmup, flush_buf, stream, clocks):
     def step(tm):
         if tm: tm.record(0)
         ops.paged_qkv_append(x, w, batch.k_pool, batch.v_pool, batch.block_table, batch.cu_q_lens,
-                             batch.seq_lens, ws, q_out=q)
+                             batch.seq_lens, ws, rope_theta=ops.QWEN3_ROPE_THETA, q_out=q)
         if tm: tm.record(1)
 
     spans, wall = run_timed(step, 2, steps, warmup, flush_buf, stream, clocks)
@@ -833,7 +834,7 @@ def e2e_qkv_measure(batch, x, w, steps, warmup, stream):
     def step():
         x_dev.copy_(x_host, non_blocking=True)
         ops.paged_qkv_append(x_dev, w, batch.k_pool, batch.v_pool, batch.block_table, batch.cu_q_lens,
-                             batch.seq_lens, ws, q_out=q_dev)
+                             batch.seq_lens, ws, rope_theta=ops.QWEN3_ROPE_THETA, q_out=q_dev)
         q_host.copy_(q_dev, non_blocking=True)
 
     for _ in range(warmup):
@@ -1129,7 +1130,8 @@ def measure(wname, steps, warmup, e2e_steps, peaks, flush_buf, stream, clocks, w
         x_ms = dist_max(x["step_ms"], world)
         e["e2e"] = {"value": world * flops / (x_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
-        cfg["projection"] = "x [4096, 4096] @ w_qkv [6144, 4096]^T; q out, k and v into their cache slots"
+        cfg["projection"] = ("x [4096, 4096] @ w_qkv [6144, 4096]^T; rotary embedding of q and k (theta 1e6); "
+                             "q out, k and v into their cache slots")
         kind = "qkv"
     elif wname == "causal_prefill":
         r = prefill_measure(batch, steps, warmup, flush_buf, stream, clocks)

@@ -138,16 +138,25 @@ pa_status kv_append(pa_shape shape, void *k_pool, void *v_pool,
  *   columns 0..4095 -> q_out[t][n / 128][n % 128];
  *   columns 4096..5119 -> K of KV head (n - 4096) / 128, dim n % 128, at the token's
  *   cache slot; columns 5120..6143 -> V likewise [P1 §4.4.2: 8 KV heads].
- * No rotary position embedding or per-head normalisation is applied (the pages define
- * neither); a caller that needs them applies them to q_out and the cache rows itself.
+ * rope_theta > 1 applies the rotary position embedding to the 32 q heads and the 8 k heads
+ * before the bf16 rounding (v is not rotated).  The pages define no position encoding; the
+ * definition is RoFormer's (Su et al. 2021) in the pairing Qwen3 uses (Qwen3: theta = 1e6):
+ * at the token's absolute position p = seq_len - q_len + i, dims d and d + 64 of a head
+ * (d < 64) become
+ *   y'[d] = y[d] cos(a) - y[d+64] sin(a),  y'[d+64] = y[d+64] cos(a) + y[d] sin(a),
+ *   a = p * rope_theta^(-d/64),
+ * in fp32 with the angle reduced to about 1e-6 rad.  rope_theta = 0 applies no rotation;
+ * with a rotation max_blocks_per_seq * 256 must not exceed 2^24 (positions exact in fp32),
+ * else PA_ERR_INVALID_ARG.  No per-head normalisation is applied.
  *   x [total_tokens][hidden] bf16, hidden a multiple of 256 (4096 for Qwen3-8B);
  *   w_qkv [6144][hidden] bf16: rows 0-4095 the q weight, 4096-5119 k, 5120-6143 v, each
  *   [out][in] as a linear layer stores it; q_out [total_tokens][32][128] bf16.
  * Pools, block_table, cu_q_lens, seq_lens and the workspace as for kv_append; a token
- * whose sequence data are inconsistent or whose block id is outside the pool gets no
- * K/V write and records PA_ERR_DEVICE (its q row is still written).
+ * whose block id is outside the pool gets no K/V write and records PA_ERR_DEVICE (its q
+ * row is still written); a token whose sequence data are inconsistent gets no K/V write
+ * either and, with a rotation, a NaN q row (its position is unknown).
  */
-pa_status paged_qkv_append(pa_shape shape, int32_t hidden, void *q_out, const void *x,
+pa_status paged_qkv_append(pa_shape shape, int32_t hidden, float rope_theta, void *q_out, const void *x,
                            const void *w_qkv, void *k_pool, void *v_pool,
                            const int32_t *block_table, int32_t max_blocks_per_seq,
                            int32_t num_blocks, const int32_t *cu_q_lens,

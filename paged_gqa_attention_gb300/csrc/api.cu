@@ -353,15 +353,19 @@ pa_status kv_append(pa_shape shape, void *k_pool, void *v_pool, const void *k_ne
     return launch_kv_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-pa_status paged_qkv_append(pa_shape shape, int32_t hidden, void *q_out, const void *x, const void *w_qkv,
-                           void *k_pool, void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
-                           int32_t num_blocks, const int32_t *cu_q_lens, const int32_t *seq_lens, int32_t num_seqs,
-                           int32_t total_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+pa_status paged_qkv_append(pa_shape shape, int32_t hidden, float rope_theta, void *q_out, const void *x,
+                           const void *w_qkv, void *k_pool, void *v_pool, const int32_t *block_table,
+                           int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t *cu_q_lens,
+                           const int32_t *seq_lens, int32_t num_seqs, int32_t total_tokens, void *workspace,
+                           size_t workspace_bytes, void *stream) {
     if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
     if (hidden < 256 || hidden % 256 != 0 || hidden > (1 << 16)) return PA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || max_blocks_per_seq < 1 || num_blocks < 1 ||
         (num_seqs == 0 && total_tokens != 0))
         return PA_ERR_INVALID_ARG;
+    // the rotation: off (0) or a base above 1; positions must stay below 2^24 (exact in fp32)
+    if (rope_theta != 0.f && !(std::isfinite(rope_theta) && rope_theta > 1.f)) return PA_ERR_INVALID_ARG;
+    if (rope_theta != 0.f && (long long)max_blocks_per_seq * kBlock > (1ll << 24)) return PA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < kHeaderBytes || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
     if (total_tokens == 0) return PA_OK;
     if (!q_out || !x || !w_qkv || !k_pool || !v_pool || !block_table || !cu_q_lens || !seq_lens)
@@ -375,7 +379,7 @@ pa_status paged_qkv_append(pa_shape shape, int32_t hidden, void *q_out, const vo
     if (!get_encoder()) return PA_ERR_CUDA;
     CUtensorMap x_map, w_map;
     if (!encode_matrix_map(&x_map, x, total_tokens, hidden, qkv_tile_rows_loaded(total_tokens)) ||
-        !encode_matrix_map(&w_map, w_qkv, kHq * kD + 2 * kHkv * kD, hidden, qkv_weight_box_rows(total_tokens)))
+        !encode_matrix_map(&w_map, w_qkv, kHq * kD + 2 * kHkv * kD, hidden, qkv_weight_box_rows()))
         return PA_ERR_INVALID_ARG;
     QkvArgs a = {};
     a.q_out = q_out;
@@ -390,6 +394,13 @@ pa_status paged_qkv_append(pa_shape shape, int32_t hidden, void *q_out, const vo
     a.total_tokens = total_tokens;
     a.hidden = hidden;
     a.err = static_cast<uint32_t *>(workspace);
+    a.rope = rope_theta != 0.f ? 1 : 0;
+    for (int i = 0; i < kRopePairs; ++i) {
+        // frequency of pair i: theta^(-2i/128), kept as a float-float pair hi + lo
+        const double f = a.rope ? std::pow((double)rope_theta, -2.0 * i / kD) : 0.0;
+        a.rope_freq_hi[i] = (float)f;
+        a.rope_freq_lo[i] = (float)(f - (double)a.rope_freq_hi[i]);
+    }
     return launch_qkv(a, x_map, w_map, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -90,6 +90,7 @@ struct PrefillArgs {
     int32_t *order;
 };
 
+constexpr int kRopePairs = 64;   // rotated pairs of a 128-dim head
 // Merged Q/K/V projection with K and V written into the cache (qkv.cu).
 struct QkvArgs {
     void *q_out;            // [total_tokens][32][128] bf16
@@ -104,14 +105,19 @@ struct QkvArgs {
     int32_t total_tokens;
     int32_t hidden;         // a multiple of 256
     uint32_t *err;
+    // Rotary position embedding of the q and k heads (rope != 0): the frequency of pair i
+    // (dims i and i + 64 of a head) as a float-float value hi + lo = theta^(-i/64).
+    int32_t rope;
+    float rope_freq_hi[kRopePairs];
+    float rope_freq_lo[kRopePairs];
 };
 
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
 
 // x_map: x [total_tokens][hidden] bf16, box {64, qkv_tile_rows_loaded(total_tokens)}; w_map:
-// w [6144][hidden] bf16, box {64, qkv_weight_box_rows(total_tokens)}; both 128-byte swizzle.
+// w [6144][hidden] bf16, box {64, qkv_weight_box_rows()}; both 128-byte swizzle.
 int qkv_tile_cols(int total_tokens);
-int qkv_weight_box_rows(int total_tokens);
+int qkv_weight_box_rows();
 int qkv_tile_rows_loaded(int total_tokens);
 cudaError_t launch_qkv(const QkvArgs &a, const CUtensorMap &x_map, const CUtensorMap &w_map, int num_sms,
                        cudaStream_t stream);

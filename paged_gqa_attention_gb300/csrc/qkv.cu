@@ -14,8 +14,18 @@
 // dim n % 128) and go to q_out[t]; columns 4096-5119 are k of KV head (n - 4096) / 128 and
 // 5120-6143 v, written to the cache slot of token t (position seq_len - q_len + i of its
 // sequence, as kv_append places it), so K and V never make a round trip through memory
-// before they reach the cache.  No rotary position embedding or per-head normalisation is
-// applied: the pages define neither.
+// before they reach the cache.
+//
+// Rotary position embedding (optional; the pages define no position encoding, so its
+// definition is RoFormer's, Su et al. 2021, in the pairing Qwen3 uses): dims i and i + 64 of
+// every q and k head are turned by the angle p * theta^(-i/64) at the token's absolute
+// position p, in fp32 on the accumulator before the single bf16 rounding; v is not turned.
+// So that one epilogue thread holds both dims of a pair, a tile's output columns are taken
+// in 32-column runs reordered as [dims 0-31 | dims 64-95 | dims 32-63 | dims 96-127] of each
+// head (the weight rows are loaded in that order); every 64 tile columns are then the two
+// halves of 32 pairs of one head.  The angle is a float-float product p * (hi + lo) of the
+// frequency, reduced by 2 pi in three parts (Cody and Waite's method) before the sine and
+// cosine: about 1e-6 rad at any position below 2^24.  No per-head normalisation is applied.
 //
 // GEMM on the 5th-generation tensor cores: with more than 256 tokens a pair of CTAs on two
 // SMs computes 256 tokens x 192 output columns (tcgen05.mma.cta_group::2, see the pair kernel
@@ -45,6 +55,21 @@ constexpr int kMmaWarp = 5;
 constexpr int kThreads = 6 * 32;
 constexpr uint32_t kParkNs = 20000;
 constexpr uint32_t kRingBytes = 192 * 1024;    // the TMA ring's share of shared memory
+constexpr int kRunCols = 32;                   // weight rows per TMA box: one run of 32 columns
+
+// Output column (weight row) where logical 32-column run r starts: runs 4h .. 4h+3 are dims
+// 0-31, 64-95, 32-63 and 96-127 of head h (heads 0-31 q, 32-39 k, 40-47 v), so logical columns
+// 64c .. 64c+63 are the two halves of pairs (32c' + e, 32c' + e + 64), c' = c % 2, of head c / 2.
+__host__ __device__ __forceinline__ int run_row(int r) {
+    return (r >> 2) * kD + (r & 1) * (kD / 2) + ((r >> 1) & 1) * kRunCols;
+}
+
+// 2 pi in three fp32 parts (hi + mid + lo, each the rounding of what remains) and 1 / (2 pi)
+constexpr double kTwoPiD = 6.28318530717958647692528676655900577;
+constexpr float kTwoPiHi = (float)kTwoPiD;
+constexpr float kTwoPiMid = (float)(kTwoPiD - (double)kTwoPiHi);
+constexpr float kTwoPiLo = (float)(kTwoPiD - (double)kTwoPiHi - (double)kTwoPiMid);
+constexpr float kInvTwoPi = (float)(1.0 / kTwoPiD);
 
 // BN output columns per tile, BMA rows of x loaded per stage (128, or 32 for <= 32 tokens).
 // A stage covers kSub adjacent sub-tiles of 64 hidden elements: with few tokens the weights
@@ -61,7 +86,6 @@ struct QkvCfg {
     static constexpr int kStages = (int)(kRingBytes / (kABytes + kBBytes));
     static constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators
     static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, false);   // both operands K-major
-    static constexpr int kWBox = BN;                                 // weight rows per TMA box
 };
 
 // A work item: tile row mt (its tokens) x `width` output columns from col0; width 0 past
@@ -134,10 +158,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     }
 }
 
-// Cache slot of token t (the kv_append rule): element offset of (slot, KV head 0, dim 0) in
-// a pool, or -1 when the token's sequence data are inconsistent or its block id is outside
-// the pool (recorded in the error word).
-__device__ __forceinline__ long long cache_row(const QkvArgs &a, int t) {
+// Cache slot and absolute position of token t (the kv_append rule).  Returns the element
+// offset of (slot, KV head 0, dim 0) in a pool, or -1 when the token's sequence data are
+// inconsistent or its block id is outside the pool (recorded in the error word); *pos gets
+// p = seq_len - q_len + i, or -1 when the sequence data are inconsistent.
+__device__ __forceinline__ long long token_slot(const QkvArgs &a, int t, int *pos) {
     int lo = 0, hi = a.num_seqs - 1;   // the sequence s with cu_q_lens[s] <= t < cu_q_lens[s + 1]
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -148,11 +173,13 @@ __device__ __forceinline__ long long cache_row(const QkvArgs &a, int t) {
     const int c0 = __ldg(a.cu_q_lens + s), c1 = __ldg(a.cu_q_lens + s + 1);
     const int seq_len = __ldg(a.seq_lens + s);
     const int q_len = c1 - c0;
+    *pos = -1;
     if (c0 > t || t >= c1 || q_len > seq_len || seq_len > a.max_blocks_per_seq * kBlock) {
         record_error(a.err, kErrDevice | kErrBadCuQ);
         return -1;
     }
     const int p = seq_len - q_len + (t - c0);
+    *pos = p;
     const int blk = __ldg(a.block_table + (size_t)s * a.max_blocks_per_seq + p / kBlock);
     if (blk < 0 || blk >= a.num_blocks) {
         record_error(a.err, kErrDevice | kErrBadBlock);
@@ -161,9 +188,79 @@ __device__ __forceinline__ long long cache_row(const QkvArgs &a, int t) {
     return ((long long)blk * kBlock + p % kBlock) * kHkv * kD;
 }
 
+// cos and sin of the rotation angle of pair i at position pf (an integer below 2^24, exact in
+// fp32).  p * freq is formed as hi + lo (the product's rounding error recovered with an fma),
+// the multiple of 2 pi nearest hi is taken off in three parts (Cody and Waite), lo is added
+// back, and the reduced angle (|r| < 4) goes to the fast sine/cosine.
+__device__ __forceinline__ void rope_cos_sin(const QkvArgs &a, int i, float pf, float &c, float &s) {
+    const float fh = a.rope_freq_hi[i], fl = a.rope_freq_lo[i];
+    const float ah = __fmul_rn(pf, fh);
+    const float al = fmaf(pf, fl, fmaf(pf, fh, -ah));
+    const float k = rintf(__fmul_rn(ah, kInvTwoPi));
+    float r = fmaf(-k, kTwoPiHi, ah);
+    r = fmaf(-k, kTwoPiMid, r);
+    r = fmaf(-k, kTwoPiLo, r);
+    __sincosf(__fadd_rn(r, al), &s, &c);
+}
+
+// The epilogue of one tile for this thread's token row: logical columns col0 .. col0+width-1
+// of the accumulator at tensor-memory address tcol, 64 at a time (the halves of 32 pairs of one
+// head), rotated when they are q or k dims and the rotation is on, rounded once to bf16 and
+// stored to q_out (q heads) or the token's cache slot (k, v heads; dst_row < 0: not written).
+// A q or k row whose position is unknown (inconsistent sequence data) comes out NaN.
+__device__ __forceinline__ void store_tile_row(const QkvArgs &a, uint32_t tcol, int col0, int width, int tok,
+                                               bool live, long long dst_row, int pos) {
+#pragma unroll 1
+    for (int j = 0; j < width / 64; ++j) {
+        const int cp = (col0 >> 6) + j;            // 64-column group over the 6144 outputs
+        const int head = cp >> 1, half = cp & 1;   // dims half*32 .. +31 and 64 + half*32 .. +31
+        uint32_t lo[32], hi[32];
+        tmem_ld32(tcol + (uint32_t)(j * 64), lo);
+        tmem_ld32(tcol + (uint32_t)(j * 64 + 32), hi);
+        tmem_wait_ld(lo);
+        tmem_wait_ld(hi);
+        if (a.rope && head < kHq + kHkv) {
+            const float pf = (float)pos;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                float c, sn;
+                rope_cos_sin(a, half * 32 + e, pf, c, sn);
+                if (pos < 0) c = sn = __int_as_float(0x7fc00000);
+                const float x0 = __uint_as_float(lo[e]), x1 = __uint_as_float(hi[e]);
+                lo[e] = __float_as_uint(fmaf(x0, c, -__fmul_rn(x1, sn)));
+                hi[e] = __float_as_uint(fmaf(x1, c, __fmul_rn(x0, sn)));
+            }
+        }
+        __nv_bfloat16 *dst = nullptr;
+        if (head < kHq) {
+            if (live) dst = static_cast<__nv_bfloat16 *>(a.q_out) + (size_t)tok * kQCols + head * kD;
+        } else if (dst_row >= 0) {
+            const bool is_k = head < kHq + kHkv;
+            dst = static_cast<__nv_bfloat16 *>(is_k ? a.k_pool : a.v_pool) + dst_row +
+                  (head - kHq - (is_k ? 0 : kHkv)) * kD;
+        }
+        if (dst) {
+            uint4 *d_lo = reinterpret_cast<uint4 *>(dst + half * 32);
+            uint4 *d_hi = reinterpret_cast<uint4 *>(dst + kD / 2 + half * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                d_lo[q] = make_uint4(pack_bf16x2(__uint_as_float(lo[8 * q]), __uint_as_float(lo[8 * q + 1])),
+                                     pack_bf16x2(__uint_as_float(lo[8 * q + 2]), __uint_as_float(lo[8 * q + 3])),
+                                     pack_bf16x2(__uint_as_float(lo[8 * q + 4]), __uint_as_float(lo[8 * q + 5])),
+                                     pack_bf16x2(__uint_as_float(lo[8 * q + 6]), __uint_as_float(lo[8 * q + 7])));
+                d_hi[q] = make_uint4(pack_bf16x2(__uint_as_float(hi[8 * q]), __uint_as_float(hi[8 * q + 1])),
+                                     pack_bf16x2(__uint_as_float(hi[8 * q + 2]), __uint_as_float(hi[8 * q + 3])),
+                                     pack_bf16x2(__uint_as_float(hi[8 * q + 4]), __uint_as_float(hi[8 * q + 5])),
+                                     pack_bf16x2(__uint_as_float(hi[8 * q + 6]), __uint_as_float(hi[8 * q + 7])));
+            }
+        }
+    }
+}
+
 template <int BN, int BMA>
 __global__ void __launch_bounds__(kThreads, 1)
-qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map, const QkvArgs a) {
+qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
+           const __grid_constant__ QkvArgs a) {
     using Cfg = QkvCfg<BN, BMA>;
     constexpr int kStages = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -225,10 +322,10 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
                     for (int j = 0; j < Cfg::kSub; ++j) {
                         const int k0 = (kc * Cfg::kSub + j) * kBK;
                         tma_load_2d(smem_u32(sm.a[s] + j * Cfg::kASub), &x_map, bar, k0, w.mt * kBM);
-                        // the weight rows in boxes of kWBox rows (128 B each), stacked
-                        for (int r = 0; r < w.width / Cfg::kWBox; ++r)
-                            tma_load_2d(smem_u32(sm.b[s] + j * Cfg::kBSub + r * Cfg::kWBox * 128), &w_map, bar, k0,
-                                        w.col0 + r * Cfg::kWBox);
+                        // the weight rows in runs of 32 (128 B each), stacked in logical order
+                        for (int r = 0; r < w.width / kRunCols; ++r)
+                            tma_load_2d(smem_u32(sm.b[s] + j * Cfg::kBSub + r * kRunCols * 128), &w_map, bar, k0,
+                                        run_row(w.col0 / kRunCols + r));
                     }
                 }
                 __syncwarp();
@@ -291,7 +388,7 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
         asm volatile("griddepcontrol.wait;" ::: "memory");
         const int row = warp * 32 + lane;                       // token row = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        int lt = 0, cached_mt = -1;
+        int lt = 0, cached_mt = -1, pos = -1;
         long long dst_row = -1;
         for (int k = 0;; ++k, ++lt) {
             const QkvItem w = qkv_item<BN>(k, m_tiles);
@@ -300,37 +397,15 @@ qkv_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CU
             const int acc = lt & 1;
             const int tok = mt * kBM + row;
             const bool live = tok < a.total_tokens;
-            const int col0 = w.col0;
-            if (col0 + w.width > kQCols && mt != cached_mt) {   // K/V columns: this token's cache slot
-                dst_row = live ? cache_row(a, tok) : -1;
+            // K/V columns need the token's cache slot, rotated q or k columns its position
+            if ((w.col0 + w.width > kQCols || a.rope) && mt != cached_mt) {
+                dst_row = live ? token_slot(a, tok, &pos) : -1;
                 cached_mt = mt;
             }
             const bool ok = wait_or_abort(smem_u32(&sm.acc_full[acc]), (lt >> 1) & 1, abort_flag, a.err);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < w.width / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(lane_base + (uint32_t)(acc * BN + c * 32), v);
-                tmem_wait_ld(v);
-                uint32_t w[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) w[e / 2] = pack_bf16x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-                const int col = col0 + c * 32;
-                __nv_bfloat16 *dst = nullptr;
-                if (col < kQCols) {
-                    if (live) dst = static_cast<__nv_bfloat16 *>(a.q_out) + (size_t)tok * kQCols + col;
-                } else if (dst_row >= 0) {
-                    const bool is_k = col < kQCols + kKVCols;
-                    const int kvc = col - kQCols - (is_k ? 0 : kKVCols);   // KV head * 128 + dim
-                    dst = static_cast<__nv_bfloat16 *>(is_k ? a.k_pool : a.v_pool) + dst_row + kvc;
-                }
-                if (dst) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-                }
-            }
+            store_tile_row(a, lane_base + (uint32_t)(acc * BN), w.col0, w.width, tok, live, dst_row, pos);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[acc]));
@@ -362,7 +437,6 @@ constexpr int kPairBN = 192;                           // 4096 tokens: 512 tiles
 constexpr uint32_t kPairABytes = kBM * kBK * 2;        // this CTA's 128 rows x 64: 16 KiB
 constexpr uint32_t kPairBBytes = (kPairBN / 2) * kBK * 2;   // this CTA's 96 weight rows: 12 KiB
 constexpr int kPairStages = (int)(kRingBytes / (kPairABytes + kPairBBytes));
-constexpr int kPairWBox = kPairBN / 2;                 // weight rows per TMA box (a CTA's half)
 constexpr uint32_t kPairIdesc = idesc_bf16(kPairBM, kPairBN, false);
 
 struct QkvPairSmem {
@@ -437,7 +511,7 @@ __device__ __forceinline__ void umma_commit_local(uint32_t bar) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 qkv_pair_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
-                const QkvArgs a) {
+                const __grid_constant__ QkvArgs a) {
     extern __shared__ uint8_t smem_raw[];
     QkvPairSmem &sm = *reinterpret_cast<QkvPairSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -504,9 +578,10 @@ qkv_pair_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
                     const uint32_t bar0 = peer_addr(bar, 0);
                     const int k0 = kc * kBK;
                     tma_load_2d_pair(smem_u32(sm.a[s]), &x_map, bar0, k0, w.mt * kPairBM + (int)rank * kBM);
-                    for (int r = 0; r < cols / kPairWBox; ++r)
-                        tma_load_2d_pair(smem_u32(sm.b[s] + r * kPairWBox * 128), &w_map, bar0, k0,
-                                         w.col0 + (int)rank * cols + r * kPairWBox);
+                    // this CTA's half of the tile's weight rows, in runs of 32 in logical order
+                    for (int r = 0; r < cols / kRunCols; ++r)
+                        tma_load_2d_pair(smem_u32(sm.b[s] + r * kRunCols * 128), &w_map, bar0, k0,
+                                         run_row((w.col0 + (int)rank * cols) / kRunCols + r));
                 }
                 __syncwarp();
             }
@@ -570,7 +645,7 @@ qkv_pair_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
         const int row = warp * 32 + lane;                       // token row = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         const uint32_t acc_empty0 = peer_addr(smem_u32(&sm.acc_empty[0]), 0);   // + 8 per accumulator
-        int lt = 0, cached_mt = -1;
+        int lt = 0, cached_mt = -1, pos = -1;
         long long dst_row = -1;
         for (int k = 0;; ++k, ++lt) {
             const QkvItem w = qkv_item_of<kPairBN>(k, m_tiles, clusters, cid);
@@ -578,36 +653,15 @@ qkv_pair_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant
             const int acc = lt & 1;
             const int tok = w.mt * kPairBM + (int)rank * kBM + row;
             const bool live = tok < a.total_tokens;
-            if (w.col0 + w.width > kQCols && w.mt != cached_mt) {   // K/V columns: this token's cache slot
-                dst_row = live ? cache_row(a, tok) : -1;
+            // K/V columns need the token's cache slot, rotated q or k columns its position
+            if ((w.col0 + w.width > kQCols || a.rope) && w.mt != cached_mt) {
+                dst_row = live ? token_slot(a, tok, &pos) : -1;
                 cached_mt = w.mt;
             }
             const bool ok = wait_or_abort(smem_u32(&sm.acc_full[acc]), (lt >> 1) & 1, abort_flag, a.err);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < w.width / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(lane_base + (uint32_t)(acc * kPairBN + c * 32), v);
-                tmem_wait_ld(v);
-                uint32_t p[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) p[e / 2] = pack_bf16x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-                const int col = w.col0 + c * 32;
-                __nv_bfloat16 *dst = nullptr;
-                if (col < kQCols) {
-                    if (live) dst = static_cast<__nv_bfloat16 *>(a.q_out) + (size_t)tok * kQCols + col;
-                } else if (dst_row >= 0) {
-                    const bool is_k = col < kQCols + kKVCols;
-                    const int kvc = col - kQCols - (is_k ? 0 : kKVCols);   // KV head * 128 + dim
-                    dst = static_cast<__nv_bfloat16 *>(is_k ? a.k_pool : a.v_pool) + dst_row + kvc;
-                }
-                if (dst) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) d4[q] = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
-                }
-            }
+            store_tile_row(a, lane_base + (uint32_t)(acc * kPairBN), w.col0, w.width, tok, live, dst_row, pos);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) arrive_remote(acc_empty0 + (uint32_t)acc * 8u);
@@ -693,7 +747,7 @@ cudaError_t launch_qkv_bn(const QkvArgs &a, const CUtensorMap &x_map, const CUte
 }  // namespace
 
 int qkv_tile_cols(int total_tokens) { return total_tokens <= 2 * kBM ? 64 : kPairBN; }
-int qkv_weight_box_rows(int total_tokens) { return total_tokens <= 2 * kBM ? 64 : kPairWBox; }
+int qkv_weight_box_rows() { return kRunCols; }
 int qkv_tile_rows_loaded(int total_tokens) { return total_tokens <= 32 ? 32 : kBM; }
 
 cudaError_t launch_qkv(const QkvArgs &a, const CUtensorMap &x_map, const CUtensorMap &w_map, int num_sms,

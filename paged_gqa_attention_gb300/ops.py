@@ -71,7 +71,8 @@ def load() -> ctypes.CDLL:
     lib.pa_check_error.restype = ctypes.c_int
     lib.kv_append.argtypes = [pa_shape, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32, vp, sz, vp]
     lib.kv_append.restype = ctypes.c_int
-    lib.paged_qkv_append.argtypes = [pa_shape, i32, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32, vp, sz,
+    lib.paged_qkv_append.argtypes = [pa_shape, i32, ctypes.c_float, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32,
+                                     vp, sz,
                                      vp]
     lib.paged_qkv_append.restype = ctypes.c_int
     lib.paged_attn_decode.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, f32, vp,
@@ -205,10 +206,14 @@ def kv_append(k_pool, v_pool, k_new, v_new, block_table, cu_q_lens, seq_lens, wo
 QKV_COLS = NUM_Q_HEADS * HEAD_DIM + 2 * NUM_KV_HEADS * HEAD_DIM   # 6144
 
 
+QWEN3_ROPE_THETA = 1.0e6
+
+
 def paged_qkv_append(x, w_qkv, k_pool, v_pool, block_table, cu_q_lens, seq_lens, workspace, *,
-                     q_out=None, stream=None) -> torch.Tensor:
+                     rope_theta: float = 0.0, q_out=None, stream=None) -> torch.Tensor:
     """Merged Q/K/V projection of the new tokens: x [T, hidden] @ w_qkv[6144, hidden]^T; returns
-    q [T, 32, 128] and writes k and v into the pools at each sequence's tail positions."""
+    q [T, 32, 128] and writes k and v into the pools at each sequence's tail positions.
+    rope_theta > 1 rotates the q and k heads at each token's position first (0: no rotation)."""
     dev = x.device
     _need(x, "x", torch.bfloat16, (None, None), dev)
     hidden = x.shape[1]
@@ -223,7 +228,7 @@ def paged_qkv_append(x, w_qkv, k_pool, v_pool, block_table, cu_q_lens, seq_lens,
     if q_out is None:
         q_out = torch.empty(x.shape[0], NUM_Q_HEADS, HEAD_DIM, dtype=torch.bfloat16, device=dev)
     _need(q_out, "q_out", torch.bfloat16, (x.shape[0], NUM_Q_HEADS, HEAD_DIM), dev)
-    st = load().paged_qkv_append(SHAPE, hidden, q_out.data_ptr(), x.data_ptr(), w_qkv.data_ptr(),
+    st = load().paged_qkv_append(SHAPE, hidden, float(rope_theta), q_out.data_ptr(), x.data_ptr(), w_qkv.data_ptr(),
                                  k_pool.data_ptr(), v_pool.data_ptr(), block_table.data_ptr(),
                                  block_table.shape[1], k_pool.shape[0], cu_q_lens.data_ptr(),
                                  seq_lens.data_ptr(), num_seqs, x.shape[0], workspace.data_ptr(),

@@ -76,14 +76,35 @@ def new_slots(b):
     return out
 
 
-def check_case(b, x, w):
+def exact_and_bound(x, w, cu_q_lens, seq_lens, rope_theta, rows=None):
+    """The oracle's exact outputs (q and k heads rotated when rope_theta > 0) and the
+    accumulation part of the bound: a rotated dim mixes the two columns of its pair, so it
+    carries both their accumulation errors, and the fp32 angle (about 1e-6 rad) adds
+    1e-5 x the pair's size."""
+    y = oracle.qkv_project(x.cpu(), w.cpu(), rows=rows)
+    a = abs_sums(x, w, rows)
+    if rope_theta:
+        pos = oracle.token_positions(cu_q_lens.cpu(), seq_lens.cpu())
+        if rows is not None:
+            pos = pos[np.asarray(rows)]
+        rot = oracle.rope(y, pos, rope_theta, first_col=0, n_heads=32)
+        rot = oracle.rope(rot, pos, rope_theta, first_col=4096, n_heads=8)
+        cols = np.arange(5120)
+        partner = cols ^ 64                       # the other dim of the pair in the same head
+        a = a.copy()
+        a[:, :5120] = a[:, cols] + a[:, partner] + 1e-5 * 2.0 ** 16 * (np.abs(y[:, cols]) + np.abs(y[:, partner]))
+        y = rot
+    return y, a
+
+
+def check_case(b, x, w, rope_theta=0.0):
     kp0 = b.k_pool.view(torch.int16).cpu().numpy().view(np.uint16).copy()
     vp0 = b.v_pool.view(torch.int16).cpu().numpy().view(np.uint16).copy()
     ws = workspace_for(b)
-    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws,
+                             rope_theta=rope_theta)
     ops.check_error(ws)
-    y = oracle.qkv_project(x.cpu(), w.cpu())
-    a = abs_sums(x, w)
+    y, a = exact_and_bound(x, w, b.cu_q_lens, b.seq_lens, rope_theta)
     qg = q.float().cpu().numpy().astype(np.float64).reshape(x.shape[0], -1)
     within_tol(qg, y[:, :4096], a[:, :4096], "q")
     rel = np.sqrt(((qg - y[:, :4096]) ** 2).sum() / (y[:, :4096] ** 2).sum())
@@ -116,6 +137,50 @@ def test_qkv_append_matches_oracle(ctx_and_q):
     check_case(b, x, w)
 
 
+@pytest.mark.parametrize("ctx_and_q", [
+    [(0, 1)],
+    [(0, 37)],                                  # 64-column tiles, 32 rows of x loaded
+    [(200, 100), (0, 64), (511, 1)],            # 64-column tiles, 128 rows
+    [(0, 300)],                                 # CTA pairs, a ragged last tile
+    [(37, 130), (1000, 0), (255, 200)],
+    [(131000, 40), (70000, 300)],               # large positions: angles of 10^5 rad
+])
+def test_qkv_append_with_rotary_embedding(ctx_and_q):
+    """Qwen3's rotary embedding (theta 1e6) on q and k before the rounding, against the
+    oracle's rotation of its exact projection at each token's absolute position."""
+    b = batch_for(ctx_and_q, seed=160 + len(ctx_and_q))
+    check_case(b, inputs(161, b.total_tokens), weights(162), rope_theta=ops.QWEN3_ROPE_THETA)
+
+
+def test_rotary_embedding_near_the_largest_position():
+    """Positions just below 2^24 (tables 65536 blocks wide, the widest a rotation accepts):
+    every table entry but the last two points at block 0, the new tokens go to blocks 1, 2."""
+    n = 40
+    seq_len = (1 << 24) - 3
+    width = 1 << 16
+    bt = torch.zeros(1, width, dtype=torch.int32)
+    p0 = seq_len - n
+    bt[0, p0 // 256] = 1
+    bt[0, (seq_len - 1) // 256] = 2
+    g = torch.Generator(device="cuda").manual_seed(170)
+    pools = [torch.randn(3, 256, 8, 128, generator=g, device="cuda").to(torch.bfloat16) for _ in range(2)]
+    b = wl.Batch(name="far", q=torch.empty(n, 32, 128, dtype=torch.bfloat16, device="cuda"),
+                 k_new=torch.empty(n, 8, 128, dtype=torch.bfloat16, device="cuda"),
+                 v_new=torch.empty(n, 8, 128, dtype=torch.bfloat16, device="cuda"),
+                 k_pool=pools[0], v_pool=pools[1], block_table=bt.cuda(),
+                 seq_lens=torch.tensor([seq_len], dtype=torch.int32, device="cuda"),
+                 cu_q_lens=torch.tensor([0, n], dtype=torch.int32, device="cuda"), max_q_len=n,
+                 seq_lens_host=[seq_len], q_lens_host=[n])
+    check_case(b, inputs(171, n), weights(172), rope_theta=ops.QWEN3_ROPE_THETA)
+    # one block wider and the positions could reach 2^24: refused before any launch
+    wide = torch.zeros(1, width + 1, dtype=torch.int32, device="cuda")
+    ws = workspace_for(b)
+    with pytest.raises(ops.PagedAttnError) as e:
+        ops.paged_qkv_append(inputs(171, n), weights(172), b.k_pool, b.v_pool, wide, b.cu_q_lens, b.seq_lens, ws,
+                             rope_theta=ops.QWEN3_ROPE_THETA)
+    assert e.value.status == 1
+
+
 @pytest.mark.parametrize("hidden", [256, 1280])
 @pytest.mark.parametrize("ctx_and_q", [[(10, 40)], [(0, 300)]])   # one CTA per tile; CTA pairs
 def test_other_hidden_sizes(hidden, ctx_and_q):
@@ -142,18 +207,20 @@ def test_decode_batch_one_token_per_sequence():
     check_case(b, inputs(64, b.total_tokens), weights(65))
 
 
-def test_full_prefill_chunk_sampled_rows():
-    """4096 new tokens (the causal prefill workload's prompt): sampled rows of q and of the
-    cache against the oracle, every other cache row untouched is not re-checked here."""
+@pytest.mark.parametrize("rope_theta", [0.0, ops.QWEN3_ROPE_THETA])
+def test_full_prefill_chunk_sampled_rows(rope_theta):
+    """4096 new tokens (the causal prefill workload's prompt), in the configuration the
+    benchmark times: sampled rows of q and of the cache against the oracle, every other
+    cache row untouched is not re-checked here."""
     b = wl.causal_prefill(device="cuda")
     x = inputs(66, b.total_tokens)
     w = weights(67)
     ws = workspace_for(b)
-    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws,
+                             rope_theta=rope_theta)
     ops.check_error(ws)
     rows = [0, 1, 127, 128, 2047, 2048, 4000, 4095]
-    y = oracle.qkv_project(x.cpu(), w.cpu(), rows=rows)
-    a = abs_sums(x, w, rows)
+    y, a = exact_and_bound(x, w, b.cu_q_lens, b.seq_lens, rope_theta, rows=rows)
     slots = new_slots(b)
     qg = q.float().cpu().numpy().astype(np.float64).reshape(b.total_tokens, -1)
     for r, t in enumerate(rows):
@@ -194,17 +261,20 @@ def test_bad_block_writes_no_kv_but_keeps_q(ctx_and_q):
     assert np.array_equal(a[~touched], o[~touched])
 
 
-def test_fused_append_feeds_the_decode():
-    """The fused projection + append followed by the decode equals the decode over the
-    oracle's appended cache (within the attention tolerance)."""
+@pytest.mark.parametrize("rope_theta", [0.0, ops.QWEN3_ROPE_THETA])
+def test_fused_append_feeds_the_decode(rope_theta):
+    """The fused projection + append (with or without the rotary embedding) followed by the
+    decode equals the decode over the oracle's appended cache (within the attention
+    tolerance)."""
     from gpu_helpers import assert_close
     b = wl.batched_decode(device="cuda", seed=71, batch=8, hi=1500, num_blocks=64)
     x = inputs(72, b.total_tokens)
     w = weights(73)
     q_ref, kp, vp = oracle.qkv_append(x.cpu(), w.cpu(), b.k_pool.cpu(), b.v_pool.cpu(), b.block_table.cpu(),
-                                      b.cu_q_lens.cpu(), b.seq_lens.cpu())
+                                      b.cu_q_lens.cpu(), b.seq_lens.cpu(), rope_theta=rope_theta)
     ws = workspace_for(b)
-    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws,
+                             rope_theta=rope_theta)
     out = ops.paged_attn_decode(q, b.k_pool, b.v_pool, b.block_table, b.seq_lens, ws)
     ops.check_error(ws)
     # the oracle attends with the GPU's q (its own q is exact fp64, the GPU's is bf16)
@@ -213,17 +283,20 @@ def test_fused_append_feeds_the_decode():
     assert_close(out, ref, "decode after the fused projection")
 
 
+@pytest.mark.parametrize("rope_theta", [0.0, ops.QWEN3_ROPE_THETA])
 @pytest.mark.parametrize("ctx_and_q", [[(0, 300)], [(0, 4096)]])
-def test_repeated_calls_are_bit_identical(ctx_and_q):
+def test_repeated_calls_are_bit_identical(ctx_and_q, rope_theta):
     """The CTA-pair path is deterministic: q and the appended cache rows repeat bit for bit."""
     b = batch_for(ctx_and_q, seed=90)
     x = inputs(91, b.total_tokens)
     w = weights(92)
     ws = workspace_for(b)
-    q1 = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws).clone()
+    q1 = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws,
+                              rope_theta=rope_theta).clone()
     k1, v1 = b.k_pool.clone(), b.v_pool.clone()
     for _ in range(3):
-        q2 = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+        q2 = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws,
+                                  rope_theta=rope_theta)
         ops.check_error(ws)
         assert torch.equal(q1.view(torch.int16), q2.view(torch.int16))
         assert torch.equal(k1.view(torch.int16), b.k_pool.view(torch.int16))
