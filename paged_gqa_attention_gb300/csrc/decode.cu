@@ -149,7 +149,11 @@ decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     const int pair = blockIdx.x;          // sequence * 8 + kv head
     const int b = pair / kHkv;
     const int g = pair % kHkv;
-    const int split = blockIdx.y;
+    // CTAs start in the order of their linear index (x fastest).  Without a cluster the
+    // highest splits go first: only long contexts have them and their splits are the longest,
+    // so the long work starts early and the short single splits of short contexts fill the
+    // tail (close to longest-first, at no cost: the split index alone decides).
+    const int split = kCluster ? (int)blockIdx.y : (int)(gridDim.y - 1 - blockIdx.y);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 

@@ -89,7 +89,8 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_consta
     const int pair = blockIdx.x;          // sequence * 8 + kv head
     const int b = pair / kHkv;
     const int g = pair % kHkv;
-    const int split = blockIdx.y;
+    // the highest splits start first (longest work first, as in decode.cu)
+    const int split = (int)(gridDim.y - 1 - blockIdx.y);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
