@@ -13,11 +13,13 @@ from paged_gqa_attention_gb300 import workloads as wl
 MAX_ABS = 1e-2
 REL_RMS = 5e-3
 # lse = m + log(sum_j p~_j), where p~_j = bf16(p_j) are the same rounded weights the PV
-# product uses (so the normalised weights sum to one).  bf16 round-to-nearest changes
-# each weight by a relative |d| <= 2^-9, hence the sum by at most 2^-9 relative and the
-# log by at most log(1 + 2^-9) = 1.95e-3; fp32 accumulation of the 128-term scores adds
-# about 1e-4.  Bar: 2.5e-3 absolute.
-LSE_ABS = 2.5e-3
+# product uses (so the normalised weights sum to one).  bf16 keeps 8 significant bits (7
+# stored, 1 implicit): between 1 and 2 its values are 2^-7 apart, so round-to-nearest
+# changes a weight by up to half of that, a relative |d| <= 2^-8 (1 + 2^-8 rounds to 1).
+# Hence the sum moves by at most 2^-8 relative and the log by at most
+# log(1 + 2^-8) = 3.90e-3, reached when one weight dominates the sum; fp32 accumulation of
+# the 128-term scores adds about 1e-4.  Bar: 4e-3 absolute.
+LSE_ABS = 4e-3
 
 
 def lib_ready():
