@@ -294,6 +294,9 @@ def decode_measure(batch, steps, warmup, flush_buf, stream, clocks):
 
 
 def prefill_measure(batch, steps, warmup, flush_buf, stream, clocks):
+    """One prefill step: the append of the prompt's K/V fused with the causal attention
+    (paged_attn_prefill_append, one kernel).  The same step as two calls (kv_append, then
+    paged_attn_prefill) is timed too, over fewer steps, for comparison."""
     import torch
 
     from paged_gqa_attention_gb300 import ops
@@ -303,6 +306,13 @@ def prefill_measure(batch, steps, warmup, flush_buf, stream, clocks):
 
     def step(tm):
         if tm: tm.record(0)
+        ops.paged_attn_prefill_append(batch.q, batch.k_new, batch.v_new, batch.k_pool, batch.v_pool,
+                                      batch.block_table, batch.cu_q_lens, batch.seq_lens, batch.max_q_len, ws,
+                                      out=out)
+        if tm: tm.record(1)
+
+    def two_calls(tm):
+        if tm: tm.record(0)
         ops.kv_append(batch.k_pool, batch.v_pool, batch.k_new, batch.v_new, batch.block_table,
                       batch.cu_q_lens, batch.seq_lens, ws)
         if tm: tm.record(1)
@@ -310,14 +320,19 @@ def prefill_measure(batch, steps, warmup, flush_buf, stream, clocks):
                                batch.cu_q_lens, batch.seq_lens, batch.max_q_len, ws, out=out)
         if tm: tm.record(2)
 
-    spans, wall = run_timed(step, 3, steps, warmup, flush_buf, stream, clocks)
+    spans, wall = run_timed(step, 2, steps, warmup, flush_buf, stream, clocks)
+    spans2, _ = run_timed(two_calls, 3, max(10, min(steps, 200)), warmup, flush_buf, stream)
     ops.check_error(ws)
-    return {"append_ms": mean([s[0] for s in spans]), "attn_ms": mean([s[1] for s in spans]),
-            "step_ms": mean([s[0] + s[1] for s in spans]), "step_pcts": pcts([s[0] + s[1] for s in spans]),
-            "wall_s": wall, "launches": 2 * steps}
+    return {"step_ms": mean([s[0] for s in spans]), "step_pcts": pcts([s[0] for s in spans]),
+            "two_call_append_ms": mean([s[0] for s in spans2]), "two_call_prefill_ms": mean([s[1] for s in spans2]),
+            "wall_s": wall, "launches": steps}
 
 
 def mixed_measure(batch, steps, warmup, flush_buf, stream, clocks):
+    """One continuous-batching step: the decode sequences' append fused into their decode
+    (paged_attn_decode_append) and the chunks' append fused into their prefill
+    (paged_attn_prefill_append): two kernels.  The same step as three calls (one kv_append for
+    every new token, the decode, the prefill) is timed too."""
     import torch
 
     from paged_gqa_attention_gb300 import ops
@@ -331,6 +346,15 @@ def mixed_measure(batch, steps, warmup, flush_buf, stream, clocks):
 
     def step(tm):
         if tm: tm.record(0)
+        ops.paged_attn_decode_append(dec.q, dec.k_new, dec.v_new, dec.k_pool, dec.v_pool, dec.block_table,
+                                     dec.seq_lens, ws, out=out_d)
+        if tm: tm.record(1)
+        ops.paged_attn_prefill_append(pre.q, pre.k_new, pre.v_new, pre.k_pool, pre.v_pool, pre.block_table,
+                                      pre.cu_q_lens, pre.seq_lens, pre.max_q_len, ws, out=out_p)
+        if tm: tm.record(2)
+
+    def three_calls(tm):
+        if tm: tm.record(0)
         ops.kv_append(batch.k_pool, batch.v_pool, batch.k_new, batch.v_new, batch.block_table,
                       batch.cu_q_lens, batch.seq_lens, ws)
         if tm: tm.record(1)
@@ -341,13 +365,14 @@ def mixed_measure(batch, steps, warmup, flush_buf, stream, clocks):
                                pre.seq_lens, pre.max_q_len, ws, out=out_p)
         if tm: tm.record(3)
 
-    spans, wall = run_timed(step, 4, steps, warmup, flush_buf, stream, clocks)
+    spans, wall = run_timed(step, 3, steps, warmup, flush_buf, stream, clocks)
+    spans3, _ = run_timed(three_calls, 4, max(10, min(steps, 200)), warmup, flush_buf, stream)
     ops.check_error(ws)
-    return {"append_ms": mean([s[0] for s in spans]), "decode_ms": mean([s[1] for s in spans]),
-            "prefill_ms": mean([s[2] for s in spans]),
+    return {"decode_ms": mean([s[0] for s in spans]), "prefill_ms": mean([s[1] for s in spans]),
             "step_ms": mean([sum(s) for s in spans]), "step_pcts": pcts([sum(s) for s in spans]),
-            "wall_s": wall, "launches": 3 * steps,
-            "dec": dec, "pre": pre}
+            "three_call": {"kv_append_ms": mean([s[0] for s in spans3]), "decode_ms": mean([s[1] for s in spans3]),
+                           "prefill_ms": mean([s[2] for s in spans3])},
+            "wall_s": wall, "launches": 2 * steps, "dec": dec, "pre": pre}
 
 
 def layered_measure(layers, steps, warmup, flush_buf, stream, clocks):
@@ -618,28 +643,27 @@ def e2e_measure(batch, kind, steps, warmup, stream):
     def step():
         for k in host:
             dev[k].copy_(host[k], non_blocking=True)
-        if kind != "decode":
-            ops.kv_append(batch.k_pool, batch.v_pool, dev["k_new"], dev["v_new"], dev["block_table"],
-                          dev["cu_q_lens"], dev["seq_lens"], ws)
         if kind == "decode":
             ops.paged_attn_decode_append(dev["q"], dev["k_new"], dev["v_new"], batch.k_pool,
                                          batch.v_pool, dev["block_table"], dev["seq_lens"], ws,
                                          out=out_dev)
         elif kind == "cascade":
+            ops.kv_append(batch.k_pool, batch.v_pool, dev["k_new"], dev["v_new"], dev["block_table"],
+                          dev["cu_q_lens"], dev["seq_lens"], ws)
             ops.paged_attn_decode_cascade(dev["q"], batch.k_pool, batch.v_pool, dev["block_table"],
                                           dev["seq_lens"], shared, cws, out=out_dev)
         elif kind == "prefill":
-            ops.paged_attn_prefill(dev["q"], batch.k_pool, batch.v_pool, dev["block_table"],
-                                   dev["cu_q_lens"], dev["seq_lens"], batch.max_q_len, ws,
-                                   out=out_dev)
+            ops.paged_attn_prefill_append(dev["q"], dev["k_new"], dev["v_new"], batch.k_pool, batch.v_pool,
+                                          dev["block_table"], dev["cu_q_lens"], dev["seq_lens"], batch.max_q_len, ws,
+                                          out=out_dev)
         else:  # mixed: decode sequences, then prefill chunks, from the same device copies
-            ops.paged_attn_decode(dev["q"][:t_dec], batch.k_pool, batch.v_pool,
-                                  dev["block_table"][:n_dec], dev["seq_lens"][:n_dec], ws,
-                                  out=out_dev[:t_dec])
+            ops.paged_attn_decode_append(dev["q"][:t_dec], dev["k_new"][:t_dec], dev["v_new"][:t_dec],
+                                         batch.k_pool, batch.v_pool, dev["block_table"][:n_dec],
+                                         dev["seq_lens"][:n_dec], ws, out=out_dev[:t_dec])
             cu_p = dev["cu_q_lens"][n_dec:] - t_dec
-            ops.paged_attn_prefill(dev["q"][t_dec:], batch.k_pool, batch.v_pool,
-                                   dev["block_table"][n_dec:], cu_p, dev["seq_lens"][n_dec:],
-                                   batch.max_q_len, ws, out=out_dev[t_dec:])
+            ops.paged_attn_prefill_append(dev["q"][t_dec:], dev["k_new"][t_dec:], dev["v_new"][t_dec:],
+                                          batch.k_pool, batch.v_pool, dev["block_table"][n_dec:], cu_p,
+                                          dev["seq_lens"][n_dec:], batch.max_q_len, ws, out=out_dev[t_dec:])
         out_host.copy_(out_dev, non_blocking=True)
 
     for _ in range(warmup):
@@ -1137,13 +1161,15 @@ def measure(wname, steps, warmup, e2e_steps, peaks, flush_buf, stream, clocks, w
         r = prefill_measure(batch, steps, warmup, flush_buf, stream, clocks)
         flops = batch.attention_flops()
         step_ms = dist_max(r["step_ms"], world)
-        attn_ms = dist_max(r["attn_ms"], world)
         e.update(value=world * flops / (step_ms * 1e-3) / 1e12, unit="TFLOP/s", ms_per_step=step_ms)
-        e["roofline"] = roofline(flops / (attn_ms * 1e-3) / 1e12, peaks["bf16_tflops"],
+        # the step is one kernel: the prefill with the prompt's append fused in
+        e["roofline"] = roofline(flops / (step_ms * 1e-3) / 1e12, peaks["bf16_tflops"],
                                  "TFLOP/s", "tensor", traffic_for("prefill", wname))
-        e["roofline"]["kernel"] = "prefill_kernel"
+        e["roofline"]["kernel"] = "prefill_kernel (append fused)"
         e["roofline"]["algorithmic_flops_per_launch"] = flops
-        e["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "prefill_us": r["attn_ms"] * 1e3}
+        e["kernels"] = {"prefill_append_us": r["step_ms"] * 1e3,
+                        "two_call_step": {"kv_append_us": r["two_call_append_ms"] * 1e3,
+                                          "prefill_us": r["two_call_prefill_ms"] * 1e3}}
         e["gpu_launches"] = r["launches"]
         x = e2e_measure(batch, "prefill", max(10, min(e2e_steps, 50)), 3, stream)
         x_ms = dist_max(x["step_ms"], world)
@@ -1161,16 +1187,16 @@ def measure(wname, steps, warmup, e2e_steps, peaks, flush_buf, stream, clocks, w
         e.update(value=world * kv_bytes / (step_ms * 1e-3) / 1e9, unit="GB/s", ms_per_step=step_ms)
         e["roofline"] = roofline(kv_bytes / (r["decode_ms"] * 1e-3) / 1e9, peaks["hbm_gbs"],
                                  "GB/s", "hbm", traffic_for("decode", wname))
-        e["roofline"]["kernel"] = "decode_kernel"
+        e["roofline"]["kernel"] = "decode_kernel (append fused)"
         e["roofline"]["algorithmic_bytes_per_launch"] = kv_bytes
         e["prefill_roofline"] = dict(roofline(flops / (r["prefill_ms"] * 1e-3) / 1e12, peaks["bf16_tflops"],
                                               "TFLOP/s", "tensor", traffic_for("prefill", wname)),
-                                     kernel="prefill_kernel (+ planning kernel)",
+                                     kernel="prefill_kernel (append fused; + planning kernel)",
                                      algorithmic_flops_per_launch=flops)
-        e["kernels"] = {"kv_append_us": r["append_ms"] * 1e3, "decode_us": r["decode_ms"] * 1e3,
-                        "prefill_us": r["prefill_ms"] * 1e3,
+        e["kernels"] = {"decode_append_us": r["decode_ms"] * 1e3, "prefill_append_us": r["prefill_ms"] * 1e3,
                         "prefill_tflops": flops / (r["prefill_ms"] * 1e-3) / 1e12,
-                        "combined_roofline_frac": (t_bw + t_tc) / step_ms}
+                        "combined_roofline_frac": (t_bw + t_tc) / step_ms,
+                        "three_call_step": {k.replace("_ms", "_us"): v * 1e3 for k, v in r["three_call"].items()}}
         e["gpu_launches"] = r["launches"]
         x = e2e_measure(batch, "mixed", max(10, min(e2e_steps, 100)), 3, stream)
         x_ms = dist_max(x["step_ms"], world)

@@ -393,6 +393,27 @@ pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *
                              size_t workspace_bytes, void *stream);
 
 /*
+ * paged_attn_prefill_append: kv_append of each sequence's new tokens followed by
+ * paged_attn_prefill, in one kernel [P1 §4.3.1 append, §4.4.1 prefill; P3 §4.2 "append,
+ * then attend"].  k_new / v_new are [total_tokens][8][128] bf16 rows grouped by sequence as
+ * in kv_append.  The attention reads the new tokens' keys and values straight from k_new /
+ * v_new (their key tiles start at each sequence's first new token) and the cache for the
+ * positions before them; a warp of every CTA meanwhile writes the new rows into their cache
+ * slots, which nothing in the call reads.  Pools are bit-identical to kv_append's; outputs
+ * are those of the two calls up to rounding (bit-identical when every sequence's earlier
+ * context is a multiple of 128 tokens, where both calls cut the keys into the same tiles).
+ * Arguments, workspace and errors as for kv_append and paged_attn_prefill.
+ */
+pa_status paged_attn_prefill_append(pa_shape shape, void *out, float *lse, const void *q,
+                                    const void *k_new, const void *v_new, void *k_pool,
+                                    void *v_pool, const int32_t *block_table,
+                                    int32_t max_blocks_per_seq, int32_t num_blocks,
+                                    const int32_t *cu_q_lens, const int32_t *seq_lens,
+                                    int32_t num_seqs, int32_t total_tokens, int32_t max_q_len,
+                                    float scale, void *workspace, size_t workspace_bytes,
+                                    void *stream);
+
+/*
  * Self-test of the bounded-wait machinery: launches one CTA that waits on a
  * barrier nothing will ever complete, with a limit of timeout_us microseconds.
  * The kernel gives up, records PA_ERR_TIMEOUT in the workspace and exits; the GPU

@@ -84,6 +84,18 @@ bool encode_q_map(CUtensorMap *map, const void *q, int tokens) {
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// New K or V rows [tokens][8][128] bf16 as a 3-D tensor (dim, head, token), box {64, 1, 128}:
+// the same shared-memory tile as a pool map with 128-slot boxes.
+bool encode_new_rows_map(CUtensorMap *map, const void *rows, int tokens) {
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kHkv, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)kTokenBytes};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)kPrefillKvTile};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(rows), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A row-major bf16 matrix [rows][cols] as a 2-D tensor (col, row), box {64, box_rows},
 // 128-byte swizzle (cols a multiple of 8 so that the row stride is 16-byte aligned).
 bool encode_matrix_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
@@ -698,11 +710,11 @@ pa_status paged_attn_decode_static(pa_shape shape, void *out, float *lse, const 
     return launch_decode(a, k_map, v_map, sms, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
-                             const void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
-                             int32_t num_blocks, const int32_t *cu_q_lens, const int32_t *seq_lens, int32_t num_seqs,
-                             int32_t total_tokens, int32_t max_q_len, float scale, void *workspace,
-                             size_t workspace_bytes, void *stream) {
+static pa_status prefill_impl(pa_shape shape, void *out, float *lse, const void *q, const void *k_new,
+                              const void *v_new, const void *k_pool, const void *v_pool, const int32_t *block_table,
+                              int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t *cu_q_lens,
+                              const int32_t *seq_lens, int32_t num_seqs, int32_t total_tokens, int32_t max_q_len,
+                              float scale, void *workspace, size_t workspace_bytes, void *stream) {
     if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || max_q_len < 0 || max_blocks_per_seq < 1 || num_blocks < 1 ||
         !std::isfinite(scale) || (num_seqs == 0 && total_tokens != 0) || max_q_len > total_tokens ||
@@ -717,12 +729,16 @@ pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned4(block_table) ||
         !aligned4(cu_q_lens) || !aligned4(seq_lens) || (lse && !aligned4(lse)))
         return PA_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+        return PA_ERR_INVALID_ARG;
     const int sms = sm_count();
     if (sms <= 0) return PA_ERR_CUDA;
     if (!get_encoder()) return PA_ERR_CUDA;
-    CUtensorMap q_map, k_map, v_map;
+    CUtensorMap q_map, k_map, v_map, kn_map, vn_map;
     if (!encode_q_map(&q_map, q, total_tokens) || !encode_pool_map(&k_map, k_pool, num_blocks, kPrefillKvTile) ||
         !encode_pool_map(&v_map, v_pool, num_blocks, kPrefillKvTile))
+        return PA_ERR_INVALID_ARG;
+    if (k_new && (!encode_new_rows_map(&kn_map, k_new, total_tokens) || !encode_new_rows_map(&vn_map, v_new, total_tokens)))
         return PA_ERR_INVALID_ARG;
     PrefillArgs a = {};
     a.out = out;
@@ -740,15 +756,42 @@ pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *
     a.prefix_len = 0;
     a.kv_split_tiles = 0;
     a.n_kv_splits = 1;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_pool_w = const_cast<void *>(k_pool);
+    a.v_pool_w = const_cast<void *>(v_pool);
     // Several sequences: the units are sorted by work first, into the workspace's partial
     // area (decode scratch, unused by the prefill) when it is large enough.
     a.order = nullptr;
     const long long plan_units = prefill_plan_units(a);
     if (plan_units > 0 && workspace_bytes >= kPartialOffset + (size_t)plan_units * sizeof(int32_t))
         a.order = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + kPartialOffset);
-    return launch_prefill(a, q_map, k_map, v_map, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? PA_OK
-               : PA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = k_new ? launch_prefill_append(a, q_map, k_map, v_map, kn_map, vn_map, sms, st)
+                                : launch_prefill(a, q_map, k_map, v_map, sms, st);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *q, const void *k_pool,
+                             const void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
+                             int32_t num_blocks, const int32_t *cu_q_lens, const int32_t *seq_lens, int32_t num_seqs,
+                             int32_t total_tokens, int32_t max_q_len, float scale, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    return prefill_impl(shape, out, lse, q, nullptr, nullptr, k_pool, v_pool, block_table, max_blocks_per_seq,
+                        num_blocks, cu_q_lens, seq_lens, num_seqs, total_tokens, max_q_len, scale, workspace,
+                        workspace_bytes, stream);
+}
+
+pa_status paged_attn_prefill_append(pa_shape shape, void *out, float *lse, const void *q, const void *k_new,
+                                    const void *v_new, void *k_pool, void *v_pool, const int32_t *block_table,
+                                    int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t *cu_q_lens,
+                                    const int32_t *seq_lens, int32_t num_seqs, int32_t total_tokens,
+                                    int32_t max_q_len, float scale, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+    if (total_tokens > 0 && (!k_new || !v_new)) return PA_ERR_INVALID_ARG;
+    return prefill_impl(shape, out, lse, q, k_new, v_new, k_pool, v_pool, block_table, max_blocks_per_seq,
+                        num_blocks, cu_q_lens, seq_lens, num_seqs, total_tokens, max_q_len, scale, workspace,
+                        workspace_bytes, stream);
 }
 
 pa_status pa_decode_graph_create(pa_shape shape, int32_t layers, void *out, float *lse, const void *q,

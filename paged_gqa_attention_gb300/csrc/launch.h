@@ -88,6 +88,13 @@ struct PrefillArgs {
     // first), written by a planning kernel launched just before the prefill; nullptr: the
     // units are dealt in their natural order (latest query blocks first).
     int32_t *order;
+    // Fused append (k_new != nullptr): the new tokens' K/V rows [total_tokens][8][128] bf16 are
+    // attended straight from k_new / v_new (key tiles of the new positions start at each
+    // sequence's first new token) and written into the pools by the kernel itself.
+    const void *k_new;
+    const void *v_new;
+    void *k_pool_w;
+    void *v_pool_w;
 };
 
 constexpr int kRopePairs = 64;   // rotated pairs of a 128-dim head
@@ -148,6 +155,12 @@ long long prefill_plan_units(const PrefillArgs &a);
 cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
                            const CUtensorMap &k_map, const CUtensorMap &v_map, int num_sms,
                            cudaStream_t stream);
+
+// The prefill with the append of the new tokens fused in (a.k_new set): kn_map / vn_map are
+// 3-D maps (dim, head, token) over k_new / v_new with box {64, 1, 128}.
+cudaError_t launch_prefill_append(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
+                                  const CUtensorMap &v_map, const CUtensorMap &kn_map, const CUtensorMap &vn_map,
+                                  int num_sms, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(uint32_t *err, uint64_t limit_ns, cudaStream_t stream);
 

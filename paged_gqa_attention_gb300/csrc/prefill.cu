@@ -54,7 +54,9 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;              // Q and K loads
 constexpr int kMmaWarp = 9;
 constexpr int kVProducerWarp = 10;            // V loads
+constexpr int kAppendWarp = 11;               // fused append only: new K/V rows into the pools
 constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
+constexpr int kThreadsAppend = kThreads + 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kHalf = kRows * 128;            // 128 rows x 64 dims x 2 B = 16 KiB
 constexpr uint32_t kTileBytes = 2 * kHalf;    // a full 128 x 128 bf16 tile
@@ -96,8 +98,23 @@ struct Unit {
     int kt0;        // first key tile visited (0 unless the keys are split)
     int n_kt;       // key tiles to visit: kt0 .. kt0 + n_kt - 1
     int ks;         // key split of the unit (shared-prefix mode)
+    // Key tiles 0 .. n_old-1 hold positions 128j .. 128j+127 of the cache, only those below c0
+    // being keys; with a fused append the tiles after them hold the new positions from c0 on,
+    // 128 a tile (c0 + 128(j - n_old) + r), read from k_new rows tok_base + 128(j - n_old) + r.
+    // Without one, c0 = seq_len and every tile is a cache tile.
+    int c0;
+    int n_old;
+    int tok_base;
 };
 
+// Position of row 0 of key tile jg and the bound past which its rows are not keys.
+__device__ __forceinline__ void key_tile_span(const Unit &t, int jg, int &base, int &limit) {
+    const bool old_tile = jg < t.n_old;
+    base = old_tile ? jg * kKT : t.c0 + (jg - t.n_old) * kKT;
+    limit = old_tile ? t.c0 : t.seq_len;
+}
+
+template <bool kAppend>
 __device__ __forceinline__ Unit unit_at(const PrefillArgs &a, int idx, int qblocks) {
     Unit t;
     const int per_qb = a.num_seqs * kHkv;
@@ -123,8 +140,17 @@ __device__ __forceinline__ Unit unit_at(const PrefillArgs &a, int idx, int qbloc
     t.pos0 = seq_len - q_len + qb * kUnitPos;
     t.seq_len = seq_len;
     t.kt0 = 0;
-    t.n_kt = (t.pos0 + t.positions - 1) / kKT + 1;
     t.ks = 0;
+    t.tok_base = c0;
+    if constexpr (kAppend) {
+        t.c0 = seq_len - q_len;
+        t.n_old = (t.c0 + kKT - 1) / kKT;
+        t.n_kt = t.n_old + (t.pos0 + t.positions - 1 - t.c0) / kKT + 1;
+    } else {
+        t.c0 = seq_len;
+        t.n_kt = (t.pos0 + t.positions - 1) / kKT + 1;
+        t.n_old = t.n_kt;
+    }
     return t;
 }
 
@@ -146,20 +172,24 @@ __device__ __forceinline__ Unit unit_at_prefix(const PrefillArgs &a, int idx, in
     t.kt0 = ks * a.kv_split_tiles;
     t.n_kt = min(a.kv_split_tiles, (a.prefix_len + kKT - 1) / kKT - t.kt0);
     t.ks = ks;
+    t.c0 = t.seq_len;
+    t.n_old = t.kt0 + t.n_kt;
+    t.tok_base = 0;
     if (t.n_kt <= 0) t.run = false;
     return t;
 }
 
-template <bool kPrefix, bool kPlanned>
+template <bool kPrefix, bool kPlanned, bool kAppend>
 __device__ __forceinline__ Unit unit_for(const PrefillArgs &a, int idx, int qblocks) {
     if constexpr (kPrefix) return unit_at_prefix(a, idx, qblocks);
-    else if constexpr (kPlanned) return unit_at(a, __ldg(a.order + idx), qblocks);
-    else return unit_at(a, idx, qblocks);
+    else if constexpr (kPlanned) return unit_at<kAppend>(a, __ldg(a.order + idx), qblocks);
+    else return unit_at<kAppend>(a, idx, qblocks);
 }
 
 // Key tiles of unit idx (the unit_at rule; 0 for a unit without work, which sorts last).
+template <bool kAppend>
 __device__ __forceinline__ int plan_key(const PrefillArgs &a, int idx, int qblocks) {
-    const Unit t = unit_at(a, idx, qblocks);
+    const Unit t = unit_at<kAppend>(a, idx, qblocks);
     return t.run ? t.n_kt : 0;
 }
 
@@ -172,6 +202,7 @@ inline int plan_keys(const PrefillArgs &a) { return 2 * a.max_blocks_per_seq + 2
 // first (longest processing time first), written as order[rank] = unit.  Units with equal
 // keys take their ranks in whatever order the atomics resolve; every unit is computed by
 // one CTA on its own, so the outputs do not depend on that order.  nk = key buckets.
+template <bool kAppend>
 __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const PrefillArgs a, int qblocks, int total,
                                                                        int nk) {
     __shared__ int hist[kPlanMaxKeys];
@@ -180,7 +211,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const Pre
     for (int k = tid; k < nk; k += kPlanThreads) hist[k] = 0;
     __syncthreads();
     for (int idx = tid; idx < total; idx += kPlanThreads)
-        atomicAdd(&hist[min(plan_key(a, idx, qblocks), nk - 1)], 1);
+        atomicAdd(&hist[min(plan_key<kAppend>(a, idx, qblocks), nk - 1)], 1);
     __syncthreads();
     // hist[k] <- first rank of key k = number of units with more key tiles.  Thread t owns
     // the keys hi, hi - 1, ..., hi - per + 1 counted from the top.
@@ -218,7 +249,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const Pre
     }
     __syncthreads();
     for (int idx = tid; idx < total; idx += kPlanThreads) {
-        const int rank = atomicAdd(&hist[min(plan_key(a, idx, qblocks), nk - 1)], 1);
+        const int rank = atomicAdd(&hist[min(plan_key<kAppend>(a, idx, qblocks), nk - 1)], 1);
         a.order[rank] = idx;
     }
     // Complete only after the kernel before this one on the stream (kv_append lets its
@@ -250,10 +281,79 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     }
 }
 
-template <bool kPrefix, bool kPlanned>
-__global__ void __launch_bounds__(kThreads, 1)
+// The fused append's warp: this CTA's share of the new tokens' K and V rows (2 KiB each, all
+// 8 KV heads) copied into their cache slots by the kv_append rule, two tokens at a time with
+// 16-byte accesses.  Nothing in this kernel reads those slots (the attention takes the new
+// rows from k_new / v_new), so the copies run beside the attention without any ordering; the
+// kernel's completion publishes them.
+__device__ __forceinline__ void append_share(const PrefillArgs &a, int lane) {
+    const long long tt = a.total_tokens;
+    const int t_lo = (int)(tt * blockIdx.x / gridDim.x), t_hi = (int)(tt * (blockIdx.x + 1) / gridDim.x);
+    if (t_lo >= t_hi) return;
+    int lo = 0, hi = a.num_seqs - 1;   // the sequence of the share's first token
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.cu_q_lens + mid) <= t_lo) lo = mid;
+        else hi = mid - 1;
+    }
+    int s = lo, q0 = __ldg(a.cu_q_lens + s), q1 = __ldg(a.cu_q_lens + s + 1), seq_len = __ldg(a.seq_lens + s);
+    int cached_j = -1, blk = -1;
+    for (int t = t_lo; t < t_hi; t += 2) {
+        uint4 r[2][8];
+        long long dst[2] = {-1, -1};
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int tu = t + u;
+            if (tu >= t_hi) break;
+            while (tu >= q1 && s + 1 < a.num_seqs) {   // next sequence (empty ones skipped)
+                ++s;
+                q0 = q1;
+                q1 = __ldg(a.cu_q_lens + s + 1);
+                seq_len = __ldg(a.seq_lens + s);
+                cached_j = -1;
+            }
+            const uint4 *ks = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.k_new) + (size_t)tu * kTokenBytes);
+            const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.v_new) + (size_t)tu * kTokenBytes);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                r[u][k] = __ldg(ks + lane + 32 * k);
+                r[u][4 + k] = __ldg(vs + lane + 32 * k);
+            }
+            const int q_len = q1 - q0, i = tu - q0;
+            if (i < 0 || i >= q_len || seq_len < q_len || seq_len > a.max_blocks_per_seq * kBlock) {
+                if (lane == 0) record_error(a.err, kErrDevice | kErrQLen);
+                continue;
+            }
+            const int p = seq_len - q_len + i;
+            if (p / kBlock != cached_j) {
+                cached_j = p / kBlock;
+                blk = __ldg(a.block_table + (size_t)s * a.max_blocks_per_seq + cached_j);
+            }
+            if (blk < 0 || blk >= a.num_blocks) {
+                if (lane == 0) record_error(a.err, kErrDevice | kErrBadBlock);
+                continue;
+            }
+            dst[u] = ((long long)blk * kBlock + p % kBlock) * kTokenBytes;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (dst[u] < 0) continue;
+            uint4 *kd = reinterpret_cast<uint4 *>(static_cast<char *>(a.k_pool_w) + dst[u]);
+            uint4 *vd = reinterpret_cast<uint4 *>(static_cast<char *>(a.v_pool_w) + dst[u]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                kd[lane + 32 * k] = r[u][k];
+                vd[lane + 32 * k] = r[u][4 + k];
+            }
+        }
+    }
+}
+
+template <bool kPrefix, bool kPlanned, bool kAppend>
+__global__ void __launch_bounds__(kAppend ? kThreadsAppend : kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
-               const __grid_constant__ CUtensorMap v_map, const PrefillArgs a) {
+               const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap kn_map,
+               const __grid_constant__ CUtensorMap vn_map, const PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
     PrefillSmem &sm = *reinterpret_cast<PrefillSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -304,8 +404,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             if (qk) {
                 tma_prefetch_map(&q_map);
                 tma_prefetch_map(&k_map);
+                if constexpr (kAppend) tma_prefetch_map(&kn_map);
             } else {
                 tma_prefetch_map(&v_map);
+                if constexpr (kAppend) tma_prefetch_map(&vn_map);
             }
         }
         // The pools may be written by the kernel just before this one on the stream
@@ -315,13 +417,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         uint64_t *empty = qk ? sm.k_empty : sm.v_empty;
         const int ns = qk ? kKStages : kVStages;
         const CUtensorMap *map = qk ? &k_map : &v_map;
+        const CUtensorMap *new_map = qk ? &kn_map : &vn_map;
         int tcount = 0, it = 0;              // units / key tiles started
         int q_issued = 0, kv_issued = 0;
         bool ok = true;
         for (int r = 0; ok; ++r) {
             const int idx = snake(r, total);
             if (idx < 0) break;
-            const Unit t = unit_for<kPrefix, kPlanned>(a, idx, qblocks);
+            const Unit t = unit_for<kPrefix, kPlanned, kAppend>(a, idx, qblocks);
             if (qk && leader && t.error) record_error(a.err, kErrDevice | kErrQLen);
             if (!t.run) continue;
             if (qk) {
@@ -344,7 +447,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             for (int j = 0; j < t.n_kt; ++j, ++it) {
                 const int st = it % ns;
                 const int jg = t.kt0 + j;              // key tile within the context
-                int blk = __ldg(bt + (jg >> 1));
+                const bool cache_tile = !kAppend || jg < t.n_old;
+                int blk = cache_tile ? __ldg(bt + (jg >> 1)) : 0;
                 if (blk < 0 || blk >= a.num_blocks) {
                     if (qk && leader) record_error(a.err, kErrDevice | kErrBadBlock);
                     blk = 0;   // stay inside the pool; the result is flagged as invalid
@@ -358,8 +462,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                     const uint32_t bar = smem_u32(&full[st]);
                     uint8_t (*dst)[kHalf] = qk ? sm.k[st] : sm.v[st];
                     mbar_arrive_expect_tx(bar, kTileBytes);
-                    tma_load_4d(smem_u32(dst[0]), map, bar, 0, t.g, off, blk);
-                    tma_load_4d(smem_u32(dst[1]), map, bar, 64, t.g, off, blk);
+                    if (cache_tile) {
+                        tma_load_4d(smem_u32(dst[0]), map, bar, 0, t.g, off, blk);
+                        tma_load_4d(smem_u32(dst[1]), map, bar, 64, t.g, off, blk);
+                    } else {
+                        // 128 new rows of k_new / v_new (past the sequence's last one: rows of
+                        // the next sequence, or zeros past the tensor's end; never keys here)
+                        const int row = t.tok_base + (jg - t.n_old) * kKT;
+                        tma_load_3d(smem_u32(dst[0]), new_map, bar, 0, t.g, row);
+                        tma_load_3d(smem_u32(dst[1]), new_map, bar, 64, t.g, row);
+                    }
                 }
                 __syncwarp();
                 ++kv_issued;
@@ -441,7 +553,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         for (int r = 0; ok; ++r) {
             const int idx = snake(r, total);
             if (idx < 0) break;
-            const Unit t = unit_for<kPrefix, kPlanned>(a, idx, qblocks);
+            const Unit t = unit_for<kPrefix, kPlanned, kAppend>(a, idx, qblocks);
             if (!t.run) continue;
             if (!(ok = wait_all(&sm.q_full, tcount & 1))) break;
             for (int j = 0; j < t.n_kt; ++j, ++it) {
@@ -467,6 +579,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         if (leader) umma_commit(smem_u32(&sm.mma_idle));
         __syncwarp();
         mbar_wait(smem_u32(&sm.mma_idle), 0);
+    } else if (kAppend && warp == kAppendWarp) {
+        // ---------------------------------------------------------------- fused append
+        // k_new / v_new and the pools may come from the kernel just before this one
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        // The copies are due only by the kernel's end: keep them off the start, where every
+        // CTA's first Q, K and V tiles are on their way, by waiting for this CTA's first
+        // O += P V product (if it has any unit to compute; bounded, then it copies anyway).
+        bool has_unit = false;
+        for (int r = 0; !has_unit; ++r) {
+            const int idx = snake(r, total);
+            if (idx < 0) break;
+            has_unit = unit_for<kPrefix, kPlanned, kAppend>(a, idx, qblocks).run;
+        }
+        if (has_unit) mbar_wait(smem_u32(&sm.o_done[0]), 0, 200000ull);
+        append_share(a, lane);
     } else {
         // ---------------------------------------------------------------- softmax warps
         // Warpgroup x (= warp / 4) owns query tile x; thread = one row = one TMEM lane.
@@ -483,7 +610,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         for (int r = 0; ok; ++r) {
             const int idx = snake(r, total);
             if (idx < 0) break;
-            const Unit t = unit_for<kPrefix, kPlanned>(a, idx, qblocks);
+            const Unit t = unit_for<kPrefix, kPlanned, kAppend>(a, idx, qblocks);
             if (!t.run) continue;
             // the last key each row may see: its own position (causal), or the whole prefix
             const int pos_first = kPrefix ? t.seq_len - 1 : t.pos0 + x * kTilePos;
@@ -500,15 +627,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tmem_wait_ld(s[c]);
 
-                // mask of the keys past each row's last visible key (only on tiles reaching
-                // past the tile's first such key) and the row maximum of the raw scores
+                // mask of the keys past each row's last visible key and of the tile's rows that
+                // are no keys (past its span; only on tiles reaching past either) and the row
+                // maximum of the raw scores
                 const int jg = t.kt0 + j;                  // key tile within the context
-                if ((jg * kKT + kKT - 1) > pos_first) {
+                int base = jg * kKT, kv_valid = t.seq_len - jg * kKT;   // rows 0 .. kv_valid-1 are keys
+                if constexpr (kAppend) {
+                    int limit;
+                    key_tile_span(t, jg, base, limit);
+                    kv_valid = limit - base;
+                }
+                // (without the fused append a tile's rows past kv_valid lie past every query's
+                // position, so the causal mask covers them)
+                if (base + kKT - 1 > pos_first || (kAppend && kv_valid < kKT)) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            if ((jg * kKT + c * 32 + e) > pos) s[c][e] = __float_as_uint(-INFINITY);
+                            if (base + c * 32 + e > pos || (kAppend && c * 32 + e >= kv_valid))
+                                s[c][e] = __float_as_uint(-INFINITY);
                 }
                 // independent partial maxima (one per 32-column chunk) keep the dependency
                 // chain short: floating-point max/add are not reassociated by the compiler
@@ -551,10 +688,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                         tmem_st8(lane_base + o_col + c * 8, o);
                     }
                 }
-                // V rows past the end of the context (the tail of the last block) may hold
-                // anything, NaN included; P is 0 there but 0 * NaN is not, so tile A (the
-                // V tile's first reader) zeroes them.
-                const int kv_valid = t.seq_len - jg * kKT;
+                // V rows that are no keys (past the end of the context, past the cached
+                // positions, or rows of another sequence in k_new) may hold anything, NaN
+                // included; P is 0 there but 0 * NaN is not, so tile A (the V tile's first
+                // reader) zeroes them.
                 if (x == 0 && kv_valid < kKT) {
                     const int vs = it % kVStages;
                     ok = wait_or_abort(smem_u32(&sm.v_full[vs]), (it / kVStages) & 1, abort_flag, a.err);
@@ -664,16 +801,17 @@ __global__ void wait_selftest_kernel(uint32_t *err, uint64_t limit_ns) {
     if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, limit_ns)) record_error(err, kErrTimeout);
 }
 
-template <bool kPrefix, bool kPlanned>
+template <bool kPrefix, bool kPlanned, bool kAppend>
 cudaError_t launch_prefill_mode(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
-                                const CUtensorMap &v_map, int num_sms, cudaStream_t stream) {
+                                const CUtensorMap &v_map, const CUtensorMap &kn_map, const CUtensorMap &vn_map,
+                                int num_sms, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     static bool configured[64] = {};
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(prefill_kernel<kPrefix, kPlanned>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes);
+        e = cudaFuncSetAttribute(prefill_kernel<kPrefix, kPlanned, kAppend>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
@@ -693,13 +831,14 @@ cudaError_t launch_prefill_mode(const PrefillArgs &a, const CUtensorMap &q_map, 
         cfg.gridDim = dim3(1);
         cfg.blockDim = dim3(kPlanThreads);
         cfg.dynamicSmemBytes = 0;
-        e = cudaLaunchKernelEx(&cfg, prefill_plan_kernel, a, (int)qblocks, (int)units, plan_keys(a));
+        e = cudaLaunchKernelEx(&cfg, prefill_plan_kernel<kAppend>, a, (int)qblocks, (int)units, plan_keys(a));
         if (e != cudaSuccess) return e;
     }
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kAppend ? kThreadsAppend : kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<kPrefix, kPlanned>, q_map, k_map, v_map, a);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<kPrefix, kPlanned, kAppend>, q_map, k_map, v_map, kn_map, vn_map,
+                              a);
 }
 
 }  // namespace
@@ -712,14 +851,23 @@ long long prefill_plan_units(const PrefillArgs &a) {
 cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
                            const CUtensorMap &v_map, int num_sms, cudaStream_t stream) {
     if (a.num_seqs == 0 || a.max_q_len == 0 || a.total_tokens == 0) return cudaSuccess;
-    if (a.order) return launch_prefill_mode<false, true>(a, q_map, k_map, v_map, num_sms, stream);
-    return launch_prefill_mode<false, false>(a, q_map, k_map, v_map, num_sms, stream);
+    // (the maps of the new rows are unused without the fused append)
+    if (a.order) return launch_prefill_mode<false, true, false>(a, q_map, k_map, v_map, k_map, v_map, num_sms, stream);
+    return launch_prefill_mode<false, false, false>(a, q_map, k_map, v_map, k_map, v_map, num_sms, stream);
+}
+
+cudaError_t launch_prefill_append(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
+                                  const CUtensorMap &v_map, const CUtensorMap &kn_map, const CUtensorMap &vn_map,
+                                  int num_sms, cudaStream_t stream) {
+    if (a.num_seqs == 0 || a.max_q_len == 0 || a.total_tokens == 0 || !a.k_new) return cudaSuccess;
+    if (a.order) return launch_prefill_mode<false, true, true>(a, q_map, k_map, v_map, kn_map, vn_map, num_sms, stream);
+    return launch_prefill_mode<false, false, true>(a, q_map, k_map, v_map, kn_map, vn_map, num_sms, stream);
 }
 
 cudaError_t launch_prefill_prefix(const PrefillArgs &a, const CUtensorMap &q_map, const CUtensorMap &k_map,
                                   const CUtensorMap &v_map, int num_sms, cudaStream_t stream) {
     if (a.num_seqs == 0 || a.max_q_len == 0 || a.total_tokens == 0) return cudaSuccess;
-    return launch_prefill_mode<true, false>(a, q_map, k_map, v_map, num_sms, stream);
+    return launch_prefill_mode<true, false, false>(a, q_map, k_map, v_map, k_map, v_map, num_sms, stream);
 }
 
 cudaError_t launch_wait_selftest(uint32_t *err, uint64_t limit_ns, cudaStream_t stream) {

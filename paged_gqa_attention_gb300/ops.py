@@ -87,6 +87,9 @@ def load() -> ctypes.CDLL:
     lib.paged_attn_prefill.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32,
                                        i32, f32, vp, sz, vp]
     lib.paged_attn_prefill.restype = ctypes.c_int
+    lib.paged_attn_prefill_append.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32,
+                                              i32, f32, vp, sz, vp]
+    lib.paged_attn_prefill_append.restype = ctypes.c_int
     lib.pa_decode_step_host_staging_bytes.argtypes = [pa_shape, i32, i32]
     lib.pa_decode_step_host_staging_bytes.restype = sz
     lib.pa_decode_step_host.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, i32, f32,
@@ -516,6 +519,37 @@ def paged_attn_prefill(q, k_pool, v_pool, block_table, cu_q_lens, seq_lens, max_
                                    num_seqs, q.shape[0], int(max_q_len), float(scale),
                                    workspace.data_ptr(), workspace.numel(), _stream(stream))
     _check("paged_attn_prefill", st)
+    return out
+
+
+def paged_attn_prefill_append(q, k_new, v_new, k_pool, v_pool, block_table, cu_q_lens, seq_lens, max_q_len: int,
+                              workspace, *, scale: float = DEFAULT_SCALE, out=None, lse=None,
+                              stream=None) -> torch.Tensor:
+    """kv_append of the new tokens' k_new / v_new [T, 8, 128] followed by the causal attention
+    of q [T, 32, 128], in one kernel; returns out [T, 32, 128] and writes the pools."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (None, NUM_Q_HEADS, HEAD_DIM), dev)
+    _need(k_new, "k_new", torch.bfloat16, (q.shape[0], NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_new, "v_new", torch.bfloat16, (q.shape[0], NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(k_pool, "k_pool", torch.bfloat16, (None, BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), dev)
+    _need(v_pool, "v_pool", torch.bfloat16, tuple(k_pool.shape), dev)
+    _need(block_table, "block_table", torch.int32, (None, None), dev)
+    num_seqs = block_table.shape[0]
+    _need(cu_q_lens, "cu_q_lens", torch.int32, (num_seqs + 1,), dev)
+    _need(seq_lens, "seq_lens", torch.int32, (num_seqs,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, tuple(q.shape), dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (q.shape[0], NUM_Q_HEADS), dev)
+    st = load().paged_attn_prefill_append(SHAPE, out.data_ptr(), _ptr(lse), q.data_ptr(), k_new.data_ptr(),
+                                          v_new.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+                                          block_table.data_ptr(), block_table.shape[1], k_pool.shape[0],
+                                          cu_q_lens.data_ptr(), seq_lens.data_ptr(), num_seqs, q.shape[0],
+                                          int(max_q_len), float(scale), workspace.data_ptr(), workspace.numel(),
+                                          _stream(stream))
+    _check("paged_attn_prefill_append", st)
     return out
 
 

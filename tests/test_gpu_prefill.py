@@ -131,3 +131,73 @@ def test_work_plan_leaves_results_unchanged():
     ref, ref_lse = oracle_attention(b, kp, vp)
     assert_close(o1, ref, "planned prefill")
     assert_lse_close(l1, ref_lse, "planned prefill")
+
+
+def fused_prefill(b, ws=None):
+    ws = workspace_for(b) if ws is None else ws
+    lse = torch.empty(b.total_tokens, 32, dtype=torch.float32, device="cuda")
+    out = ops.paged_attn_prefill_append(b.q, b.k_new, b.v_new, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens,
+                                        b.seq_lens, b.max_q_len, ws, lse=lse)
+    ops.check_error(ws)
+    return out, lse
+
+
+def pool_bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("ctx_and_q", [
+    [(0, 1)],
+    [(0, 300)],                       # from position 0: the same key tiles as the two calls
+    [(0, 777)],
+    [(200, 100)],                     # a chunk after a context ending mid-tile
+    [(100, 28)],                      # a chunk inside one key tile of the context
+    [(511, 1), (1, 1), (0, 1)],
+    [(0, 64), (37, 1), (255, 130), (1000, 77), (128, 128)],   # several sequences (planned order)
+    [(10, 0), (300, 513), (40, 3)],   # an empty sequence
+])
+def test_prefill_append_matches_oracle(ctx_and_q):
+    """paged_attn_prefill_append: the pools equal the oracle's append bit for bit (sentinels
+    included) and the outputs and lse match the oracle."""
+    b = small_batch(ctx_and_q, seed=len(ctx_and_q) * 100 + ctx_and_q[0][1] + 7)
+    kp, vp = oracle_appended_pools(b)
+    out, lse = fused_prefill(b)
+    assert np.array_equal(pool_bits(b.k_pool), kp)
+    assert np.array_equal(pool_bits(b.v_pool), vp)
+    ref, ref_lse = oracle_attention(b, kp, vp)
+    assert_close(out, ref, f"fused prefill {ctx_and_q}")
+    assert_lse_close(lse, ref_lse, f"fused prefill {ctx_and_q}")
+
+
+@pytest.mark.parametrize("ctx_and_q", [[(0, 300)], [(256, 100)], [(128, 77), (0, 5), (384, 260)]])
+def test_prefill_append_equals_the_two_calls_on_aligned_contexts(ctx_and_q):
+    """Where every earlier context is a multiple of 128 tokens both paths cut the keys into the
+    same tiles: the fused call gives the bits of kv_append followed by paged_attn_prefill."""
+    b = small_batch(ctx_and_q, seed=61 + len(ctx_and_q))
+    k0, v0 = b.k_pool.clone(), b.v_pool.clone()
+    out1, lse1 = append_and_prefill(b)
+    b.k_pool, b.v_pool = k0, v0
+    out2, lse2 = fused_prefill(b)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1.view(torch.int32), lse2.view(torch.int32))
+
+
+def test_prefill_append_bad_block_is_reported_and_writes_nothing_stray():
+    b = small_batch([(0, 300), (100, 20)], seed=66, extra_blocks=6)
+    bt = b.block_table.clone()
+    bt[1, 0] = b.num_blocks + 3                 # sequence 1's only block is outside the pool
+    kp0 = pool_bits(b.k_pool).copy()
+    kp, vp = oracle_appended_pools(b)           # (the oracle appends with the valid table)
+    ws = workspace_for(b)
+    ops.paged_attn_prefill_append(b.q, b.k_new, b.v_new, b.k_pool, b.v_pool, bt, b.cu_q_lens, b.seq_lens,
+                                  b.max_q_len, ws)
+    with pytest.raises(ops.PagedAttnError) as e:
+        ops.check_error(ws)
+    assert e.value.status == 4
+    # sequence 0's rows are appended as the oracle does; no byte of sequence 1's goes anywhere
+    got = pool_bits(b.k_pool)
+    seq0_blocks = [int(x) for x in b.block_table[0, :2].cpu()]
+    assert np.array_equal(got[seq0_blocks], kp[seq0_blocks])
+    others = np.ones(b.num_blocks, dtype=bool)
+    others[seq0_blocks] = False
+    assert np.array_equal(got[others], kp0[others])
