@@ -424,19 +424,7 @@ def e2e_layered_measure(layers, graph, out, steps, warmup, stream):
         graph.launch()
         out_host.copy_(out, non_blocking=True)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    times = []
-    for _ in range(steps):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step()
-        e1.record(stream)
-        e1.synchronize()
-        times.append(e0.elapsed_time(e1))
-    return {"step_ms": mean(times), "h2d": h2d, "d2h": d2h}
+    return dict(e2e_run(step, steps, warmup, stream), h2d=h2d, d2h=d2h)
 
 
 FP8_ROW_BYTES = 2 * (128 + 4)       # one token of one KV head in the 8-bit cache: K and V codes + scales
@@ -512,20 +500,9 @@ def e2e_fp8_measure(batch, cache, steps, warmup, stream):
                                          dev["seq_lens"], ws, out=out_dev)
         out_host.copy_(out_dev, non_blocking=True)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    times = []
-    for _ in range(steps):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step()
-        e1.record(stream)
-        e1.synchronize()
-        times.append(e0.elapsed_time(e1))
+    r = e2e_run(step, steps, warmup, stream)
     ops.check_error(ws)
-    return {"step_ms": mean(times), "h2d": h2d, "d2h": d2h}
+    return dict(r, h2d=h2d, d2h=d2h)
 
 
 def oracle_sample_fp8(batch):
@@ -585,9 +562,51 @@ def cascade_measure(batch, shared_blocks, steps, warmup, flush_buf, stream, cloc
             "wall_s": wall, "launches": 3 * steps}
 
 
-def e2e_decode_measure(batch, steps, warmup, stream):
+E2E_HOW = ("value / ms_per_step: steps issued back to back through the public call, each reading its inputs "
+           "from pinned host memory and leaving its result in host memory, the run bracketed by CUDA events; "
+           "latency_ms_per_step: the same step with the host waiting for each result; host_call_us: the host's "
+           "time to issue one step")
+
+
+def e2e_run(step, steps, warmup, stream):
+    """Time one end-to-end step (inputs from pinned host memory, result back to host memory,
+    through the public call) two ways: back to back, the whole run bracketed by events and
+    the host issuing each step without waiting for the last (the throughput a serving loop
+    sees; every step still reads its inputs from and leaves its result in host memory), and
+    one at a time, the host waiting for each step's result before issuing the next (the
+    latency of one request).  Also the host's own time per call (issue only)."""
+    import torch
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    host_s = 0.0
+    e0.record(stream)
+    for _ in range(steps):
+        h0 = time.perf_counter()
+        step()
+        host_s += time.perf_counter() - h0
+    e1.record(stream)
+    e1.synchronize()
+    piped = e0.elapsed_time(e1) / steps
+    times = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        b.synchronize()          # the result is on the host when the step ends
+        times.append(a.elapsed_time(b))
+    return {"step_ms": piped, "latency_ms": mean(times), "host_call_us": host_s / steps * 1e6}
+
+
+def e2e_decode_measure(batch, steps, warmup, stream, flush_buf=None):
     """The decode step through the C ABI with host buffers (pa_decode_step_host): pinned
-    host inputs copied in, fused append + decode, output copied back, every step."""
+    host inputs read in place over the host link, fused append + decode, output written back
+    to host memory, every step.  With flush_buf, also the same step device-timed as the
+    device-input step is (L2 flushed, queued behind a spin): the cost of the host inputs
+    alone."""
     import torch
 
     from paged_gqa_attention_gb300 import ops
@@ -604,20 +623,29 @@ def e2e_decode_measure(batch, steps, warmup, stream):
         ops.decode_step_host(out_host, host["q"], host["k_new"], host["v_new"], host["block_table"],
                              host["seq_lens"], batch.k_pool, batch.v_pool, staging, ws)
 
-    for _ in range(warmup):
-        step()
+    r = e2e_run(step, steps, warmup, stream)
+    # the host's time to issue one step through the C entry point alone (no Python checks)
+    lib = ops.load()
+    args = (ops.SHAPE, out_host.data_ptr(), None, host["q"].data_ptr(), host["k_new"].data_ptr(),
+            host["v_new"].data_ptr(), host["block_table"].data_ptr(), host["seq_lens"].data_ptr(), batch.num_seqs,
+            batch.max_blocks_per_seq, batch.k_pool.data_ptr(), batch.v_pool.data_ptr(), batch.k_pool.shape[0],
+            ops.DEFAULT_SCALE, staging.data_ptr(), staging.numel(), ws.data_ptr(), ws.numel(), stream.cuda_stream)
     torch.cuda.synchronize()
-    times = []
+    h0 = time.perf_counter()
     for _ in range(steps):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step()
-        e1.record(stream)
-        e1.synchronize()          # the result is on the host when the step ends
-        times.append(e0.elapsed_time(e1))
+        if lib.pa_decode_step_host(*args) != 0:
+            raise RuntimeError("pa_decode_step_host failed")
+    r["host_call_c_abi_us"] = (time.perf_counter() - h0) / steps * 1e6
+    torch.cuda.synchronize()
+    if flush_buf is not None:
+        def timed(tm):
+            if tm: tm.record(0)
+            step()
+            if tm: tm.record(1)
+        spans, _ = run_timed(timed, 2, steps, warmup, flush_buf, stream)
+        r["device_timed_ms"] = mean([x[0] for x in spans])
     ops.check_error(ws)
-    return {"step_ms": mean(times), "h2d": h2d, "d2h": d2h}
+    return dict(r, h2d=h2d, d2h=d2h)
 
 
 def e2e_measure(batch, kind, steps, warmup, stream):
@@ -666,20 +694,9 @@ def e2e_measure(batch, kind, steps, warmup, stream):
                                           dev["seq_lens"][n_dec:], batch.max_q_len, ws, out=out_dev[t_dec:])
         out_host.copy_(out_dev, non_blocking=True)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    times = []
-    for _ in range(steps):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step()
-        e1.record(stream)
-        e1.synchronize()          # the result is on the host when the step ends
-        times.append(e0.elapsed_time(e1))
+    r = e2e_run(step, steps, warmup, stream)
     ops.check_error(ws)
-    return {"step_ms": mean(times), "h2d": h2d, "d2h": d2h}
+    return dict(r, h2d=h2d, d2h=d2h)
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -861,17 +878,9 @@ def e2e_qkv_measure(batch, x, w, steps, warmup, stream):
                              batch.seq_lens, ws, rope_theta=ops.QWEN3_ROPE_THETA, q_out=q_dev)
         q_host.copy_(q_dev, non_blocking=True)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    r = e2e_run(step, steps, warmup, stream)
     ops.check_error(ws)
-    return {"step_ms": e0.elapsed_time(e1) / steps, "h2d": x_host.numel() * 2, "d2h": q_host.numel() * 2}
+    return dict(r, h2d=x_host.numel() * 2, d2h=q_host.numel() * 2)
 
 
 def oracle_sample_qkv(tokens):
@@ -1053,11 +1062,13 @@ def measure(wname, steps, warmup, e2e_steps, peaks, flush_buf, stream, clocks, w
         if wname == "single_decode":
             e["warm_l2_latency"] = warm_l2_latency(batch, stream)
         e["gpu_launches"] = r["launches"]
-        x = e2e_decode_measure(batch, e2e_steps, 5, stream)
+        x = e2e_decode_measure(batch, e2e_steps, 5, stream, flush_buf)
         x_ms = dist_max(x["step_ms"], world)
         e["e2e"] = {"value": world * kv_bytes / (x_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms,
-                    "via": "pa_decode_step_host (C ABI, host buffers)"}
+                    "via": "pa_decode_step_host (C ABI, host buffers)",
+                    "latency_ms_per_step": x["latency_ms"], "host_call_us": x["host_call_us"], "how": E2E_HOW,
+                    "device_timed_step_us": x["device_timed_ms"] * 1e3, "host_call_c_abi_us": x["host_call_c_abi_us"]}
         kind = "decode"
     elif wname == "layered_decode":
         r = layered_measure(layers, steps, warmup, flush_buf, stream, clocks)
@@ -1079,7 +1090,8 @@ def measure(wname, steps, warmup, e2e_steps, peaks, flush_buf, stream, clocks, w
         x = e2e_layered_measure(layers, r["graph"], r["out"], e2e_steps, 5, stream)
         x_ms = dist_max(x["step_ms"], world)
         e["e2e"] = {"value": world * kv_bytes / (x_ms * 1e-3) / 1e9, "unit": "GB/s",
-                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms,
+                    "latency_ms_per_step": x["latency_ms"], "host_call_us": x["host_call_us"], "how": E2E_HOW}
         r["graph"].close()
         kind = "decode"
     elif wname == "prefix_shared_decode_cascade":
@@ -1101,7 +1113,8 @@ def measure(wname, steps, warmup, e2e_steps, peaks, flush_buf, stream, clocks, w
         x = e2e_measure(batch, "cascade", max(10, min(e2e_steps, 50)), 3, stream)
         x_ms = dist_max(x["step_ms"], world)
         e["e2e"] = {"value": world * kv_bytes / (x_ms * 1e-3) / 1e9, "unit": "GB/s",
-                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms,
+                    "latency_ms_per_step": x["latency_ms"], "host_call_us": x["host_call_us"], "how": E2E_HOW}
         kind = "decode"
     elif wname == "batched_decode_fp8":
         cache = fp8_prepare(batch)
@@ -1126,7 +1139,8 @@ def measure(wname, steps, warmup, e2e_steps, peaks, flush_buf, stream, clocks, w
         x = e2e_fp8_measure(batch, cache, e2e_steps, 5, stream)
         x_ms = dist_max(x["step_ms"], world)
         e["e2e"] = {"value": world * kv_bytes / (x_ms * 1e-3) / 1e9, "unit": "GB/s",
-                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms,
+                    "latency_ms_per_step": x["latency_ms"], "host_call_us": x["host_call_us"], "how": E2E_HOW}
         cfg["kv_cache"] = "8-bit: E4M3 codes + one fp32 scale per token and KV head"
         e["dtype"] = "f16 products over e4m3 codes"
         kind = "decode_fp8"
@@ -1153,7 +1167,8 @@ def measure(wname, steps, warmup, e2e_steps, peaks, flush_buf, stream, clocks, w
         x = e2e_qkv_measure(batch, x_in, w, max(10, min(e2e_steps, 50)), 3, stream)
         x_ms = dist_max(x["step_ms"], world)
         e["e2e"] = {"value": world * flops / (x_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms,
+                    "latency_ms_per_step": x["latency_ms"], "host_call_us": x["host_call_us"], "how": E2E_HOW}
         cfg["projection"] = ("x [4096, 4096] @ w_qkv [6144, 4096]^T; rotary embedding of q and k (theta 1e6); "
                              "q out, k and v into their cache slots")
         kind = "qkv"
@@ -1174,7 +1189,8 @@ def measure(wname, steps, warmup, e2e_steps, peaks, flush_buf, stream, clocks, w
         x = e2e_measure(batch, "prefill", max(10, min(e2e_steps, 50)), 3, stream)
         x_ms = dist_max(x["step_ms"], world)
         e["e2e"] = {"value": world * flops / (x_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms,
+                    "latency_ms_per_step": x["latency_ms"], "host_call_us": x["host_call_us"], "how": E2E_HOW}
         kind = "prefill"
     else:  # mixed_batch
         r = mixed_measure(batch, steps, warmup, flush_buf, stream, clocks)
@@ -1201,7 +1217,8 @@ def measure(wname, steps, warmup, e2e_steps, peaks, flush_buf, stream, clocks, w
         x = e2e_measure(batch, "mixed", max(10, min(e2e_steps, 100)), 3, stream)
         x_ms = dist_max(x["step_ms"], world)
         e["e2e"] = {"value": world * kv_bytes / (x_ms * 1e-3) / 1e9, "unit": "GB/s",
-                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms}
+                    "h2d_bytes_per_step": x["h2d"], "d2h_bytes_per_step": x["d2h"], "ms_per_step": x_ms,
+                    "latency_ms_per_step": x["latency_ms"], "host_call_us": x["host_call_us"], "how": E2E_HOW}
         kind = "decode"
     if r.get("step_pcts"):
         e["step_ms_percentiles"] = r["step_pcts"]   # this rank's timed steps (rank 0 prints)
