@@ -280,3 +280,20 @@ def test_fused_append_decode_on_the_cluster_merge_path(lens):
     ops.check_error(ws)
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     assert torch.equal(lse, lse2)
+
+
+@pytest.mark.parametrize("batch,hi,seed", [(70, 3000, 51), (200, 2500, 52), (512, 700, 53), (513, 700, 54)])
+def test_decode_many_sequences(batch, hi, seed):
+    """Batches of 70 to 513 sequences whose splits take several waves of CTAs: the result must
+    match the oracle and repeat bit for bit (the merge counters put themselves back)."""
+    lens = wl.randint_lens(seed, batch, 1, hi)
+    b = decode_batch(lens, seed=seed, maxb=(hi + 255) // 256)
+    ref, ref_lse = oracle_attention(b)
+    ws = workspace_for(b)
+    out, lse = run_decode(b, ws)
+    assert_close(out, ref, f"streaming decode, batch {batch}")
+    assert_lse_close(lse, ref_lse, f"streaming decode, batch {batch}")
+    for _ in range(2):
+        again, lse2 = run_decode(b, ws)
+        assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+        assert torch.equal(lse, lse2)
