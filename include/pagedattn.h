@@ -383,6 +383,8 @@ pa_status paged_attn_decode_static(pa_shape shape, void *out, float *lse, const 
  * units (64 positions x one KV head) by the number of key tiles they visit, into the
  * workspace's split-K area, so that the longest are started first; a workspace too
  * small for that list gets the natural order.  Results do not depend on the order.
+ * out must be 32-byte aligned (the kernel writes whole 32-byte sectors), else
+ * PA_ERR_INVALID_ARG; a view starting at any token of a larger tensor qualifies.
  */
 pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *q,
                              const void *k_pool, const void *v_pool,
@@ -402,7 +404,8 @@ pa_status paged_attn_prefill(pa_shape shape, void *out, float *lse, const void *
  * slots, which nothing in the call reads.  Pools are bit-identical to kv_append's; outputs
  * are those of the two calls up to rounding (bit-identical when every sequence's earlier
  * context is a multiple of 128 tokens, where both calls cut the keys into the same tiles).
- * Arguments, workspace and errors as for kv_append and paged_attn_prefill.
+ * Arguments, workspace and errors as for kv_append and paged_attn_prefill (out
+ * 32-byte aligned).
  */
 pa_status paged_attn_prefill_append(pa_shape shape, void *out, float *lse, const void *q,
                                     const void *k_new, const void *v_new, void *k_pool,

@@ -31,6 +31,7 @@ bool shape_ok(const pa_shape &s) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // ------------------------------------------------------------------ driver entry point
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -726,7 +727,7 @@ static pa_status prefill_impl(pa_shape shape, void *out, float *lse, const void 
         (long long)max_blocks_per_seq * kBlock > (1ll << 30))
         return PA_ERR_INVALID_ARG;
     if (!out || !q || !k_pool || !v_pool || !block_table || !cu_q_lens || !seq_lens) return PA_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned4(block_table) ||
+    if (!aligned32(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned4(block_table) ||
         !aligned4(cu_q_lens) || !aligned4(seq_lens) || (lse && !aligned4(lse)))
         return PA_ERR_INVALID_ARG;
     if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))

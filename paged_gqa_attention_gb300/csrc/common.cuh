@@ -277,6 +277,14 @@ __device__ __forceinline__ float add_bf16_hi(uint32_t v, float c) {
     return d;
 }
 
+// One 32-byte store of eight 32-bit words (sm_100 family); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_32b(void *p, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                              uint32_t w4, uint32_t w5, uint32_t w6, uint32_t w7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w0), "r"(w1), "r"(w2),
+                 "r"(w3), "r"(w4), "r"(w5), "r"(w6), "r"(w7)
+                 : "memory");
+}
+
 // Approximate reciprocal (rcp.approx, subnormal inputs kept).
 __device__ __forceinline__ float fast_rcp(float x) {
     float y;

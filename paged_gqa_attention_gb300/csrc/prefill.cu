@@ -523,13 +523,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         };
         // O_x += P_x V over 128 keys in 8 steps of 16; V is [128 keys][128 dims] with dims
         // contiguous (MN-major), its two 64-dim halves 16 KiB apart.
+        // Tile A (x = 0) takes keys 0-63 as soon as their P is stored and keys 64-127 when the
+        // rest is.  Tile B's product is issued a key tile later, when its P is long complete:
+        // it waits only for the second half (whose barrier completes after every softmax warp
+        // has arrived on the first), and not for V, which tile A's product already waited for.
+        // Every wait costs the issuing thread time in which the tensor core can run dry.
         auto issue_pv = [&](int x, int pit, int pj) -> bool {
             const int vs = pit % kVStages;
-            if (!wait_all(&sm.v_full[vs], (pit / kVStages) & 1)) return false;
+            if (x == 0 && !wait_all(&sm.v_full[vs], (pit / kVStages) & 1)) return false;
             const uint64_t vb = vd0 + (uint64_t)(vs * 2048);
             const uint32_t pa = tmem + col_s(x);
-            // keys 0-63 as soon as their P is stored, keys 64-127 when the rest is
-            if (!wait_all(&sm.p_half[x][0], pit & 1)) return false;
+            if (!wait_all(&sm.p_half[x][x], pit & 1)) return false;
             tc_fence_after();
             if (leader) {
                 umma_ts(tmem + col_o(x), pa, vb, kIdescPV, pj > 0 ? 1u : 0u);
@@ -538,8 +542,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                     umma_ts_c<true>(tmem + col_o(x), pa + kk * 8, vb + (uint64_t)(kk * 128), kIdescPV);
             }
             __syncwarp();
-            if (!wait_all(&sm.p_half[x][1], pit & 1)) return false;
-            tc_fence_after();
+            if (x == 0) {
+                if (!wait_all(&sm.p_half[x][1], pit & 1)) return false;
+                tc_fence_after();
+            }
             if (leader) {
 #pragma unroll
                 for (int kk = kKT / 32; kk < kKT / 16; ++kk)
@@ -572,9 +578,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                 pend_it = it;
                 pend_j = j;
             }
+            // the unit's last O_B += P_B V now, not behind the next unit's Q and first S_A
+            if (ok && pend_it >= 0) ok = issue_pv(1, pend_it, pend_j);
+            pend_it = -1;
             ++tcount;
         }
-        if (ok && pend_it >= 0) issue_pv(1, pend_it, pend_j);
         // Every MMA issued must have finished before tensor memory is released.
         if (leader) umma_commit(smem_u32(&sm.mma_idle));
         __syncwarp();
@@ -768,11 +776,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 #pragma unroll
                     for (int e = 0; e < 32; e += 2)
                         w[e / 2] = pack_bf16x2(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
+                    // 32-byte stores: each writes whole sectors (out is 32-byte aligned, rows
+                    // are 256 bytes); 16-byte ones left every sector of a warp's store half written
                     if (row_ok) {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * kD + c * 32);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+                        __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(a.out) + orow * kD + c * 32;
+                        st_global_32b(d, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                        st_global_32b(d + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
                     }
                 }
             }

@@ -104,6 +104,20 @@ def test_empty_calls_are_no_ops(lib):
                                   0, 0, 0, 0.1, wsp, 4096, None) == 0
 
 
+def test_prefill_output_must_be_32_byte_aligned(lib):
+    """The prefill writes whole 32-byte sectors: an out pointer that is 16- but not 32-byte
+    aligned is rejected on the host (PA_ERR_INVALID_ARG) before any CUDA work.  (The pointers
+    are host addresses, so no call here may get past validation.)"""
+    buf = (ctypes.c_uint8 * 8192)()
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    ws = ctypes.c_void_p(base)
+    p = lambda off: ctypes.c_void_p(base + 1024 + off)
+    args = lambda out: (ops.SHAPE, out, None, p(256), p(512), p(768), p(1024), 1, 1, p(1280), p(1536), 1, 4, 4, 0.1,
+                        ws, 1024, None)
+    assert lib.paged_attn_prefill(*args(p(16))) == 1
+    assert lib.paged_attn_prefill(*args(p(48))) == 1
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ops, "_lib", None)
     monkeypatch.setattr(ops, "_LIB_PATH", str(tmp_path / "missing.so"))
