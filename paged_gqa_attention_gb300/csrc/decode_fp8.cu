@@ -289,19 +289,25 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_consta
             } else {  // padding heads 4..7: finite dummies, results discarded
                 x0 = x1 = x2 = x3 = 0.f;
             }
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            }
             // lazy rescaling: the running max moves only when the tile's max exceeds it by
-            // more than 2^8 (weights stay <= 2^8, far inside f16), so most tiles rescale nothing
-            const bool up0 = mx0 > m0 + 8.f, up1 = mx1 > m1 + 8.f;   // also when m == -inf
-            const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
-            const float alpha0 = up0 ? fast_exp2(m0 - mn0) : 1.f, alpha1 = up1 ? fast_exp2(m1 - mn1) : 1.f;
-            m0 = mn0;
-            m1 = mn1;
+            // more than 2^8 (weights stay <= 2^8, far inside f16), so most tiles rescale
+            // nothing; one vote finds those tiles, and only they reduce the maxima over the
+            // warp (six dependent shuffles off the common path)
+            float alpha0 = 1.f, alpha1 = 1.f;
+            if (__any_sync(0xffffffffu, fmaxf(x0, x2) > m0 + 8.f || fmaxf(x1, x3) > m1 + 8.f)) {
+                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                const bool up0 = mx0 > m0 + 8.f, up1 = mx1 > m1 + 8.f;   // also when m == -inf
+                const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
+                alpha0 = up0 ? fast_exp2(m0 - mn0) : 1.f;
+                alpha1 = up1 ? fast_exp2(m1 - mn1) : 1.f;
+                m0 = mn0;
+                m1 = mn1;
+            }
             const float p0 = fast_exp2(x0 - m0), p1 = fast_exp2(x1 - m1);
             const float p2 = fast_exp2(x2 - m0), p3 = fast_exp2(x3 - m1);
             l0 = l0 * alpha0 + p0 + p2;
@@ -311,20 +317,23 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_consta
             // may hold anything) and their maximum
             const float sv_lo = v_lo_ok ? vsc[gq] : 0.f;
             const float sv_hi = v_hi_ok ? vsc[gq + 8] : 0.f;
-            float svm = fmaxf(sv_lo, sv_hi);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, o));
             // the accumulator's reference V scale grows with the largest scale seen; its
             // reciprocal is recomputed only then (an approximate reciprocal: the factor it
             // introduces is undone exactly by the same values in grow and the final sigma)
             // (floored at 2^-100 so that the reciprocal stays finite: a V row whose scale is
             // below it contributes less than the output's bf16 resolution near zero)
+            // (one vote finds the stages that raise it; only they reduce over the warp)
             float grow = 1.f;
-            const float svr = fmaxf(svm, 0x1p-100f);
-            if (svr > sigma) {
-                inv_sigma = fast_rcp(svr);
-                grow = sigma * inv_sigma;                  // 0 on the first tile (acc is 0)
-                sigma = svr;
+            if (__any_sync(0xffffffffu, fmaxf(fmaxf(sv_lo, sv_hi), 0x1p-100f) > sigma)) {
+                float svm = fmaxf(sv_lo, sv_hi);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, o));
+                const float svr = fmaxf(svm, 0x1p-100f);
+                if (svr > sigma) {
+                    inv_sigma = fast_rcp(svr);
+                    grow = sigma * inv_sigma;              // 0 on the first tile (acc is 0)
+                    sigma = svr;
+                }
             }
             const float r_lo = sv_lo * inv_sigma, r_hi = sv_hi * inv_sigma;
             const uint32_t pp_lo = pack_f16x2(p0 * r_lo, p1 * r_lo);   // token gq:   heads 2tq, 2tq+1
