@@ -51,17 +51,17 @@ HEAD_START_CYCLES = 200_000      # ~0.1 ms spin so a step's launches are all que
 # whose sources changed since reports traffic null.
 TRAFFIC = {
     # one ncu capture of the batched decode step (32 sequences, 243.9 MB of K/V)
-    "decode": {"bytes_per_launch": 249330688 + 3646208, "sources": ("decode.cu", "common.cuh"),
-               "sha": "c142d4ea0a9be97f", "workload": "batched_decode"},
+    "decode": {"bytes_per_launch": 249650432 + 4694272, "sources": ("decode.cu", "common.cuh"),
+               "sha": "8933af376eb543b1", "workload": "batched_decode"},
     # one ncu capture of the fused 8-bit decode step (batch 32, 126 MB of 8-bit K/V)
-    "decode_fp8": {"bytes_per_launch": 131073024 + 4144384, "sources": ("decode_fp8.cu", "common.cuh"),
-                   "sha": "67c2060515e80bb8", "workload": "batched_decode_fp8"},
-    # one ncu capture of the causal prefill of 4096 tokens
-    "prefill": {"bytes_per_launch": 50676480 + 1682944, "sources": ("prefill.cu", "common.cuh"),
-                "sha": "b0aea3dbb3034acb", "workload": "causal_prefill"},
+    "decode_fp8": {"bytes_per_launch": 131116800 + 4321280, "sources": ("decode_fp8.cu", "common.cuh"),
+                   "sha": "fa1e86d11026bb58", "workload": "batched_decode_fp8"},
+    # one ncu capture of the causal prefill of 4096 tokens with the prompt's append fused in
+    "prefill": {"bytes_per_launch": 50473472 + 15075584, "sources": ("prefill.cu", "common.cuh"),
+                "sha": "91b7de4c6764e9bf", "workload": "causal_prefill"},
     # one ncu capture of the merged Q/K/V projection of 4096 tokens (hidden 4096)
-    "qkv": {"bytes_per_launch": 117843712 + 37423616, "sources": ("qkv.cu", "common.cuh"),
-            "sha": "3d86c5c3900fc01e", "workload": "qkv_append"},
+    "qkv": {"bytes_per_launch": 119763200 + 36756480, "sources": ("qkv.cu", "common.cuh"),
+            "sha": "f741adbd51856a48", "workload": "qkv_append"},
 }
 
 
