@@ -85,6 +85,34 @@ def test_decode_fp8_matches_oracle(lens):
     assert_lse_close(lse, ref_lse, f"fp8 decode {lens}")
 
 
+@pytest.mark.parametrize("split_tokens", [1024, 0])
+def test_decode_fp8_late_score_spike(split_tokens):
+    """A key late in the context whose score exceeds everything before it by far more than
+    the rescale threshold (2^8).  With 1024-token splits each spike lies in a later stage of a
+    warp that has already accumulated earlier stages, so that warp must take the warp-wide
+    maximum path and rescale its accumulator (the library's own split, with this few
+    sequences, gives each CTA one stage)."""
+    lens = [3000, 700, 1800]
+    b = wl.build_batch("fp8_spike", 61, lens, [1] * len(lens), num_blocks=sum((l + 255) // 256 for l in lens) + 3,
+                       device="cuda")
+    for s_, pos in ((0, 2500), (1, 650), (2, 1300)):
+        blk = int(b.block_table[s_, pos // 256])
+        for g in range(ops.NUM_KV_HEADS):
+            # aligned with the group's first query head, 8 times its length: a score ~ 8 |q|^2 / sqrt(128)
+            b.k_pool[blk, pos % 256, g] = (8.0 * b.q[s_, 4 * g].float()).to(torch.bfloat16)
+    cache = oracle_cache(b)
+    kc, vc, ks, vs = upload(cache)
+    ws = workspace_for(b)
+    lse = torch.empty(b.num_seqs, ops.NUM_Q_HEADS, dtype=torch.float32, device="cuda")
+    out = ops.paged_attn_decode_fp8(b.q, kc, vc, ks, vs, b.block_table, b.seq_lens, ws, lse=lse,
+                                    split_tokens=split_tokens)
+    ops.check_error(ws)
+    ref, ref_lse = oracle.attention_fp8(to_cpu(b.q), *cache, to_cpu(b.block_table), to_cpu(b.cu_q_lens),
+                                        to_cpu(b.seq_lens), scale=wl.SCALE)
+    assert_close(out, ref, f"fp8 decode, late score spike (split {split_tokens})")
+    assert_lse_close(lse, ref_lse, f"fp8 decode, late score spike (split {split_tokens})")
+
+
 def test_decode_fp8_after_gpu_append_of_the_new_tokens():
     """The decode step over the 8-bit cache: the context before the new tokens quantised by
     the oracle, the new tokens appended by the GPU, then the GPU decode."""

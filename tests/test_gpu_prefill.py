@@ -53,6 +53,39 @@ def test_prefill_matches_oracle(ctx_and_q):
     assert_lse_close(lse, ref_lse, f"prefill {ctx_and_q}")
 
 
+def plant_score_spikes(b, spikes):
+    """Make the new key at token `key_tok` (a row of k_new) 8 times the first query head of
+    each KV group at token `q_tok`: that row's score jumps by ~130 (log2 units) and about a
+    quarter of the other rows' by more than 8, far past the running maximum of the key tiles
+    before it."""
+    for key_tok, q_tok in spikes:
+        for g in range(ops.NUM_KV_HEADS):
+            b.k_new[key_tok, g] = (8.0 * b.q[q_tok, 4 * g].float()).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_prefill_late_score_spikes(fused):
+    """Scores that exceed the running maximum by far more than the rescale threshold (2^8) in
+    a key tile after the first: the rows must rescale their O accumulator mid-way (the
+    threshold-crossing path), in the plain and the fused-append prefill alike."""
+    b = small_batch([(0, 1000), (300, 700)], seed=23)
+    plant_score_spikes(b, [(700, 900), (450, 999), (1000 + 500, 1000 + 650)])
+    kp, vp = oracle_appended_pools(b)
+    ws = workspace_for(b)
+    lse = torch.empty(b.total_tokens, 32, dtype=torch.float32, device="cuda")
+    if fused:
+        out = ops.paged_attn_prefill_append(b.q, b.k_new, b.v_new, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens,
+                                            b.seq_lens, b.max_q_len, ws, lse=lse)
+    else:
+        ops.kv_append(b.k_pool, b.v_pool, b.k_new, b.v_new, b.block_table, b.cu_q_lens, b.seq_lens, ws)
+        out = ops.paged_attn_prefill(b.q, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens,
+                                     b.max_q_len, ws, lse=lse)
+    ops.check_error(ws)
+    ref, ref_lse = oracle_attention(b, kp, vp)
+    assert_close(out, ref, f"prefill with late score spikes (fused={fused})")
+    assert_lse_close(lse, ref_lse, f"prefill with late score spikes (fused={fused})")
+
+
 def test_decode_equals_last_prefill_row():
     b = small_batch([(0, 700)], seed=21)
     out, _ = append_and_prefill(b)
