@@ -57,8 +57,8 @@ TRAFFIC = {
     "decode_fp8": {"bytes_per_launch": 131116800 + 4321280, "sources": ("decode_fp8.cu", "common.cuh"),
                    "sha": "fa1e86d11026bb58", "workload": "batched_decode_fp8"},
     # one ncu capture of the causal prefill of 4096 tokens with the prompt's append fused in
-    "prefill": {"bytes_per_launch": 50473472 + 15075584, "sources": ("prefill.cu", "common.cuh"),
-                "sha": "91b7de4c6764e9bf", "workload": "causal_prefill"},
+    "prefill": {"bytes_per_launch": 50459392 + 14682880, "sources": ("prefill.cu", "common.cuh"),
+                "sha": "fec1d9b4cc5c409b", "workload": "causal_prefill"},
     # one ncu capture of the merged Q/K/V projection of 4096 tokens (hidden 4096)
     "qkv": {"bytes_per_launch": 119763200 + 36756480, "sources": ("qkv.cu", "common.cuh"),
             "sha": "f741adbd51856a48", "workload": "qkv_append"},
