@@ -992,6 +992,23 @@ def load_workload(wname):
     return wl.WORKLOADS[wname](device="cuda"), None
 
 
+def timing_floor(flush_buf, stream, steps=300):
+    """The time this method gives a step that does almost nothing: one torch kernel adding 1 to
+    32 floats, timed like every step (L2 flushed, queued behind a device spin, CUDA events
+    around it).  The launch after the step's first event is part of every measured step."""
+    import torch
+
+    x = torch.zeros(32, device="cuda")
+
+    def step(tm):
+        if tm: tm.record(0)
+        x.add_(1.0)
+        if tm: tm.record(1)
+
+    spans, _ = run_timed(step, 2, steps, 20, flush_buf, stream)
+    return mean([s[0] for s in spans]) * 1e3
+
+
 def warm_l2_latency(batch, stream, steps=200):
     """The fused decode step back to back with nothing flushed in between (the whole working
     set stays in L2): mean latency of one call, in us."""
@@ -1307,6 +1324,7 @@ def main():
         line["configs"] = subs
     line["clocks"] = clocks.stop()
     line["peaks"] = peaks
+    line["timing_floor_us"] = timing_floor(flush_buf, stream)
     if rank == 0:
         print(json.dumps(line), flush=True)
     dist_barrier(world)
