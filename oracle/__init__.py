@@ -12,12 +12,13 @@ GPU sees and return float64 results.  The 8-bit KV cache (E4M3 codes, one fp32 s
 
 The merged Q/K/V projection (page 1 §4.4.3) is ``qkv_project``; ``qkv_append`` adds the
 append of its k and v (rounded once to bf16 by ``bf16_round``) to the cache, optionally after
-the rotary position embedding of q and k (``rope``; RoFormer's definition, not on the pages)
-at each token's position (``token_positions``).
+the per-head RMS normalisation of q and k (``rms_norm_heads``; Qwen3's QK-norm, not on the
+pages) and the rotary position embedding of q and k (``rope``; RoFormer's definition, not on
+the pages) at each token's position (``token_positions``).
 
 Parity status: every function here is pinned by the CPU tests in
-``tests/test_oracle_pins.py``, ``tests/test_oracle_fp8.py``, ``tests/test_oracle_qkv.py`` and
-``tests/test_oracle_rope.py`` (closed forms, library
+``tests/test_oracle_pins.py``, ``tests/test_oracle_fp8.py``, ``tests/test_oracle_qkv.py``,
+``tests/test_oracle_rope.py`` and ``tests/test_oracle_qknorm.py`` (closed forms, library
 routines on tiny cases -- torch SDPA, torch's float8_e4m3fn -- invariants, the format's
 error bound and a high-precision brute force).
 """
@@ -85,6 +86,8 @@ def load_library(path: str):
     lib.oracle_token_positions.restype = ci
     lib.oracle_rope.argtypes = [f64p, ci, ci, ci, ci, ci, i32p, ctypes.c_double]
     lib.oracle_rope.restype = ci
+    lib.oracle_rms_norm_heads.argtypes = [f64p, ci, ci, ci, ci, ci, u16p, ctypes.c_double]
+    lib.oracle_rms_norm_heads.restype = ci
     return lib
 
 
@@ -325,18 +328,49 @@ def rope(y, positions, theta: float, *, first_col: int = 0, n_heads: int = 1, he
     return out
 
 
+def rms_norm_heads(y, gain, eps: float, *, first_col: int = 0, n_heads: int = 1, head_dim: int = 128,
+                   lib=None) -> np.ndarray:
+    """Per-head RMS normalisation (QK-norm: RMSNorm of each head vector with the bf16 gain
+    [head_dim], eps inside the square root) of n_heads head vectors of each row of y from
+    column first_col on; returns a normalised copy."""
+    out = np.array(y, dtype=np.float64, copy=True, order="C")
+    if out.ndim == 1:
+        out = out.reshape(1, -1)
+    g = _bits(gain).reshape(-1)
+    assert g.size == head_dim
+    rc = (lib or _load()).oracle_rms_norm_heads(_p(out, ctypes.c_double), out.shape[0], out.shape[1], first_col,
+                                                n_heads, head_dim, _p(g, ctypes.c_uint16), float(eps))
+    if rc:
+        raise ValueError(f"oracle_rms_norm_heads rejected its input (code {rc})")
+    return out
+
+
+def _bf16_values(v, lib=None) -> np.ndarray:
+    """float64 values rounded to bf16 and widened back (exact)."""
+    bits = bf16_round(v, lib=lib).astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64)
+
+
 def qkv_append(x, w, k_pool, v_pool, block_table, cu_q_lens, seq_lens, *, rope_theta: float = 0.0,
-               num_threads: int = 0, lib=None):
+               q_norm=None, k_norm=None, norm_eps: float = 1e-6, num_threads: int = 0, lib=None):
     """The merged projection of every new token with its k and v appended to the cache.
 
     Returns (q [tokens, 32, 128] float64, k_pool', v_pool' uint16): q is exact; the cache
     holds k and v rounded once to bf16 (its format), placed by ``kv_append``'s rule.  With
-    rope_theta > 0 the 32 q heads and the 8 k heads of each token are first rotated at the
-    token's absolute position (``rope``); v is never rotated.
+    q_norm and k_norm (bf16 gains [128]) the q and k columns are rounded to bf16 (the
+    projection's output format) and every q head and k head is normalised (``rms_norm_heads``,
+    eps norm_eps) before the rotation.  With rope_theta > 0 the 32 q heads and the 8 k heads of
+    each token are then rotated at the token's absolute position (``rope``); v is never
+    normalised or rotated.
     """
     y = qkv_project(x, w, num_threads=num_threads, lib=lib)
     t = y.shape[0]
     assert y.shape[1] == Q_COLS + 2 * KV_COLS
+    assert (q_norm is None) == (k_norm is None), "QK-norm takes both gains"
+    if q_norm is not None:
+        y[:, :Q_COLS + KV_COLS] = _bf16_values(y[:, :Q_COLS + KV_COLS], lib=lib)
+        y = rms_norm_heads(y, q_norm, norm_eps, first_col=0, n_heads=32, lib=lib)
+        y = rms_norm_heads(y, k_norm, norm_eps, first_col=Q_COLS, n_heads=8, lib=lib)
     if rope_theta:
         pos = token_positions(cu_q_lens, seq_lens, lib=lib)
         y = rope(y, pos, rope_theta, first_col=0, n_heads=32, lib=lib)

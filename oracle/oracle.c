@@ -48,7 +48,9 @@
  *   y        [tokens][n_out]                       double
  *
  * Rotary position embedding of q and k heads (not on the pages; RoFormer's definition,
- * given at oracle_rope below) acts on the projection's output in place.
+ * given at oracle_rope below) acts on the projection's output in place, and so does the
+ * per-head RMS normalisation of q and k (QK-norm; not on the pages either, defined at
+ * oracle_rms_norm_heads below).
  *
  * Functions return 0 on success and a negative code on inconsistent input.
  */
@@ -549,6 +551,35 @@ int oracle_rope(double *y, int tokens, int row_stride, int first_col, int n_head
                 v[i] = lo * c - hi * s;
                 v[i + half] = hi * c + lo * s;
             }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Per-head RMS normalisation (QK-norm).  The pages do not define it; Qwen3 normalises each
+ * q and k head before the rotary embedding (the Qwen3 technical report, 2025, §2: QK-Norm)
+ * with RMSNorm (Zhang and Sennrich, 2019, "Root Mean Square Layer Normalization", §3): a
+ * head vector x of D values, divided by its root mean square, times a learned gain g of D
+ * values, with Qwen3's eps inside the square root (its configuration: 1e-6):
+ *     y[d] = g[d] * x[d] / sqrt((x[0]^2 + ... + x[D-1]^2) / D + eps)
+ * y: [tokens][row_stride] doubles; the n_heads head vectors of head_dim values from column
+ * first_col on are normalised in place, each on its own.  gain: head_dim bf16 bit patterns
+ * (one gain for all the heads).  Double precision throughout.
+ */
+int oracle_rms_norm_heads(double *y, int tokens, int row_stride, int first_col, int n_heads, int head_dim,
+                          const uint16_t *gain, double eps)
+{
+    if (tokens < 0 || head_dim < 1 || n_heads < 0 || first_col < 0 ||
+        first_col + n_heads * head_dim > row_stride || !(eps >= 0.0))
+        return -1;
+    for (int t = 0; t < tokens; ++t) {
+        for (int h = 0; h < n_heads; ++h) {
+            double *v = y + (size_t)t * row_stride + first_col + (size_t)h * head_dim;
+            double sum_sq = 0.0;
+            for (int d = 0; d < head_dim; ++d) sum_sq += v[d] * v[d];
+            const double rms = sqrt(sum_sq / head_dim + eps);
+            for (int d = 0; d < head_dim; ++d) v[d] = bf16_to_double(gain[d]) * v[d] / rms;
         }
     }
     return 0;

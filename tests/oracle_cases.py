@@ -224,6 +224,23 @@ def pin_battery(lib):
 
     check("rope_complex_form", rope_complex)
     check("rope_token_positions", rope_positions)
+
+    # ---- the per-head RMS normalisation of q and k (QK-norm)
+    def qknorm_torch():
+        gen = np.random.default_rng(37)
+        y = gen.standard_normal((5, 3 * 128)) * np.exp2(gen.uniform(-6, 6, (5, 3))).repeat(128, axis=1)
+        g = torch.from_numpy(1.0 + 0.5 * gen.standard_normal(128)).to(torch.bfloat16)
+        got = oracle.rms_norm_heads(y, g, 0.25, n_heads=3, lib=lib)
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(y).view(5, 3, 128), (128,), weight=g.double(),
+                                           eps=0.25).reshape(5, -1).numpy()
+        return np.allclose(got, ref, rtol=1e-13, atol=0)
+
+    def qknorm_constant_head():
+        got = oracle.rms_norm_heads(np.full((1, 128), 0.5), torch.ones(128, dtype=torch.bfloat16), 1e-6, lib=lib)
+        return np.allclose(got, 0.5 / np.sqrt(0.25 + 1e-6), rtol=1e-14, atol=0)
+
+    check("qknorm_torch", qknorm_torch)
+    check("qknorm_constant_head", qknorm_constant_head)
     return failed
 
 

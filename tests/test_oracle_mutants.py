@@ -84,6 +84,18 @@ MUTANTS = {
                          "                v[2 * i + 1] = hi * c + lo * s;"),
     # rotary embedding at the chunk-relative position
     "rope_relative_position": ("pos[cu_q_lens[s] + i] = seq_lens[s] - q_len + i;", "pos[cu_q_lens[s] + i] = i;"),
+    # QK-norm: eps left out of the square root
+    "rms_no_eps": ("const double rms = sqrt(sum_sq / head_dim + eps);", "const double rms = sqrt(sum_sq / head_dim);"),
+    # QK-norm: the sum of squares instead of their mean
+    "rms_sum_not_mean": ("const double rms = sqrt(sum_sq / head_dim + eps);", "const double rms = sqrt(sum_sq + eps);"),
+    # QK-norm: the mean square itself instead of its root
+    "rms_no_sqrt": ("const double rms = sqrt(sum_sq / head_dim + eps);", "const double rms = sum_sq / head_dim + eps;"),
+    # QK-norm: the gain read in reverse order
+    "rms_gain_reversed": ("v[d] = bf16_to_double(gain[d]) * v[d] / rms;",
+                          "v[d] = bf16_to_double(gain[head_dim - 1 - d]) * v[d] / rms;"),
+    # QK-norm: every head normalised by the first head's root mean square
+    "rms_first_head_only": ("for (int d = 0; d < head_dim; ++d) sum_sq += v[d] * v[d];",
+                            "for (int d = 0; d < head_dim; ++d) sum_sq += v[d - h * head_dim] * v[d - h * head_dim];"),
     # append writes at the chunk-relative position
     "append_relative_position": ("int p = seq_lens[s] - q_len + i;            /* absolute position */",
                                  "int p = i;            /* absolute position */"),
