@@ -836,26 +836,33 @@ def qkv_inputs(tokens, seed, device="cuda"):
     return x, w
 
 
-def qkv_measure(batch, x, w, steps, warmup, flush_buf, stream, clocks):
+def qkv_measure(batch, x, w, steps, warmup, flush_buf, stream, clocks, qk_norm=False):
     """One paged_qkv_append call (one kernel): q of every new token out, k and v into the cache,
-    q and k rotated by Qwen3's rotary embedding (theta 1e6) at each token's position."""
+    q and k rotated by Qwen3's rotary embedding (theta 1e6) at each token's position.  With
+    qk_norm, the call with Qwen3's per-head normalisation of q and k first (synthetic gains;
+    two kernels: the projection, then the in-place norm and rotation)."""
     import torch
 
     from paged_gqa_attention_gb300 import ops
 
     ws = ops.make_workspace(batch.num_seqs, batch.max_blocks_per_seq)
     q = torch.empty(x.shape[0], 32, 128, dtype=torch.bfloat16, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(9)
+    gq, gk = ((1.0 + 0.5 * torch.randn(128, generator=g, device="cuda")).to(torch.bfloat16) if qk_norm else None
+              for _ in range(2))
 
     def step(tm):
         if tm: tm.record(0)
         ops.paged_qkv_append(x, w, batch.k_pool, batch.v_pool, batch.block_table, batch.cu_q_lens,
-                             batch.seq_lens, ws, rope_theta=ops.QWEN3_ROPE_THETA, q_out=q)
+                             batch.seq_lens, ws, rope_theta=ops.QWEN3_ROPE_THETA, q_norm_weight=gq,
+                             k_norm_weight=gk, q_out=q)
         if tm: tm.record(1)
 
     spans, wall = run_timed(step, 2, steps, warmup, flush_buf, stream, clocks)
     ops.check_error(ws)
     return {"step_ms": mean([sp[0] for sp in spans]), "step_pcts": pcts([sp[0] for sp in spans]), "wall_s": wall,
-            "launches": steps}
+            "launches": steps * (2 if qk_norm else 1)}
 
 
 def e2e_qkv_measure(batch, x, w, steps, warmup, stream):
@@ -1180,7 +1187,19 @@ def measure(wname, steps, warmup, e2e_steps, peaks, flush_buf, stream, clocks, w
                         "decode_batch": {"tokens": db.total_tokens, "qkv_us": dr["step_ms"] * 1e3,
                                          "bytes": wbytes, "gbs": wbytes / (dr["step_ms"] * 1e-3) / 1e9,
                                          "hbm_frac": wbytes / (dr["step_ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
-        e["gpu_launches"] = r["launches"] + dr["launches"]
+        # the same call with Qwen3's QK-norm: the projection without the rotation, then one
+        # memory-bound pass that reads and rewrites every new q and k row
+        nr = qkv_measure(batch, x_in, w, max(20, min(steps, 200)), warmup, flush_buf, stream, None, qk_norm=True)
+        pr = qkv_measure(batch, x_in, w, max(20, min(steps, 200)), warmup, flush_buf, stream, None)
+        norm_bytes = 2 * batch.total_tokens * (32 + 8) * 128 * 2
+        extra_us = (nr["step_ms"] - pr["step_ms"]) * 1e3
+        e["kernels"]["qk_norm"] = {
+            "call_us": nr["step_ms"] * 1e3, "plain_call_us": pr["step_ms"] * 1e3, "extra_us": extra_us,
+            "norm_pass_bytes": norm_bytes,
+            "norm_pass_gbs_if_extra": norm_bytes / (extra_us * 1e-6) / 1e9 if extra_us > 0 else None,
+            "how": "the call with QK-norm and the plain call, each timed over the same steps; extra_us is "
+                   "their difference (the norm pass plus the launch between the two kernels)"}
+        e["gpu_launches"] = r["launches"] + dr["launches"] + nr["launches"] + pr["launches"]
         x = e2e_qkv_measure(batch, x_in, w, max(10, min(e2e_steps, 50)), 3, stream)
         x_ms = dist_max(x["step_ms"], world)
         e["e2e"] = {"value": world * flops / (x_ms * 1e-3) / 1e12, "unit": "TFLOP/s",

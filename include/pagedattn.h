@@ -147,7 +147,8 @@ pa_status kv_append(pa_shape shape, void *k_pool, void *v_pool,
  *   a = p * rope_theta^(-d/64),
  * in fp32 with the angle reduced to about 1e-6 rad.  rope_theta = 0 applies no rotation;
  * with a rotation max_blocks_per_seq * 256 must not exceed 2^24 (positions exact in fp32),
- * else PA_ERR_INVALID_ARG.  No per-head normalisation is applied.
+ * else PA_ERR_INVALID_ARG.  No per-head normalisation is applied (paged_qkv_append_qknorm
+ * below applies it).
  *   x [total_tokens][hidden] bf16, hidden a multiple of 256 (4096 for Qwen3-8B);
  *   w_qkv [6144][hidden] bf16: rows 0-4095 the q weight, 4096-5119 k, 5120-6143 v, each
  *   [out][in] as a linear layer stores it; q_out [total_tokens][32][128] bf16.
@@ -162,6 +163,28 @@ pa_status paged_qkv_append(pa_shape shape, int32_t hidden, float rope_theta, voi
                            int32_t num_blocks, const int32_t *cu_q_lens,
                            const int32_t *seq_lens, int32_t num_seqs, int32_t total_tokens,
                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * paged_qkv_append_qknorm: paged_qkv_append with the per-head normalisation of q and k that
+ * Qwen3 applies before the rotary embedding (QK-norm; the pages define none: RMSNorm,
+ * Zhang and Sennrich 2019, §3).  The projection's q and k heads are rounded to bf16 (its
+ * output format), then each 128-dim q head and k head x becomes
+ *   y[d] = g[d] * x[d] / sqrt((x[0]^2 + ... + x[127]^2) / 128 + norm_eps)
+ * in fp32, g = q_norm_weight for q heads and k_norm_weight for k heads; then, with
+ * rope_theta > 1, y is rotated as above, and the result is rounded to bf16 into q_out and the
+ * token's cache slot.  v is neither normalised nor rotated.  Qwen3: norm_eps = 1e-6.
+ *   q_norm_weight, k_norm_weight: [128] bf16 device arrays, 16-byte aligned, read only;
+ *   norm_eps: finite, >= 0.  Otherwise PA_ERR_INVALID_ARG.
+ * Two launches on `stream` (the projection, then an in-place pass over the new q and k
+ * rows); every other argument, layout, error and rule as paged_qkv_append.
+ */
+pa_status paged_qkv_append_qknorm(pa_shape shape, int32_t hidden, float rope_theta,
+                                  const void *q_norm_weight, const void *k_norm_weight, float norm_eps,
+                                  void *q_out, const void *x, const void *w_qkv, void *k_pool,
+                                  void *v_pool, const int32_t *block_table, int32_t max_blocks_per_seq,
+                                  int32_t num_blocks, const int32_t *cu_q_lens, const int32_t *seq_lens,
+                                  int32_t num_seqs, int32_t total_tokens, void *workspace,
+                                  size_t workspace_bytes, void *stream);
 
 /*
  * paged_attn_decode: one query token per sequence [P1 §4.4.2].

@@ -289,6 +289,70 @@ CascadePlan cascade_plan(int batch, int max_blocks_per_seq, int shared_blocks, i
     return p;
 }
 
+// paged_qkv_append with or without the per-head normalisation of q and k (q_norm, k_norm:
+// the bf16 gains, or null for none; the caller has checked them).
+pa_status qkv_impl(pa_shape shape, int32_t hidden, float rope_theta, const void *q_norm, const void *k_norm,
+                   float norm_eps, void *q_out, const void *x, const void *w_qkv, void *k_pool, void *v_pool,
+                   const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_blocks,
+                   const int32_t *cu_q_lens, const int32_t *seq_lens, int32_t num_seqs, int32_t total_tokens,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+    if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
+    if (hidden < 256 || hidden % 256 != 0 || hidden > (1 << 16)) return PA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+        (num_seqs == 0 && total_tokens != 0))
+        return PA_ERR_INVALID_ARG;
+    // the rotation: off (0) or a base above 1; positions must stay below 2^24 (exact in fp32)
+    if (rope_theta != 0.f && !(std::isfinite(rope_theta) && rope_theta > 1.f)) return PA_ERR_INVALID_ARG;
+    if (rope_theta != 0.f && (long long)max_blocks_per_seq * kBlock > (1ll << 24)) return PA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kHeaderBytes || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
+    if (total_tokens == 0) return PA_OK;
+    if (!q_out || !x || !w_qkv || !k_pool || !v_pool || !block_table || !cu_q_lens || !seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(q_out) || !aligned16(x) || !aligned16(w_qkv) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned4(block_table) || !aligned4(cu_q_lens) || !aligned4(seq_lens))
+        return PA_ERR_INVALID_ARG;
+    if ((long long)max_blocks_per_seq * kBlock > (1ll << 30)) return PA_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms <= 0) return PA_ERR_CUDA;
+    if (!get_encoder()) return PA_ERR_CUDA;
+    CUtensorMap x_map, w_map;
+    if (!encode_matrix_map(&x_map, x, total_tokens, hidden, qkv_tile_rows_loaded(total_tokens)) ||
+        !encode_matrix_map(&w_map, w_qkv, kHq * kD + 2 * kHkv * kD, hidden, qkv_weight_box_rows()))
+        return PA_ERR_INVALID_ARG;
+    QkvArgs a = {};
+    a.q_out = q_out;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.block_table = block_table;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.cu_q_lens = cu_q_lens;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.total_tokens = total_tokens;
+    a.hidden = hidden;
+    a.err = static_cast<uint32_t *>(workspace);
+    a.rope = rope_theta != 0.f ? 1 : 0;
+    for (int i = 0; i < kRopePairs; ++i) {
+        // frequency of pair i: theta^(-2i/128), kept as a float-float pair hi + lo
+        const double f = a.rope ? std::pow((double)rope_theta, -2.0 * i / kD) : 0.0;
+        a.rope_freq_hi[i] = (float)f;
+        a.rope_freq_lo[i] = (float)(f - (double)a.rope_freq_hi[i]);
+    }
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!q_norm) return launch_qkv(a, x_map, w_map, sms, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    // QK-norm: the projection without the rotation, then every q and k head normalised and
+    // rotated in place by a second kernel (the norm needs whole heads)
+    a.q_norm = q_norm;
+    a.k_norm = k_norm;
+    a.norm_eps = norm_eps;
+    QkvArgs plain = a;
+    plain.rope = 0;
+    if (launch_qkv(plain, x_map, w_map, sms, st) != cudaSuccess) return PA_ERR_CUDA;
+    return launch_qk_norm(a, sms, st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+
 }  // namespace
 
 extern "C" {
@@ -371,50 +435,23 @@ pa_status paged_qkv_append(pa_shape shape, int32_t hidden, float rope_theta, voi
                            int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t *cu_q_lens,
                            const int32_t *seq_lens, int32_t num_seqs, int32_t total_tokens, void *workspace,
                            size_t workspace_bytes, void *stream) {
-    if (!shape_ok(shape)) return PA_ERR_UNSUPPORTED;
-    if (hidden < 256 || hidden % 256 != 0 || hidden > (1 << 16)) return PA_ERR_UNSUPPORTED;
-    if (num_seqs < 0 || total_tokens < 0 || max_blocks_per_seq < 1 || num_blocks < 1 ||
-        (num_seqs == 0 && total_tokens != 0))
+    return qkv_impl(shape, hidden, rope_theta, nullptr, nullptr, 0.f, q_out, x, w_qkv, k_pool, v_pool, block_table,
+                    max_blocks_per_seq, num_blocks, cu_q_lens, seq_lens, num_seqs, total_tokens, workspace,
+                    workspace_bytes, stream);
+}
+
+pa_status paged_qkv_append_qknorm(pa_shape shape, int32_t hidden, float rope_theta, const void *q_norm_weight,
+                                  const void *k_norm_weight, float norm_eps, void *q_out, const void *x,
+                                  const void *w_qkv, void *k_pool, void *v_pool, const int32_t *block_table,
+                                  int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t *cu_q_lens,
+                                  const int32_t *seq_lens, int32_t num_seqs, int32_t total_tokens,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    if (!q_norm_weight || !k_norm_weight || !aligned16(q_norm_weight) || !aligned16(k_norm_weight) ||
+        !(std::isfinite(norm_eps) && norm_eps >= 0.f))
         return PA_ERR_INVALID_ARG;
-    // the rotation: off (0) or a base above 1; positions must stay below 2^24 (exact in fp32)
-    if (rope_theta != 0.f && !(std::isfinite(rope_theta) && rope_theta > 1.f)) return PA_ERR_INVALID_ARG;
-    if (rope_theta != 0.f && (long long)max_blocks_per_seq * kBlock > (1ll << 24)) return PA_ERR_INVALID_ARG;
-    if (!workspace || workspace_bytes < kHeaderBytes || !aligned16(workspace)) return PA_ERR_INVALID_ARG;
-    if (total_tokens == 0) return PA_OK;
-    if (!q_out || !x || !w_qkv || !k_pool || !v_pool || !block_table || !cu_q_lens || !seq_lens)
-        return PA_ERR_INVALID_ARG;
-    if (!aligned16(q_out) || !aligned16(x) || !aligned16(w_qkv) || !aligned16(k_pool) || !aligned16(v_pool) ||
-        !aligned4(block_table) || !aligned4(cu_q_lens) || !aligned4(seq_lens))
-        return PA_ERR_INVALID_ARG;
-    if ((long long)max_blocks_per_seq * kBlock > (1ll << 30)) return PA_ERR_INVALID_ARG;
-    const int sms = sm_count();
-    if (sms <= 0) return PA_ERR_CUDA;
-    if (!get_encoder()) return PA_ERR_CUDA;
-    CUtensorMap x_map, w_map;
-    if (!encode_matrix_map(&x_map, x, total_tokens, hidden, qkv_tile_rows_loaded(total_tokens)) ||
-        !encode_matrix_map(&w_map, w_qkv, kHq * kD + 2 * kHkv * kD, hidden, qkv_weight_box_rows()))
-        return PA_ERR_INVALID_ARG;
-    QkvArgs a = {};
-    a.q_out = q_out;
-    a.k_pool = k_pool;
-    a.v_pool = v_pool;
-    a.block_table = block_table;
-    a.max_blocks_per_seq = max_blocks_per_seq;
-    a.num_blocks = num_blocks;
-    a.cu_q_lens = cu_q_lens;
-    a.seq_lens = seq_lens;
-    a.num_seqs = num_seqs;
-    a.total_tokens = total_tokens;
-    a.hidden = hidden;
-    a.err = static_cast<uint32_t *>(workspace);
-    a.rope = rope_theta != 0.f ? 1 : 0;
-    for (int i = 0; i < kRopePairs; ++i) {
-        // frequency of pair i: theta^(-2i/128), kept as a float-float pair hi + lo
-        const double f = a.rope ? std::pow((double)rope_theta, -2.0 * i / kD) : 0.0;
-        a.rope_freq_hi[i] = (float)f;
-        a.rope_freq_lo[i] = (float)(f - (double)a.rope_freq_hi[i]);
-    }
-    return launch_qkv(a, x_map, w_map, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return qkv_impl(shape, hidden, rope_theta, q_norm_weight, k_norm_weight, norm_eps, q_out, x, w_qkv, k_pool,
+                    v_pool, block_table, max_blocks_per_seq, num_blocks, cu_q_lens, seq_lens, num_seqs,
+                    total_tokens, workspace, workspace_bytes, stream);
 }
 
 pa_status kv_append_fp8(pa_shape shape, void *k_codes, void *v_codes, float *k_scale, float *v_scale,

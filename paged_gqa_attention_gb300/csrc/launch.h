@@ -117,6 +117,11 @@ struct QkvArgs {
     int32_t rope;
     float rope_freq_hi[kRopePairs];
     float rope_freq_lo[kRopePairs];
+    // Per-head RMS normalisation of q and k (launch_qk_norm only): bf16 gains [128] for the
+    // q heads and for the k heads, and the eps under the square root.
+    const void *q_norm;
+    const void *k_norm;
+    float norm_eps;
 };
 
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
@@ -128,6 +133,9 @@ int qkv_weight_box_rows();
 int qkv_tile_rows_loaded(int total_tokens);
 cudaError_t launch_qkv(const QkvArgs &a, const CUtensorMap &x_map, const CUtensorMap &w_map, int num_sms,
                        cudaStream_t stream);
+// In place over q_out and the new tokens' k rows in the cache, after launch_qkv without a
+// rotation: each q and k head normalised by its RMS and gain, then rotated when a.rope is set.
+cudaError_t launch_qk_norm(const QkvArgs &a, int num_sms, cudaStream_t stream);
 
 // k_map / v_map: 4-D tensor maps over the pools (see api.cu for the boxes).
 // One-time per-device kernel setup (dynamic shared memory size) of the decode kernel;

@@ -25,7 +25,10 @@
 // head (the weight rows are loaded in that order); every 64 tile columns are then the two
 // halves of 32 pairs of one head.  The angle is a float-float product p * (hi + lo) of the
 // frequency, reduced by 2 pi in three parts (Cody and Waite's method) before the sine and
-// cosine: about 1e-6 rad at any position below 2^24.  No per-head normalisation is applied.
+// cosine: about 1e-6 rad at any position below 2^24.  The optional per-head normalisation of
+// q and k (QK-norm) needs whole heads, which the product tiles below do not hold: it runs as a
+// second, memory-bound kernel (qk_norm_kernel, at the end of this file) over the rows the
+// projection wrote without a rotation, and applies the rotation after it.
 //
 // GEMM on the 5th-generation tensor cores: with more than 256 tokens a pair of CTAs on two
 // SMs computes 256 tokens x 192 output columns (tcgen05.mma.cta_group::2, see the pair kernel
@@ -162,7 +165,9 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 // offset of (slot, KV head 0, dim 0) in a pool, or -1 when the token's sequence data are
 // inconsistent or its block id is outside the pool (recorded in the error word); *pos gets
 // p = seq_len - q_len + i, or -1 when the sequence data are inconsistent.
-__device__ __forceinline__ long long token_slot(const QkvArgs &a, int t, int *pos) {
+// Token t's sequence (*seq) and absolute position p = seq_len - q_len + i, or -1 when the
+// sequence data are inconsistent (recorded in the error word).
+__device__ __forceinline__ int token_position(const QkvArgs &a, int t, int *seq) {
     int lo = 0, hi = a.num_seqs - 1;   // the sequence s with cu_q_lens[s] <= t < cu_q_lens[s + 1]
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -170,16 +175,22 @@ __device__ __forceinline__ long long token_slot(const QkvArgs &a, int t, int *po
         else hi = mid - 1;
     }
     const int s = lo;
+    *seq = s;
     const int c0 = __ldg(a.cu_q_lens + s), c1 = __ldg(a.cu_q_lens + s + 1);
     const int seq_len = __ldg(a.seq_lens + s);
     const int q_len = c1 - c0;
-    *pos = -1;
     if (c0 > t || t >= c1 || q_len > seq_len || seq_len > a.max_blocks_per_seq * kBlock) {
         record_error(a.err, kErrDevice | kErrBadCuQ);
         return -1;
     }
-    const int p = seq_len - q_len + (t - c0);
+    return seq_len - q_len + (t - c0);
+}
+
+__device__ __forceinline__ long long token_slot(const QkvArgs &a, int t, int *pos) {
+    int s;
+    const int p = token_position(a, t, &s);
     *pos = p;
+    if (p < 0) return -1;
     const int blk = __ldg(a.block_table + (size_t)s * a.max_blocks_per_seq + p / kBlock);
     if (blk < 0 || blk >= a.num_blocks) {
         record_error(a.err, kErrDevice | kErrBadBlock);
@@ -188,12 +199,11 @@ __device__ __forceinline__ long long token_slot(const QkvArgs &a, int t, int *po
     return ((long long)blk * kBlock + p % kBlock) * kHkv * kD;
 }
 
-// cos and sin of the rotation angle of pair i at position pf (an integer below 2^24, exact in
-// fp32).  p * freq is formed as hi + lo (the product's rounding error recovered with an fma),
+// cos and sin of the rotation angle at position pf (an integer below 2^24, exact in fp32) for
+// the frequency fh + fl (pair i's: rope_cos_sin).  p * freq is formed as hi + lo (the product's rounding error recovered with an fma),
 // the multiple of 2 pi nearest hi is taken off in three parts (Cody and Waite), lo is added
 // back, and the reduced angle (|r| < 4) goes to the fast sine/cosine.
-__device__ __forceinline__ void rope_cos_sin(const QkvArgs &a, int i, float pf, float &c, float &s) {
-    const float fh = a.rope_freq_hi[i], fl = a.rope_freq_lo[i];
+__device__ __forceinline__ void angle_cos_sin(float pf, float fh, float fl, float &c, float &s) {
     const float ah = __fmul_rn(pf, fh);
     const float al = fmaf(pf, fl, fmaf(pf, fh, -ah));
     const float k = rintf(__fmul_rn(ah, kInvTwoPi));
@@ -201,6 +211,10 @@ __device__ __forceinline__ void rope_cos_sin(const QkvArgs &a, int i, float pf, 
     r = fmaf(-k, kTwoPiMid, r);
     r = fmaf(-k, kTwoPiLo, r);
     __sincosf(__fadd_rn(r, al), &s, &c);
+}
+
+__device__ __forceinline__ void rope_cos_sin(const QkvArgs &a, int i, float pf, float &c, float &s) {
+    angle_cos_sin(pf, a.rope_freq_hi[i], a.rope_freq_lo[i], c, s);
 }
 
 // The epilogue of one tile for this thread's token row: logical columns col0 .. col0+width-1
@@ -744,6 +758,142 @@ cudaError_t launch_qkv_bn(const QkvArgs &a, const CUtensorMap &x_map, const CUte
     return cudaLaunchKernelEx(&cfg, qkv_kernel<BN, BMA>, x_map, w_map, a);
 }
 
+// ------------------------------------------------------------------ QK-norm (optional)
+// Per-head RMS normalisation of the q and k heads.  The pages define none; Qwen3 normalises
+// each q and k head before the rotary embedding with RMSNorm (Zhang and Sennrich 2019, §3):
+// a head x of 128 values, as the projection wrote it (bf16, not rotated), becomes
+//     y[d] = g[d] * x[d] / sqrt(mean(x^2) + eps)
+// in fp32, g the q or the k gain; with the rotation on it is then turned by the token's
+// angles (the rotation store_tile_row applies), and it is rounded to bf16 in place.
+//
+// A token's heads come in 5 groups of 8: groups 0-3 are q heads 8g .. 8g+7 (2 KiB contiguous
+// in q_out), group 4 the token's 8 k heads (2 KiB contiguous at its cache slot).  A warp takes
+// `groups_per_warp` consecutive groups of one token (all 5 when there are many tokens, so the
+// token's lookup and angles are computed once; 1 when there are few, for parallelism).  Lane l
+// holds dims 2l, 2l+1, 64+2l and 65+2l of each head -- both dims of two rotation pairs -- so
+// only the sums of squares cross lanes, and every load and store of the warp is 128 contiguous
+// bytes.  The pass is bound by its instruction count more than by memory (the rows it reads
+// were just written by the projection and sit in L2), hence the packed fp32 arithmetic and a
+// reduce-scatter of the eight sums (17 shuffles instead of 40).
+constexpr int kNormGroups = kHq / 8 + 1;       // 4 groups of q heads + the k heads
+constexpr int kNormThreads = 256;
+constexpr int kNormCtasPerSm = 4;              // 64 registers a thread
+
+__device__ __forceinline__ float bf16_low_half(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_high_half(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// The sums of v[0..7] over the warp, for every lane: reduce-scatter (after the steps over lane
+// bits 16, 8 and 4 a lane holds a partial of head h(lane) = 4 b16 + 2 b8 + b4, the steps over
+// bits 2 and 1 complete it; lanes that share h compute the same value since each addition
+// commutes), then one shuffle per head from a lane that holds it.  f(total) is applied once per
+// lane, before the gather.
+template <typename F>
+__device__ __forceinline__ void warp_sums8(float (&v)[8], int lane, F f) {
+    const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
+    float u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float keep = b16 ? v[i + 4] : v[i], send = b16 ? v[i] : v[i + 4];
+        u[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    float t[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float keep = b8 ? u[i + 2] : u[i], send = b8 ? u[i] : u[i + 2];
+        t[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float r = (b4 ? t[1] : t[0]) + __shfl_xor_sync(0xffffffffu, b4 ? t[0] : t[1], 4);
+    r += __shfl_xor_sync(0xffffffffu, r, 2);
+    r += __shfl_xor_sync(0xffffffffu, r, 1);
+    r = f(r);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __shfl_sync(0xffffffffu, r, ((j & 4) << 2) | ((j & 2) << 2) | ((j & 1) << 2));
+}
+
+__global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm)
+qk_norm_kernel(const __grid_constant__ QkvArgs a, int groups_per_warp) {
+    // q_out and the cache rows are the projection's, launched just before on the stream
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    // the rotation frequencies, copied once into shared memory: read from the argument space at
+    // an index that differs between lanes, every read would be serialised
+    __shared__ float2 freq[kRopePairs];            // (hi, lo) of pair i
+    if (threadIdx.x < kRopePairs) freq[threadIdx.x] = make_float2(a.rope_freq_hi[threadIdx.x], a.rope_freq_lo[threadIdx.x]);
+    __syncthreads();
+    const int chunks = (kNormGroups + groups_per_warp - 1) / groups_per_warp;
+    const long long work = (long long)a.total_tokens * chunks;
+    const long long step = (long long)gridDim.x * (kNormThreads / 32);
+    for (long long w = (long long)blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5); w < work; w += step) {
+        const int tok = (int)(w / chunks);
+        const int g0 = (int)(w % chunks) * groups_per_warp;
+        const int g1 = min(kNormGroups, g0 + groups_per_warp);
+        int pos = -1;
+        long long slot = -1;
+        if (g1 == kNormGroups) {
+            slot = token_slot(a, tok, &pos);
+        } else if (a.rope) {
+            int seq;
+            pos = token_position(a, tok, &seq);
+        }
+        float c0 = 1.f, s0 = 0.f, c1 = 1.f, s1 = 0.f;   // pairs 2l and 2l+1
+        if (a.rope) {
+            const float pf = (float)pos;
+            const float2 f0 = freq[2 * lane], f1 = freq[2 * lane + 1];
+            angle_cos_sin(pf, f0.x, f0.y, c0, s0);
+            angle_cos_sin(pf, f1.x, f1.y, c1, s1);
+            if (pos < 0) c0 = s0 = c1 = s1 = __int_as_float(0x7fc00000);   // position unknown
+        }
+        for (int g = g0; g < g1; ++g) {
+            const bool is_k = g == kNormGroups - 1;
+            if (is_k && slot < 0) break;          // no k row was written for this token
+            uint32_t *row = is_k ? reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(a.k_pool) + slot)
+                                 : reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(a.q_out) +
+                                                                ((size_t)tok * kHq + g * 8) * kD);
+            uint32_t w_lo[8], w_hi[8];            // dims (2l, 2l+1) and (64+2l, 65+2l) of 8 heads
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                w_lo[h] = row[h * (kD / 2) + lane];
+                w_hi[h] = row[h * (kD / 2) + 32 + lane];
+            }
+            // out[2l]   = inv (x[2l] g c0 - x[64+2l] g' s0),  out[64+2l] = inv (x[64+2l] g' c0 + x[2l] g s0)
+            // (and the same for dims 2l+1, 65+2l with c1, s1): per-group coefficients
+            // this lane's gains (dims 2l, 2l+1, 64+2l, 65+2l), from L1 after the first group
+            const uint32_t *gw = static_cast<const uint32_t *>(is_k ? a.k_norm : a.q_norm);
+            const uint32_t gl = __ldg(gw + lane), gh = __ldg(gw + 32 + lane);
+            const float G0 = bf16_low_half(gl), G1 = bf16_high_half(gl);
+            const float G2 = bf16_low_half(gh), G3 = bf16_high_half(gh);
+            const float A0 = G0 * c0, A1 = G1 * c1, nB0 = -(G2 * s0), nB1 = -(G3 * s1);   // -> dims 2l, 2l+1
+            const float A2 = G2 * c0, A3 = G3 * c1, B2 = G0 * s0, B3 = G1 * s1;           // -> dims 64+2l, 65+2l
+            float ss[8];
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const float x0 = bf16_low_half(w_lo[h]), x1 = bf16_high_half(w_lo[h]);
+                const float x2 = bf16_low_half(w_hi[h]), x3 = bf16_high_half(w_hi[h]);
+                float p, q;
+                ffma2(p, q, x0, x1, x0, x1, 0.f, 0.f);
+                ffma2(p, q, x2, x3, x2, x3, p, q);
+                ss[h] = p + q;
+            }
+            const float eps = a.norm_eps;
+            warp_sums8(ss, lane, [eps](float t) { return rsqrtf(fmaf(t, 1.0f / kD, eps)); });
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const float x0 = bf16_low_half(w_lo[h]), x1 = bf16_high_half(w_lo[h]);
+                const float x2 = bf16_low_half(w_hi[h]), x3 = bf16_high_half(w_hi[h]);
+                float o0, o1, o2, o3;
+                ffma2(o0, o1, x0, x1, A0, A1, 0.f, 0.f);
+                ffma2(o0, o1, x2, x3, nB0, nB1, o0, o1);
+                ffma2(o0, o1, o0, o1, ss[h], ss[h], 0.f, 0.f);
+                ffma2(o2, o3, x2, x3, A2, A3, 0.f, 0.f);
+                ffma2(o2, o3, x0, x1, B2, B3, o2, o3);
+                ffma2(o2, o3, o2, o3, ss[h], ss[h], 0.f, 0.f);
+                row[h * (kD / 2) + lane] = pack_bf16x2(o0, o1);
+                row[h * (kD / 2) + 32 + lane] = pack_bf16x2(o2, o3);
+            }
+        }
+    }
+}
+
 }  // namespace
 
 int qkv_tile_cols(int total_tokens) { return total_tokens <= 2 * kBM ? 64 : kPairBN; }
@@ -756,6 +906,26 @@ cudaError_t launch_qkv(const QkvArgs &a, const CUtensorMap &x_map, const CUtenso
     if (qkv_tile_rows_loaded(a.total_tokens) == 32) return launch_qkv_bn<64, 32>(a, x_map, w_map, num_sms, stream);
     if (a.total_tokens <= 2 * kBM) return launch_qkv_bn<64, 128>(a, x_map, w_map, num_sms, stream);
     return launch_qkv_pair(a, x_map, w_map, num_sms, stream);
+}
+
+cudaError_t launch_qk_norm(const QkvArgs &a, int num_sms, cudaStream_t stream) {
+    if (a.total_tokens == 0) return cudaSuccess;
+    const long long resident = (long long)num_sms * kNormCtasPerSm * (kNormThreads / 32);   // warps in one wave
+    // many tokens: a warp per token (lookup and angles once); few: a warp per group of 8 heads
+    const int groups_per_warp = (long long)a.total_tokens * kNormGroups > 2 * resident ? kNormGroups : 1;
+    const long long work = (long long)a.total_tokens * ((kNormGroups + groups_per_warp - 1) / groups_per_warp);
+    const long long need = (work + kNormThreads / 32 - 1) / (kNormThreads / 32);
+    const long long ctas = (long long)num_sms * kNormCtasPerSm;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(need < ctas ? need : ctas));
+    cfg.blockDim = dim3(kNormThreads);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qk_norm_kernel, a, groups_per_warp);
 }
 
 }  // namespace pa

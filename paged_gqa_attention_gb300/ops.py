@@ -75,6 +75,9 @@ def load() -> ctypes.CDLL:
                                      vp, sz,
                                      vp]
     lib.paged_qkv_append.restype = ctypes.c_int
+    lib.paged_qkv_append_qknorm.argtypes = [pa_shape, i32, ctypes.c_float, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp,
+                                            vp, i32, i32, vp, vp, i32, i32, vp, sz, vp]
+    lib.paged_qkv_append_qknorm.restype = ctypes.c_int
     lib.paged_attn_decode.argtypes = [pa_shape, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, f32, vp,
                                       sz, vp]
     lib.paged_attn_decode.restype = ctypes.c_int
@@ -210,13 +213,18 @@ QKV_COLS = NUM_Q_HEADS * HEAD_DIM + 2 * NUM_KV_HEADS * HEAD_DIM   # 6144
 
 
 QWEN3_ROPE_THETA = 1.0e6
+# Qwen3's eps inside the square root of its RMS normalisation (QK-norm)
+QWEN3_NORM_EPS = 1.0e-6
 
 
 def paged_qkv_append(x, w_qkv, k_pool, v_pool, block_table, cu_q_lens, seq_lens, workspace, *,
-                     rope_theta: float = 0.0, q_out=None, stream=None) -> torch.Tensor:
+                     rope_theta: float = 0.0, q_norm_weight=None, k_norm_weight=None,
+                     norm_eps: float = QWEN3_NORM_EPS, q_out=None, stream=None) -> torch.Tensor:
     """Merged Q/K/V projection of the new tokens: x [T, hidden] @ w_qkv[6144, hidden]^T; returns
     q [T, 32, 128] and writes k and v into the pools at each sequence's tail positions.
-    rope_theta > 1 rotates the q and k heads at each token's position first (0: no rotation)."""
+    rope_theta > 1 rotates the q and k heads at each token's position first (0: no rotation).
+    q_norm_weight / k_norm_weight (bf16 [128], both or neither) normalise every q and k head by
+    its RMS before the rotation (QK-norm, eps norm_eps; paged_qkv_append_qknorm)."""
     dev = x.device
     _need(x, "x", torch.bfloat16, (None, None), dev)
     hidden = x.shape[1]
@@ -231,12 +239,25 @@ def paged_qkv_append(x, w_qkv, k_pool, v_pool, block_table, cu_q_lens, seq_lens,
     if q_out is None:
         q_out = torch.empty(x.shape[0], NUM_Q_HEADS, HEAD_DIM, dtype=torch.bfloat16, device=dev)
     _need(q_out, "q_out", torch.bfloat16, (x.shape[0], NUM_Q_HEADS, HEAD_DIM), dev)
-    st = load().paged_qkv_append(SHAPE, hidden, float(rope_theta), q_out.data_ptr(), x.data_ptr(), w_qkv.data_ptr(),
-                                 k_pool.data_ptr(), v_pool.data_ptr(), block_table.data_ptr(),
-                                 block_table.shape[1], k_pool.shape[0], cu_q_lens.data_ptr(),
-                                 seq_lens.data_ptr(), num_seqs, x.shape[0], workspace.data_ptr(),
-                                 workspace.numel(), _stream(stream))
-    _check("paged_qkv_append", st)
+    if (q_norm_weight is None) != (k_norm_weight is None):
+        raise ValueError("QK-norm takes both q_norm_weight and k_norm_weight")
+    if q_norm_weight is None:
+        st = load().paged_qkv_append(SHAPE, hidden, float(rope_theta), q_out.data_ptr(), x.data_ptr(),
+                                     w_qkv.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), block_table.data_ptr(),
+                                     block_table.shape[1], k_pool.shape[0], cu_q_lens.data_ptr(),
+                                     seq_lens.data_ptr(), num_seqs, x.shape[0], workspace.data_ptr(),
+                                     workspace.numel(), _stream(stream))
+        _check("paged_qkv_append", st)
+        return q_out
+    _need(q_norm_weight, "q_norm_weight", torch.bfloat16, (HEAD_DIM,), dev)
+    _need(k_norm_weight, "k_norm_weight", torch.bfloat16, (HEAD_DIM,), dev)
+    st = load().paged_qkv_append_qknorm(SHAPE, hidden, float(rope_theta), q_norm_weight.data_ptr(),
+                                        k_norm_weight.data_ptr(), float(norm_eps), q_out.data_ptr(), x.data_ptr(),
+                                        w_qkv.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+                                        block_table.data_ptr(), block_table.shape[1], k_pool.shape[0],
+                                        cu_q_lens.data_ptr(), seq_lens.data_ptr(), num_seqs, x.shape[0],
+                                        workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check("paged_qkv_append_qknorm", st)
     return q_out
 
 

@@ -118,6 +118,22 @@ def test_prefill_output_must_be_32_byte_aligned(lib):
     assert lib.paged_attn_prefill(*args(p(48))) == 1
 
 
+def test_qknorm_gains_and_eps_are_checked_on_the_host(lib):
+    """paged_qkv_append_qknorm rejects a missing or misaligned gain and an eps that is
+    negative or not finite (PA_ERR_INVALID_ARG) before any CUDA work.  (Host addresses: no
+    call here may get past validation.)"""
+    buf = (ctypes.c_uint8 * 8192)()
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    p = lambda off: ctypes.c_void_p(base + 1024 + off)
+    args = lambda gq, gk, eps: (ops.SHAPE, 256, 0.0, gq, gk, eps, p(0), p(256), p(512), p(768), p(1024), p(1280),
+                                1, 1, p(1536), p(1792), 1, 1, ctypes.c_void_p(base), 1024, None)
+    assert lib.paged_qkv_append_qknorm(*args(None, p(2048), 1e-6)) == 1
+    assert lib.paged_qkv_append_qknorm(*args(p(2048), None, 1e-6)) == 1
+    assert lib.paged_qkv_append_qknorm(*args(p(2056), p(2048), 1e-6)) == 1
+    for eps in (-1e-6, float("nan"), float("inf")):
+        assert lib.paged_qkv_append_qknorm(*args(p(2048), p(2304), eps)) == 1
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ops, "_lib", None)
     monkeypatch.setattr(ops, "_LIB_PATH", str(tmp_path / "missing.so"))

@@ -59,7 +59,8 @@ def within_tol(got, exact, abs_sum, what):
     got = np.asarray(got, dtype=np.float64)
     tol = np.abs(exact) * 2.0 ** -8 + abs_sum * 2.0 ** -16
     err = np.abs(got - exact)
-    i = np.unravel_index(np.argmax(err / tol), err.shape)
+    with np.errstate(divide="ignore", invalid="ignore"):      # zero rows: 0 / 0 in the report only
+        i = np.unravel_index(np.nanargmax(np.where(tol > 0, err / tol, np.where(err > 0, np.inf, 0.0))), err.shape)
     assert (err <= tol).all(), (f"{what}: worst element {i}: got {got[i]!r} exact {exact[i]!r} "
                                 f"tolerance {tol[i]!r} ({(err > tol).sum()} elements beyond it)")
 
@@ -301,3 +302,169 @@ def test_repeated_calls_are_bit_identical(ctx_and_q, rope_theta):
         assert torch.equal(q1.view(torch.int16), q2.view(torch.int16))
         assert torch.equal(k1.view(torch.int16), b.k_pool.view(torch.int16))
         assert torch.equal(v1.view(torch.int16), b.v_pool.view(torch.int16))
+
+
+# ------------------------------------------------------------------ QK-norm (paged_qkv_append_qknorm)
+
+def norm_gains(seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    q = (1.0 + 0.5 * torch.randn(128, generator=g, device="cuda")).to(torch.bfloat16)
+    k = (1.0 + 0.5 * torch.randn(128, generator=g, device="cuda")).to(torch.bfloat16)
+    return q, k
+
+
+def qknorm_exact_and_bound(x, w, cu_q_lens, seq_lens, rope_theta, gq, gk, eps, rows=None):
+    """The oracle's q and k after the norm and the rotation (exact, before the last rounding),
+    and per element the part of the bound that the projection's own error carries through
+    the norm.  The GPU normalises its bf16 projection p', the oracle the rounded exact one p:
+    |p' - p| <= d = 2^-7 |y| + 2^-16 sum|x w| (the projection's bound plus the oracle's half
+    step).  To first order that moves n = g p / r (r the head's RMS with eps) by
+    |g| d / r + |g p| (sum_j |p_j| d_j) / (128 r^3); a rotated dim mixes the two dims of its
+    pair, and the fp32 arithmetic and angle add 1e-5 of the pair's size.  Returned scaled by
+    2^16, in the units ``within_tol`` takes for its second term."""
+    y = oracle.qkv_project(x.cpu(), w.cpu(), rows=rows)
+    a = abs_sums(x, w, rows)
+    p = (oracle.bf16_round(y[:, :5120]).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    d = 2.0 ** -7 * np.abs(y[:, :5120]) + 2.0 ** -16 * a[:, :5120]
+    n = np.concatenate([oracle.rms_norm_heads(p[:, :4096], gq.cpu(), eps, n_heads=32),
+                        oracle.rms_norm_heads(p[:, 4096:], gk.cpu(), eps, n_heads=8)], axis=1)
+    g = np.concatenate([np.tile(gq.double().cpu().numpy(), 32), np.tile(gk.double().cpu().numpy(), 8)])
+    ph, dh = p.reshape(len(p), 40, 128), d.reshape(len(p), 40, 128)
+    r = np.sqrt((ph ** 2).mean(axis=2) + eps)[:, :, None]
+    cross = (np.abs(ph) * dh).sum(axis=2)[:, :, None]
+    dn = (np.abs(g).reshape(1, 40, 128) * (dh / r + np.abs(ph) * cross / (128 * r ** 3))).reshape(len(p), 5120)
+    if rope_theta:
+        pos = oracle.token_positions(cu_q_lens.cpu(), seq_lens.cpu())
+        if rows is not None:
+            pos = pos[np.asarray(rows)]
+        e = oracle.rope(n, pos, rope_theta, first_col=0, n_heads=32)
+        e = oracle.rope(e, pos, rope_theta, first_col=4096, n_heads=8)
+        cols = np.arange(5120)
+        partner = cols ^ 64
+        bound = dn[:, cols] + dn[:, partner] + 1e-5 * (np.abs(n[:, cols]) + np.abs(n[:, partner]))
+    else:
+        e = n
+        bound = dn + 1e-6 * np.abs(n)
+    return e, bound * 2.0 ** 16, y, a
+
+
+def check_qknorm_case(b, x, w, rope_theta, eps=ops.QWEN3_NORM_EPS, seed=90):
+    gq, gk = norm_gains(seed)
+    kp0 = b.k_pool.view(torch.int16).cpu().numpy().copy()
+    vp0 = b.v_pool.view(torch.int16).cpu().numpy().copy()
+    ws = workspace_for(b)
+    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws,
+                             rope_theta=rope_theta, q_norm_weight=gq, k_norm_weight=gk, norm_eps=eps)
+    ops.check_error(ws)
+    e, bound, y, a = qknorm_exact_and_bound(x, w, b.cu_q_lens, b.seq_lens, rope_theta, gq, gk, eps)
+    qg = q.float().cpu().numpy().astype(np.float64).reshape(x.shape[0], -1)
+    within_tol(qg, e[:, :4096], bound[:, :4096], "normalised q")
+    rel = np.sqrt(((qg - e[:, :4096]) ** 2).sum() / (e[:, :4096] ** 2).sum())
+    assert rel <= 5e-3, rel
+    kp = b.k_pool.view(torch.int16).cpu().numpy()
+    vp = b.v_pool.view(torch.int16).cpu().numpy()
+    touched = np.zeros(kp.shape[:2], dtype=bool)
+    for t, (blk, slot) in enumerate(new_slots(b)):
+        touched[blk, slot] = True
+        kf = b.k_pool[blk, slot].double().cpu().numpy().reshape(-1)
+        vf = b.v_pool[blk, slot].double().cpu().numpy().reshape(-1)
+        within_tol(kf, e[t, 4096:], bound[t, 4096:], f"normalised k row of token {t}")
+        within_tol(vf, y[t, 5120:], a[t, 5120:], f"v row of token {t}")
+    assert np.array_equal(kp[~touched], kp0[~touched]), "k pool written outside the new slots"
+    assert np.array_equal(vp[~touched], vp0[~touched]), "v pool written outside the new slots"
+    return q
+
+
+@pytest.mark.parametrize("rope_theta", [0.0, ops.QWEN3_ROPE_THETA])
+@pytest.mark.parametrize("ctx_and_q", [
+    [(0, 1)],
+    [(0, 37)],                                  # 64-column tiles, 32 rows of x loaded
+    [(200, 100), (0, 64), (511, 1)],            # chunks after context, a decode-like row
+    [(0, 300)],                                 # CTA pairs, a ragged last tile
+    [(37, 130), (1000, 0), (255, 200)],         # a sequence with no new token
+    [(131000, 40), (70000, 300)],               # large positions
+])
+def test_qkv_append_qknorm_matches_oracle(ctx_and_q, rope_theta):
+    """Qwen3's QK-norm (RMSNorm of every q and k head with its own gain, eps 1e-6) on the bf16
+    projection, then the rotation, against the oracle's norm and rotation."""
+    b = batch_for(ctx_and_q, seed=180 + len(ctx_and_q))
+    check_qknorm_case(b, inputs(181, b.total_tokens), weights(182), rope_theta)
+
+
+def test_qknorm_large_eps_and_a_zero_row():
+    """eps large against the heads' mean square (0.5 of it) weighs in the result; a zero input
+    row gives zero q and k heads (0 / sqrt(eps))."""
+    b = batch_for([(10, 50)], seed=183)
+    x = inputs(184, b.total_tokens)
+    x[7] = 0
+    w = weights(185)
+    q = check_qknorm_case(b, x, w, ops.QWEN3_ROPE_THETA, eps=0.5)
+    assert torch.count_nonzero(q[7]).item() == 0
+
+
+def test_qknorm_full_prefill_chunk_sampled_rows():
+    """4096 new tokens: sampled rows of q and of the cache against the oracle."""
+    b = wl.causal_prefill(device="cuda")
+    x = inputs(186, b.total_tokens)
+    w = weights(187)
+    gq, gk = norm_gains(188)
+    ws = workspace_for(b)
+    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws,
+                             rope_theta=ops.QWEN3_ROPE_THETA, q_norm_weight=gq, k_norm_weight=gk)
+    ops.check_error(ws)
+    rows = [0, 1, 127, 128, 2047, 2048, 4000, 4095]
+    e, bound, y, a = qknorm_exact_and_bound(x, w, b.cu_q_lens, b.seq_lens, ops.QWEN3_ROPE_THETA, gq, gk,
+                                            ops.QWEN3_NORM_EPS, rows=rows)
+    slots = new_slots(b)
+    qg = q.float().cpu().numpy().astype(np.float64).reshape(b.total_tokens, -1)
+    for r, t in enumerate(rows):
+        within_tol(qg[t], e[r, :4096], bound[r, :4096], f"q row {t}")
+        blk, slot = slots[t]
+        kf = b.k_pool[blk, slot].double().cpu().numpy().reshape(-1)
+        vf = b.v_pool[blk, slot].double().cpu().numpy().reshape(-1)
+        within_tol(kf, e[r, 4096:], bound[r, 4096:], f"k row {t}")
+        within_tol(vf, y[r, 5120:], a[r, 5120:], f"v row {t}")
+
+
+def test_qknorm_bad_block_writes_no_kv_but_keeps_q():
+    """A token whose block is outside the pool: no k or v row anywhere, its q still
+    normalised and rotated, PA_ERR_DEVICE recorded."""
+    b = batch_for([(0, 40), (100, 20)], seed=189)
+    x = inputs(190, b.total_tokens)
+    w = weights(191)
+    gq, gk = norm_gains(192)
+    bt = b.block_table.clone()
+    bt[1, 0] = b.num_blocks + 7
+    kp0, vp0 = b.k_pool.clone(), b.v_pool.clone()
+    ws = workspace_for(b)
+    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, bt, b.cu_q_lens, b.seq_lens, ws,
+                             rope_theta=ops.QWEN3_ROPE_THETA, q_norm_weight=gq, k_norm_weight=gk)
+    with pytest.raises(ops.PagedAttnError) as err:
+        ops.check_error(ws)
+    assert err.value.status == 4
+    e, bound, _, _ = qknorm_exact_and_bound(x, w, b.cu_q_lens, b.seq_lens, ops.QWEN3_ROPE_THETA, gq, gk,
+                                            ops.QWEN3_NORM_EPS)
+    qg = q.float().cpu().numpy().astype(np.float64).reshape(b.total_tokens, -1)
+    within_tol(qg, e[:, :4096], bound[:, :4096], "q")
+    touched = np.zeros((b.num_blocks, 256), dtype=bool)
+    for blk, slot in new_slots(b)[:40]:
+        touched[blk, slot] = True
+    for pool, pool0 in ((b.k_pool, kp0), (b.v_pool, vp0)):
+        a = pool.view(torch.int16).cpu().numpy()
+        o = pool0.view(torch.int16).cpu().numpy()
+        assert np.array_equal(a[~touched], o[~touched])
+
+
+def test_qknorm_rejects_bad_gains():
+    b = batch_for([(0, 8)], seed=193)
+    x, w = inputs(194, 8), weights(195)
+    gq, gk = norm_gains(196)
+    ws = workspace_for(b)
+    for kw in (dict(norm_eps=-1.0), dict(norm_eps=float("nan")), dict(norm_eps=float("inf"))):
+        with pytest.raises(ops.PagedAttnError) as err:
+            ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws,
+                                 q_norm_weight=gq, k_norm_weight=gk, **kw)
+        assert err.value.status == 1
+    with pytest.raises(ValueError):
+        ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws, q_norm_weight=gq)
