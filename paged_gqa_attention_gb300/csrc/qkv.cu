@@ -855,9 +855,9 @@ qk_norm_kernel(const __grid_constant__ QkvArgs a, int groups_per_warp) {
                 w_lo[h] = row[h * (kD / 2) + lane];
                 w_hi[h] = row[h * (kD / 2) + 32 + lane];
             }
-            // out[2l]   = inv (x[2l] g c0 - x[64+2l] g' s0),  out[64+2l] = inv (x[64+2l] g' c0 + x[2l] g s0)
-            // (and the same for dims 2l+1, 65+2l with c1, s1): per-group coefficients
-            // this lane's gains (dims 2l, 2l+1, 64+2l, 65+2l), from L1 after the first group
+            // this lane's gains (dims 2l, 2l+1, 64+2l, 65+2l), from L1 after the first group, and the
+            // coefficients of out[2l] = inv (x[2l] g c0 - x[64+2l] g' s0), out[64+2l] = inv (x[64+2l] g' c0
+            // + x[2l] g s0) (the same for dims 2l+1, 65+2l with c1, s1), inv = 1 / the head's RMS
             const uint32_t *gw = static_cast<const uint32_t *>(is_k ? a.k_norm : a.q_norm);
             const uint32_t gl = __ldg(gw + lane), gh = __ldg(gw + 32 + lane);
             const float G0 = bf16_low_half(gl), G1 = bf16_high_half(gl);
