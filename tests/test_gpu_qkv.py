@@ -468,3 +468,38 @@ def test_qknorm_rejects_bad_gains():
         assert err.value.status == 1
     with pytest.raises(ValueError):
         ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws, q_norm_weight=gq)
+
+
+@pytest.mark.parametrize("qknorm", [False, True])
+def test_inconsistent_sequence_gets_nan_q_and_no_kv(qknorm):
+    """A sequence whose new tokens outnumber its length (q_len 20 > seq_len 5): its tokens get no
+    K/V row anywhere and, with the rotation, NaN q rows (their positions are unknown); the other
+    sequence is computed as usual; PA_ERR_DEVICE is recorded."""
+    b = batch_for([(10, 30), (0, 20)], seed=197)
+    x, w = inputs(198, b.total_tokens), weights(199)
+    bad_lens = b.seq_lens.clone()
+    bad_lens[1] = 5
+    gq, gk = norm_gains(200) if qknorm else (None, None)
+    kp0, vp0 = b.k_pool.clone(), b.v_pool.clone()
+    ws = workspace_for(b)
+    q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, bad_lens, ws,
+                             rope_theta=ops.QWEN3_ROPE_THETA, q_norm_weight=gq, k_norm_weight=gk)
+    with pytest.raises(ops.PagedAttnError) as err:
+        ops.check_error(ws)
+    assert err.value.status == 4
+    assert torch.isnan(q[30:].float()).all()
+    rows = list(range(30))
+    if qknorm:
+        e, bound, _, _ = qknorm_exact_and_bound(x, w, b.cu_q_lens, b.seq_lens, ops.QWEN3_ROPE_THETA, gq, gk,
+                                                ops.QWEN3_NORM_EPS, rows=rows)
+    else:
+        e, bound = exact_and_bound(x, w, b.cu_q_lens, b.seq_lens, ops.QWEN3_ROPE_THETA, rows=rows)
+    qg = q[:30].float().cpu().numpy().astype(np.float64).reshape(30, -1)
+    within_tol(qg, e[:, :4096], bound[:, :4096], "q of the consistent sequence")
+    touched = np.zeros((b.num_blocks, 256), dtype=bool)
+    for blk, slot in new_slots(b)[:30]:
+        touched[blk, slot] = True
+    for pool, pool0 in ((b.k_pool, kp0), (b.v_pool, vp0)):
+        a = pool.view(torch.int16).cpu().numpy()
+        o = pool0.view(torch.int16).cpu().numpy()
+        assert np.array_equal(a[~touched], o[~touched])
