@@ -772,15 +772,13 @@ cudaError_t launch_qkv_bn(const QkvArgs &a, const CUtensorMap &x_map, const CUte
 // token's lookup and angles are computed once; 1 when there are few, for parallelism).  Lane l
 // holds dims 2l, 2l+1, 64+2l and 65+2l of each head -- both dims of two rotation pairs -- so
 // only the sums of squares cross lanes, and every load and store of the warp is 128 contiguous
-// bytes.  The pass is bound by its instruction count more than by memory (the rows it reads
-// were just written by the projection and sit in L2), hence the packed fp32 arithmetic and a
-// reduce-scatter of the eight sums (17 shuffles instead of 40).
+// bytes.  The rows it reads were just written by the projection and sit in L2; its instruction
+// count mattered (a first form with 40 shuffles and an IEEE division and square root per head
+// took twice as long), hence the packed fp32 arithmetic, rsqrtf and a reduce-scatter of the eight
+// sums (17 shuffles instead of 40).
 constexpr int kNormGroups = kHq / 8 + 1;       // 4 groups of q heads + the k heads
 constexpr int kNormThreads = 256;
 constexpr int kNormCtasPerSm = 4;              // 64 registers a thread
-
-__device__ __forceinline__ float bf16_low_half(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_high_half(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // The sums of v[0..7] over the warp, for every lane: reduce-scatter (after the steps over lane
 // bits 16, 8 and 4 a lane holds a partial of head h(lane) = 4 b16 + 2 b8 + b4, the steps over
@@ -860,15 +858,15 @@ qk_norm_kernel(const __grid_constant__ QkvArgs a, int groups_per_warp) {
             // + x[2l] g s0) (the same for dims 2l+1, 65+2l with c1, s1), inv = 1 / the head's RMS
             const uint32_t *gw = static_cast<const uint32_t *>(is_k ? a.k_norm : a.q_norm);
             const uint32_t gl = __ldg(gw + lane), gh = __ldg(gw + 32 + lane);
-            const float G0 = bf16_low_half(gl), G1 = bf16_high_half(gl);
-            const float G2 = bf16_low_half(gh), G3 = bf16_high_half(gh);
+            const float G0 = bf16_lo(gl), G1 = bf16_hi(gl);
+            const float G2 = bf16_lo(gh), G3 = bf16_hi(gh);
             const float A0 = G0 * c0, A1 = G1 * c1, nB0 = -(G2 * s0), nB1 = -(G3 * s1);   // -> dims 2l, 2l+1
             const float A2 = G2 * c0, A3 = G3 * c1, B2 = G0 * s0, B3 = G1 * s1;           // -> dims 64+2l, 65+2l
             float ss[8];
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
-                const float x0 = bf16_low_half(w_lo[h]), x1 = bf16_high_half(w_lo[h]);
-                const float x2 = bf16_low_half(w_hi[h]), x3 = bf16_high_half(w_hi[h]);
+                const float x0 = bf16_lo(w_lo[h]), x1 = bf16_hi(w_lo[h]);
+                const float x2 = bf16_lo(w_hi[h]), x3 = bf16_hi(w_hi[h]);
                 float p, q;
                 ffma2(p, q, x0, x1, x0, x1, 0.f, 0.f);
                 ffma2(p, q, x2, x3, x2, x3, p, q);
@@ -878,8 +876,8 @@ qk_norm_kernel(const __grid_constant__ QkvArgs a, int groups_per_warp) {
             warp_sums8(ss, lane, [eps](float t) { return rsqrtf(fmaf(t, 1.0f / kD, eps)); });
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
-                const float x0 = bf16_low_half(w_lo[h]), x1 = bf16_high_half(w_lo[h]);
-                const float x2 = bf16_low_half(w_hi[h]), x3 = bf16_high_half(w_hi[h]);
+                const float x0 = bf16_lo(w_lo[h]), x1 = bf16_hi(w_lo[h]);
+                const float x2 = bf16_lo(w_hi[h]), x3 = bf16_hi(w_hi[h]);
                 float o0, o1, o2, o3;
                 ffma2(o0, o1, x0, x1, A0, A1, 0.f, 0.f);
                 ffma2(o0, o1, x2, x3, nB0, nB1, o0, o1);
