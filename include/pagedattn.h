@@ -205,6 +205,10 @@ pa_status paged_attn_decode(pa_shape shape, void *out, float *lse, const void *q
  * As paged_attn_decode, with the split length fixed by the caller: split_tokens is
  * the number of context tokens one CTA handles (a positive multiple of 64), or 0
  * for the library's own choice.  Exposed for tuning and for split-invariance tests.
+ * A split shorter than the library's choice needs more partial results than
+ * pa_workspace_bytes() provides for: batch * 8 * ceil(max_blocks_per_seq * 256 /
+ * split_tokens) entries of 2080 bytes past the fixed part; a smaller workspace
+ * returns PA_ERR_WORKSPACE and launches nothing.
  */
 pa_status paged_attn_decode_split(pa_shape shape, void *out, float *lse, const void *q,
                                   const void *k_pool, const void *v_pool,
