@@ -77,13 +77,13 @@ def new_slots(b):
     return out
 
 
-def exact_and_bound(x, w, cu_q_lens, seq_lens, rope_theta, rows=None):
+def exact_and_bound(x, w, cu_q_lens, seq_lens, rope_theta, rows=None, projected=None):
     """The oracle's exact outputs (q and k heads rotated when rope_theta > 0) and the
     accumulation part of the bound: a rotated dim mixes the two columns of its pair, so it
     carries both their accumulation errors, and the fp32 angle (about 1e-6 rad) adds
-    1e-5 x the pair's size."""
-    y = oracle.qkv_project(x.cpu(), w.cpu(), rows=rows)
-    a = abs_sums(x, w, rows)
+    1e-5 x the pair's size.  projected: (y, sum|x w|) of the listed rows, if already at hand."""
+    y, a = projected if projected is not None else (oracle.qkv_project(x.cpu(), w.cpu(), rows=rows),
+                                                    abs_sums(x, w, rows))
     if rope_theta:
         pos = oracle.token_positions(cu_q_lens.cpu(), seq_lens.cpu())
         if rows is not None:
@@ -314,7 +314,7 @@ def norm_gains(seed):
     return q, k
 
 
-def qknorm_exact_and_bound(x, w, cu_q_lens, seq_lens, rope_theta, gq, gk, eps, rows=None):
+def qknorm_exact_and_bound(x, w, cu_q_lens, seq_lens, rope_theta, gq, gk, eps, rows=None, projected=None):
     """The oracle's q and k after the norm and the rotation (exact, before the last rounding),
     and per element the part of the bound that the projection's own error carries through
     the norm.  The GPU normalises its bf16 projection p', the oracle the rounded exact one p:
@@ -323,8 +323,8 @@ def qknorm_exact_and_bound(x, w, cu_q_lens, seq_lens, rope_theta, gq, gk, eps, r
     |g| d / r + |g p| (sum_j |p_j| d_j) / (128 r^3); a rotated dim mixes the two dims of its
     pair, and the fp32 arithmetic and angle add 1e-5 of the pair's size.  Returned scaled by
     2^16, in the units ``within_tol`` takes for its second term."""
-    y = oracle.qkv_project(x.cpu(), w.cpu(), rows=rows)
-    a = abs_sums(x, w, rows)
+    y, a = projected if projected is not None else (oracle.qkv_project(x.cpu(), w.cpu(), rows=rows),
+                                                    abs_sums(x, w, rows))
     p = (oracle.bf16_round(y[:, :5120]).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     d = 2.0 ** -7 * np.abs(y[:, :5120]) + 2.0 ** -16 * a[:, :5120]
     n = np.concatenate([oracle.rms_norm_heads(p[:, :4096], gq.cpu(), eps, n_heads=32),
@@ -503,3 +503,50 @@ def test_inconsistent_sequence_gets_nan_q_and_no_kv(qknorm):
         a = pool.view(torch.int16).cpu().numpy()
         o = pool0.view(torch.int16).cpu().numpy()
         assert np.array_equal(a[~touched], o[~touched])
+
+
+# ------------------------------------------------------------------ whole tensors at full size
+
+@pytest.fixture(scope="module")
+def full_chunk():
+    """The 4096-token prompt of the causal prefill workload (the benchmark's projection): inputs
+    and the oracle's exact projection of every row, computed once for the tests below."""
+    b = wl.causal_prefill(device="cuda")
+    x, w = inputs(66, b.total_tokens), weights(67)
+    return b, x, w, (oracle.qkv_project(x.cpu(), w.cpu()), abs_sums(x, w))
+
+
+def cache_rows(b, pool):
+    """The new tokens' rows of a pool, [tokens, 8 * 128] float64, in token order."""
+    blk, slot = (torch.tensor(v, device=pool.device) for v in zip(*new_slots(b)))
+    return pool[blk, slot].double().cpu().numpy().reshape(len(blk), -1)
+
+
+@pytest.mark.parametrize("qknorm", [False, True])
+def test_full_prefill_chunk_whole_tensors(full_chunk, qknorm):
+    """Every element of q and of the appended k and v rows for all 4096 new tokens, with Qwen3's
+    rotary embedding (and, in the second case, its QK-norm), against the oracle."""
+    b0, x, w, projected = full_chunk
+    b = wl.causal_prefill(device="cuda")          # fresh pools for each case
+    ws = workspace_for(b)
+    if qknorm:
+        gq, gk = norm_gains(201)
+        q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws,
+                                 rope_theta=ops.QWEN3_ROPE_THETA, q_norm_weight=gq, k_norm_weight=gk)
+        e, bound, y, a = qknorm_exact_and_bound(x, w, b.cu_q_lens, b.seq_lens, ops.QWEN3_ROPE_THETA, gq, gk,
+                                                ops.QWEN3_NORM_EPS, projected=projected)
+        k_exact, k_bound = e[:, 4096:], bound[:, 4096:]
+    else:
+        q = ops.paged_qkv_append(x, w, b.k_pool, b.v_pool, b.block_table, b.cu_q_lens, b.seq_lens, ws,
+                                 rope_theta=ops.QWEN3_ROPE_THETA)
+        e, bound = exact_and_bound(x, w, b.cu_q_lens, b.seq_lens, ops.QWEN3_ROPE_THETA, projected=projected)
+        y, a = projected
+        k_exact, k_bound = e[:, 4096:5120], bound[:, 4096:5120]
+    ops.check_error(ws)
+    qg = q.float().cpu().numpy().astype(np.float64).reshape(b.total_tokens, -1)
+    within_tol(qg, e[:, :4096], bound[:, :4096], "q")
+    rel = np.sqrt(((qg - e[:, :4096]) ** 2).sum() / (e[:, :4096] ** 2).sum())
+    assert rel <= 5e-3, rel
+    within_tol(cache_rows(b, b.k_pool), k_exact, k_bound, "k rows in the cache")
+    within_tol(cache_rows(b, b.v_pool), y[:, 5120:], a[:, 5120:], "v rows in the cache")
+
