@@ -149,15 +149,28 @@ def test_decode_fp8_single_key_returns_its_row():
 
 
 def test_decode_fp8_full_size_batched():
+    """The benchmark's 8-bit workload (batch 32, contexts U{128..4096}): the plain decode over the
+    oracle's cache, and the benchmark's fused step (each new token appended, then the decode) on
+    the cache without the new tokens; all 32 x 32 rows and their lse against the oracle, the
+    appended codes and scales bit-exact."""
     b = wl.batched_decode(device="cuda")
-    cache = oracle_cache(b)
-    kc, vc, ks, vs = upload(cache)
+    full = oracle_cache(b)
     ws = workspace_for(b)
-    out = ops.paged_attn_decode_fp8(b.q, kc, vc, ks, vs, b.block_table, b.seq_lens, ws)
+    lse = torch.empty(b.num_seqs, ops.NUM_Q_HEADS, dtype=torch.float32, device="cuda")
+    out = ops.paged_attn_decode_fp8(b.q, *upload(full), b.block_table, b.seq_lens, ws, lse=lse)
     ops.check_error(ws)
-    ref, _ = oracle.attention_fp8(to_cpu(b.q), *cache, to_cpu(b.block_table), to_cpu(b.cu_q_lens),
-                                  to_cpu(b.seq_lens), scale=wl.SCALE)
+    ref, ref_lse = oracle.attention_fp8(to_cpu(b.q), *full, to_cpu(b.block_table), to_cpu(b.cu_q_lens),
+                                        to_cpu(b.seq_lens), scale=wl.SCALE)
     assert_close(out, ref, "fp8 batched decode, full size")
+    assert_lse_close(lse, ref_lse, "fp8 batched decode, full size")
+    c1 = upload(oracle_cache(b, drop_last=1))
+    lse_f = torch.empty_like(lse)
+    out_f = ops.paged_attn_decode_append_fp8(b.q, b.k_new, b.v_new, *c1, b.block_table, b.seq_lens, ws, lse=lse_f)
+    ops.check_error(ws)
+    for got, want in zip(c1, full):
+        assert same_bits(got, want)
+    assert_close(out_f, ref, "fp8 fused append + decode, full size")
+    assert_lse_close(lse_f, ref_lse, "fp8 fused append + decode, full size")
 
 
 def test_decode_fp8_bad_block_is_reported():
