@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import gpu, lib_ready, workspace_for
+from gpu_helpers import REPORT, gpu, lib_ready, workspace_for
 from paged_gqa_attention_gb300 import ops
 from paged_gqa_attention_gb300 import workloads as wl
 
@@ -60,7 +60,9 @@ def within_tol(got, exact, abs_sum, what):
     tol = np.abs(exact) * 2.0 ** -8 + abs_sum * 2.0 ** -16
     err = np.abs(got - exact)
     with np.errstate(divide="ignore", invalid="ignore"):      # zero rows: 0 / 0 in the report only
-        i = np.unravel_index(np.nanargmax(np.where(tol > 0, err / tol, np.where(err > 0, np.inf, 0.0))), err.shape)
+        ratio = np.where(tol > 0, err / tol, np.where(err > 0, np.inf, 0.0))
+    i = np.unravel_index(np.nanargmax(ratio), err.shape)
+    REPORT.append({"what": what, "kind": "bound", "max_ratio": float(ratio[i]), "elements": int(err.size)})
     assert (err <= tol).all(), (f"{what}: worst element {i}: got {got[i]!r} exact {exact[i]!r} "
                                 f"tolerance {tol[i]!r} ({(err > tol).sum()} elements beyond it)")
 
